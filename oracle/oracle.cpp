@@ -1,0 +1,369 @@
+// CPU ORACLE — test infrastructure only (see oracle.h).  Plain fp64 code that
+// follows the pages step by step; no blocking, fusion or reordering beyond a
+// split of independent output rows across threads, which leaves every output's
+// summation order unchanged (so results do not depend on the thread count).
+#include "oracle.h"
+
+#include <cmath>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+// ---- number formats ------------------------------------------------------
+
+double f16_to_double(uint16_t h) {
+    int s = (h >> 15) & 1, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0)
+        v = std::ldexp((double)m, -24);  // subnormal: m * 2^-24
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = std::ldexp((double)(1024 + m), e - 25);  // (1 + m/1024) * 2^(e-15)
+    return s ? -v : v;
+}
+
+// Nearest binary16 value of x (ties to even), as a double.
+double round_f16(double x) {
+    if (std::isnan(x) || x == 0.0) return x;
+    double a = std::fabs(x);
+    if (a >= 65520.0) return std::copysign(INFINITY, x);
+    int e;
+    std::frexp(a, &e);                        // a = f * 2^e, f in [0.5, 1)
+    int q = e - 11;                           // spacing 2^(e-11) for normals (11 significant bits)
+    if (q < -24) q = -24;                     // subnormal spacing
+    double scaled = std::ldexp(a, -q);        // exact
+    double r = std::nearbyint(scaled);        // default rounding mode: ties to even
+    return std::copysign(std::ldexp(r, q), x);
+}
+
+double round_f32(double x) { return (double)(float)x; }
+
+// ---- GGUF blocks (Shimmy v2.0 Architecture, "Quantization") --------------
+
+size_t block_bytes(int32_t wtype) { return wtype == ORC_Q8_0 ? 34 : (wtype == ORC_Q4_0 ? 18 : 0); }
+
+// Q8_0: fp16 scale d, then 32 signed bytes q; element j = d * q_j.
+// Q4_0: fp16 scale d, then 16 bytes; element j uses the low nibble of byte j
+// (j < 16) or the high nibble of byte j-16 (j >= 16); value = d * (nibble - 8).
+void dequant_block(int32_t wtype, const uint8_t* b, double* out) {
+    uint16_t dbits = (uint16_t)(b[0] | (b[1] << 8));
+    double d = f16_to_double(dbits);
+    if (wtype == ORC_Q8_0) {
+        for (int j = 0; j < 32; j++) out[j] = d * (double)(int8_t)b[2 + j];
+    } else {
+        for (int j = 0; j < 16; j++) {
+            out[j] = d * (double)((b[2 + j] & 0x0F) - 8);
+            out[j + 16] = d * (double)((b[2 + j] >> 4) - 8);
+        }
+    }
+}
+
+void dequant_row(int32_t wtype, const uint8_t* blocks, int64_t k, double* out) {
+    size_t bb = block_bytes(wtype);
+    for (int64_t b = 0; b < k / 32; b++) dequant_block(wtype, blocks + b * bb, out + b * 32);
+}
+
+// Run f(i) for i in [0, n) over n_threads threads (contiguous ranges).
+template <class F>
+void parallel_for(int64_t n, int n_threads, F f) {
+    if (n_threads <= 1 || n < 2) {
+        for (int64_t i = 0; i < n; i++) f(i);
+        return;
+    }
+    if (n_threads > n) n_threads = (int)n;
+    std::vector<std::thread> th;
+    for (int t = 0; t < n_threads; t++)
+        th.emplace_back([&, t] {
+            for (int64_t i = n * t / n_threads; i < n * (t + 1) / n_threads; i++) f(i);
+        });
+    for (auto& x : th) x.join();
+}
+
+double dot(const double* a, const double* b, int64_t n) {
+    double s = 0.0;
+    for (int64_t j = 0; j < n; j++) s += a[j] * b[j];
+    return s;
+}
+
+// Y[m][i] = W_i . X_m : dequantize weight row i once, then dot it with every input row.
+void qgemm(int32_t wtype, const uint8_t* W, int64_t n, int64_t k, const double* X, int64_t M, double* Y,
+           int n_threads) {
+    size_t row_bytes = (size_t)(k / 32) * block_bytes(wtype);
+    parallel_for(n, n_threads, [&](int64_t i) {
+        std::vector<double> w(k);
+        dequant_row(wtype, W + (size_t)i * row_bytes, k, w.data());
+        for (int64_t m = 0; m < M; m++) Y[m * n + i] = dot(w.data(), X + m * k, k);
+    });
+}
+
+void rmsnorm(const double* x, const float* w, int64_t n, double eps, double* y) {
+    double ss = 0.0;
+    for (int64_t j = 0; j < n; j++) ss += x[j] * x[j];
+    double inv = 1.0 / std::sqrt(ss / (double)n + eps);
+    for (int64_t j = 0; j < n; j++) y[j] = (double)w[j] * (x[j] * inv);
+}
+
+double yarn_scale(int32_t max_ctx, int32_t native_ctx) {
+    return (native_ctx > 0 && max_ctx > native_ctx) ? (double)max_ctx / (double)native_ctx : 1.0;
+}
+
+// Airframe GPU_PIPELINE.md, RoPE step: theta(t, i) = (t / yarn_scale) / base^(2i / head_dim).
+double rope_theta(int64_t t, int32_t i, int32_t head_dim, double base, double ys) {
+    return ((double)t / ys) / std::pow(base, (2.0 * i) / (double)head_dim);
+}
+
+// Pair (2i, 2i+1) of every head rotated by theta(t, i): [c -s; s c].
+void rope(double* v, int32_t n_heads, int32_t head_dim, int64_t t, double base, double ys) {
+    for (int32_t h = 0; h < n_heads; h++)
+        for (int32_t i = 0; i < head_dim / 2; i++) {
+            double th = rope_theta(t, i, head_dim, base, ys);
+            double c = std::cos(th), s = std::sin(th);
+            double* p = v + (size_t)h * head_dim + 2 * i;
+            double a = p[0], b = p[1];
+            p[0] = a * c - b * s;
+            p[1] = a * s + b * c;
+        }
+}
+
+// SwiGLU activation on the gate: gate * sigmoid(gate).
+double silu(double g) { return g / (1.0 + std::exp(-g)); }
+
+void softmax(double* s, int64_t n) {
+    double mx = s[0];
+    for (int64_t j = 1; j < n; j++) mx = s[j] > mx ? s[j] : mx;
+    double sum = 0.0;
+    for (int64_t j = 0; j < n; j++) {
+        s[j] = std::exp(s[j] - mx);
+        sum += s[j];
+    }
+    for (int64_t j = 0; j < n; j++) s[j] /= sum;
+}
+
+// scores = q_h . K_j / sqrt(head_dim), softmax over j, out_h = sum_j a_j V_j.
+// GQA: query head h reads kv head h / (n_heads / n_kv_heads).
+void attention(const double* q, int32_t H, int32_t KVH, int32_t D, const double* kc, const double* vc,
+               int64_t head_stride, int64_t n_keys, double* out) {
+    int32_t group = H / KVH;
+    std::vector<double> s(n_keys);
+    double scale = 1.0 / std::sqrt((double)D);
+    for (int32_t h = 0; h < H; h++) {
+        int32_t g = h / group;
+        const double* K = kc + (size_t)g * head_stride;
+        const double* V = vc + (size_t)g * head_stride;
+        for (int64_t j = 0; j < n_keys; j++) s[j] = dot(q + (size_t)h * D, K + (size_t)j * D, D) * scale;
+        softmax(s.data(), n_keys);
+        for (int32_t d = 0; d < D; d++) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < n_keys; j++) acc += s[j] * V[(size_t)j * D + d];
+            out[(size_t)h * D + d] = acc;
+        }
+    }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+struct orc_model {
+    orc_config c;
+    std::vector<const uint8_t*> layers;
+    const uint8_t* token_embd;
+    const float* output_norm;
+    const uint8_t* output;
+    uint64_t off[10];
+    int64_t slots;
+    std::vector<double> kcache, vcache;  // [L][KVH][slots][D], values rounded to the cache dtype
+    double ys;
+};
+
+extern "C" {
+
+double orc_f16_to_double(uint16_t h) { return f16_to_double(h); }
+double orc_round_f16(double x) { return round_f16(x); }
+double orc_round_f32(double x) { return round_f32(x); }
+
+int orc_dequant_row(int32_t wtype, const uint8_t* blocks, int64_t k, double* out) {
+    if (!block_bytes(wtype) || k % 32) return -1;
+    dequant_row(wtype, blocks, k, out);
+    return 0;
+}
+
+int orc_qgemv(int32_t wtype, const uint8_t* W, int64_t n, int64_t k, const double* x, double* y, int n_threads) {
+    return orc_qgemm(wtype, W, n, k, x, 1, y, n_threads);
+}
+
+int orc_qgemv_rows(int32_t wtype, const uint8_t* W, int64_t k, const int64_t* rows, int64_t n_rows, const double* x,
+                   double* y, int n_threads) {
+    if (!block_bytes(wtype) || k % 32) return -1;
+    size_t row_bytes = (size_t)(k / 32) * block_bytes(wtype);
+    parallel_for(n_rows, n_threads, [&](int64_t r) {
+        std::vector<double> w(k);
+        dequant_row(wtype, W + (size_t)rows[r] * row_bytes, k, w.data());
+        y[r] = dot(w.data(), x, k);
+    });
+    return 0;
+}
+
+int orc_qgemm(int32_t wtype, const uint8_t* W, int64_t n, int64_t k, const double* X, int64_t M, double* Y,
+              int n_threads) {
+    if (!block_bytes(wtype) || k % 32) return -1;
+    qgemm(wtype, W, n, k, X, M, Y, n_threads);
+    return 0;
+}
+
+void orc_rmsnorm(const double* x, const float* w, int64_t n, double eps, double* y) { rmsnorm(x, w, n, eps, y); }
+double orc_yarn_scale(int32_t max_ctx, int32_t native_ctx) { return yarn_scale(max_ctx, native_ctx); }
+double orc_rope_theta(int64_t t, int32_t i, int32_t head_dim, double base, double ys) {
+    return rope_theta(t, i, head_dim, base, ys);
+}
+void orc_rope(double* v, int32_t n_heads, int32_t head_dim, int64_t t, double base, double ys) {
+    rope(v, n_heads, head_dim, t, base, ys);
+}
+double orc_silu(double g) { return silu(g); }
+void orc_softmax(double* s, int64_t n) { softmax(s, n); }
+void orc_attention(const double* q, int32_t H, int32_t KVH, int32_t D, const double* kc, const double* vc,
+                   int64_t head_stride, int64_t n_keys, double* out) {
+    attention(q, H, KVH, D, kc, vc, head_stride, n_keys, out);
+}
+
+int orc_layer_offsets(const orc_config* c, uint64_t off[10]) {
+    size_t bb = block_bytes(c->wtype);
+    if (!bb || c->n_embd % 32 || c->n_ff % 32 || (c->n_heads * c->head_dim) % 32) return -1;
+    size_t E = c->n_embd, QD = (size_t)c->n_heads * c->head_dim, KVD = (size_t)c->n_kv_heads * c->head_dim;
+    size_t F = c->n_ff;
+    // attn_norm, attn_q, attn_k, attn_v, attn_o, ffn_norm, ffn_gate, ffn_up, ffn_down
+    size_t sz[9] = {E * 4, QD * (E / 32) * bb, KVD * (E / 32) * bb, KVD * (E / 32) * bb, E * (QD / 32) * bb,
+                    E * 4, F * (E / 32) * bb, F * (E / 32) * bb, E * (F / 32) * bb};
+    size_t o = 0;
+    for (int i = 0; i < 9; i++) {
+        off[i] = o;
+        o = align256(o + sz[i]);
+    }
+    off[9] = o;
+    return 0;
+}
+
+// Airframe GPU_PIPELINE.md, "KV cache": L * KVH * max_ctx * head_dim * elem, times 2 (K and V).
+uint64_t orc_kv_bytes(const orc_config* c) {
+    return (uint64_t)c->n_layers * c->n_kv_heads * c->max_ctx * c->head_dim * (c->kv_f16 ? 2 : 4) * 2;
+}
+
+orc_model* orc_model_create(const orc_config* c, const uint8_t* const* layer_blobs, const uint8_t* token_embd,
+                            const float* output_norm, const uint8_t* output, int64_t kv_slots) {
+    if (c->n_heads % c->n_kv_heads || c->head_dim % 2) return nullptr;
+    orc_model* m = new orc_model();
+    m->c = *c;
+    if (orc_layer_offsets(c, m->off)) {
+        delete m;
+        return nullptr;
+    }
+    m->layers.assign(layer_blobs, layer_blobs + c->n_layers);
+    m->token_embd = token_embd;
+    m->output_norm = output_norm;
+    m->output = output;
+    m->slots = (kv_slots > 0 && kv_slots < c->max_ctx) ? kv_slots : c->max_ctx;
+    size_t n = (size_t)c->n_layers * c->n_kv_heads * m->slots * c->head_dim;
+    m->kcache.assign(n, 0.0);
+    m->vcache.assign(n, 0.0);
+    m->ys = yarn_scale(c->max_ctx, c->native_ctx);
+    return m;
+}
+
+void orc_model_destroy(orc_model* m) { delete m; }
+
+int orc_kv_read(const orc_model* m, int32_t layer, int32_t kvh, int64_t pos, double* k, double* v) {
+    const orc_config& c = m->c;
+    if (layer < 0 || layer >= c.n_layers || kvh < 0 || kvh >= c.n_kv_heads || pos < 0 || pos >= m->slots) return -1;
+    size_t base = (((size_t)layer * c.n_kv_heads + kvh) * m->slots + pos) * c.head_dim;
+    std::memcpy(k, &m->kcache[base], sizeof(double) * c.head_dim);
+    std::memcpy(v, &m->vcache[base], sizeof(double) * c.head_dim);
+    return 0;
+}
+
+int64_t orc_argmax(const double* v, int64_t n) {
+    int64_t best = 0;
+    for (int64_t i = 1; i < n; i++)
+        if (v[i] > v[best]) best = i;
+    return best;
+}
+
+// Forward pass over n tokens at positions start_pos.. (Airframe per-layer op
+// order; a decode step is the case n = 1).  All rows write their K/V before any
+// row attends; row r attends to cache slots 0..start_pos+r (causal).
+int orc_forward(orc_model* m, const int32_t* tokens, int64_t n, int64_t start_pos, double* logits, double* capture,
+                int n_threads) {
+    const orc_config& c = m->c;
+    if (n <= 0 || start_pos < 0 || start_pos + n > m->slots) return -1;
+    for (int64_t r = 0; r < n; r++)
+        if (tokens[r] < 0 || tokens[r] >= c.n_vocab) return -2;
+    const int64_t E = c.n_embd, H = c.n_heads, KVH = c.n_kv_heads, D = c.head_dim, F = c.n_ff;
+    const int64_t QD = H * D, KVD = KVH * D;
+    const size_t bb = block_bytes(c.wtype);
+
+    std::vector<double> X(n * E), Y(n * E), Q(n * QD), K(n * KVD), V(n * KVD), A(n * QD), O(n * E);
+    std::vector<double> G(n * F), U(n * F), Hh(n * F);
+
+    // embedding lookup: dequantized row of token_embd
+    for (int64_t r = 0; r < n; r++)
+        dequant_row(c.wtype, m->token_embd + (size_t)tokens[r] * (E / 32) * bb, E, &X[r * E]);
+    if (capture) std::memcpy(capture, X.data(), sizeof(double) * n * E);
+
+    for (int32_t l = 0; l < c.n_layers; l++) {
+        const uint8_t* blob = m->layers[l];
+        const float* attn_norm = (const float*)(blob + m->off[0]);
+        const uint8_t* Wq = blob + m->off[1];
+        const uint8_t* Wk = blob + m->off[2];
+        const uint8_t* Wv = blob + m->off[3];
+        const uint8_t* Wo = blob + m->off[4];
+        const float* ffn_norm = (const float*)(blob + m->off[5]);
+        const uint8_t* Wg = blob + m->off[6];
+        const uint8_t* Wu = blob + m->off[7];
+        const uint8_t* Wd = blob + m->off[8];
+
+        for (int64_t r = 0; r < n; r++) rmsnorm(&X[r * E], attn_norm, E, c.rms_eps, &Y[r * E]);
+        qgemm(c.wtype, Wq, QD, E, Y.data(), n, Q.data(), n_threads);
+        qgemm(c.wtype, Wk, KVD, E, Y.data(), n, K.data(), n_threads);
+        qgemm(c.wtype, Wv, KVD, E, Y.data(), n, V.data(), n_threads);
+        for (int64_t r = 0; r < n; r++) {
+            rope(&Q[r * QD], (int32_t)H, (int32_t)D, start_pos + r, c.rope_base, m->ys);
+            rope(&K[r * KVD], (int32_t)KVH, (int32_t)D, start_pos + r, c.rope_base, m->ys);
+        }
+        // KV write at position t, rounded to the cache's element type
+        for (int64_t r = 0; r < n; r++)
+            for (int64_t g = 0; g < KVH; g++)
+                for (int64_t d = 0; d < D; d++) {
+                    size_t idx = (((size_t)l * KVH + g) * m->slots + start_pos + r) * D + d;
+                    double kv = K[r * KVD + g * D + d], vv = V[r * KVD + g * D + d];
+                    m->kcache[idx] = c.kv_f16 ? round_f16(kv) : round_f32(kv);
+                    m->vcache[idx] = c.kv_f16 ? round_f16(vv) : round_f32(vv);
+                }
+        const double* kc = &m->kcache[(size_t)l * KVH * m->slots * D];
+        const double* vc = &m->vcache[(size_t)l * KVH * m->slots * D];
+        parallel_for(n, n_threads, [&](int64_t r) {
+            attention(&Q[r * QD], (int32_t)H, (int32_t)KVH, (int32_t)D, kc, vc, m->slots * D, start_pos + r + 1,
+                      &A[r * QD]);
+        });
+        qgemm(c.wtype, Wo, E, QD, A.data(), n, O.data(), n_threads);
+        for (int64_t i = 0; i < n * E; i++) X[i] += O[i];
+
+        for (int64_t r = 0; r < n; r++) rmsnorm(&X[r * E], ffn_norm, E, c.rms_eps, &Y[r * E]);
+        qgemm(c.wtype, Wg, F, E, Y.data(), n, G.data(), n_threads);
+        qgemm(c.wtype, Wu, F, E, Y.data(), n, U.data(), n_threads);
+        for (int64_t i = 0; i < n * F; i++) Hh[i] = silu(G[i]) * U[i];
+        qgemm(c.wtype, Wd, E, F, Hh.data(), n, O.data(), n_threads);
+        for (int64_t i = 0; i < n * E; i++) X[i] += O[i];
+        if (capture) std::memcpy(capture + (size_t)(l + 1) * n * E, X.data(), sizeof(double) * n * E);
+    }
+    if (logits) {
+        // final RMS norm on the last position only, then the LM head
+        std::vector<double> last(E);
+        rmsnorm(&X[(n - 1) * E], m->output_norm, E, c.rms_eps, last.data());
+        qgemm(c.wtype, m->output, c.n_vocab, E, last.data(), 1, logits, n_threads);
+    }
+    return 0;
+}
+
+}  // extern "C"
