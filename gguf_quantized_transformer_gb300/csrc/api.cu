@@ -1,0 +1,623 @@
+// C ABI (include/af.h): validation, weight repacking, buffers and the launch
+// sequences of prefill and decode.
+//
+// Launch sequence per layer (Airframe "GPU_PIPELINE.md" per-layer ops; dotLLM
+// "GPU Inference", "Forward Pass" and "Synchronization Model": one stream, no
+// host sync inside the pass):
+//   decode : GEMV[RMSNorm | QKV -> RoPE -> q, KV write]  -> attention(split-KV)
+//            -> GEMV[O -> x +=] -> GEMV[RMSNorm | gate,up -> SwiGLU]
+//            -> GEMV[down -> x +=];  head: GEMV[RMSNorm | LM head -> logits, argmax]
+//   prefill: RMSNorm rows -> GEMM[QKV -> RoPE, KV write] -> causal attention
+//            -> GEMM[O -> x +=] -> RMSNorm rows -> GEMM[gate,up -> SwiGLU]
+//            -> GEMM[down -> x +=]; LM head on the last row only.
+// The decode step after its first kernel is captured once into a CUDA graph
+// (position and token are read from device memory, so the graph is reused).
+#include <algorithm>
+#include <cstdarg>
+#include <new>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+using namespace af;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+#define CK(call)                                                                                 \
+    do {                                                                                         \
+        cudaError_t e_ = (call);                                                                 \
+        if (e_ != cudaSuccess) return fail(AF_ECUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                                           __FILE__, __LINE__);                                  \
+    } while (0)
+
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t block_bytes(int wtype) { return wtype == AF_Q8_0 ? 34 : (wtype == AF_Q4_0 ? 18 : 0); }
+
+// Tracks device allocations of one object so a failed create frees everything.
+struct Allocs {
+    std::vector<void*> p;
+    void* get(size_t bytes) {
+        void* q = nullptr;
+        if (cudaMalloc(&q, bytes ? bytes : 1) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        p.push_back(q);
+        return q;
+    }
+    void free_all() {
+        for (void* q : p) cudaFree(q);
+        p.clear();
+    }
+};
+
+Planes make_planes(Allocs& A, int wtype, int N, int K) {
+    Planes P;
+    size_t qs_bytes = 0;
+    size_t total = planes_bytes(wtype, N, K, &qs_bytes);
+    uint8_t* buf = (uint8_t*)A.get(total);
+    if (!buf) return P;
+    P.qs = buf;
+    P.sc = (const __half*)(buf + qs_bytes);
+    P.N = N;
+    P.K = K;
+    P.Kp = padded_k(wtype, K);
+    P.wtype = wtype;
+    return P;
+}
+
+cudaError_t repack_into(const Planes& P, const void* src, int N, int row0, int step, cudaStream_t s) {
+    return launch_repack((const uint8_t*)src, P.wtype, N, P.K, (uint8_t*)P.qs, (__half*)P.sc, P.Kp, row0, step, s);
+}
+
+struct LayerW {
+    Planes qkv, o, gu, down;
+    const float* attn_norm = nullptr;
+    const float* ffn_norm = nullptr;
+};
+
+int check_config(const af_config* c) {
+    if (!c) return fail(AF_EINVAL, "null config");
+    if (c->wtype != AF_Q4_0 && c->wtype != AF_Q8_0) return fail(AF_EINVAL, "wtype must be AF_Q4_0 or AF_Q8_0");
+    if (c->kv_dtype != AF_F32 && c->kv_dtype != AF_F16) return fail(AF_EINVAL, "kv_dtype must be AF_F32 or AF_F16");
+    if (c->n_layers <= 0 || c->n_embd <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+        c->n_ff <= 0 || c->n_vocab <= 0 || c->max_ctx <= 0)
+        return fail(AF_EINVAL, "all sizes must be positive");
+    if (c->max_chunk < 0 || c->native_ctx < 0) return fail(AF_EINVAL, "negative max_chunk / native_ctx");
+    if (c->n_embd % 32 || c->n_ff % 32 || (c->n_heads * c->head_dim) % 32)
+        return fail(AF_EINVAL, "n_embd, n_ff and n_heads*head_dim must be multiples of 32 (GGUF block)");
+    if (c->n_heads % c->n_kv_heads) return fail(AF_EINVAL, "n_heads must be a multiple of n_kv_heads");
+    if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return fail(AF_EINVAL, "bad rms_eps / rope_base");
+    if (!attn_supported(c->n_heads, c->n_kv_heads, c->head_dim))
+        return fail(AF_ENOTIMPL, "attention supports head_dim 64/128 and group size 1/2/4/8");
+    if (c->n_embd % 64 || c->n_ff % 64 || (c->n_heads * c->head_dim) % 64 || c->n_vocab % 2)
+        return fail(AF_ENOTIMPL, "n_embd, n_ff, n_heads*head_dim must be multiples of 64 and n_vocab even");
+    return AF_OK;
+}
+
+}  // namespace
+
+struct af_model {
+    af_config c{};
+    cudaStream_t s = nullptr;
+    bool own_stream = false;
+    Allocs A;
+    std::vector<LayerW> L;
+    Planes emb, out;
+    const float* out_norm = nullptr;
+    void* kc = nullptr;
+    void* vc = nullptr;
+    size_t kv_layer_elems = 0;
+    float2* rope = nullptr;
+    int chunk = 512;
+    float* x = nullptr;      // [chunk][E] residual stream
+    float* q = nullptr;      // [chunk][H*D] rotated q
+    float* attn = nullptr;   // [H*D] decode attention output
+    float* h = nullptr;      // [F] decode SwiGLU output
+    __half* y16 = nullptr;   // [chunk][max(E, ...)] normalized activations (GEMM operand)
+    __half* a16 = nullptr;   // [chunk][H*D] attention output (GEMM operand)
+    __half* h16 = nullptr;   // [chunk][F] SwiGLU output (GEMM operand)
+    int* tok = nullptr;      // [chunk]
+    float* logits = nullptr; // [V] default logits
+    GemvScratch gs;
+    AttnScratch as;
+    StepState* st = nullptr;
+    float* capture = nullptr;
+    bool use_graph = true;
+    cudaGraphExec_t gexec = nullptr;
+    float* graph_logits = nullptr;
+
+    int E() const { return c.n_embd; }
+    int QD() const { return c.n_heads * c.head_dim; }
+    int KVD() const { return c.n_kv_heads * c.head_dim; }
+    void* kl(int l) const { return (char*)kc + (size_t)l * kv_layer_elems * (c.kv_dtype == AF_F16 ? 2 : 4); }
+    void* vl(int l) const { return (char*)vc + (size_t)l * kv_layer_elems * (c.kv_dtype == AF_F16 ? 2 : 4); }
+};
+
+struct af_qweight {
+    Planes p;
+    Allocs A;
+    GemvScratch gs;
+    __half* x16 = nullptr;
+    int x16_rows = 0;
+};
+
+extern "C" {
+
+const char* af_last_error(void) { return g_err.c_str(); }
+
+int af_layer_offsets(const af_config* c, uint64_t off[10]) {
+    if (!c || !off) return fail(AF_EINVAL, "null argument");
+    size_t bb = block_bytes(c->wtype);
+    if (!bb) return fail(AF_EINVAL, "bad wtype");
+    if (c->n_embd <= 0 || c->n_ff <= 0 || c->n_heads <= 0 || c->head_dim <= 0 || c->n_kv_heads <= 0 ||
+        c->n_embd % 32 || c->n_ff % 32 || (c->n_heads * c->head_dim) % 32)
+        return fail(AF_EINVAL, "bad shape");
+    const size_t E = c->n_embd, QD = (size_t)c->n_heads * c->head_dim, KVD = (size_t)c->n_kv_heads * c->head_dim;
+    const size_t F = c->n_ff;
+    const size_t sz[9] = {E * 4, QD * (E / 32) * bb, KVD * (E / 32) * bb, KVD * (E / 32) * bb, E * (QD / 32) * bb,
+                          E * 4, F * (E / 32) * bb, F * (E / 32) * bb, E * (F / 32) * bb};
+    size_t o = 0;
+    for (int i = 0; i < 9; i++) {
+        off[i] = o;
+        o = al256(o + sz[i]);
+    }
+    off[9] = o;
+    return AF_OK;
+}
+
+uint64_t af_kv_bytes(const af_config* c) {
+    if (!c || c->n_layers <= 0 || c->n_kv_heads <= 0 || c->max_ctx <= 0 || c->head_dim <= 0) return 0;
+    return (uint64_t)c->n_layers * c->n_kv_heads * c->max_ctx * c->head_dim * (c->kv_dtype == AF_F16 ? 2 : 4) * 2;
+}
+
+void af_model_destroy(af_model* m) {
+    if (!m) return;
+    if (m->gexec) cudaGraphExecDestroy(m->gexec);
+    if (m->s) cudaStreamSynchronize(m->s);
+    m->A.free_all();
+    if (m->own_stream) cudaStreamDestroy(m->s);
+    delete m;
+}
+
+int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_model** out) {
+    if (!out) return fail(AF_EINVAL, "null out");
+    *out = nullptr;
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (!w || !w->layer_blob || !w->token_embd || !w->output_norm || !w->output)
+        return fail(AF_EINVAL, "null weight pointer");
+    for (int l = 0; l < cfg->n_layers; l++)
+        if (!w->layer_blob[l]) return fail(AF_EINVAL, "null layer blob %d", l);
+    uint64_t off[10];
+    af_layer_offsets(cfg, off);
+
+    af_model* m = new (std::nothrow) af_model();
+    if (!m) return fail(AF_ENOMEM, "host allocation failed");
+    m->c = *cfg;
+    if (m->c.max_chunk == 0) m->c.max_chunk = 512;
+    m->chunk = m->c.max_chunk;
+    m->s = (cudaStream_t)stream;
+    if (!m->s) {  // a blocking stream of our own: ordered with the legacy default stream, and capturable
+        if (cudaStreamCreate(&m->s) != cudaSuccess) {
+            cudaGetLastError();
+            delete m;
+            return fail(AF_ECUDA, "cudaStreamCreate failed");
+        }
+        m->own_stream = true;
+    }
+    const af_config& c = m->c;
+    const int E = c.n_embd, QD = m->QD(), KVD = m->KVD(), F = c.n_ff, V = c.n_vocab, D = c.head_dim;
+    const int wt = c.wtype;
+    cudaStream_t s = m->s;
+    Allocs& A = m->A;
+    auto oom = [&](const char* what) {
+        m->A.free_all();
+        if (m->own_stream) cudaStreamDestroy(m->s);
+        delete m;
+        return fail(AF_ENOMEM, "device allocation failed: %s", what);
+    };
+    auto cuda_fail = [&](cudaError_t e, const char* what) {
+        cudaStreamSynchronize(m->s);
+        m->A.free_all();
+        if (m->own_stream) cudaStreamDestroy(m->s);
+        delete m;
+        return fail(AF_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+    };
+
+    // weights
+    m->L.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers; l++) {
+        LayerW& lw = m->L[l];
+        const uint8_t* blob = (const uint8_t*)w->layer_blob[l];
+        lw.qkv = make_planes(A, wt, QD + 2 * KVD, E);
+        lw.o = make_planes(A, wt, E, QD);
+        lw.gu = make_planes(A, wt, 2 * F, E);
+        lw.down = make_planes(A, wt, E, F);
+        float* norms = (float*)A.get(2 * al256((size_t)E * 4));
+        if (!lw.qkv.qs || !lw.o.qs || !lw.gu.qs || !lw.down.qs || !norms) return oom("layer weights");
+        lw.attn_norm = norms;
+        lw.ffn_norm = (const float*)((char*)norms + al256((size_t)E * 4));
+        cudaError_t e = cudaSuccess;
+        if (!e) e = cudaMemcpyAsync(norms, blob + off[0], (size_t)E * 4, cudaMemcpyDeviceToDevice, s);
+        if (!e) e = cudaMemcpyAsync((void*)lw.ffn_norm, blob + off[5], (size_t)E * 4, cudaMemcpyDeviceToDevice, s);
+        if (!e) e = repack_into(lw.qkv, blob + off[1], QD, 0, 1, s);
+        if (!e) e = repack_into(lw.qkv, blob + off[2], KVD, QD, 1, s);
+        if (!e) e = repack_into(lw.qkv, blob + off[3], KVD, QD + KVD, 1, s);
+        if (!e) e = repack_into(lw.o, blob + off[4], E, 0, 1, s);
+        if (!e) e = repack_into(lw.gu, blob + off[6], F, 0, 2, s);  // gate rows -> even
+        if (!e) e = repack_into(lw.gu, blob + off[7], F, 1, 2, s);  // up rows   -> odd
+        if (!e) e = repack_into(lw.down, blob + off[8], E, 0, 1, s);
+        if (e) return cuda_fail(e, "weight repack");
+    }
+    m->emb = make_planes(A, wt, V, E);
+    m->out = make_planes(A, wt, V, E);
+    float* onorm = (float*)A.get((size_t)E * 4);
+    if (!m->emb.qs || !m->out.qs || !onorm) return oom("embedding / output");
+    m->out_norm = onorm;
+    {
+        cudaError_t e = repack_into(m->emb, w->token_embd, V, 0, 1, s);
+        if (!e) e = repack_into(m->out, w->output, V, 0, 1, s);
+        if (!e) e = cudaMemcpyAsync(onorm, w->output_norm, (size_t)E * 4, cudaMemcpyDeviceToDevice, s);
+        if (e) return cuda_fail(e, "output repack");
+    }
+
+    // KV cache, RoPE table
+    m->kv_layer_elems = (size_t)c.n_kv_heads * c.max_ctx * D;
+    const size_t kvb = af_kv_bytes(&c) / 2;
+    m->kc = A.get(kvb);
+    m->vc = A.get(kvb);
+    m->rope = (float2*)A.get((size_t)c.max_ctx * (D / 2) * sizeof(float2));
+    if (!m->kc || !m->vc || !m->rope) return oom("KV cache");
+    const double ys = (c.native_ctx > 0 && c.max_ctx > c.native_ctx) ? (double)c.max_ctx / c.native_ctx : 1.0;
+    {
+        cudaError_t e = cudaMemsetAsync(m->kc, 0, kvb, s);
+        if (!e) e = cudaMemsetAsync(m->vc, 0, kvb, s);
+        if (!e) e = launch_rope_table(m->rope, c.max_ctx, D, (double)c.rope_base, ys, s);
+        if (e) return cuda_fail(e, "KV init");
+    }
+
+    // activations and scratch
+    const int S = m->chunk;
+    m->x = (float*)A.get((size_t)S * E * 4);
+    m->q = (float*)A.get((size_t)S * QD * 4);
+    m->attn = (float*)A.get((size_t)QD * 4);
+    m->h = (float*)A.get((size_t)F * 4);
+    m->y16 = (__half*)A.get((size_t)S * E * 2);
+    m->a16 = (__half*)A.get((size_t)S * QD * 2);
+    m->h16 = (__half*)A.get((size_t)S * F * 2);
+    m->tok = (int*)A.get((size_t)S * 4);
+    m->logits = (float*)A.get((size_t)V * 4);
+    m->st = (StepState*)A.get(sizeof(StepState));
+    size_t part = 0, cnt = 0;
+    for (const Planes* P : {&m->L[0].qkv, &m->L[0].o, &m->L[0].gu, &m->L[0].down, &m->out}) {
+        part = std::max(part, qgemv_part_elems(*P));
+        cnt = std::max(cnt, (size_t)P->N / 2);
+    }
+    m->gs.part = (float*)A.get(part * 4);
+    m->gs.cnt = (unsigned*)A.get(cnt * 4);
+    m->as.ns = attn_decode_splits(c.n_kv_heads);
+    m->as.part = (float*)A.get(attn_decode_part_elems(c.n_heads, D, m->as.ns) * 4);
+    m->as.cnt = (unsigned*)A.get((size_t)c.n_kv_heads * 4);
+    if (!m->x || !m->q || !m->attn || !m->h || !m->y16 || !m->a16 || !m->h16 || !m->tok || !m->logits || !m->st ||
+        !m->gs.part || !m->gs.cnt || !m->as.part || !m->as.cnt)
+        return oom("activations");
+    {
+        cudaError_t e = cudaMemsetAsync(m->gs.cnt, 0, cnt * 4, s);
+        if (!e) e = cudaMemsetAsync(m->as.cnt, 0, (size_t)c.n_kv_heads * 4, s);
+        if (!e) e = cudaMemsetAsync(m->st, 0, sizeof(StepState), s);
+        if (!e) e = cudaStreamSynchronize(s);
+        if (e) return cuda_fail(e, "model init");
+    }
+    *out = m;
+    return AF_OK;
+}
+
+void* af_model_stream(const af_model* m) { return m ? (void*)m->s : nullptr; }
+
+const int32_t* af_model_next_token_dev(const af_model* m) { return m ? &m->st->next_token : nullptr; }
+
+int af_model_kv_cache(const af_model* m, void** k_dev, void** v_dev) {
+    if (!m || !k_dev || !v_dev) return fail(AF_EINVAL, "null argument");
+    *k_dev = m->kc;
+    *v_dev = m->vc;
+    return AF_OK;
+}
+
+int af_reset(af_model* m) {
+    if (!m) return fail(AF_EINVAL, "null model");
+    const size_t kvb = af_kv_bytes(&m->c) / 2;
+    CK(cudaMemsetAsync(m->kc, 0, kvb, m->s));
+    CK(cudaMemsetAsync(m->vc, 0, kvb, m->s));
+    return AF_OK;
+}
+
+int af_debug_capture(af_model* m, float* hidden_dev) {
+    if (!m || !hidden_dev) return fail(AF_EINVAL, "null argument");
+    m->capture = hidden_dev;
+    return AF_OK;
+}
+
+int af_set_decode_graph(af_model* m, int enable) {
+    if (!m) return fail(AF_EINVAL, "null model");
+    m->use_graph = enable != 0;
+    return AF_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+int capture_copy(af_model* m, int slot, int n) {
+    if (!m->capture) return AF_OK;
+    const size_t bytes = (size_t)n * m->E() * 4;
+    CK(cudaMemcpyAsync(m->capture + (size_t)slot * n * m->E(), m->x, bytes, cudaMemcpyDeviceToDevice, m->s));
+    return AF_OK;
+}
+
+Epi epi_qkv(af_model* m, int l, float* qout, __half* q16, const int* pos_dev, int pos0) {
+    Epi e;
+    e.kind = EPI_QKV;
+    e.out = qout;
+    e.out16 = q16;
+    e.ld = m->QD();
+    e.qd = m->QD();
+    e.kvd = m->KVD();
+    e.head_dim = m->c.head_dim;
+    e.max_ctx = m->c.max_ctx;
+    e.kv_f16 = m->c.kv_dtype == AF_F16;
+    e.kcache = m->kl(l);
+    e.vcache = m->vl(l);
+    e.rope = m->rope;
+    e.pos_dev = pos_dev;
+    e.pos0 = pos0;
+    return e;
+}
+
+Epi epi_simple(int kind, float* out, int ld) {
+    Epi e;
+    e.kind = kind;
+    e.out = out;
+    e.ld = ld;
+    return e;
+}
+
+// Decode body after step_begin: reads token/pos from m->st.
+int decode_body(af_model* m, float* logits) {
+    const af_config& c = m->c;
+    cudaStream_t s = m->s;
+    const int* pos_dev = &m->st->pos;
+    CK(launch_embed(m->emb, &m->st->token, 1, m->x, m->E(), s));
+    int rc = capture_copy(m, 0, 1);
+    if (rc) return rc;
+    for (int l = 0; l < c.n_layers; l++) {
+        const LayerW& lw = m->L[l];
+        CK(launch_qgemv(lw.qkv, m->x, lw.attn_norm, c.rms_eps, epi_qkv(m, l, m->q, nullptr, pos_dev, 0), m->gs, s));
+        CK(launch_attn_decode(m->q, m->kl(l), m->vl(l), c.kv_dtype == AF_F16, c.n_heads, c.n_kv_heads, c.head_dim,
+                              c.max_ctx, pos_dev, 0, m->as, m->attn, s));
+        CK(launch_qgemv(lw.o, m->attn, nullptr, 0.f, epi_simple(EPI_RESID, m->x, m->E()), m->gs, s));
+        CK(launch_qgemv(lw.gu, m->x, lw.ffn_norm, c.rms_eps, epi_simple(EPI_SWIGLU, m->h, c.n_ff), m->gs, s));
+        CK(launch_qgemv(lw.down, m->h, nullptr, 0.f, epi_simple(EPI_RESID, m->x, m->E()), m->gs, s));
+        rc = capture_copy(m, l + 1, 1);
+        if (rc) return rc;
+    }
+    Epi el = epi_simple(EPI_LOGITS, logits, 0);
+    el.argmax = &m->st->argmax;
+    CK(launch_qgemv(m->out, m->x, m->out_norm, c.rms_eps, el, m->gs, s));
+    CK(launch_step_end(m->st, s));
+    return AF_OK;
+}
+
+int prefill_impl(af_model* m, const int* tok_dev, int n, int start_pos, float* logits) {
+    const af_config& c = m->c;
+    cudaStream_t s = m->s;
+    const int E = m->E(), QD = m->QD(), F = c.n_ff;
+    CK(launch_embed(m->emb, tok_dev, n, m->x, E, s));
+    int rc = capture_copy(m, 0, n);
+    if (rc) return rc;
+    for (int l = 0; l < c.n_layers; l++) {
+        const LayerW& lw = m->L[l];
+        CK(launch_rmsnorm_rows(m->x, n, E, lw.attn_norm, c.rms_eps, nullptr, m->y16, s));
+        CK(launch_qgemm(lw.qkv, m->y16, E, n, epi_qkv(m, l, m->q, nullptr, nullptr, start_pos), s));
+        CK(launch_attn_prefill(m->q, QD, m->kl(l), m->vl(l), c.kv_dtype == AF_F16, c.n_heads, c.n_kv_heads,
+                               c.head_dim, c.max_ctx, start_pos, n, nullptr, m->a16, QD, s));
+        CK(launch_qgemm(lw.o, m->a16, QD, n, epi_simple(EPI_RESID, m->x, E), s));
+        CK(launch_rmsnorm_rows(m->x, n, E, lw.ffn_norm, c.rms_eps, nullptr, m->y16, s));
+        Epi eg = epi_simple(EPI_SWIGLU, nullptr, F);
+        eg.out16 = m->h16;
+        CK(launch_qgemm(lw.gu, m->y16, E, n, eg, s));
+        CK(launch_qgemm(lw.down, m->h16, F, n, epi_simple(EPI_RESID, m->x, E), s));
+        rc = capture_copy(m, l + 1, n);
+        if (rc) return rc;
+    }
+    if (logits) {
+        CK(launch_step_begin(m->st, 0, start_pos + n - 1, s));  // resets the argmax word
+        Epi el = epi_simple(EPI_LOGITS, logits, 0);
+        el.argmax = &m->st->argmax;
+        CK(launch_qgemv(m->out, m->x + (size_t)(n - 1) * E, m->out_norm, c.rms_eps, el, m->gs, s));
+        CK(launch_step_end(m->st, s));
+    }
+    m->capture = nullptr;
+    return AF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int af_prefill_dev(af_model* m, const int32_t* tokens_dev, int32_t n, int32_t start_pos, float* logits_dev) {
+    if (!m || !tokens_dev) return fail(AF_EINVAL, "null argument");
+    if (n < 1 || n > m->chunk) return fail(AF_ERANGE, "n=%d outside [1, max_chunk=%d]", n, m->chunk);
+    if (start_pos < 0 || (int64_t)start_pos + n > m->c.max_ctx)
+        return fail(AF_ERANGE, "positions %d..%d outside the cache (max_ctx %d)", start_pos, start_pos + n - 1,
+                    m->c.max_ctx);
+    return prefill_impl(m, tokens_dev, n, start_pos, logits_dev);
+}
+
+int af_prefill(af_model* m, const int32_t* tokens_host, int32_t n, int32_t start_pos, float* logits_dev) {
+    if (!m || !tokens_host) return fail(AF_EINVAL, "null argument");
+    if (n < 1 || n > m->chunk) return fail(AF_ERANGE, "n=%d outside [1, max_chunk=%d]", n, m->chunk);
+    if (start_pos < 0 || (int64_t)start_pos + n > m->c.max_ctx)
+        return fail(AF_ERANGE, "positions %d..%d outside the cache (max_ctx %d)", start_pos, start_pos + n - 1,
+                    m->c.max_ctx);
+    for (int i = 0; i < n; i++)
+        if (tokens_host[i] < 0 || tokens_host[i] >= m->c.n_vocab)
+            return fail(AF_ERANGE, "token %d at index %d outside [0, %d)", tokens_host[i], i, m->c.n_vocab);
+    CK(cudaMemcpyAsync(m->tok, tokens_host, (size_t)n * 4, cudaMemcpyHostToDevice, m->s));
+    return prefill_impl(m, m->tok, n, start_pos, logits_dev);
+}
+
+int af_decode_step(af_model* m, int32_t token, int32_t pos, float* logits_dev, int32_t* next_token_host) {
+    if (!m) return fail(AF_EINVAL, "null model");
+    if (pos < 0 || pos >= m->c.max_ctx) return fail(AF_ERANGE, "pos %d outside [0, %d)", pos, m->c.max_ctx);
+    if (token < -1 || token >= m->c.n_vocab) return fail(AF_ERANGE, "token %d outside [-1, %d)", token, m->c.n_vocab);
+    float* logits = logits_dev ? logits_dev : m->logits;
+    CK(launch_step_begin(m->st, token, pos, m->s));
+    if (m->use_graph && !m->capture) {
+        if (!m->gexec || m->graph_logits != logits) {
+            if (m->gexec) {
+                cudaGraphExecDestroy(m->gexec);
+                m->gexec = nullptr;
+            }
+            cudaGraph_t g = nullptr;
+            CK(cudaStreamBeginCapture(m->s, cudaStreamCaptureModeThreadLocal));
+            int rc = decode_body(m, logits);
+            cudaError_t e = cudaStreamEndCapture(m->s, &g);
+            if (rc) {
+                if (g) cudaGraphDestroy(g);
+                return rc;
+            }
+            if (e != cudaSuccess) return fail(AF_ECUDA, "graph capture: %s", cudaGetErrorString(e));
+            e = cudaGraphInstantiate(&m->gexec, g, 0);
+            cudaGraphDestroy(g);
+            if (e != cudaSuccess) {
+                m->gexec = nullptr;
+                return fail(AF_ECUDA, "graph instantiate: %s", cudaGetErrorString(e));
+            }
+            m->graph_logits = logits;
+        }
+        CK(cudaGraphLaunch(m->gexec, m->s));
+    } else {
+        int rc = decode_body(m, logits);
+        m->capture = nullptr;
+        if (rc) return rc;
+    }
+    if (next_token_host) {
+        CK(cudaMemcpyAsync(next_token_host, &m->st->next_token, 4, cudaMemcpyDeviceToHost, m->s));
+        CK(cudaStreamSynchronize(m->s));
+    }
+    return AF_OK;
+}
+
+// ---------------------------------------------------------------- standalone matmuls
+
+void af_qweight_destroy(af_qweight* w) {
+    if (!w) return;
+    w->A.free_all();
+    delete w;
+}
+
+int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t K, void* stream, af_qweight** out) {
+    if (!out) return fail(AF_EINVAL, "null out");
+    *out = nullptr;
+    if (wtype != AF_Q4_0 && wtype != AF_Q8_0) return fail(AF_EINVAL, "bad wtype");
+    if (!blocks_dev) return fail(AF_EINVAL, "null blocks");
+    if (N <= 0 || K <= 0 || K % 32) return fail(AF_EINVAL, "need N > 0 and K a positive multiple of 32");
+    if (N % 2) return fail(AF_ENOTIMPL, "N must be even");
+    af_qweight* w = new (std::nothrow) af_qweight();
+    if (!w) return fail(AF_ENOMEM, "host allocation failed");
+    cudaStream_t s = (cudaStream_t)stream;
+    w->p = make_planes(w->A, wtype, N, K);
+    w->gs.part = (float*)w->A.get(qgemv_part_elems(w->p) * 4);
+    w->gs.cnt = (unsigned*)w->A.get((size_t)N / 2 * 4);
+    if (!w->p.qs || !w->gs.part || !w->gs.cnt) {
+        af_qweight_destroy(w);
+        return fail(AF_ENOMEM, "device allocation failed");
+    }
+    cudaError_t e = repack_into(w->p, blocks_dev, N, 0, 1, s);
+    if (!e) e = cudaMemsetAsync(w->gs.cnt, 0, (size_t)N / 2 * 4, s);
+    if (!e) e = cudaStreamSynchronize(s);
+    if (e) {
+        af_qweight_destroy(w);
+        return fail(AF_ECUDA, "qweight repack: %s", cudaGetErrorString(e));
+    }
+    *out = w;
+    return AF_OK;
+}
+
+int af_qgemv(const af_qweight* w, const float* x_dev, float* y_dev, void* stream) {
+    if (!w || !x_dev || !y_dev) return fail(AF_EINVAL, "null argument");
+    CK(launch_qgemv(w->p, x_dev, nullptr, 0.f, epi_simple(EPI_STORE, y_dev, w->p.N), w->gs, (cudaStream_t)stream));
+    return AF_OK;
+}
+
+int af_qgemm(const af_qweight* wc, const float* X_dev, int32_t M, float* Y_dev, void* stream) {
+    if (!wc || !X_dev || !Y_dev) return fail(AF_EINVAL, "null argument");
+    if (M < 1) return fail(AF_ERANGE, "M must be >= 1");
+    af_qweight* w = const_cast<af_qweight*>(wc);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (w->x16_rows < M) {
+        CK(cudaStreamSynchronize(s));  // the old buffer may still be in use
+        if (w->x16) {
+            cudaFree(w->x16);
+            for (auto& p : w->A.p)
+                if (p == w->x16) p = nullptr;
+        }
+        w->x16 = (__half*)w->A.get((size_t)M * w->p.K * 2);
+        w->x16_rows = w->x16 ? M : 0;
+        if (!w->x16) return fail(AF_ENOMEM, "operand buffer");
+    }
+    CK(launch_f32_to_f16(X_dev, w->x16, (int64_t)M * w->p.K, s));
+    CK(launch_qgemm(w->p, w->x16, w->p.K, M, epi_simple(EPI_STORE, Y_dev, w->p.N), s));
+    return AF_OK;
+}
+
+// ---------------------------------------------------------------- standalone attention
+
+int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev, int32_t kv_dtype, int32_t H,
+                        int32_t KVH, int32_t D, int32_t ctx, int32_t pos, float* out_dev, void* stream) {
+    if (!q_dev || !k_dev || !v_dev || !out_dev) return fail(AF_EINVAL, "null argument");
+    if (kv_dtype != AF_F32 && kv_dtype != AF_F16) return fail(AF_EINVAL, "bad kv_dtype");
+    if (H <= 0 || KVH <= 0 || D <= 0 || ctx <= 0) return fail(AF_EINVAL, "sizes must be positive");
+    if (!attn_supported(H, KVH, D)) return fail(AF_ENOTIMPL, "unsupported head_dim / group size");
+    if (pos < 0 || pos >= ctx) return fail(AF_ERANGE, "pos %d outside [0, %d)", pos, ctx);
+    cudaStream_t s = (cudaStream_t)stream;
+    AttnScratch as;
+    as.ns = attn_decode_splits(KVH);
+    const size_t pe = attn_decode_part_elems(H, D, as.ns);
+    if (cudaMalloc(&as.part, pe * 4) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(AF_ENOMEM, "scratch");
+    }
+    if (cudaMalloc(&as.cnt, (size_t)KVH * 4) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(as.part);
+        return fail(AF_ENOMEM, "scratch");
+    }
+    cudaError_t e = cudaMemsetAsync(as.cnt, 0, (size_t)KVH * 4, s);
+    if (!e) e = launch_attn_decode(q_dev, k_dev, v_dev, kv_dtype == AF_F16, H, KVH, D, ctx, nullptr, pos, as, out_dev, s);
+    cudaError_t e2 = cudaStreamSynchronize(s);
+    cudaFree(as.part);
+    cudaFree(as.cnt);
+    if (e) return fail(AF_ECUDA, "attention: %s", cudaGetErrorString(e));
+    if (e2) return fail(AF_ECUDA, "attention sync: %s", cudaGetErrorString(e2));
+    return AF_OK;
+}
+
+}  // extern "C"

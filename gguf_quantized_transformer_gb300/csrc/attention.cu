@@ -1,0 +1,405 @@
+// Causal GQA attention over the KV cache (Airframe "GPU_PIPELINE.md": scores
+// Q K^T / sqrt(head_dim), softmax over the sequence, weighted sum of V; the
+// cache holds slots 0..t; dotLLM "Attention on GPU": GQA via
+// group = n_heads / n_kv_heads, fp32 accumulation).
+//
+// Decode (one query row at position p): split-KV.  CTA (s, g) owns kv head g
+// and the slot range s*chunk..: it serves all G query heads of the group, so
+// each K/V byte is read once.  Within the CTA, pass 1 writes scores to shared
+// memory, pass 2 exponentiates against the CTA maximum and accumulates P V.
+// Each CTA stores (o, max, sum) for its range; the last CTA of a kv head to
+// finish (acq_rel counter) merges the splits with the usual max-rescaling.
+//
+// Prefill (S query rows at positions p0..p0+S-1): CTA per (query tile, kv
+// head) with 32 query vectors (QT rows x G heads); K/V tiles of 64 slots in
+// shared memory; online softmax per query vector; causal mask j <= p0 + r.
+#include <math_constants.h>
+
+#include "common.cuh"
+
+namespace af {
+
+namespace {
+
+template <typename T>
+__device__ __forceinline__ void load_vec(const T* p, float* out, int n);
+template <>
+__device__ __forceinline__ void load_vec<float>(const float* p, float* out, int n) {
+    for (int i = 0; i < n; i += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(p + i);
+        out[i] = v.x;
+        out[i + 1] = v.y;
+        out[i + 2] = v.z;
+        out[i + 3] = v.w;
+    }
+}
+template <>
+__device__ __forceinline__ void load_vec<__half>(const __half* p, float* out, int n) {
+    for (int i = 0; i < n; i += 8) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(p + i);
+        const __half2* h = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const float2 f = __half22float2(h[e]);
+            out[i + 2 * e] = f.x;
+            out[i + 2 * e + 1] = f.y;
+        }
+    }
+}
+
+constexpr int kDecThreads = 128;  // 16 position groups x 8 lanes
+
+template <int D, int G, typename KT>
+__global__ void __launch_bounds__(kDecThreads)
+    attn_decode_kernel(const float* __restrict__ q, const KT* __restrict__ kc, const KT* __restrict__ vc, int max_ctx,
+                       const int* __restrict__ pos_dev, int pos_arg, float* __restrict__ part,
+                       unsigned* __restrict__ cnt, float* __restrict__ out) {
+    constexpr int DL = D / 8;  // dims per lane
+    extern __shared__ float sc[];  // [chunk][G] scores
+    __shared__ float red_m[4][G], red_l[4][G];
+    __shared__ float red_o[4][G][D];
+    __shared__ unsigned last;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gi = tid >> 3, li = tid & 7;
+    const int g = blockIdx.y, s = blockIdx.x, ns = gridDim.x;
+    const int pos = pos_dev ? *pos_dev : pos_arg;
+    const int n = pos + 1;
+    const int chunk = (n + ns - 1) / ns;
+    const int j0 = s * chunk;
+    const int j1 = min(n, j0 + chunk);
+    const KT* K = kc + (int64_t)g * max_ctx * D;
+    const KT* V = vc + (int64_t)g * max_ctx * D;
+    const float scale = rsqrtf((float)D);
+
+    float qv[G][DL];
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        load_vec<float>(q + (int64_t)(g * G + h) * D + li * DL, qv[h], DL);
+#pragma unroll
+        for (int d = 0; d < DL; d++) qv[h][d] *= scale;
+    }
+
+    // pass 1: scores
+    for (int jb = j0; jb < j1; jb += 16) {  // uniform trip count: every lane reaches the shuffles
+        const int j = jb + gi;
+        const bool ok = j < j1;
+        float kf[DL];
+        if (ok) {
+            load_vec<KT>(K + (int64_t)j * D + li * DL, kf, DL);
+        } else {
+#pragma unroll
+            for (int d = 0; d < DL; d++) kf[d] = 0.f;
+        }
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            float a = 0.f;
+#pragma unroll
+            for (int d = 0; d < DL; d++) a = fmaf(qv[h][d], kf[d], a);
+            a += __shfl_xor_sync(0xffffffffu, a, 1);
+            a += __shfl_xor_sync(0xffffffffu, a, 2);
+            a += __shfl_xor_sync(0xffffffffu, a, 4);
+            if (ok && li == 0) sc[(j - j0) * G + h] = a;
+        }
+    }
+    __syncthreads();
+
+    // CTA maximum per head
+    float mh[G];
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        float m = -CUDART_INF_F;
+        for (int j = tid; j < j1 - j0; j += kDecThreads) m = fmaxf(m, sc[j * G + h]);
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) red_m[warp][h] = m;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < G; h++) mh[h] = fmaxf(fmaxf(red_m[0][h], red_m[1][h]), fmaxf(red_m[2][h], red_m[3][h]));
+
+    // pass 2: P V
+    float acc[G][DL], lsum[G];
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        lsum[h] = 0.f;
+#pragma unroll
+        for (int d = 0; d < DL; d++) acc[h][d] = 0.f;
+    }
+    for (int j = j0 + gi; j < j1; j += 16) {
+        float vf[DL];
+        load_vec<KT>(V + (int64_t)j * D + li * DL, vf, DL);
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            const float p = __expf(sc[(j - j0) * G + h] - mh[h]);
+            lsum[h] += p;
+#pragma unroll
+            for (int d = 0; d < DL; d++) acc[h][d] = fmaf(p, vf[d], acc[h][d]);
+        }
+    }
+    // reduce over the 4 position groups of a warp (lanes li, li+8, li+16, li+24)
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 8);
+        lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 16);
+#pragma unroll
+        for (int d = 0; d < DL; d++) {
+            acc[h][d] += __shfl_xor_sync(0xffffffffu, acc[h][d], 8);
+            acc[h][d] += __shfl_xor_sync(0xffffffffu, acc[h][d], 16);
+        }
+    }
+    __syncthreads();  // red_m reads done before reuse of shared memory below
+    if (lane < 8) {
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+#pragma unroll
+            for (int d = 0; d < DL; d++) red_o[warp][h][li * DL + d] = acc[h][d];
+            if (li == 0) red_l[warp][h] = lsum[h];
+        }
+    }
+    __syncthreads();
+    // this CTA's partial: part[((g*ns + s)*G + h)*(D+2) + {0..D-1: o, D: max, D+1: sum}]
+    float* my = part + ((int64_t)(g * ns + s) * G) * (D + 2);
+    for (int t = tid; t < G * D; t += kDecThreads) {
+        const int h = t / D, d = t % D;
+        my[h * (D + 2) + d] = red_o[0][h][d] + red_o[1][h][d] + red_o[2][h][d] + red_o[3][h][d];
+    }
+    if (tid < G) {
+        my[tid * (D + 2) + D] = mh[tid];
+        my[tid * (D + 2) + D + 1] = red_l[0][tid] + red_l[1][tid] + red_l[2][tid] + red_l[3][tid];
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned old = atomicAdd(&cnt[g], 1u);
+        last = (old == (unsigned)ns - 1u);
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    // merge the ns partials of this kv head
+    const float* pg = part + ((int64_t)g * ns * G) * (D + 2);
+    for (int t = tid; t < G * D; t += kDecThreads) {
+        const int h = t / D, d = t % D;
+        float M = -CUDART_INF_F;
+        for (int ss = 0; ss < ns; ss++) M = fmaxf(M, __ldcg(pg + ((int64_t)ss * G + h) * (D + 2) + D));
+        float num = 0.f, den = 0.f;
+        for (int ss = 0; ss < ns; ss++) {
+            const float* ps = pg + ((int64_t)ss * G + h) * (D + 2);
+            const float l = __ldcg(ps + D + 1);
+            if (l == 0.f) continue;  // empty split
+            const float w = __expf(__ldcg(ps + D) - M);
+            num = fmaf(w, __ldcg(ps + d), num);
+            den = fmaf(w, l, den);
+        }
+        out[(int64_t)(g * G + h) * D + d] = num / den;
+    }
+    if (tid == 0) cnt[g] = 0u;
+}
+
+// ---------------------------------------------------------------- prefill
+constexpr int kPreThreads = 256;  // 8 warps x 4 query vectors
+constexpr int kKT = 64;           // keys per tile
+
+template <int D, int G, typename KT>
+__global__ void __launch_bounds__(kPreThreads)
+    attn_prefill_kernel(const float* __restrict__ q, int64_t ldq, const KT* __restrict__ kc, const KT* __restrict__ vc,
+                        int max_ctx, int pos0, int S, float* __restrict__ out, __half* __restrict__ out16,
+                        int64_t ldo) {
+    constexpr int QT = 32 / G;  // query rows per CTA
+    constexpr int DP = D + 1;   // padded K row
+    extern __shared__ float smem[];
+    float* Qs = smem;                 // [32][D]   query vector v = rr*G + h
+    float* Ks = Qs + 32 * D;          // [kKT][DP]
+    float* Vs = Ks + kKT * DP;        // [kKT][D]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = blockIdx.y, r0 = blockIdx.x * QT;
+    const KT* K = kc + (int64_t)g * max_ctx * D;
+    const KT* V = vc + (int64_t)g * max_ctx * D;
+    const float scale = rsqrtf((float)D);
+
+    for (int t = tid; t < 32 * D; t += kPreThreads) {
+        const int v = t / D, d = t % D, rr = v / G, h = v % G;
+        const int r = min(r0 + rr, S - 1);
+        Qs[t] = q[(int64_t)r * ldq + (g * G + h) * D + d] * scale;
+    }
+    constexpr int DD = D / 32;  // dims per lane in the accumulator
+    float acc[4][DD], mrow[4], lrow[4];
+#pragma unroll
+    for (int a = 0; a < 4; a++) {
+        mrow[a] = -CUDART_INF_F;
+        lrow[a] = 0.f;
+#pragma unroll
+        for (int d = 0; d < DD; d++) acc[a][d] = 0.f;
+    }
+    const int rmax = min(r0 + QT, S) - 1;
+    const int nkeys = pos0 + rmax + 1;
+    for (int kt = 0; kt < nkeys; kt += kKT) {
+        __syncthreads();
+        for (int t = tid; t < kKT * D / 4; t += kPreThreads) {
+            const int j = t / (D / 4), d4 = (t % (D / 4)) * 4;
+            float kf[4], vf[4];
+            if (kt + j < nkeys) {
+                if (sizeof(KT) == 4) {
+                    load_vec<float>(reinterpret_cast<const float*>(K) + (int64_t)(kt + j) * D + d4, kf, 4);
+                    load_vec<float>(reinterpret_cast<const float*>(V) + (int64_t)(kt + j) * D + d4, vf, 4);
+                } else {
+                    const __half* kh = reinterpret_cast<const __half*>(K) + (int64_t)(kt + j) * D + d4;
+                    const __half* vh = reinterpret_cast<const __half*>(V) + (int64_t)(kt + j) * D + d4;
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        kf[e] = __half2float(kh[e]);
+                        vf[e] = __half2float(vh[e]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; e++) kf[e] = vf[e] = 0.f;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                Ks[j * DP + d4 + e] = kf[e];
+                Vs[j * D + d4 + e] = vf[e];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int a = 0; a < 4; a++) {
+            const int v = warp * 4 + a, rr = v / G;
+            const int r = r0 + rr;
+            if (r >= S) continue;  // warp-uniform
+            const int lim = pos0 + r;  // causal: keys j <= pos0 + r
+            const float* qv = Qs + v * D;
+            float s0 = 0.f, s1 = 0.f;
+            const float* k0 = Ks + lane * DP;
+            const float* k1 = Ks + (lane + 32) * DP;
+#pragma unroll 8
+            for (int d = 0; d < D; d++) {
+                const float qd = qv[d];
+                s0 = fmaf(qd, k0[d], s0);
+                s1 = fmaf(qd, k1[d], s1);
+            }
+            if (kt + lane > lim) s0 = -CUDART_INF_F;
+            if (kt + lane + 32 > lim) s1 = -CUDART_INF_F;
+            float mt = fmaxf(s0, s1);
+            for (int o = 16; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+            const float mnew = fmaxf(mrow[a], mt);
+            if (mnew == -CUDART_INF_F) continue;  // whole tile masked (cannot happen for kt <= lim)
+            const float alpha = __expf(mrow[a] - mnew);
+            const float p0 = __expf(s0 - mnew), p1 = __expf(s1 - mnew);
+            float ps = p0 + p1;
+            for (int o = 16; o; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+            lrow[a] = lrow[a] * alpha + ps;
+            mrow[a] = mnew;
+#pragma unroll
+            for (int d = 0; d < DD; d++) acc[a][d] *= alpha;
+            for (int j = 0; j < 32; j++) {
+                const float pj0 = __shfl_sync(0xffffffffu, p0, j);
+                const float pj1 = __shfl_sync(0xffffffffu, p1, j);
+#pragma unroll
+                for (int d = 0; d < DD; d++) {
+                    acc[a][d] = fmaf(pj0, Vs[j * D + lane + 32 * d], acc[a][d]);
+                    acc[a][d] = fmaf(pj1, Vs[(j + 32) * D + lane + 32 * d], acc[a][d]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; a++) {
+        const int v = warp * 4 + a, rr = v / G, h = v % G;
+        const int r = r0 + rr;
+        if (r >= S) continue;
+        const float inv = 1.f / lrow[a];
+#pragma unroll
+        for (int d = 0; d < DD; d++) {
+            const float o = acc[a][d] * inv;
+            const int64_t idx = (int64_t)r * ldo + (g * G + h) * D + lane + 32 * d;
+            if (out) out[idx] = o;
+            if (out16) out16[idx] = __float2half_rn(o);
+        }
+    }
+}
+
+template <int D, int G>
+cudaError_t dispatch_decode(const float* q, const void* kc, const void* vc, int kv_f16, int max_ctx,
+                            const int* pos_dev, int pos, const AttnScratch& scr, float* out, int KVH, cudaStream_t s) {
+    const int ns = scr.ns;
+    const int cap = (max_ctx + ns - 1) / ns;
+    const size_t smem = (size_t)cap * G * sizeof(float);
+    dim3 grid(ns, KVH);
+    if (kv_f16) {
+        auto k = attn_decode_kernel<D, G, __half>;
+        if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, kDecThreads, smem, s>>>(q, (const __half*)kc, (const __half*)vc, max_ctx, pos_dev, pos, scr.part,
+                                          scr.cnt, out);
+    } else {
+        auto k = attn_decode_kernel<D, G, float>;
+        if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, kDecThreads, smem, s>>>(q, (const float*)kc, (const float*)vc, max_ctx, pos_dev, pos, scr.part,
+                                          scr.cnt, out);
+    }
+    return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t dispatch_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int KVH,
+                             int max_ctx, int pos0, int S, float* out, __half* out16, int64_t ldo, cudaStream_t s) {
+    constexpr int QT = 32 / G;
+    const size_t smem = sizeof(float) * (32 * D + kKT * (D + 1) + kKT * D);
+    dim3 grid((S + QT - 1) / QT, KVH);
+    if (kv_f16) {
+        auto k = attn_prefill_kernel<D, G, __half>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, kPreThreads, smem, s>>>(q, ldq, (const __half*)kc, (const __half*)vc, max_ctx, pos0, S, out, out16,
+                                          ldo);
+    } else {
+        auto k = attn_prefill_kernel<D, G, float>;
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        k<<<grid, kPreThreads, smem, s>>>(q, ldq, (const float*)kc, (const float*)vc, max_ctx, pos0, S, out, out16,
+                                          ldo);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_supported(int H, int KVH, int D) {
+    if (KVH <= 0 || H % KVH) return false;
+    const int G = H / KVH;
+    return (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
+int attn_decode_splits(int n_kv_heads) {
+    int ns = (2 * num_sms() + n_kv_heads - 1) / n_kv_heads;
+    return ns < 1 ? 1 : ns;
+}
+
+size_t attn_decode_part_elems(int n_heads, int head_dim, int ns) { return (size_t)ns * n_heads * (head_dim + 2); }
+
+#define AF_ATTN_DISPATCH(FN, ...)                                          \
+    switch (D * 100 + G) {                                                 \
+        case 6401: return FN<64, 1>(__VA_ARGS__);                          \
+        case 6402: return FN<64, 2>(__VA_ARGS__);                          \
+        case 6404: return FN<64, 4>(__VA_ARGS__);                          \
+        case 6408: return FN<64, 8>(__VA_ARGS__);                          \
+        case 12801: return FN<128, 1>(__VA_ARGS__);                        \
+        case 12802: return FN<128, 2>(__VA_ARGS__);                        \
+        case 12804: return FN<128, 4>(__VA_ARGS__);                        \
+        case 12808: return FN<128, 8>(__VA_ARGS__);                        \
+        default: return cudaErrorInvalidValue;                             \
+    }
+
+cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, int kv_f16, int H, int KVH, int D,
+                               int max_ctx, const int* pos_dev, int pos, const AttnScratch& scr, float* out,
+                               cudaStream_t s) {
+    const int G = H / KVH;
+    AF_ATTN_DISPATCH(dispatch_decode, q, kc, vc, kv_f16, max_ctx, pos_dev, pos, scr, out, KVH, s)
+}
+
+cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int H,
+                                int KVH, int D, int max_ctx, int pos0, int S, float* out, __half* out16,
+                                int64_t ldo, cudaStream_t s) {
+    const int G = H / KVH;
+    AF_ATTN_DISPATCH(dispatch_prefill, q, ldq, kc, vc, kv_f16, KVH, max_ctx, pos0, S, out, out16, ldo, s)
+}
+
+}  // namespace af

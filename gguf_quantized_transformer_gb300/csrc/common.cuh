@@ -1,0 +1,182 @@
+// Shared device/host definitions of the CUDA library (not part of the C ABI).
+#pragma once
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/af.h"
+
+namespace af {
+
+// ---------------------------------------------------------------------------
+// Repacked weight layout ("planes").
+//
+// A GGUF [N, K] block matrix is split into two 16-byte aligned planes:
+//   qs : N rows x (Kp/32) blocks x QB bytes   (QB = 16 for Q4_0, 32 for Q8_0)
+//   sc : N rows x (Kp/32) fp16 scales
+// Kp = K rounded up to one GEMV chunk (1024 weights for Q4_0, 512 for Q8_0);
+// blocks past K hold zero quants and a zero scale, so they contribute 0.
+// Q4_0 quant bytes keep GGUF's nibble order (byte j: element j low, j+16 high).
+// ---------------------------------------------------------------------------
+struct Planes {
+    const uint8_t* qs = nullptr;
+    const __half* sc = nullptr;
+    int N = 0, K = 0, Kp = 0, wtype = 0;
+    __host__ __device__ int qb() const { return wtype == AF_Q8_0 ? 32 : 16; }
+    __host__ __device__ int64_t qs_pitch() const { return (int64_t)(Kp / 32) * qb(); }  // bytes per row
+    __host__ __device__ int sc_pitch() const { return Kp / 32; }                          // halves per row
+};
+
+inline int chunk_weights(int wtype) { return wtype == AF_Q8_0 ? 512 : 1024; }
+inline int padded_k(int wtype, int K) { int c = chunk_weights(wtype); return (K + c - 1) / c * c; }
+inline size_t planes_bytes(int wtype, int N, int K, size_t* qs_bytes) {
+    int Kp = padded_k(wtype, K);
+    size_t q = (size_t)N * (Kp / 32) * (wtype == AF_Q8_0 ? 32 : 16);
+    q = (q + 255) & ~(size_t)255;
+    if (qs_bytes) *qs_bytes = q;
+    return q + (((size_t)N * (Kp / 32) * 2 + 255) & ~(size_t)255);
+}
+
+// ---------------------------------------------------------------------------
+// Fused epilogues, shared by the decode GEMV and the prefill GEMM.  Each is
+// applied to an adjacent column pair (n, n+1) of one output row m.
+// ---------------------------------------------------------------------------
+enum EpiKind { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3, EPI_LOGITS = 4 };
+
+struct Epi {
+    int kind = EPI_STORE;
+    float* out = nullptr;  // STORE: Y [M][ld]; RESID: x [M][ld]; QKV: q [M][ld]; SWIGLU: h [M][ld]; LOGITS: [N]
+    int ld = 0;
+    __half* out16 = nullptr;  // optional fp16 copy of SWIGLU/QKV-q output (GEMM operand), same ld
+    // EPI_QKV: columns [0, qd) are q, [qd, qd+kvd) k, [qd+kvd, qd+2kvd) v
+    int qd = 0, kvd = 0, head_dim = 0, max_ctx = 0, kv_f16 = 0;
+    void* kcache = nullptr;  // this layer's [KVH][max_ctx][D]
+    void* vcache = nullptr;
+    const float2* rope = nullptr;  // [max_ctx][D/2] (cos, sin) of theta(t, i)
+    const int* pos_dev = nullptr;  // if set: position of row m is *pos_dev + m
+    int pos0 = 0;                  // else: pos0 + m
+    unsigned long long* argmax = nullptr;  // EPI_LOGITS: packed (value, ~index) maximum
+};
+
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+    unsigned u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // order-preserving map of floats to unsigned
+    return ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)idx);
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, float v1) {
+    switch (e.kind) {
+        case EPI_STORE: {
+            e.out[(int64_t)m * e.ld + n] = v0;
+            e.out[(int64_t)m * e.ld + n + 1] = v1;
+        } break;
+        case EPI_RESID: {
+            float* p = e.out + (int64_t)m * e.ld + n;
+            p[0] += v0;
+            p[1] += v1;
+        } break;
+        case EPI_SWIGLU: {  // columns (2r, 2r+1) hold (gate_r, up_r)
+            float h = silu_f(v0) * v1;
+            if (e.out) e.out[(int64_t)m * e.ld + (n >> 1)] = h;
+            if (e.out16) e.out16[(int64_t)m * e.ld + (n >> 1)] = __float2half_rn(h);
+        } break;
+        case EPI_LOGITS: {
+            e.out[n] = v0;
+            e.out[n + 1] = v1;
+            unsigned long long k = argmax_key(v0, n), k1 = argmax_key(v1, n + 1);
+            atomicMax(e.argmax, k > k1 ? k : k1);
+        } break;
+        case EPI_QKV: {
+            const int pos = (e.pos_dev ? *e.pos_dev : e.pos0) + m;
+            const int D = e.head_dim;
+            if (n < e.qd + e.kvd) {  // q or k: rotate the pair (2i, 2i+1) by theta(pos, i)
+                const int d = (n < e.qd ? n : n - e.qd) % D;
+                const float2 cs = e.rope[(int64_t)pos * (D / 2) + (d >> 1)];
+                const float r0 = v0 * cs.x - v1 * cs.y, r1 = v0 * cs.y + v1 * cs.x;
+                v0 = r0;
+                v1 = r1;
+            }
+            if (n < e.qd) {
+                if (e.out) {
+                    e.out[(int64_t)m * e.ld + n] = v0;
+                    e.out[(int64_t)m * e.ld + n + 1] = v1;
+                }
+                if (e.out16) {
+                    e.out16[(int64_t)m * e.ld + n] = __float2half_rn(v0);
+                    e.out16[(int64_t)m * e.ld + n + 1] = __float2half_rn(v1);
+                }
+            } else {
+                const bool isk = n < e.qd + e.kvd;
+                const int c = isk ? n - e.qd : n - e.qd - e.kvd;
+                const int g = c / D, d = c % D;
+                const int64_t idx = ((int64_t)g * e.max_ctx + pos) * D + d;
+                void* base = isk ? e.kcache : e.vcache;
+                if (e.kv_f16) {
+                    *reinterpret_cast<__half2*>((__half*)base + idx) = __floats2half2_rn(v0, v1);
+                } else {
+                    *reinterpret_cast<float2*>((float*)base + idx) = make_float2(v0, v1);
+                }
+            }
+        } break;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launchers (defined in the .cu files).
+// ---------------------------------------------------------------------------
+struct GemvScratch {
+    float* part = nullptr;     // [NC][N] per-chunk partial sums
+    unsigned* cnt = nullptr;   // [N/2] arrival counters, zero between launches
+    size_t part_elems = 0, cnt_elems = 0;
+};
+
+int num_sms();
+
+cudaError_t launch_repack(const uint8_t* src, int wtype, int N, int K, uint8_t* qs, __half* sc, int Kp,
+                          int dst_row0, int dst_row_step, cudaStream_t s);
+cudaError_t launch_rope_table(float2* tab, int max_ctx, int head_dim, double base, double yarn_scale,
+                              cudaStream_t s);
+cudaError_t launch_embed(const Planes& emb, const int* tok_dev, int n, float* x, int64_t ldx, cudaStream_t s);
+cudaError_t launch_rmsnorm_rows(const float* x, int n, int E, const float* w, float eps, float* y, __half* y16,
+                                cudaStream_t s);
+cudaError_t launch_f32_to_f16(const float* x, __half* y, int64_t n, cudaStream_t s);
+
+// y-part of the decode path: one matrix-vector product with optional RMSNorm
+// prologue (norm_w != nullptr) and a fused epilogue.
+cudaError_t launch_qgemv(const Planes& W, const float* x, const float* norm_w, float eps, const Epi& epi,
+                         const GemvScratch& scr, cudaStream_t s);
+size_t qgemv_part_elems(const Planes& W);
+
+// Prefill GEMM: Y = X W^T for M rows with a fused epilogue.  X is fp16 [M][ldx].
+cudaError_t launch_qgemm(const Planes& W, const __half* X16, int64_t ldx, int M, const Epi& epi, cudaStream_t s);
+
+// Attention
+struct AttnScratch {
+    float* part = nullptr;    // [KVH][NS][G][D+2]
+    unsigned* cnt = nullptr;  // [KVH]
+    int ns = 0;
+};
+int attn_decode_splits(int n_kv_heads);
+size_t attn_decode_part_elems(int n_heads, int head_dim, int ns);
+cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, int kv_f16, int H, int KVH, int D,
+                               int max_ctx, const int* pos_dev, int pos, const AttnScratch& scr, float* out,
+                               cudaStream_t s);
+cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int H,
+                                int KVH, int D, int max_ctx, int pos0, int S, float* out, __half* out16,
+                                int64_t ldo, cudaStream_t s);
+bool attn_supported(int H, int KVH, int D);
+
+// Decode-step bookkeeping
+struct StepState {
+    int token;  // token of this step
+    int pos;    // position of this step
+    unsigned long long argmax;
+    int next_token;
+    int pad;
+};
+cudaError_t launch_step_begin(StepState* st, int token, int pos, cudaStream_t s);
+cudaError_t launch_step_end(StepState* st, cudaStream_t s);
+
+}  // namespace af

@@ -1,0 +1,196 @@
+/*
+ * af.h — C ABI of the GB300 (sm_103a) forward pass of a GGUF-quantized
+ * Llama-style decoder.
+ *
+ * What it computes (page title, section):
+ *  - Airframe "GPU_PIPELINE.md" (Shimmy docs), per-layer operation diagram:
+ *    RMS norm -> Q/K/V projections with inline dequantization -> RoPE with
+ *    theta(t, i) = (t / yarn_scale) / base^(2i / head_dim) and
+ *    yarn_scale = max_ctx / native_ctx when max_ctx > native_ctx -> K, V written
+ *    to the KV cache at position t -> softmax(Q K^T / sqrt(head_dim)) V ->
+ *    O projection + residual -> RMS norm -> gate, up -> gate*sigmoid(gate)*up
+ *    -> down + residual.  "Prefill": prompts run in chunks of up to 512 tokens
+ *    that fill KV slots start_pos..start_pos+n-1; only the last chunk's logits
+ *    are used.  "Decode": one token at position t attends to slots 0..t.
+ *    "Output head": LM head on the last position.  "KV cache": layout
+ *    [n_layers][n_kv_heads][max_ctx][head_dim], K and V separate.
+ *  - "Shimmy v2.0 Architecture", "Quantization": GGUF Q4_0 and Q8_0
+ *    32-element blocks; "Extended Context (YaRN)": the theta scale applies to
+ *    all positions.
+ *  - "GPU Inference — dotLLM", "Forward Pass" (final RmsNorm on the last token,
+ *    LM head, one host sync per step) and "Attention on GPU" (causal, GQA with
+ *    group = n_heads / n_kv_heads).
+ *
+ * Conventions.
+ *  - Every call returns an af_status.  Arguments are validated on the host
+ *    before anything is launched; a call that fails validation changes nothing.
+ *    af_last_error() returns a thread-local message for the last failure.
+ *  - "_dev" pointers are device pointers on the current CUDA device; "_host"
+ *    pointers are ordinary host memory.  `stream` is a cudaStream_t (NULL =
+ *    legacy default stream).  Unless stated otherwise a call only enqueues
+ *    work on the model's (or the given) stream and returns.
+ *  - The caller owns every pointer it passes.  af_model_create and
+ *    af_qweight_create copy (repack) the weights into memory they own, so the
+ *    caller may free its blobs once the call has returned and the stream has
+ *    been synchronised.
+ *  - Weights: GGUF blocks, little-endian.
+ *      Q8_0 (34 B): fp16 d, int8 q[32];             w_j = d * q_j
+ *      Q4_0 (18 B): fp16 d, uint8 qs[16];            w_j = d * (n_j - 8),
+ *                   n_j = qs[j] & 15 (j < 16), qs[j - 16] >> 4 (j >= 16)
+ *    A matrix [N, K] is N rows of K/32 blocks each (K % 32 == 0).
+ */
+#ifndef AF_H
+#define AF_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum af_status {
+    AF_OK = 0,
+    AF_EINVAL = 1,   /* bad argument: null pointer, unsupported shape or type */
+    AF_ERANGE = 2,   /* position / token id / size out of range */
+    AF_ENOMEM = 3,   /* device or host allocation failed (nothing leaked) */
+    AF_ECUDA = 4,    /* a CUDA runtime call failed; see af_last_error() */
+    AF_ETIMEOUT = 5, /* a bounded device-side wait gave up */
+    AF_ENOTIMPL = 6  /* valid request this build does not implement */
+} af_status;
+
+typedef enum af_wtype { AF_Q4_0 = 2, AF_Q8_0 = 8 } af_wtype; /* own ids, not GGUF's */
+typedef enum af_dtype { AF_F32 = 0, AF_F16 = 1 } af_dtype;
+
+typedef struct af_config {
+    int32_t n_layers, n_embd, n_heads, n_kv_heads, head_dim, n_ff, n_vocab;
+    int32_t wtype;      /* af_wtype of every matrix and of token_embd */
+    int32_t kv_dtype;   /* af_dtype of the KV cache */
+    int32_t max_ctx;    /* KV slots */
+    int32_t native_ctx; /* yarn_scale = max_ctx / native_ctx if max_ctx > native_ctx, else 1 */
+    int32_t max_chunk;  /* largest n accepted by af_prefill (0 = 512) */
+    float rms_eps;      /* RMSNorm epsilon */
+    float rope_base;    /* RoPE base */
+} af_config;
+
+/*
+ * Layer blob (Airframe "GPU_PIPELINE.md", bindless layer buffer): one device
+ * buffer per layer holding, in this order, each section at a 256-byte aligned
+ * offset (see af_layer_offsets):
+ *   attn_norm f32[E] | attn_q [H*D, E] | attn_k [KVH*D, E] | attn_v [KVH*D, E] |
+ *   attn_o [E, H*D] | ffn_norm f32[E] | ffn_gate [F, E] | ffn_up [F, E] | ffn_down [E, F]
+ * Matrices are [out, in] in GGUF blocks along `in`.
+ */
+typedef struct af_weights {
+    const void* const* layer_blob; /* host array of n_layers device pointers */
+    const void* token_embd;        /* device, [n_vocab, n_embd] blocks */
+    const float* output_norm;      /* device, f32 [n_embd] */
+    const void* output;            /* device, [n_vocab, n_embd] blocks (LM head, not tied) */
+} af_weights;
+
+typedef struct af_model af_model;
+typedef struct af_qweight af_qweight;
+
+/* Section offsets of a layer blob: off[0..8] in the order above, off[9] = blob bytes. */
+int af_layer_offsets(const af_config* cfg, uint64_t off[10]);
+
+/* KV cache bytes, n_layers * n_kv_heads * max_ctx * head_dim * elem * 2
+ * (Airframe "GPU_PIPELINE.md", "KV cache" size formula). 0 on a bad config. */
+uint64_t af_kv_bytes(const af_config* cfg);
+
+/*
+ * Create a model on the current device.  Repacks every matrix into the
+ * model's own layout, allocates the KV cache (zeroed) and the step scratch,
+ * and builds the RoPE table.  Synchronises `stream` before returning.  With
+ * stream == NULL the model creates (and later destroys) a blocking stream of
+ * its own, which is ordered with the legacy default stream.
+ * Supported: head_dim in {64, 128}, n_heads % n_kv_heads == 0 with
+ * n_heads / n_kv_heads in {1, 2, 4, 8}, n_embd, n_ff, n_heads*head_dim
+ * multiples of 64, even n_vocab.  Errors: AF_EINVAL, AF_ENOMEM, AF_ECUDA,
+ * AF_ENOTIMPL (valid but unsupported shape).  *out is NULL on failure.
+ */
+int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_model** out);
+
+/*
+ * Prefill n tokens (1 <= n <= max_chunk) at absolute positions
+ * start_pos..start_pos+n-1 (start_pos + n <= max_ctx).  Writes those KV slots;
+ * row r attends to slots 0..start_pos+r.  The caller runs longer prompts as
+ * consecutive chunks with increasing start_pos.  If logits_dev is not NULL it
+ * receives the n_vocab fp32 logits of the last row.  tokens_host is copied
+ * before the call returns.  Errors: AF_EINVAL, AF_ERANGE (token id outside
+ * [0, n_vocab) or positions past max_ctx), AF_ECUDA.
+ */
+int af_prefill(af_model* m, const int32_t* tokens_host, int32_t n, int32_t start_pos, float* logits_dev);
+
+/* As af_prefill with the token ids already in device memory.  They are not
+ * validated on the host; an id outside [0, n_vocab) reads embedding row 0. */
+int af_prefill_dev(af_model* m, const int32_t* tokens_dev, int32_t n, int32_t start_pos, float* logits_dev);
+
+/*
+ * One decode step: the token at position pos (0 <= pos < max_ctx) attends to
+ * slots 0..pos.  token = -1 feeds the previous step's greedy token (from the
+ * device, no host round trip).  logits_dev (nullable) receives the fp32
+ * logits.  If next_token_host is not NULL the call synchronises the model's
+ * stream once and stores the greedy token there (argmax, lowest index on
+ * ties); otherwise it only enqueues.
+ */
+int af_decode_step(af_model* m, int32_t token, int32_t pos, float* logits_dev, int32_t* next_token_host);
+
+/* Greedy token of the last af_decode_step / af_prefill with logits (device int32, valid after the stream). */
+const int32_t* af_model_next_token_dev(const af_model* m);
+
+/* Device pointers of the model's KV cache: K and V each [n_layers][n_kv_heads][max_ctx][head_dim]
+ * in kv_dtype (Airframe "GPU_PIPELINE.md", "KV cache" layout).  Owned by the model. */
+int af_model_kv_cache(const af_model* m, void** k_dev, void** v_dev);
+
+/* Zero the KV cache (the service is stateless between requests). */
+int af_reset(af_model* m);
+
+/* Model's stream (as given to af_model_create). */
+void* af_model_stream(const af_model* m);
+
+/* Capture the residual stream after the embedding and after every layer of the
+ * next af_prefill / af_decode_step into hidden_dev [n_layers+1][n][n_embd] fp32
+ * (n = that call's token count).  One-shot; test instrumentation. */
+int af_debug_capture(af_model* m, float* hidden_dev);
+
+/* Use (1) or stop using (0) a CUDA graph for af_decode_step (default 1). */
+int af_set_decode_graph(af_model* m, int enable);
+
+void af_model_destroy(af_model* m);
+
+/*
+ * Standalone quantized matmuls (north-star "af_qgemv / af_qgemm").
+ * af_qweight_create repacks a [N, K] block matrix (N even, K % 64 == 0) into
+ * its own device memory (and scratch for the GEMV); synchronises `stream`.
+ *   af_qgemv: y[i]    = sum_j W[i][j] x[j]        x_dev fp32 [K], y_dev fp32 [N]
+ *   af_qgemm: Y[m][i] = sum_j X[m][j] W[i][j]     X_dev fp32 [M, K] row-major,
+ *                                                 Y_dev fp32 [M, N], M >= 1
+ * Calls that share one af_qweight must be ordered on one stream (they share
+ * its scratch).  af_qgemm converts X to fp16 for the tensor cores and
+ * accumulates in fp32.
+ */
+int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t K, void* stream, af_qweight** out);
+int af_qgemv(const af_qweight* w, const float* x_dev, float* y_dev, void* stream);
+int af_qgemm(const af_qweight* w, const float* X_dev, int32_t M, float* Y_dev, void* stream);
+void af_qweight_destroy(af_qweight* w);
+
+/*
+ * Standalone causal GQA attention for one query row at position pos over a
+ * caller's cache (Airframe per-layer ops: softmax(q K^T / sqrt(D)) V over
+ * slots 0..pos; dotLLM "Attention on GPU": GQA group = H / KVH).
+ *   q_dev   fp32 [H*D] (already rotated)
+ *   k_dev, v_dev  [KVH][ctx][D] in kv_dtype
+ *   out_dev fp32 [H*D]
+ * Scratch (split partials) is allocated per call and freed after the stream
+ * completes (the call synchronises `stream`).
+ */
+int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev, int32_t kv_dtype, int32_t n_heads,
+                        int32_t n_kv_heads, int32_t head_dim, int32_t ctx, int32_t pos, float* out_dev, void* stream);
+
+/* Thread-local message for the last failed call on this thread ("" if none). */
+const char* af_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,90 @@
+"""The C-ABI library loads and exports every symbol include/af.h declares;
+host-only entry points agree with the oracle; validation errors come back as
+status codes before anything touches a GPU.  No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _af():
+    import gguf_quantized_transformer_gb300 as af
+    af.build()
+    return af
+
+
+def declared_symbols():
+    hdr = open(os.path.join(ROOT, "include", "af.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    return sorted(set(re.findall(r"\b(af_[a-z_0-9]+)\s*\(", hdr)))
+
+
+def test_every_declared_symbol_is_exported():
+    af = _af()
+    L = af.lib()
+    syms = declared_symbols()
+    assert "af_model_create" in syms and "af_qgemv" in syms and "af_qgemm" in syms
+    assert "af_prefill" in syms and "af_decode_step" in syms
+    for s in syms:
+        assert hasattr(L, s), s
+
+
+def test_python_binding_has_same_names():
+    af = _af()
+    for s in declared_symbols():
+        assert hasattr(af, s), s
+
+
+@pytest.mark.parametrize("idx", range(5))
+def test_layer_offsets_and_kv_bytes_match_oracle(idx):
+    af = _af()
+    cfg = synth.CONFIGS[idx]
+    c = af.make_config(cfg)
+    assert af.af_layer_offsets(c) == oracle.layer_offsets(cfg) == synth.layer_offsets(cfg)
+    assert af.af_kv_bytes(c) == oracle.kv_bytes(cfg)
+
+
+def test_tinyllama_kv_bytes_worked_example():
+    af = _af()
+    assert af.af_kv_bytes(af.make_config(synth.CONFIGS[1])) == 92274688
+
+
+def test_validation_errors_without_gpu():
+    af = _af()
+    L = af.lib()
+    out = ctypes.c_void_p()
+    assert L.af_model_create(None, None, None, ctypes.byref(out)) == af.AF_EINVAL
+    c = af.make_config(synth.CONFIGS[0])
+    c.wtype = 99
+    assert L.af_model_create(ctypes.byref(c), None, None, ctypes.byref(out)) == af.AF_EINVAL
+    assert "wtype" in af.af_last_error()
+    c = af.make_config(synth.CONFIGS[0])
+    c.n_kv_heads = 3
+    assert L.af_model_create(ctypes.byref(c), None, None, ctypes.byref(out)) == af.AF_EINVAL
+    c = af.make_config(synth.CONFIGS[0])
+    c.head_dim = 96  # valid but not implemented
+    c.n_heads = 8
+    w = af.af_weights()
+    assert L.af_model_create(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(out)) == af.AF_ENOTIMPL
+    assert out.value is None
+    assert L.af_qweight_create(af.AF_Q8_0, None, 4, 32, None, ctypes.byref(out)) == af.AF_EINVAL
+    assert L.af_qweight_create(af.AF_Q8_0, 1, 4, 48, None, ctypes.byref(out)) == af.AF_EINVAL
+    assert L.af_prefill(None, None, 1, 0, None) == af.AF_EINVAL
+    assert L.af_decode_step(None, 0, 0, None, None) == af.AF_EINVAL
+    assert L.af_attention_decode(None, None, None, 0, 8, 4, 64, 16, 0, None, None) == af.AF_EINVAL
+    assert af.af_kv_bytes(af.af_config()) == 0
+
+
+def test_product_path_has_no_cpu_fallback():
+    # the package must not import the oracle or any CPU implementation
+    pkg = os.path.join(ROOT, "gguf_quantized_transformer_gb300")
+    for f in os.listdir(pkg):
+        if f.endswith(".py"):
+            src = open(os.path.join(pkg, f)).read()
+            assert "import oracle" not in src and "from oracle" not in src, f
