@@ -1,0 +1,402 @@
+#!/usr/bin/env python3
+"""Throughput of the GGUF-quantized Llama-style decoder forward pass on GB300.
+
+One step = the whole workload of one synthetic config: prefill of the prompt in
+512-token chunks (logits of the last chunk only), then greedy decode steps fed
+from the device argmax.  Default: the Llama-3-8B-shaped Q4_0 model with a
+4096-token prompt (8 chunks) and 256 decode steps over an fp16 KV cache.
+
+Headline `value`: decode tokens/s (aggregate over ranks).  Also reported:
+prefill tokens/s, decode HBM GB/s against the measured copy bandwidth
+(algorithmic bytes = quantized weights + LM head + embedding row + norms +
+K/V read for slots 0..pos, per token), the prefill GEMM rate, the oracle on
+the host cores (cpu_baseline) and an end-to-end run through the host API.
+
+Multi-GPU: the path does not shard at batch 1; N ranks run N independent
+replicas (no collective on the data path), `scaling` = "weak".
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    try:
+        p = json.load(open(PEAKS_FILE))
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured", p
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback", {}
+
+
+def decode_bytes_per_token(cfg, pos):
+    """Algorithmic HBM bytes of one decode step at position pos."""
+    bpe = 34 / 32 if cfg.wtype == "q8_0" else 18 / 32
+    E, QD, KVD, F, V, L = (cfg.n_embd, cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim, cfg.n_ff,
+                           cfg.n_vocab, cfg.n_layers)
+    layer_w = (E * (QD + 2 * KVD) + QD * E + 2 * F * E + F * E) * bpe + 2 * E * 4
+    head = V * E * bpe + E * 4 + E * bpe  # LM head + final norm + one embedding row
+    kvb = 2 if cfg.kv_dtype == "f16" else 4
+    kv = 2 * L * KVD * (pos + 1) * kvb
+    return L * layer_w + head + kv
+
+
+def prefill_flops(cfg, n_tokens, chunk):
+    """Algorithmic flops of prefilling n_tokens from position 0 (GEMMs + causal attention + one LM head)."""
+    E, QD, KVD, F, V, L = (cfg.n_embd, cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim, cfg.n_ff,
+                           cfg.n_vocab, cfg.n_layers)
+    params = E * (QD + 2 * KVD) + QD * E + 3 * F * E
+    gemm = 2.0 * L * params * n_tokens
+    attn = 4.0 * cfg.n_heads * cfg.head_dim * L * (n_tokens * (n_tokens + 1) / 2)
+    return gemm + attn + 2.0 * V * E, gemm
+
+
+def gemm_flops(cfg, n_tokens):
+    E, QD, KVD, F, L = (cfg.n_embd, cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim, cfg.n_ff,
+                        cfg.n_layers)
+    return 2.0 * L * (E * (QD + 2 * KVD) + QD * E + 3 * F * E) * n_tokens
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.p = None
+        self.path = None
+
+    def start(self):
+        out_dir = os.path.join(ROOT, "gpurun_out")
+        os.makedirs(out_dir, exist_ok=True)
+        self.path = os.path.join(out_dir, f"clocks_bench_{os.getpid()}.csv")
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if _cuda_ok() else "gloo")
+    return world, rank, local
+
+
+def _cuda_ok():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if _cuda_ok() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- oracle on the host cores
+
+def oracle_sample(hm, cfg, n_decode, threads):
+    """Time the oracle: a 4-token prefill then n_decode decode steps.  Returns (decode tok/s, seconds)."""
+    import oracle
+    om = oracle.Model.from_host(hm, kv_slots=4 + n_decode + 1)
+    prompt = hm.prompt(4)
+    logits, _ = om.forward(prompt, 0, nthreads=threads)
+    tok = oracle.argmax(logits)
+    t0 = time.perf_counter()
+    for i in range(n_decode):
+        logits, _ = om.forward([tok], 4 + i, nthreads=threads)
+        tok = oracle.argmax(logits)
+    dt = time.perf_counter() - t0
+    return n_decode / dt, dt
+
+
+def run_reference(args, cfg, world, rank):
+    """The reference arm: the CPU oracle on the host cores, bounded sample per step."""
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    hm = synth.HostModel(cfg, synth.seed_of(args.config))
+    n_dec = args.ref_decode
+    for _ in range(args.warmup):
+        oracle_sample(hm, cfg, 1, threads)
+    total_t, total_tok = 0.0, 0
+    for _ in range(args.steps):
+        _, dt = oracle_sample(hm, cfg, n_dec, threads)
+        total_t += dt
+        total_tok += n_dec
+    v = total_tok / total_t
+    sample = f"{n_dec} oracle decode steps after a 4-token prefill per step, fp64, {threads} threads"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_obj(cfg, args),
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "decode tok/s + HBM GB/s frac of peak (8B-shape Q4_0); prefill tok/s"
+
+
+def config_obj(cfg, args):
+    return {"workload": f"{cfg.name}: {args.prompt}-token prompt in {args.chunk}-token chunks + {args.decode} "
+                        f"greedy decode steps, KV {cfg.kv_dtype} max_ctx {cfg.max_ctx}",
+            "layers": cfg.n_layers, "n_embd": cfg.n_embd, "heads": f"{cfg.n_heads}/{cfg.n_kv_heads}x{cfg.head_dim}",
+            "n_ff": cfg.n_ff, "vocab": cfg.n_vocab, "weights": cfg.wtype, "seed": synth.seed_of(args.config),
+            "l2": "inputs larger than L2 (weights %.2f GB streamed per decode step)"
+                  % (decode_bytes_per_token(cfg, 0) / 1e9), "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, cfg, world, rank, local):
+    import torch
+
+    import gguf_quantized_transformer_gb300 as af
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, bf16_peak, bf16_sust, peak_src, _ = peaks()
+
+    t0 = time.time()
+    hm = synth.HostModel(cfg, synth.seed_of(args.config))
+    gen_s = time.time() - t0
+    layers = [torch.from_numpy(b).to(dev) for b in hm.layers]
+    emb = torch.from_numpy(hm.token_embd).to(dev)
+    onorm = torch.from_numpy(hm.output_norm).to(dev)
+    out = torch.from_numpy(hm.output).to(dev)
+    m = af.Model(cfg, layers, emb, onorm, out, max_chunk=args.chunk)
+    torch.cuda.synchronize()
+    del layers, emb, onorm, out
+    torch.cuda.empty_cache()
+    stream = torch.cuda.ExternalStream(af.af_model_stream(m.h))
+    prompt = hm.prompt(args.prompt)
+    prompt_dev = torch.from_numpy(prompt).to(dev)
+    logits = torch.empty(cfg.n_vocab, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    P, ND, C = args.prompt, args.decode, args.chunk
+
+    def one_step(ev):
+        ev[0].record(stream)
+        for p in range(0, P, C):
+            n = min(C, P - p)
+            last = p + n >= P
+            af.af_prefill_dev(m.h, prompt_dev[p:p + n], n, p, logits if last else None)
+        ev[1].record(stream)
+        for i in range(ND):
+            af.af_decode_step(m.h, -1, P + i, logits)
+        ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        one_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for k in range(args.steps):
+        one_step(evs[k])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - w0
+    barrier(world)
+    clk = clocks.stop()
+    pre_ms = [evs[k][0].elapsed_time(evs[k][1]) for k in range(args.steps)]
+    dec_ms = [evs[k][1].elapsed_time(evs[k][2]) for k in range(args.steps)]
+    step_ms = max_over_ranks(world, float(np.mean([a + b for a, b in zip(pre_ms, dec_ms)])))
+    pre_s = max_over_ranks(world, float(np.sum(pre_ms)) / 1000)
+    dec_s = max_over_ranks(world, float(np.sum(dec_ms)) / 1000)
+    decode_tps = world * ND * args.steps / dec_s
+    prefill_tps = world * P * args.steps / pre_s
+
+    # decode roofline: algorithmic bytes of the timed decode steps / their time (per replica)
+    dec_bytes = sum(decode_bytes_per_token(cfg, P + i) for i in range(ND))
+    dec_gbs = dec_bytes * args.steps / (dec_s) / 1e9
+    pf_total, pf_gemm = prefill_flops(cfg, P, C)
+    pf_tflops = pf_total * args.steps / pre_s / 1e12
+
+    # per-kernel: the decode GEMV alone, at this model's largest per-layer matrix (gate|up), CUDA events
+    qg = qgemv_roofline(af, cfg, dev, hbm_peak)
+
+    # end to end through the host API: host token ids in, greedy token ids out, one sync per decode step
+    e2e = e2e_run(af, m, prompt, cfg, args)
+
+    launches_per_step = (P + C - 1) // C * (1 + 7 * cfg.n_layers) + 3 + ND * (3 + 5 * cfg.n_layers + 1)
+
+    line = {
+        "metric": METRIC, "value": decode_tps, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (weights q4_0/q8_0 decoded exactly; fp32 accumulate)",
+        "data": "synthetic (seeded random-init weights and prompt)", "config": config_obj(cfg, args),
+        "prefill_tok_s": prefill_tps, "decode_tok_s": decode_tps,
+        "decode_hbm_gbs": dec_gbs, "decode_hbm_frac": dec_gbs / hbm_peak,
+        "prefill_tflops": pf_tflops,
+        "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": dec_gbs / hbm_peak, "traffic": None,
+                     "kernel": "decode step (GEMVs + attention + LM head; per-token algorithmic bytes = "
+                               "quantized weights + KV read)", "peak_source": peak_src},
+        "roofline_qgemv": qg,
+        "cpu_baseline": None,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed": wall, "gen_s": gen_s,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        v, dt = oracle_sample(hm, cfg, args.ref_decode, threads)
+        line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{args.ref_decode} decode steps after a 4-token prefill "
+                                          f"({dt:.1f} s, fp64, {threads} threads)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    m.close()
+
+
+def qgemv_roofline(af, cfg, dev, hbm_peak, reps=50):
+    """Standalone af_qgemv on the model's gate|up shape [2F, E]: algorithmic bytes / event time."""
+    import torch
+    N, K = 2 * cfg.n_ff, cfg.n_embd
+    W = synth.matrix(cfg.wtype, 7, synth.TID_TEST_BASE + 99, N, K)
+    Wd = torch.from_numpy(W).to(dev)
+    h = af.af_qweight_create(af.WTYPE[cfg.wtype], Wd, N, K)
+    del Wd
+    x = torch.randn(K, device=dev)
+    y = torch.empty(N, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
+    s = torch.cuda.current_stream()
+    times = []
+    for i in range(reps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        af.af_qgemv(h, x, y)
+        b.record(s)
+        b.synchronize()
+        if i >= 3:
+            times.append(a.elapsed_time(b))
+    af.af_qweight_destroy(h)
+    bpe = 34 / 32 if cfg.wtype == "q8_0" else 18 / 32
+    nbytes = N * K * bpe + K * 4 + N * 4
+    ms = float(np.mean(times))
+    gbs = nbytes / (ms / 1000) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+            "traffic": None, "kernel": f"qgemv {cfg.wtype} [{N}x{K}] (L2 flushed between launches)",
+            "bytes_per_launch": nbytes, "us_per_launch": ms * 1000}
+
+
+def e2e_run(af, m, prompt, cfg, args):
+    """Host-API run: prompt ids from pinned host memory, greedy ids back to the host every step."""
+    import torch
+    P, ND, C = args.prompt, args.decode, args.chunk
+    host_prompt = torch.from_numpy(prompt).pin_memory()
+    hp = host_prompt.numpy()
+    logits = torch.empty(cfg.n_vocab, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for p in range(0, P, C):
+        n = min(C, P - p)
+        af.af_prefill(m.h, hp[p:p + n], n, p, logits if p + n >= P else None)
+    tok = -1  # first decode step takes the prefill's greedy token from the device
+    t1 = time.perf_counter()
+    for i in range(ND):
+        tok = af.af_decode_step(m.h, tok, P + i, None, want_next=True)
+    t2 = time.perf_counter()
+    return {"value": ND / (t2 - t1), "unit": "tok/s", "prefill_tok_s": P / (t1 - t0),
+            "h2d_bytes_per_step": P * 4 + ND * 4, "d2h_bytes_per_step": ND * 4,
+            "note": "af_prefill from pinned host ids + af_decode_step with the host feeding back each greedy "
+                    "id it reads (one stream sync per token); wall clock; prefill time excludes its final sync"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--prompt", type=int, default=0, help="prompt tokens (default: the config's)")
+    ap.add_argument("--decode", type=int, default=0, help="decode steps (default: the config's)")
+    ap.add_argument("--chunk", type=int, default=512)
+    ap.add_argument("--ref-decode", type=int, default=2, help="oracle decode steps per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    cfg = synth.CONFIGS[args.config]
+    args.prompt = args.prompt or cfg.prompt_len
+    args.decode = args.decode or cfg.n_decode
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, cfg, world, rank)
+    else:
+        run_ours(args, cfg, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -130,9 +130,9 @@ struct af_model {
     float* q = nullptr;      // [chunk][H*D] rotated q
     float* attn = nullptr;   // [H*D] decode attention output
     float* h = nullptr;      // [F] decode SwiGLU output
-    __half* y16 = nullptr;   // [chunk][max(E, ...)] normalized activations (GEMM operand)
-    __half* a16 = nullptr;   // [chunk][H*D] attention output (GEMM operand)
-    __half* h16 = nullptr;   // [chunk][F] SwiGLU output (GEMM operand)
+    float* y = nullptr;      // [chunk][E] normalized activations (GEMM operand)
+    float* a = nullptr;      // [chunk][H*D] attention output (GEMM operand)
+    float* hp = nullptr;     // [chunk][F] SwiGLU output (GEMM operand)
     int* tok = nullptr;      // [chunk]
     float* logits = nullptr; // [V] default logits
     GemvScratch gs;
@@ -154,8 +154,6 @@ struct af_qweight {
     Planes p;
     Allocs A;
     GemvScratch gs;
-    __half* x16 = nullptr;
-    int x16_rows = 0;
 };
 
 extern "C" {
@@ -299,9 +297,9 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     m->q = (float*)A.get((size_t)S * QD * 4);
     m->attn = (float*)A.get((size_t)QD * 4);
     m->h = (float*)A.get((size_t)F * 4);
-    m->y16 = (__half*)A.get((size_t)S * E * 2);
-    m->a16 = (__half*)A.get((size_t)S * QD * 2);
-    m->h16 = (__half*)A.get((size_t)S * F * 2);
+    m->y = (float*)A.get((size_t)S * E * 4);
+    m->a = (float*)A.get((size_t)S * QD * 4);
+    m->hp = (float*)A.get((size_t)S * F * 4);
     m->tok = (int*)A.get((size_t)S * 4);
     m->logits = (float*)A.get((size_t)V * 4);
     m->st = (StepState*)A.get(sizeof(StepState));
@@ -315,7 +313,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     m->as.ns = attn_decode_splits(c.n_kv_heads);
     m->as.part = (float*)A.get(attn_decode_part_elems(c.n_heads, D, m->as.ns) * 4);
     m->as.cnt = (unsigned*)A.get((size_t)c.n_kv_heads * 4);
-    if (!m->x || !m->q || !m->attn || !m->h || !m->y16 || !m->a16 || !m->h16 || !m->tok || !m->logits || !m->st ||
+    if (!m->x || !m->q || !m->attn || !m->h || !m->y || !m->a || !m->hp || !m->tok || !m->logits || !m->st ||
         !m->gs.part || !m->gs.cnt || !m->as.part || !m->as.cnt)
         return oom("activations");
     {
@@ -433,16 +431,14 @@ int prefill_impl(af_model* m, const int* tok_dev, int n, int start_pos, float* l
     if (rc) return rc;
     for (int l = 0; l < c.n_layers; l++) {
         const LayerW& lw = m->L[l];
-        CK(launch_rmsnorm_rows(m->x, n, E, lw.attn_norm, c.rms_eps, nullptr, m->y16, s));
-        CK(launch_qgemm(lw.qkv, m->y16, E, n, epi_qkv(m, l, m->q, nullptr, nullptr, start_pos), s));
+        CK(launch_rmsnorm_rows(m->x, n, E, lw.attn_norm, c.rms_eps, m->y, nullptr, s));
+        CK(launch_qgemm(lw.qkv, m->y, E, n, epi_qkv(m, l, m->q, nullptr, nullptr, start_pos), s));
         CK(launch_attn_prefill(m->q, QD, m->kl(l), m->vl(l), c.kv_dtype == AF_F16, c.n_heads, c.n_kv_heads,
-                               c.head_dim, c.max_ctx, start_pos, n, nullptr, m->a16, QD, s));
-        CK(launch_qgemm(lw.o, m->a16, QD, n, epi_simple(EPI_RESID, m->x, E), s));
-        CK(launch_rmsnorm_rows(m->x, n, E, lw.ffn_norm, c.rms_eps, nullptr, m->y16, s));
-        Epi eg = epi_simple(EPI_SWIGLU, nullptr, F);
-        eg.out16 = m->h16;
-        CK(launch_qgemm(lw.gu, m->y16, E, n, eg, s));
-        CK(launch_qgemm(lw.down, m->h16, F, n, epi_simple(EPI_RESID, m->x, E), s));
+                               c.head_dim, c.max_ctx, start_pos, n, m->a, nullptr, QD, s));
+        CK(launch_qgemm(lw.o, m->a, QD, n, epi_simple(EPI_RESID, m->x, E), s));
+        CK(launch_rmsnorm_rows(m->x, n, E, lw.ffn_norm, c.rms_eps, m->y, nullptr, s));
+        CK(launch_qgemm(lw.gu, m->y, E, n, epi_simple(EPI_SWIGLU, m->hp, F), s));
+        CK(launch_qgemm(lw.down, m->hp, F, n, epi_simple(EPI_RESID, m->x, E), s));
         rc = capture_copy(m, l + 1, n);
         if (rc) return rc;
     }
@@ -570,21 +566,7 @@ int af_qgemv(const af_qweight* w, const float* x_dev, float* y_dev, void* stream
 int af_qgemm(const af_qweight* wc, const float* X_dev, int32_t M, float* Y_dev, void* stream) {
     if (!wc || !X_dev || !Y_dev) return fail(AF_EINVAL, "null argument");
     if (M < 1) return fail(AF_ERANGE, "M must be >= 1");
-    af_qweight* w = const_cast<af_qweight*>(wc);
-    cudaStream_t s = (cudaStream_t)stream;
-    if (w->x16_rows < M) {
-        CK(cudaStreamSynchronize(s));  // the old buffer may still be in use
-        if (w->x16) {
-            cudaFree(w->x16);
-            for (auto& p : w->A.p)
-                if (p == w->x16) p = nullptr;
-        }
-        w->x16 = (__half*)w->A.get((size_t)M * w->p.K * 2);
-        w->x16_rows = w->x16 ? M : 0;
-        if (!w->x16) return fail(AF_ENOMEM, "operand buffer");
-    }
-    CK(launch_f32_to_f16(X_dev, w->x16, (int64_t)M * w->p.K, s));
-    CK(launch_qgemm(w->p, w->x16, w->p.K, M, epi_simple(EPI_STORE, Y_dev, w->p.N), s));
+    CK(launch_qgemm(wc->p, X_dev, wc->p.K, M, epi_simple(EPI_STORE, Y_dev, wc->p.N), (cudaStream_t)stream));
     return AF_OK;
 }
 

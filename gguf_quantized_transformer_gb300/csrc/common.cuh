@@ -149,8 +149,8 @@ cudaError_t launch_qgemv(const Planes& W, const float* x, const float* norm_w, f
                          const GemvScratch& scr, cudaStream_t s);
 size_t qgemv_part_elems(const Planes& W);
 
-// Prefill GEMM: Y = X W^T for M rows with a fused epilogue.  X is fp16 [M][ldx].
-cudaError_t launch_qgemm(const Planes& W, const __half* X16, int64_t ldx, int M, const Epi& epi, cudaStream_t s);
+// Prefill GEMM: Y = X W^T for M rows with a fused epilogue.  X is fp32 [M][ldx].
+cudaError_t launch_qgemm(const Planes& W, const float* X, int64_t ldx, int M, const Epi& epi, cudaStream_t s);
 
 // Attention
 struct AttnScratch {

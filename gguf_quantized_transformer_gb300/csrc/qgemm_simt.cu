@@ -2,7 +2,7 @@
 // quantized W dequantized into shared memory one 32-weight block column at a
 // time (dotLLM "GPU Inference", "Weight Strategy", approach 1: dequantized
 // values never touch device memory) and the fused epilogue applied per column
-// pair.  X is fp16 (the operand precision of the tensor-core path), products
+// pair.  X and the dequantized weights are exact fp32 operands; products
 // accumulate in fp32.
 #include "common.cuh"
 
@@ -12,7 +12,7 @@ namespace {
 
 constexpr int BM = 64, BN = 64, BK = 32;
 
-__global__ void __launch_bounds__(256) qgemm_simt_kernel(Planes W, const __half* __restrict__ X, int64_t ldx, int M,
+__global__ void __launch_bounds__(256) qgemm_simt_kernel(Planes W, const float* __restrict__ X, int64_t ldx, int M,
                                                          Epi epi) {
     __shared__ float Xs[BK][BM + 4];
     __shared__ float Ws[BK][BN + 4];
@@ -22,15 +22,15 @@ __global__ void __launch_bounds__(256) qgemm_simt_kernel(Planes W, const __half*
     float acc[4][4] = {};
     const int nkb = W.K / 32;
     for (int kb = 0; kb < nkb; kb++) {
-        {  // X tile: 64 rows x 32 halves, 8 halves per thread
+        {  // X tile: 64 rows x 32 floats, 8 per thread
             const int r = tid >> 2, q = tid & 3;
             const int m = m0 + r;
             float v[8];
             if (m < M) {
-                const uint4 raw = *reinterpret_cast<const uint4*>(X + (int64_t)m * ldx + kb * 32 + q * 8);
-                const __half* h = reinterpret_cast<const __half*>(&raw);
-#pragma unroll
-                for (int e = 0; e < 8; e++) v[e] = __half2float(h[e]);
+                const float4* xp = reinterpret_cast<const float4*>(X + (int64_t)m * ldx + kb * 32 + q * 8);
+                const float4 a = xp[0], b = xp[1];
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; e++) v[e] = 0.f;
@@ -93,9 +93,9 @@ __global__ void __launch_bounds__(256) qgemm_simt_kernel(Planes W, const __half*
 
 }  // namespace
 
-cudaError_t launch_qgemm(const Planes& W, const __half* X16, int64_t ldx, int M, const Epi& epi, cudaStream_t s) {
+cudaError_t launch_qgemm(const Planes& W, const float* X, int64_t ldx, int M, const Epi& epi, cudaStream_t s) {
     dim3 grid((W.N + BN - 1) / BN, (M + BM - 1) / BM);
-    qgemm_simt_kernel<<<grid, 256, 0, s>>>(W, X16, ldx, M, epi);
+    qgemm_simt_kernel<<<grid, 256, 0, s>>>(W, X, ldx, M, epi);
     return cudaGetLastError();
 }
 

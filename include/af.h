@@ -166,8 +166,7 @@ void af_model_destroy(af_model* m);
  *   af_qgemm: Y[m][i] = sum_j X[m][j] W[i][j]     X_dev fp32 [M, K] row-major,
  *                                                 Y_dev fp32 [M, N], M >= 1
  * Calls that share one af_qweight must be ordered on one stream (they share
- * its scratch).  af_qgemm converts X to fp16 for the tensor cores and
- * accumulates in fp32.
+ * its scratch).  Products accumulate in fp32.
  */
 int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t K, void* stream, af_qweight** out);
 int af_qgemv(const af_qweight* w, const float* x_dev, float* y_dev, void* stream);
