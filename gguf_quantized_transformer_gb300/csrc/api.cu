@@ -108,6 +108,11 @@ int check_config(const af_config* c) {
         return fail(AF_ENOTIMPL, "attention supports head_dim 64/128 and group size 1/2/4/8");
     if (c->n_embd % 64 || c->n_ff % 64 || (c->n_heads * c->head_dim) % 64 || c->n_vocab % 2)
         return fail(AF_ENOTIMPL, "n_embd, n_ff, n_heads*head_dim must be multiples of 64 and n_vocab even");
+    {
+        const int kmax = std::max(std::max(c->n_embd, c->n_ff), c->n_heads * c->head_dim);
+        if (padded_k(c->wtype, kmax) / chunk_weights(c->wtype) > qgemv_max_chunks())
+            return fail(AF_ENOTIMPL, "matrix rows longer than %d weights", qgemv_max_chunks() * chunk_weights(c->wtype));
+    }
     return AF_OK;
 }
 
@@ -142,6 +147,7 @@ struct af_model {
     bool use_graph = true;
     cudaGraphExec_t gexec = nullptr;
     float* graph_logits = nullptr;
+    unsigned err_host = 0;
 
     int E() const { return c.n_embd; }
     int QD() const { return c.n_heads * c.head_dim; }
@@ -303,21 +309,16 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     m->tok = (int*)A.get((size_t)S * 4);
     m->logits = (float*)A.get((size_t)V * 4);
     m->st = (StepState*)A.get(sizeof(StepState));
-    size_t part = 0, cnt = 0;
-    for (const Planes* P : {&m->L[0].qkv, &m->L[0].o, &m->L[0].gu, &m->L[0].down, &m->out}) {
-        part = std::max(part, qgemv_part_elems(*P));
-        cnt = std::max(cnt, (size_t)P->N / 2);
-    }
-    m->gs.part = (float*)A.get(part * 4);
-    m->gs.cnt = (unsigned*)A.get(cnt * 4);
+    m->gs.err = (unsigned*)A.get(sizeof(unsigned));
     m->as.ns = attn_decode_splits(c.n_kv_heads);
     m->as.part = (float*)A.get(attn_decode_part_elems(c.n_heads, D, m->as.ns) * 4);
     m->as.cnt = (unsigned*)A.get((size_t)c.n_kv_heads * 4);
     if (!m->x || !m->q || !m->attn || !m->h || !m->y || !m->a || !m->hp || !m->tok || !m->logits || !m->st ||
-        !m->gs.part || !m->gs.cnt || !m->as.part || !m->as.cnt)
+        !m->gs.err || !m->as.part || !m->as.cnt)
         return oom("activations");
     {
-        cudaError_t e = cudaMemsetAsync(m->gs.cnt, 0, cnt * 4, s);
+        cudaError_t e = qgemv_prepare();
+        if (!e) e = cudaMemsetAsync(m->gs.err, 0, sizeof(unsigned), s);
         if (!e) e = cudaMemsetAsync(m->as.cnt, 0, (size_t)c.n_kv_heads * 4, s);
         if (!e) e = cudaMemsetAsync(m->st, 0, sizeof(StepState), s);
         if (!e) e = cudaStreamSynchronize(s);
@@ -516,7 +517,9 @@ int af_decode_step(af_model* m, int32_t token, int32_t pos, float* logits_dev, i
     }
     if (next_token_host) {
         CK(cudaMemcpyAsync(next_token_host, &m->st->next_token, 4, cudaMemcpyDeviceToHost, m->s));
+        CK(cudaMemcpyAsync(&m->err_host, m->gs.err, 4, cudaMemcpyDeviceToHost, m->s));
         CK(cudaStreamSynchronize(m->s));
+        if (m->err_host) return fail(AF_ETIMEOUT, "a bounded device-side wait gave up (code %u)", m->err_host);
     }
     return AF_OK;
 }
@@ -536,18 +539,20 @@ int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t 
     if (!blocks_dev) return fail(AF_EINVAL, "null blocks");
     if (N <= 0 || K <= 0 || K % 32) return fail(AF_EINVAL, "need N > 0 and K a positive multiple of 32");
     if (N % 2) return fail(AF_ENOTIMPL, "N must be even");
+    if (padded_k(wtype, K) / chunk_weights(wtype) > qgemv_max_chunks())
+        return fail(AF_ENOTIMPL, "K above %d", qgemv_max_chunks() * chunk_weights(wtype));
     af_qweight* w = new (std::nothrow) af_qweight();
     if (!w) return fail(AF_ENOMEM, "host allocation failed");
     cudaStream_t s = (cudaStream_t)stream;
     w->p = make_planes(w->A, wtype, N, K);
-    w->gs.part = (float*)w->A.get(qgemv_part_elems(w->p) * 4);
-    w->gs.cnt = (unsigned*)w->A.get((size_t)N / 2 * 4);
-    if (!w->p.qs || !w->gs.part || !w->gs.cnt) {
+    w->gs.err = (unsigned*)w->A.get(sizeof(unsigned));
+    if (!w->p.qs || !w->gs.err) {
         af_qweight_destroy(w);
         return fail(AF_ENOMEM, "device allocation failed");
     }
-    cudaError_t e = repack_into(w->p, blocks_dev, N, 0, 1, s);
-    if (!e) e = cudaMemsetAsync(w->gs.cnt, 0, (size_t)N / 2 * 4, s);
+    cudaError_t e = qgemv_prepare();
+    if (!e) e = repack_into(w->p, blocks_dev, N, 0, 1, s);
+    if (!e) e = cudaMemsetAsync(w->gs.err, 0, sizeof(unsigned), s);
     if (!e) e = cudaStreamSynchronize(s);
     if (e) {
         af_qweight_destroy(w);

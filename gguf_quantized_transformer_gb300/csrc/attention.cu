@@ -15,6 +15,8 @@
 // shared memory; online softmax per query vector; causal mask j <= p0 + r.
 #include <math_constants.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace af {
@@ -47,7 +49,9 @@ __device__ __forceinline__ void load_vec<__half>(const __half* p, float* out, in
     }
 }
 
-constexpr int kDecThreads = 128;  // 16 position groups x 8 lanes
+constexpr int kDecThreads = 256;  // 32 position groups x 8 lanes
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kMinPerSplit = 64;   // positions per split before another split is used
 
 template <int D, int G, typename KT>
 __global__ void __launch_bounds__(kDecThreads)
@@ -55,9 +59,10 @@ __global__ void __launch_bounds__(kDecThreads)
                        const int* __restrict__ pos_dev, int pos_arg, float* __restrict__ part,
                        unsigned* __restrict__ cnt, float* __restrict__ out) {
     constexpr int DL = D / 8;  // dims per lane
-    extern __shared__ float sc[];  // [chunk][G] scores
-    __shared__ float red_m[4][G], red_l[4][G];
-    __shared__ float red_o[4][G][D];
+    extern __shared__ float sc[];  // [chunk][G] scores; reused for the merge weights [ns][G]
+    __shared__ float red_m[kDecWarps][G], red_l[kDecWarps][G];
+    __shared__ float red_o[kDecWarps][G][D];
+    __shared__ float mh_s[G], inv_den[G];
     __shared__ unsigned last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -65,107 +70,118 @@ __global__ void __launch_bounds__(kDecThreads)
     const int g = blockIdx.y, s = blockIdx.x, ns = gridDim.x;
     const int pos = pos_dev ? *pos_dev : pos_arg;
     const int n = pos + 1;
-    const int chunk = (n + ns - 1) / ns;
+    int ns_eff = (n + kMinPerSplit - 1) / kMinPerSplit;
+    ns_eff = ns_eff < ns ? ns_eff : ns;
+    const int chunk = (n + ns_eff - 1) / ns_eff;
     const int j0 = s * chunk;
     const int j1 = min(n, j0 + chunk);
     const KT* K = kc + (int64_t)g * max_ctx * D;
     const KT* V = vc + (int64_t)g * max_ctx * D;
-    const float scale = rsqrtf((float)D);
-
-    float qv[G][DL];
-#pragma unroll
-    for (int h = 0; h < G; h++) {
-        load_vec<float>(q + (int64_t)(g * G + h) * D + li * DL, qv[h], DL);
-#pragma unroll
-        for (int d = 0; d < DL; d++) qv[h][d] *= scale;
-    }
-
-    // pass 1: scores
-    for (int jb = j0; jb < j1; jb += 16) {  // uniform trip count: every lane reaches the shuffles
-        const int j = jb + gi;
-        const bool ok = j < j1;
-        float kf[DL];
-        if (ok) {
-            load_vec<KT>(K + (int64_t)j * D + li * DL, kf, DL);
-        } else {
-#pragma unroll
-            for (int d = 0; d < DL; d++) kf[d] = 0.f;
-        }
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            float a = 0.f;
-#pragma unroll
-            for (int d = 0; d < DL; d++) a = fmaf(qv[h][d], kf[d], a);
-            a += __shfl_xor_sync(0xffffffffu, a, 1);
-            a += __shfl_xor_sync(0xffffffffu, a, 2);
-            a += __shfl_xor_sync(0xffffffffu, a, 4);
-            if (ok && li == 0) sc[(j - j0) * G + h] = a;
-        }
-    }
-    __syncthreads();
-
-    // CTA maximum per head
-    float mh[G];
-#pragma unroll
-    for (int h = 0; h < G; h++) {
-        float m = -CUDART_INF_F;
-        for (int j = tid; j < j1 - j0; j += kDecThreads) m = fmaxf(m, sc[j * G + h]);
-        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) red_m[warp][h] = m;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < G; h++) mh[h] = fmaxf(fmaxf(red_m[0][h], red_m[1][h]), fmaxf(red_m[2][h], red_m[3][h]));
-
-    // pass 2: P V
-    float acc[G][DL], lsum[G];
-#pragma unroll
-    for (int h = 0; h < G; h++) {
-        lsum[h] = 0.f;
-#pragma unroll
-        for (int d = 0; d < DL; d++) acc[h][d] = 0.f;
-    }
-    for (int j = j0 + gi; j < j1; j += 16) {
-        float vf[DL];
-        load_vec<KT>(V + (int64_t)j * D + li * DL, vf, DL);
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            const float p = __expf(sc[(j - j0) * G + h] - mh[h]);
-            lsum[h] += p;
-#pragma unroll
-            for (int d = 0; d < DL; d++) acc[h][d] = fmaf(p, vf[d], acc[h][d]);
-        }
-    }
-    // reduce over the 4 position groups of a warp (lanes li, li+8, li+16, li+24)
-#pragma unroll
-    for (int h = 0; h < G; h++) {
-        lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 8);
-        lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 16);
-#pragma unroll
-        for (int d = 0; d < DL; d++) {
-            acc[h][d] += __shfl_xor_sync(0xffffffffu, acc[h][d], 8);
-            acc[h][d] += __shfl_xor_sync(0xffffffffu, acc[h][d], 16);
-        }
-    }
-    __syncthreads();  // red_m reads done before reuse of shared memory below
-    if (lane < 8) {
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-#pragma unroll
-            for (int d = 0; d < DL; d++) red_o[warp][h][li * DL + d] = acc[h][d];
-            if (li == 0) red_l[warp][h] = lsum[h];
-        }
-    }
-    __syncthreads();
-    // this CTA's partial: part[((g*ns + s)*G + h)*(D+2) + {0..D-1: o, D: max, D+1: sum}]
     float* my = part + ((int64_t)(g * ns + s) * G) * (D + 2);
-    for (int t = tid; t < G * D; t += kDecThreads) {
-        const int h = t / D, d = t % D;
-        my[h * (D + 2) + d] = red_o[0][h][d] + red_o[1][h][d] + red_o[2][h][d] + red_o[3][h][d];
-    }
-    if (tid < G) {
-        my[tid * (D + 2) + D] = mh[tid];
-        my[tid * (D + 2) + D + 1] = red_l[0][tid] + red_l[1][tid] + red_l[2][tid] + red_l[3][tid];
+
+    if (s < ns_eff) {
+        const float scale = rsqrtf((float)D);
+        float qv[G][DL];
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            load_vec<float>(q + (int64_t)(g * G + h) * D + li * DL, qv[h], DL);
+#pragma unroll
+            for (int d = 0; d < DL; d++) qv[h][d] *= scale;
+        }
+        // pass 1: scores of this split's slots into shared memory
+        for (int jb = j0; jb < j1; jb += 32) {  // uniform trip count: every lane reaches the shuffles
+            const int j = jb + gi;
+            const bool ok = j < j1;
+            float kf[DL];
+            if (ok) {
+                load_vec<KT>(K + (int64_t)j * D + li * DL, kf, DL);
+            } else {
+#pragma unroll
+                for (int d = 0; d < DL; d++) kf[d] = 0.f;
+            }
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                float a = 0.f;
+#pragma unroll
+                for (int d = 0; d < DL; d++) a = fmaf(qv[h][d], kf[d], a);
+                a += __shfl_xor_sync(0xffffffffu, a, 1);
+                a += __shfl_xor_sync(0xffffffffu, a, 2);
+                a += __shfl_xor_sync(0xffffffffu, a, 4);
+                if (ok && li == 0) sc[(j - j0) * G + h] = a;
+            }
+        }
+        __syncthreads();
+        // split maximum per head
+        float mh[G];
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            float m = -CUDART_INF_F;
+            for (int j = tid; j < j1 - j0; j += kDecThreads) m = fmaxf(m, sc[j * G + h]);
+            for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) red_m[warp][h] = m;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            float m = red_m[0][h];
+#pragma unroll
+            for (int w = 1; w < kDecWarps; w++) m = fmaxf(m, red_m[w][h]);
+            mh[h] = m;
+        }
+        // pass 2: P V
+        float acc[G][DL], lsum[G];
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            lsum[h] = 0.f;
+#pragma unroll
+            for (int d = 0; d < DL; d++) acc[h][d] = 0.f;
+        }
+        for (int j = j0 + gi; j < j1; j += 32) {
+            float vf[DL];
+            load_vec<KT>(V + (int64_t)j * D + li * DL, vf, DL);
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                const float p = __expf(sc[(j - j0) * G + h] - mh[h]);
+                lsum[h] += p;
+#pragma unroll
+                for (int d = 0; d < DL; d++) acc[h][d] = fmaf(p, vf[d], acc[h][d]);
+            }
+        }
+        // reduce over the 4 position groups of a warp (lanes li, li+8, li+16, li+24)
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 8);
+            lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 16);
+#pragma unroll
+            for (int d = 0; d < DL; d++) {
+                acc[h][d] += __shfl_xor_sync(0xffffffffu, acc[h][d], 8);
+                acc[h][d] += __shfl_xor_sync(0xffffffffu, acc[h][d], 16);
+            }
+        }
+        if (lane < 8) {
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+#pragma unroll
+                for (int d = 0; d < DL; d++) red_o[warp][h][li * DL + d] = acc[h][d];
+                if (li == 0) red_l[warp][h] = lsum[h];
+            }
+        }
+        __syncthreads();
+        // this split's partial: part[((g*ns + s)*G + h)*(D+2) + {0..D-1: o, D: max, D+1: sum}]
+        for (int t = tid; t < G * D; t += kDecThreads) {
+            const int h = t / D, d = t % D;
+            float o = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; w++) o += red_o[w][h][d];
+            my[h * (D + 2) + d] = o;
+        }
+        if (tid < G) {
+            float l = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDecWarps; w++) l += red_l[w][tid];
+            my[tid * (D + 2) + D] = j1 > j0 ? mh[tid] : -CUDART_INF_F;
+            my[tid * (D + 2) + D + 1] = l;
+        }
     }
     __threadfence();
     __syncthreads();
@@ -176,22 +192,41 @@ __global__ void __launch_bounds__(kDecThreads)
     __syncthreads();
     if (!last) return;
     __threadfence();
-    // merge the ns partials of this kv head
+    // merge the ns_eff partials of this kv head: weights exp(m_s - M) / sum_s exp(m_s - M) l_s
     const float* pg = part + ((int64_t)g * ns * G) * (D + 2);
+    float* wsm = sc;  // [ns_eff][G]
+    for (int t = tid; t < ns_eff * G; t += kDecThreads) wsm[t] = __ldcg(pg + (int64_t)t * (D + 2) + D);
+    __syncthreads();
+    if (tid < G) {
+        float M = -CUDART_INF_F;
+        for (int ss = 0; ss < ns_eff; ss++) M = fmaxf(M, wsm[ss * G + tid]);
+        float den = 0.f;
+        for (int ss = 0; ss < ns_eff; ss++) {
+            const float l = __ldcg(pg + ((int64_t)ss * G + tid) * (D + 2) + D + 1);
+            if (l > 0.f) den = fmaf(__expf(wsm[ss * G + tid] - M), l, den);
+        }
+        mh_s[tid] = M;
+        inv_den[tid] = 1.f / den;
+    }
+    __syncthreads();
+    for (int t = tid; t < ns_eff * G; t += kDecThreads) {
+        const int h = t % G;
+        const float m = wsm[t];
+        wsm[t] = m == -CUDART_INF_F ? 0.f : __expf(m - mh_s[h]) * inv_den[h];
+    }
+    __syncthreads();
     for (int t = tid; t < G * D; t += kDecThreads) {
         const int h = t / D, d = t % D;
-        float M = -CUDART_INF_F;
-        for (int ss = 0; ss < ns; ss++) M = fmaxf(M, __ldcg(pg + ((int64_t)ss * G + h) * (D + 2) + D));
-        float num = 0.f, den = 0.f;
-        for (int ss = 0; ss < ns; ss++) {
-            const float* ps = pg + ((int64_t)ss * G + h) * (D + 2);
-            const float l = __ldcg(ps + D + 1);
-            if (l == 0.f) continue;  // empty split
-            const float w = __expf(__ldcg(ps + D) - M);
-            num = fmaf(w, __ldcg(ps + d), num);
-            den = fmaf(w, l, den);
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        int ss = 0;
+        for (; ss + 4 <= ns_eff; ss += 4) {
+            a0 = fmaf(wsm[(ss + 0) * G + h], __ldcg(pg + ((int64_t)(ss + 0) * G + h) * (D + 2) + d), a0);
+            a1 = fmaf(wsm[(ss + 1) * G + h], __ldcg(pg + ((int64_t)(ss + 1) * G + h) * (D + 2) + d), a1);
+            a2 = fmaf(wsm[(ss + 2) * G + h], __ldcg(pg + ((int64_t)(ss + 2) * G + h) * (D + 2) + d), a2);
+            a3 = fmaf(wsm[(ss + 3) * G + h], __ldcg(pg + ((int64_t)(ss + 3) * G + h) * (D + 2) + d), a3);
         }
-        out[(int64_t)(g * G + h) * D + d] = num / den;
+        for (; ss < ns_eff; ss++) a0 = fmaf(wsm[ss * G + h], __ldcg(pg + ((int64_t)ss * G + h) * (D + 2) + d), a0);
+        out[(int64_t)(g * G + h) * D + d] = (a0 + a1) + (a2 + a3);
     }
     if (tid == 0) cnt[g] = 0u;
 }
@@ -323,7 +358,7 @@ template <int D, int G>
 cudaError_t dispatch_decode(const float* q, const void* kc, const void* vc, int kv_f16, int max_ctx,
                             const int* pos_dev, int pos, const AttnScratch& scr, float* out, int KVH, cudaStream_t s) {
     const int ns = scr.ns;
-    const int cap = (max_ctx + ns - 1) / ns;
+    const int cap = std::max((max_ctx + ns - 1) / ns, std::max(ns, kMinPerSplit));
     const size_t smem = (size_t)cap * G * sizeof(float);
     dim3 grid(ns, KVH);
     if (kv_f16) {

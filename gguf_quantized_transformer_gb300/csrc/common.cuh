@@ -127,9 +127,7 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, f
 // Host-side launchers (defined in the .cu files).
 // ---------------------------------------------------------------------------
 struct GemvScratch {
-    float* part = nullptr;     // [NC][N] per-chunk partial sums
-    unsigned* cnt = nullptr;   // [N/2] arrival counters, zero between launches
-    size_t part_elems = 0, cnt_elems = 0;
+    unsigned* err = nullptr;  // device error word (DEV_OK / DEV_TIMEOUT), zero when healthy
 };
 
 int num_sms();
@@ -147,7 +145,10 @@ cudaError_t launch_f32_to_f16(const float* x, __half* y, int64_t n, cudaStream_t
 // prologue (norm_w != nullptr) and a fused epilogue.
 cudaError_t launch_qgemv(const Planes& W, const float* x, const float* norm_w, float eps, const Epi& epi,
                          const GemvScratch& scr, cudaStream_t s);
-size_t qgemv_part_elems(const Planes& W);
+// Opt the GEMV kernels in to their shared-memory ring (call once, before any stream capture).
+cudaError_t qgemv_prepare();
+// Largest number of K chunks (Kp / chunk_weights) a GEMV supports.
+int qgemv_max_chunks();
 
 // Prefill GEMM: Y = X W^T for M rows with a fused epilogue.  X is fp32 [M][ldx].
 cudaError_t launch_qgemm(const Planes& W, const float* X, int64_t ldx, int M, const Epi& epi, cudaStream_t s);

@@ -3,54 +3,115 @@
 // ops: "Dequantization happens inline ... No separate dequantize-then-multiply
 // step"; decode is bound by reading the weights, "Decode loop").
 //
-// Work split.  A row of Kp weights is NC chunks of 32 sixteen-byte units
-// (Q4_0: one unit = one 32-weight block; Q8_0: half a block).  The N*NC
-// (chunk, row) items, ordered chunk-major, are divided evenly over all warps of
-// the grid, so every warp streams the same number of bytes (+-1 item)
-// whatever N and K are.  Lane l of a warp owns unit l of the chunk, keeps that
-// unit's x slice in registers and walks down the rows, issuing one 128-bit
-// streaming load per row, 8 rows at a time.
+// Streaming.  One CTA per SM owns a contiguous, even-aligned range of rows
+// (N/#SM rows +-2).  Rows are contiguous in the quant and scale planes, so a
+// stage of R whole rows is two bulk asynchronous copies (cp.async.bulk,
+// mbarrier completion, L2 evict-first) into a shared-memory ring of a few
+// stages; one thread keeps the ring full while all warps compute.  The first
+// stages are issued before griddepcontrol.wait (the weights do not depend on
+// the previous kernel), and the ring is small enough (<= 96 KB, <= 128
+// registers/thread) for the next kernel's CTA to be resident and pre-fill
+// its own ring while this one drains.
 //
-// Reduction.  The 8 per-lane row partials are reduced across the warp with a
-// transpose-reduce (3 exchange steps + 2 butterfly steps), leaving row j's
-// chunk sum in lanes 4j..4j+3.  It is stored to part[c][row]; an acq_rel
-// counter per row pair counts arrivals, and the lane that completes a pair
-// sums its NC partials in chunk order (deterministic) and applies the fused
-// epilogue to the pair, then re-zeroes the counter for the next launch.
+// Compute.  Each lane keeps its slice of x (RMS-normalized in the prologue)
+// in registers for the whole kernel: the K axis of a row is NC chunks of 32
+// sixteen-byte units and warp (rs, wk) owns chunks wk, wk+WK, ... of the rows
+// of row stream rs, lane l unit l of each.  Per stage a warp dequantizes its
+// units straight from shared memory and reduces its row partials with a
+// transpose-reduce; the WK partials of each row are summed in a fixed order
+// (deterministic) and the fused epilogue is applied per row pair.
 //
-// Dequantization in registers.
-//   Q4_0: byte_perm places a nibble n in bits 16..19 under exponent 0x3F0,
-//         giving the float 0.5 + n/256 in one instruction.  With S the FMA sum
-//         of those floats times x over the block and sx = sum(x):
-//           sum_j (n_j - 8) x_j = 256 S - 136 sx,   block value = d * that.
-//   Q8_0: byte_perm places (q + 128) under 0x4B00 00.., i.e. 2^23 + q + 128,
-//         and one FADD recovers q exactly.
+// Dot products in integer arithmetic.  In the prologue each lane converts the
+// x values of each of its 32-element units (16 for Q8_0) to 24-bit fixed
+// point with a per-unit power-of-two scale s (max|x| / s in [2^22, 2^23)):
+// x ~= s * xi, error <= s/2, the same order as fp32 rounding of the products
+// (and exact for values that fit, e.g. a one-hot x reads a weight exactly).  xi is kept as
+// three byte planes (top byte signed), four elements per register, so the
+// products with the weight codes are dp4a instructions (3 per 4 weights):
+//   Q4_0: code n in 0..15 (nibbles unpacked with 1 LOP3 per 4),
+//         sum_j (n_j - 8) x_j = s * (65536 A + 256 B + C) - 8 sum_j x_j
+//   Q8_0: code q in -127..127,  sum_j q_j x_j = s * (65536 A + 256 B + C)
+// with A, B, C the int32 dp4a sums over the top, middle and low byte planes.
+// The block value is d * that, accumulated in fp32 per row.
+//
+// Every mbarrier wait is bounded; on a timeout the kernel records DEV_TIMEOUT
+// in its error word, drains its outstanding copies (bounded) and returns.
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace af {
 
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;
+constexpr int kMaxCtaRows = 512;  // residual rows a CTA may own (x preloaded to shared memory)
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
+
+
+
+
+
+__device__ __forceinline__ int dp4a_uu(unsigned a, unsigned b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_us(unsigned a, unsigned b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_ss(unsigned a, unsigned b, int c) {
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_su(unsigned a, unsigned b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
-    unsigned old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
-}
+// One lane's x values for one 16-byte weight unit, in 24-bit fixed point:
+// p[k][g] packs byte plane k (0 = low, 2 = signed top) of elements 4g..4g+3
+// of the unit (Q4_0: groups 0..3 are elements 0..15, groups 4..7 are 16..31).
+template <int G>
+struct XUnit {
+    unsigned p[3][G];
+    float s;    // fixed-point scale
+    float sx8;  // -8 * sum of the unit's x values (Q4_0 offset term)
+};
 
-__device__ __forceinline__ float ld_relaxed(const float* p) {
-    float v;
-    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-    return v;
+template <int UW>
+__device__ __forceinline__ void quantize_unit(const float (&xs)[UW], XUnit<UW / 4>& xu) {
+    float m = 0.f, sum = 0.f;
+#pragma unroll
+    for (int e = 0; e < UW; e++) {
+        m = fmaxf(m, fabsf(xs[e]));
+        sum += xs[e];
+    }
+    // power-of-two scale: m = f 2^E with f in [0.5, 1) gives |x| / s < 2^23 and s * xi exact
+    int E = 0;
+    frexpf(m, &E);
+    const float inv = m > 0.f ? ldexpf(1.f, 23 - E) : 0.f;
+    xu.s = m > 0.f ? ldexpf(1.f, E - 23) : 0.f;
+    xu.sx8 = -8.f * sum;
+#pragma unroll
+    for (int g = 0; g < UW / 4; g++) {
+        unsigned w0 = 0, w1 = 0, w2 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            int q = __float2int_rn(xs[4 * g + i] * inv);
+            q = max(-8388607, min(8388607, q));
+            const unsigned u = (unsigned)q;
+            w0 |= (u & 0xFFu) << (8 * i);
+            w1 |= ((u >> 8) & 0xFFu) << (8 * i);
+            w2 |= ((u >> 16) & 0xFFu) << (8 * i);
+        }
+        xu.p[0][g] = w0;
+        xu.p[1][g] = w1;
+        xu.p[2][g] = w2;
+    }
 }
 
 template <int WT>
@@ -58,197 +119,431 @@ struct Q;
 template <>
 struct Q<AF_Q4_0> {
     static constexpr int UW = 32;  // weights per 16-byte unit
-    static __device__ __forceinline__ float dot(uint4 q, const float* xv, float sx) {
+    // sum_j (n_j - 8) x_j over the block; byte j of the unit holds n_j (low) and n_{j+16} (high)
+    static __device__ __forceinline__ float dot(uint4 q, const XUnit<8>& x) {
         const unsigned w[4] = {q.x, q.y, q.z, q.w};
-        float s0 = 0.f, s1 = 0.f;
+        int A = 0, B = 0, C = 0;
 #pragma unroll
         for (int t = 0; t < 4; t++) {
             const unsigned lo = w[t] & 0x0F0F0F0Fu, hi = (w[t] >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-            for (int b = 0; b < 4; b++) {
-                const unsigned sel = 0x7044u | ((unsigned)b << 8);
-                s0 = fmaf(__uint_as_float(__byte_perm(lo, 0x3F000000u, sel)), xv[4 * t + b], s0);
-                s1 = fmaf(__uint_as_float(__byte_perm(hi, 0x3F000000u, sel)), xv[16 + 4 * t + b], s1);
-            }
+            A = dp4a_us(lo, x.p[2][t], A);
+            A = dp4a_us(hi, x.p[2][4 + t], A);
+            B = dp4a_uu(lo, x.p[1][t], B);
+            B = dp4a_uu(hi, x.p[1][4 + t], B);
+            C = dp4a_uu(lo, x.p[0][t], C);
+            C = dp4a_uu(hi, x.p[0][4 + t], C);
         }
-        return 256.f * (s0 + s1) - 136.f * sx;
+        // |256 A + B| < 2^24: both conversions are exact
+        const float v = fmaf(256.f, (float)(A * 256 + B), (float)C);
+        return fmaf(x.s, v, x.sx8);
     }
 };
 template <>
 struct Q<AF_Q8_0> {
     static constexpr int UW = 16;
-    static __device__ __forceinline__ float dot(uint4 q, const float* xv, float) {
-        const unsigned w[4] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u, q.z ^ 0x80808080u, q.w ^ 0x80808080u};
-        float s0 = 0.f, s1 = 0.f;
+    // sum_j q_j x_j over the half block
+    static __device__ __forceinline__ float dot(uint4 q, const XUnit<4>& x) {
+        const unsigned w[4] = {q.x, q.y, q.z, q.w};
+        int A = 0, B = 0, C = 0;
 #pragma unroll
         for (int t = 0; t < 4; t++) {
-#pragma unroll
-            for (int b = 0; b < 4; b += 2) {
-                const float q0 = __uint_as_float(__byte_perm(w[t], 0x4B000000u, 0x7440u | b)) - 8388736.f;
-                const float q1 = __uint_as_float(__byte_perm(w[t], 0x4B000000u, 0x7440u | (b + 1))) - 8388736.f;
-                s0 = fmaf(q0, xv[4 * t + b], s0);
-                s1 = fmaf(q1, xv[4 * t + b + 1], s1);
-            }
+            A = dp4a_ss(w[t], x.p[2][t], A);
+            B = dp4a_su(w[t], x.p[1][t], B);
+            C = dp4a_su(w[t], x.p[0][t], C);
         }
-        return s0 + s1;
+        const float v = fmaf(65536.f, (float)A, fmaf(256.f, (float)B, (float)C));
+        return x.s * v;
     }
 };
 
-// Reduce v[0..7] over the 32 lanes; afterwards lanes 4j..4j+3 hold sum of v[j].
-__device__ __forceinline__ float transpose_reduce8(float v[8], int lane) {
-    {
-        const bool up = lane & 16;
+// Reduce v[0..RW-1] over the 32 lanes; afterwards lanes (32/RW)*t .. hold the sum of v[t].
+template <int RW>
+__device__ __forceinline__ float transpose_reduce(float (&v)[RW], int lane) {
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const float send = up ? v[k] : v[k + 4], keep = up ? v[k + 4] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-        }
-    }
-    {
-        const bool up = lane & 8;
+    for (int half = RW / 2, bit = 16; half >= 1; half >>= 1, bit >>= 1) {
+        const bool up = lane & bit;
 #pragma unroll
-        for (int k = 0; k < 2; k++) {
-            const float send = up ? v[k] : v[k + 2], keep = up ? v[k + 2] : v[k];
-            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+        for (int k = 0; k < half; k++) {
+            const float send = up ? v[k] : v[k + half], keep = up ? v[k + half] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
         }
-    }
-    {
-        const bool up = lane & 4;
-        const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
-        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
     }
     float r = v[0];
-    r += __shfl_xor_sync(0xffffffffu, r, 2);
-    r += __shfl_xor_sync(0xffffffffu, r, 1);
+#pragma unroll
+    for (int bit = 16 / RW; bit >= 1; bit >>= 1) r += __shfl_xor_sync(0xffffffffu, r, bit);
     return r;
 }
 
-template <int WT, bool NORM>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+constexpr int kMaxRing = 8;
+constexpr int kRingBytes = 160 * 1024;  // stage ring budget (one CTA per SM)
+
+// Epilogue of the decode GEMV.  Everything it reads from global memory (the
+// residual rows of this CTA, the RoPE row of the position) was preloaded into
+// shared memory, so per-stage epilogues only store; the LM-head argmax is kept
+// per CTA in shared memory and published with one atomic at the end.
+struct GemvEpiCtx {
+    const float* xres;       // shared: x[r0 + i] for EPI_RESID
+    const float2* rope;      // shared: (cos, sin) of theta(pos, i) for EPI_QKV
+    int pos;
+    unsigned long long* amax;  // shared: CTA argmax key for EPI_LOGITS
+    int r0;
+};
+
+__device__ __forceinline__ void gemv_epi(const Epi& e, const GemvEpiCtx& c, int n, float v0, float v1) {
+    switch (e.kind) {
+        case EPI_STORE:
+            e.out[n] = v0;
+            e.out[n + 1] = v1;
+            break;
+        case EPI_RESID:
+            e.out[n] = c.xres[n - c.r0] + v0;
+            e.out[n + 1] = c.xres[n - c.r0 + 1] + v1;
+            break;
+        case EPI_SWIGLU:
+            e.out[n >> 1] = silu_f(v0) * v1;
+            break;
+        case EPI_LOGITS: {
+            e.out[n] = v0;
+            e.out[n + 1] = v1;
+            const unsigned long long k0 = argmax_key(v0, n), k1 = argmax_key(v1, n + 1);
+            atomicMax(c.amax, k0 > k1 ? k0 : k1);
+        } break;
+        case EPI_QKV: {
+            const int D = e.head_dim;
+            if (n < e.qd + e.kvd) {
+                const int d = (n < e.qd ? n : n - e.qd) % D;
+                const float2 cs = c.rope[d >> 1];
+                const float r0 = v0 * cs.x - v1 * cs.y, r1 = v0 * cs.y + v1 * cs.x;
+                v0 = r0;
+                v1 = r1;
+            }
+            if (n < e.qd) {
+                e.out[n] = v0;
+                e.out[n + 1] = v1;
+            } else {
+                const bool isk = n < e.qd + e.kvd;
+                const int cc = isk ? n - e.qd : n - e.qd - e.kvd;
+                const int64_t idx = ((int64_t)(cc / D) * e.max_ctx + c.pos) * D + cc % D;
+                void* base = isk ? e.kcache : e.vcache;
+                if (e.kv_f16)
+                    *reinterpret_cast<__half2*>((__half*)base + idx) = __floats2half2_rn(v0, v1);
+                else
+                    *reinterpret_cast<float2*>((float*)base + idx) = make_float2(v0, v1);
+            }
+        } break;
+    }
+}
+
+template <int WT, bool NORM, int R, int WK>
+__global__ void __launch_bounds__(kWarps * 32, 1)
     qgemv_kernel(Planes W, const float* __restrict__ x, const float* __restrict__ nw, float eps, Epi epi,
-                 float* __restrict__ part, unsigned* __restrict__ cnt) {
+                 int ring, unsigned* __restrict__ err) {
     constexpr int UW = Q<WT>::UW;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int RS = kWarps / WK;                 // row streams (rows j, j + RS, ... of a stage)
+    constexpr int RW = R / RS;                      // rows per warp per stage
+    constexpr int UPL = WT == AF_Q4_0 ? 2 : 4;      // chunk slots per warp (NC <= WK * UPL)
+    static_assert(RW >= 1 && RS * RW == R, "R must be a multiple of the row streams");
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint64_t full[kMaxRing];
+    __shared__ unsigned done_cnt[kMaxRing];    // warps finished with the slot's current stage
+    __shared__ unsigned issues[kMaxRing];      // copies issued into the slot so far
+    __shared__ float red[kMaxRing][kWarps][RW];
+    __shared__ float ssum[kWarps];
+    __shared__ float xres[kMaxCtaRows];
+    __shared__ float2 rope_s[64];
+    __shared__ unsigned long long amax_s;
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rs = warp / WK, wk = warp % WK;
     const int N = W.N, K = W.K;
     const int NC = W.Kp / (32 * UW);
+    const int64_t pitch = W.qs_pitch();
+    const int scp = W.sc_pitch();
+    const int qstage = R * (int)pitch;
+    const int stage_bytes = (qstage + R * scp * 2 + 127) & ~127;
+    const int np = N / 2;
+    const int pa = (int)((int64_t)np * blockIdx.x / gridDim.x), pb = (int)((int64_t)np * (blockIdx.x + 1) / gridDim.x);
+    const int r0 = 2 * pa, nrows = 2 * (pb - pa);
+    const int nst = (nrows + R - 1) / R;
+
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < ring; s++) {
+            mbar_init(&full[s], 1);
+            done_cnt[s] = 0;
+            issues[s] = 0;
+        }
+        abort_flag = 0;
+        amax_s = 0ull;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int st) {  // one thread: stage st (rows r0 + st*R ..) into its slot
+        const int slot = st % ring;
+        const int ra = r0 + st * R, nr = min(R, r0 + nrows - ra);
+        const unsigned qb = (unsigned)(nr * pitch), sb = (unsigned)(nr * scp * 2);
+        uint8_t* dst = smem + slot * stage_bytes;
+        issues[slot]++;
+        mbar_arrive_expect_tx(&full[slot], qb + sb);
+        bulk_g2s_evict_first(dst, W.qs + (int64_t)ra * pitch, qb, &full[slot], pol);
+        bulk_g2s_evict_first(dst + qstage, W.sc + (int64_t)ra * scp, sb, &full[slot], pol);
+    };
+    if (tid == 0)
+        for (int st = 0; st < min(nst, ring); st++) issue(st);
+
+    pdl_wait();  // x (and the residual rows) are written by the previous kernel
 
     float rstd = 1.f;
     if (NORM) {  // RMSNorm prologue: every CTA reduces sum(x^2) over the whole input
-        __shared__ float red[kWarps];
         float ss = 0.f;
         const float4* x4 = reinterpret_cast<const float4*>(x);
-        for (int k = threadIdx.x; k < K / 4; k += blockDim.x) {
-            const float4 v = x4[k];
+        for (int k4 = tid; k4 < K / 4; k4 += kWarps * 32) {
+            const float4 v = x4[k4];
             ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
         }
         for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) red[warp] = ss;
-        __syncthreads();
+        if (lane == 0) ssum[warp] = ss;
+    }
+    // epilogue inputs into shared memory
+    if (epi.kind == EPI_RESID)
+        for (int i = tid; i < nrows; i += kWarps * 32) xres[i] = epi.out[r0 + i];
+    GemvEpiCtx ectx;
+    ectx.xres = xres;
+    ectx.rope = rope_s;
+    ectx.amax = &amax_s;
+    ectx.r0 = r0;
+    ectx.pos = 0;
+    if (epi.kind == EPI_QKV) {
+        ectx.pos = epi.pos_dev ? *epi.pos_dev : epi.pos0;
+        for (int i = tid; i < epi.head_dim / 2; i += kWarps * 32)
+            rope_s[i] = epi.rope[(int64_t)ectx.pos * (epi.head_dim / 2) + i];
+    }
+    __syncthreads();
+    if (NORM) {
         float t = 0.f;
 #pragma unroll
-        for (int i = 0; i < kWarps; i++) t += red[i];
+        for (int i = 0; i < kWarps; i++) t += ssum[i];
         rstd = rsqrtf(t / (float)K + eps);
     }
 
-    const int64_t T = (int64_t)NC * N;
-    const int64_t Wt = (int64_t)gridDim.x * kWarps, wg = (int64_t)blockIdx.x * kWarps + warp;
-    const int64_t i0 = T * wg / Wt, i1 = T * (wg + 1) / Wt;
-    const int64_t pitch = W.qs_pitch();
-    const int scp = W.sc_pitch();
-
-    float xv[UW];
-    float sx = 0.f;
-    int cur_c = -1;
-    for (int64_t i = i0; i < i1;) {
-        const int c = (int)(i / N);
-        const int r = (int)(i - (int64_t)c * N);
-        int rows = N - r;
-        if (rows > 8) rows = 8;
-        if ((int64_t)rows > i1 - i) rows = (int)(i1 - i);
-        const int unit = c * 32 + lane;  // this lane's unit within the row
-        if (c != cur_c) {                // (re)load the x slice for this chunk
-            const int k0 = unit * UW;
-            sx = 0.f;
-            if (k0 < K) {
-                const float4* xp = reinterpret_cast<const float4*>(x + k0);
+    // this lane's x slices (chunk wk + WK*u, unit lane) in 24-bit fixed point
+    XUnit<UW / 4> xq[UPL];
 #pragma unroll
-                for (int e = 0; e < UW / 4; e++) {
-                    float4 v = xp[e];
-                    if (NORM) {
-                        const float4 g = reinterpret_cast<const float4*>(nw + k0)[e];
-                        v.x = g.x * (v.x * rstd);
-                        v.y = g.y * (v.y * rstd);
-                        v.z = g.z * (v.z * rstd);
-                        v.w = g.w * (v.w * rstd);
-                    }
-                    xv[4 * e] = v.x;
-                    xv[4 * e + 1] = v.y;
-                    xv[4 * e + 2] = v.z;
-                    xv[4 * e + 3] = v.w;
+    for (int u = 0; u < UPL; u++) {
+        const int c = wk + WK * u;
+        const int k0 = (c * 32 + lane) * UW;
+        float xs[UW];
+        if (c < NC && k0 < K) {
+#pragma unroll
+            for (int e = 0; e < UW; e += 4) {
+                float4 v = *reinterpret_cast<const float4*>(x + k0 + e);
+                if (NORM) {
+                    const float4 g = *reinterpret_cast<const float4*>(nw + k0 + e);
+                    v = make_float4(g.x * (v.x * rstd), g.y * (v.y * rstd), g.z * (v.z * rstd), g.w * (v.w * rstd));
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < UW; e++) xv[e] = 0.f;
+                xs[e] = v.x;
+                xs[e + 1] = v.y;
+                xs[e + 2] = v.z;
+                xs[e + 3] = v.w;
             }
+        } else {
 #pragma unroll
-            for (int e = 0; e < UW; e++) sx += xv[e];
-            cur_c = c;
+            for (int e = 0; e < UW; e++) xs[e] = 0.f;
         }
-        const uint8_t* qrow = W.qs + (int64_t)r * pitch + (int64_t)unit * 16;
-        const __half* srow = W.sc + (int64_t)r * scp + (WT == AF_Q8_0 ? unit >> 1 : unit);
-        uint4 q[8];
-        float d[8];
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            if (j < rows) {
-                q[j] = ld_stream(qrow + (int64_t)j * pitch);
-                d[j] = __half2float(srow[(int64_t)j * scp]);
-            }
-        }
-        float v[8];
-#pragma unroll
-        for (int j = 0; j < 8; j++) v[j] = (j < rows) ? d[j] * Q<WT>::dot(q[j], xv, sx) : 0.f;
-        const float s = transpose_reduce8(v, lane);
-        const int jr = lane >> 2;
-        if ((lane & 3) == 0 && jr < rows) {
-            const int row = r + jr;
-            part[(int64_t)c * N + row] = s;
-            const unsigned old = atom_add_acq_rel(&cnt[row >> 1], 1u);
-            if (old == 2u * (unsigned)NC - 1u) {  // this lane completed the pair
-                const int r0 = row & ~1;
-                float y0 = 0.f, y1 = 0.f;
-                for (int cc = 0; cc < NC; cc++) {
-                    y0 += ld_relaxed(part + (int64_t)cc * N + r0);
-                    y1 += ld_relaxed(part + (int64_t)cc * N + r0 + 1);
-                }
-                epi_pair(epi, 0, r0, y0, y1);
-                cnt[row >> 1] = 0u;
-            }
-        }
-        i += rows;
+        quantize_unit<UW>(xs, xq[u]);
     }
+
+    // main loop: warps run independently; the last warp to finish a stage combines
+    // the row partials, applies the epilogue and refills the slot
+    for (int st = 0; st < nst; st++) {
+        const int slot = st % ring;
+        const unsigned par = (unsigned)((st / ring) & 1);
+        bool ok = false;
+        for (unsigned it = 0; it < kWaitLimit && !ok; it++) {
+            ok = mbar_try_wait(&full[slot], par);
+            if (!ok && abort_flag) break;
+        }
+        if (!ok) {
+            if (lane == 0) {
+                abort_flag = 1;
+                atomicExch(err, (unsigned)DEV_TIMEOUT);
+            }
+            break;
+        }
+        const uint8_t* qsm = smem + slot * stage_bytes;
+        const unsigned short* ssm = reinterpret_cast<const unsigned short*>(qsm + qstage);
+        const int ra = r0 + st * R, nr = min(R, r0 + nrows - ra);
+        float acc[RW];
+#pragma unroll
+        for (int t = 0; t < RW; t++) {
+            const int j = rs + RS * t;
+            acc[t] = 0.f;
+            if (j < nr) {
+#pragma unroll
+                for (int u = 0; u < UPL; u++) {
+                    const int c = wk + WK * u;
+                    if (c < NC) {
+                        const int unit = c * 32 + lane;
+                        const uint4 q = *reinterpret_cast<const uint4*>(qsm + j * pitch + unit * 16);
+                        const float d = __half2float(__ushort_as_half(ssm[j * scp + (WT == AF_Q8_0 ? unit >> 1 : unit)]));
+                        acc[t] = fmaf(d, Q<WT>::dot(q, xq[u]), acc[t]);
+                    }
+                }
+            }
+        }
+        const float r = transpose_reduce<RW>(acc, lane);
+        if ((lane & (32 / RW - 1)) == 0) red[slot][warp][lane / (32 / RW)] = r;
+        __syncwarp();
+        unsigned last = 0;
+        if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&done_cnt[slot], 1u) == (unsigned)kWarps - 1u;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {  // every warp is done with this slot
+            __threadfence_block();
+            if (lane < nr / 2) {  // rows (2 lane, 2 lane + 1) of the stage
+                float y[2];
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int j = 2 * lane + h, jrs = j % RS, jt = j / RS;
+                    float a = 0.f;
+#pragma unroll
+                    for (int w = 0; w < WK; w++) a += red[slot][jrs * WK + w][jt];
+                    y[h] = a;
+                }
+                gemv_epi(epi, ectx, ra + 2 * lane, y[0], y[1]);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                done_cnt[slot] = 0;
+                if (st + ring < nst) {
+                    fence_proxy_async_shared();
+                    issue(st + ring);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (abort_flag) {  // drain every copy still in flight before the CTA exits
+        if (tid == 0)
+            for (int s = 0; s < ring; s++)
+                if (issues[s]) mbar_wait_bounded(&full[s], (issues[s] - 1u) & 1u);
+        __syncthreads();
+        return;
+    }
+    if (epi.kind == EPI_LOGITS && tid == 0 && amax_s) atomicMax(epi.argmax, amax_s);
+}
+
+struct Shape {
+    int R, WK, ring, stage_bytes;
+};
+
+Shape pick_shape(const Planes& W) {
+    const int UW = W.wtype == AF_Q8_0 ? 16 : 32;
+    const int NC = W.Kp / (32 * UW);
+    Shape s;
+    s.WK = NC >= 8 ? 8 : (NC > 4 ? 8 : (NC > 2 ? 4 : NC));
+    const int RS = kWarps / s.WK;
+    const int row_bytes = (int)W.qs_pitch() + W.sc_pitch() * 2;
+    s.R = 32;
+    while (s.R > RS && s.R * row_bytes > 40 * 1024) s.R /= 2;
+    s.stage_bytes = (s.R * (int)W.qs_pitch() + s.R * W.sc_pitch() * 2 + 127) & ~127;
+    s.ring = kRingBytes / s.stage_bytes;
+    s.ring = s.ring < 2 ? 2 : (s.ring > kMaxRing ? kMaxRing : s.ring);
+    return s;
+}
+
+template <int WT, bool NORM, int R, int WK>
+cudaError_t launch_t(const Planes& W, const float* x, const float* nw, float eps, const Epi& epi, const Shape& sh,
+                     unsigned* err, cudaStream_t s) {
+    auto kern = qgemv_kernel<WT, NORM, R, WK>;
+    const size_t smem = (size_t)sh.ring * sh.stage_bytes;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms());
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, W, x, nw, eps, epi, sh.ring, err);
+}
+
+template <int WT, bool NORM>
+cudaError_t dispatch(const Planes& W, const float* x, const float* nw, float eps, const Epi& epi, unsigned* err,
+                     cudaStream_t s) {
+    const Shape sh = pick_shape(W);
+#define AF_GEMV_CASE(RR, WW) \
+    if (sh.R == RR && sh.WK == WW) return launch_t<WT, NORM, RR, WW>(W, x, nw, eps, epi, sh, err, s);
+    AF_GEMV_CASE(16, 1)
+    AF_GEMV_CASE(32, 1)
+    AF_GEMV_CASE(8, 2)
+    AF_GEMV_CASE(16, 2)
+    AF_GEMV_CASE(32, 2)
+    AF_GEMV_CASE(4, 4)
+    AF_GEMV_CASE(8, 4)
+    AF_GEMV_CASE(16, 4)
+    AF_GEMV_CASE(32, 4)
+    AF_GEMV_CASE(2, 8)
+    AF_GEMV_CASE(4, 8)
+    AF_GEMV_CASE(8, 8)
+    AF_GEMV_CASE(16, 8)
+    AF_GEMV_CASE(32, 8)
+#undef AF_GEMV_CASE
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-size_t qgemv_part_elems(const Planes& W) { return (size_t)(W.Kp / chunk_weights(W.wtype)) * (size_t)W.N; }
+cudaError_t qgemv_prepare() {
+    // every instantiation may use up to kRingBytes of dynamic shared memory (its stage ring); done once,
+    // outside any stream capture
+    static bool done = false;
+    if (done) return cudaSuccess;
+    const int smem = kRingBytes;
+    cudaError_t e = cudaSuccess;
+#define AF_GEMV_ATTR(WT, NORM, RR, WW) \
+    if (!e) e = cudaFuncSetAttribute(qgemv_kernel<WT, NORM, RR, WW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+#define AF_GEMV_ATTR4(RR, WW)                 \
+    AF_GEMV_ATTR(AF_Q4_0, true, RR, WW)       \
+    AF_GEMV_ATTR(AF_Q4_0, false, RR, WW)      \
+    AF_GEMV_ATTR(AF_Q8_0, true, RR, WW)       \
+    AF_GEMV_ATTR(AF_Q8_0, false, RR, WW)
+    AF_GEMV_ATTR4(16, 1)
+    AF_GEMV_ATTR4(32, 1)
+    AF_GEMV_ATTR4(8, 2)
+    AF_GEMV_ATTR4(16, 2)
+    AF_GEMV_ATTR4(32, 2)
+    AF_GEMV_ATTR4(4, 4)
+    AF_GEMV_ATTR4(8, 4)
+    AF_GEMV_ATTR4(16, 4)
+    AF_GEMV_ATTR4(32, 4)
+    AF_GEMV_ATTR4(2, 8)
+    AF_GEMV_ATTR4(4, 8)
+    AF_GEMV_ATTR4(8, 8)
+    AF_GEMV_ATTR4(16, 8)
+    AF_GEMV_ATTR4(32, 8)
+#undef AF_GEMV_ATTR4
+#undef AF_GEMV_ATTR
+    if (!e) done = true;
+    return e;
+}
+
+int qgemv_max_chunks() { return 32; }
+
 
 cudaError_t launch_qgemv(const Planes& W, const float* x, const float* norm_w, float eps, const Epi& epi,
                          const GemvScratch& scr, cudaStream_t s) {
-    const int grid = 2 * num_sms();
-    const int threads = kWarps * 32;
-    if (W.wtype == AF_Q4_0) {
-        if (norm_w)
-            qgemv_kernel<AF_Q4_0, true><<<grid, threads, 0, s>>>(W, x, norm_w, eps, epi, scr.part, scr.cnt);
-        else
-            qgemv_kernel<AF_Q4_0, false><<<grid, threads, 0, s>>>(W, x, norm_w, eps, epi, scr.part, scr.cnt);
-    } else {
-        if (norm_w)
-            qgemv_kernel<AF_Q8_0, true><<<grid, threads, 0, s>>>(W, x, norm_w, eps, epi, scr.part, scr.cnt);
-        else
-            qgemv_kernel<AF_Q8_0, false><<<grid, threads, 0, s>>>(W, x, norm_w, eps, epi, scr.part, scr.cnt);
-    }
-    return cudaGetLastError();
+    if (W.wtype == AF_Q4_0)
+        return norm_w ? dispatch<AF_Q4_0, true>(W, x, norm_w, eps, epi, scr.err, s)
+                      : dispatch<AF_Q4_0, false>(W, x, norm_w, eps, epi, scr.err, s);
+    return norm_w ? dispatch<AF_Q8_0, true>(W, x, norm_w, eps, epi, scr.err, s)
+                  : dispatch<AF_Q8_0, false>(W, x, norm_w, eps, epi, scr.err, s);
 }
 
 }  // namespace af

@@ -159,8 +159,9 @@ int af_set_decode_graph(af_model* m, int enable);
 void af_model_destroy(af_model* m);
 
 /*
- * Standalone quantized matmuls (north-star "af_qgemv / af_qgemm").
- * af_qweight_create repacks a [N, K] block matrix (N even, K % 64 == 0) into
+ * Standalone quantized matmuls.
+ * af_qweight_create repacks a [N, K] block matrix (N even, K % 32 == 0,
+ * K <= 32768 for Q4_0 and <= 16384 for Q8_0, else AF_ENOTIMPL) into
  * its own device memory (and scratch for the GEMV); synchronises `stream`.
  *   af_qgemv: y[i]    = sum_j W[i][j] x[j]        x_dev fp32 [K], y_dev fp32 [N]
  *   af_qgemm: Y[m][i] = sum_j X[m][j] W[i][j]     X_dev fp32 [M, K] row-major,
