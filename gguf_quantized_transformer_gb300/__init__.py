@@ -60,11 +60,15 @@ def lib():
         L.af_model_next_token_dev.argtypes = [vp]
         L.af_model_next_token_dev.restype = vp
         L.af_reset.argtypes = [vp]
+        L.af_model_sync.argtypes = [vp, vp]
         L.af_model_kv_cache.argtypes = [vp, P(vp), P(vp)]
         L.af_model_stream.argtypes = [vp]
         L.af_model_stream.restype = vp
         L.af_debug_capture.argtypes = [vp, vp]
+        L.af_debug_trace.argtypes = [vp, vp]
         L.af_set_decode_graph.argtypes = [vp, ctypes.c_int]
+        L.af_set_decode_mode.argtypes = [vp, ctypes.c_int]
+        L.af_get_decode_mode.argtypes = [vp]
         L.af_model_destroy.argtypes = [vp]
         L.af_model_destroy.restype = None
         L.af_qweight_create.argtypes = [i32, vp, i32, i32, vp, P(vp)]
@@ -145,6 +149,12 @@ def af_model_next_token_dev(m) -> int:
     return lib().af_model_next_token_dev(m)
 
 
+def af_model_sync(m, want_next: bool = False):
+    nxt = ctypes.c_int32(-1)
+    check(lib().af_model_sync(m, ctypes.byref(nxt) if want_next else None))
+    return nxt.value if want_next else None
+
+
 def af_model_stream(m) -> int:
     return lib().af_model_stream(m) or 0
 
@@ -161,6 +171,21 @@ def af_reset(m):
 
 def af_debug_capture(m, hidden_dev):
     return check(lib().af_debug_capture(m, _ptr(hidden_dev)))
+
+
+AF_DECODE_PERSISTENT, AF_DECODE_KERNELS = 0, 1
+
+
+def af_set_decode_mode(m, mode: int):
+    return check(lib().af_set_decode_mode(m, mode))
+
+
+def af_get_decode_mode(m) -> int:
+    return lib().af_get_decode_mode(m)
+
+
+def af_debug_trace(m, trace_dev):
+    return check(lib().af_debug_trace(m, _ptr(trace_dev)))
 
 
 def af_set_decode_graph(m, enable: bool):

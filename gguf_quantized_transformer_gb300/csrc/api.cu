@@ -92,6 +92,14 @@ struct LayerW {
     const float* ffn_norm = nullptr;
 };
 
+Epi epi_simple(int kind, float* out, int ld) {
+    Epi e;
+    e.kind = kind;
+    e.out = out;
+    e.ld = ld;
+    return e;
+}
+
 int check_config(const af_config* c) {
     if (!c) return fail(AF_EINVAL, "null config");
     if (c->wtype != AF_Q4_0 && c->wtype != AF_Q8_0) return fail(AF_EINVAL, "wtype must be AF_Q4_0 or AF_Q8_0");
@@ -144,7 +152,12 @@ struct af_model {
     AttnScratch as;
     StepState* st = nullptr;
     float* capture = nullptr;
+    unsigned long long* trace = nullptr;
     bool use_graph = true;
+    int decode_mode = AF_DECODE_KERNELS;
+    DecodePlan dplan;
+    LayerPlan* d_layers = nullptr;
+    bool persistent_ok = false;
     cudaGraphExec_t gexec = nullptr;
     float* graph_logits = nullptr;
     unsigned err_host = 0;
@@ -155,6 +168,24 @@ struct af_model {
     void* kl(int l) const { return (char*)kc + (size_t)l * kv_layer_elems * (c.kv_dtype == AF_F16 ? 2 : 4); }
     void* vl(int l) const { return (char*)vc + (size_t)l * kv_layer_elems * (c.kv_dtype == AF_F16 ? 2 : 4); }
 };
+
+namespace {
+Epi epi_qkv_plan(af_model* m, int l) {
+    Epi e;
+    e.kind = EPI_QKV;
+    e.out = m->q;
+    e.ld = m->QD();
+    e.qd = m->QD();
+    e.kvd = m->KVD();
+    e.head_dim = m->c.head_dim;
+    e.max_ctx = m->c.max_ctx;
+    e.kv_f16 = m->c.kv_dtype == AF_F16;
+    e.kcache = m->kl(l);
+    e.vcache = m->vl(l);
+    e.rope = m->rope;
+    return e;
+}
+}  // namespace
 
 struct af_qweight {
     Planes p;
@@ -310,12 +341,74 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     m->logits = (float*)A.get((size_t)V * 4);
     m->st = (StepState*)A.get(sizeof(StepState));
     m->gs.err = (unsigned*)A.get(sizeof(unsigned));
-    m->as.ns = attn_decode_splits(c.n_kv_heads);
+    m->as.ns = std::max(attn_decode_splits(c.n_kv_heads), decode_attn_splits(c.n_kv_heads));
     m->as.part = (float*)A.get(attn_decode_part_elems(c.n_heads, D, m->as.ns) * 4);
     m->as.cnt = (unsigned*)A.get((size_t)c.n_kv_heads * 4);
     if (!m->x || !m->q || !m->attn || !m->h || !m->y || !m->a || !m->hp || !m->tok || !m->logits || !m->st ||
         !m->gs.err || !m->as.part || !m->as.cnt)
         return oom("activations");
+    // persistent decode plan: per-layer GEMV tasks on the device, barrier words
+    unsigned* words = (unsigned*)A.get(4 * sizeof(unsigned));
+    m->d_layers = (LayerPlan*)A.get(sizeof(LayerPlan) * c.n_layers);
+    if (!words || !m->d_layers) return oom("decode plan");
+    {
+        DecodePlan& P = m->dplan;
+        P.wtype = wt;
+        P.n_layers = c.n_layers;
+        P.H = c.n_heads;
+        P.KVH = c.n_kv_heads;
+        P.D = D;
+        P.max_ctx = c.max_ctx;
+        P.kv_f16 = c.kv_dtype == AF_F16;
+        P.attn_splits = std::min(decode_attn_splits(c.n_kv_heads), 1216 / (c.n_heads / c.n_kv_heads));
+        P.eps = c.rms_eps;
+        P.layers = m->d_layers;
+        P.emb = m->emb;
+        P.x = m->x;
+        P.q = m->q;
+        P.attn = m->attn;
+        P.attn_part = m->as.part;
+        P.attn_cnt = m->as.cnt;
+        P.st = m->st;
+        P.bar_count = words;
+        P.bar_gen = words + 1;
+        P.abort = words + 2;
+        P.err = m->gs.err;
+        std::vector<LayerPlan> lp(c.n_layers);
+        bool ok = true;
+        for (int l = 0; l < c.n_layers; l++) {
+            const LayerW& lw = m->L[l];
+            LayerPlan& L = lp[l];
+            ok = ok && decode_gemv_task(lw.qkv, L.qkv) && decode_gemv_task(lw.o, L.o) &&
+                 decode_gemv_task(lw.gu, L.gu) && decode_gemv_task(lw.down, L.down);
+            L.kc = m->kl(l);
+            L.vc = m->vl(l);
+            L.qkv.x = m->x;
+            L.qkv.nw = lw.attn_norm;
+            L.qkv.epi = epi_qkv_plan(m, l);
+            L.o.x = m->attn;
+            L.o.epi = epi_simple(EPI_RESID, m->x, E);
+            L.gu.x = m->x;
+            L.gu.nw = lw.ffn_norm;
+            L.gu.epi = epi_simple(EPI_SWIGLU, m->h, F);
+            L.down.x = m->h;
+            L.down.epi = epi_simple(EPI_RESID, m->x, E);
+        }
+        ok = ok && decode_gemv_task(m->out, P.head);
+        P.head.x = m->x;
+        P.head.nw = m->out_norm;
+        P.head.epi = epi_simple(EPI_LOGITS, m->logits, 0);
+        P.head.epi.argmax = &m->st->argmax;
+        m->persistent_ok = ok && E / num_sms() + 2 <= decode_max_cta_rows() && E <= 4096;
+        cudaError_t e = cudaMemcpyAsync(m->d_layers, lp.data(), sizeof(LayerPlan) * c.n_layers, cudaMemcpyHostToDevice, s);
+        if (!e) e = cudaMemsetAsync(words, 0, 4 * sizeof(unsigned), s);
+        if (!e) e = cudaStreamSynchronize(s);  // lp is a host temporary
+        if (e) return cuda_fail(e, "decode plan");
+        if (m->persistent_ok && decode_prepare(P) != cudaSuccess) {
+            cudaGetLastError();
+            m->persistent_ok = false;  // cannot be resident on this device
+        }
+    }
     {
         cudaError_t e = qgemv_prepare();
         if (!e) e = cudaMemsetAsync(m->gs.err, 0, sizeof(unsigned), s);
@@ -331,6 +424,15 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
 void* af_model_stream(const af_model* m) { return m ? (void*)m->s : nullptr; }
 
 const int32_t* af_model_next_token_dev(const af_model* m) { return m ? &m->st->next_token : nullptr; }
+
+int af_model_sync(af_model* m, int32_t* next_token_host) {
+    if (!m) return fail(AF_EINVAL, "null model");
+    if (next_token_host) CK(cudaMemcpyAsync(next_token_host, &m->st->next_token, 4, cudaMemcpyDeviceToHost, m->s));
+    CK(cudaMemcpyAsync(&m->err_host, m->gs.err, 4, cudaMemcpyDeviceToHost, m->s));
+    CK(cudaStreamSynchronize(m->s));
+    if (m->err_host) return fail(AF_ETIMEOUT, "a bounded device-side wait gave up (code %u)", m->err_host);
+    return AF_OK;
+}
 
 int af_model_kv_cache(const af_model* m, void** k_dev, void** v_dev) {
     if (!m || !k_dev || !v_dev) return fail(AF_EINVAL, "null argument");
@@ -352,6 +454,23 @@ int af_debug_capture(af_model* m, float* hidden_dev) {
     m->capture = hidden_dev;
     return AF_OK;
 }
+
+int af_debug_trace(af_model* m, uint64_t* trace_dev) {
+    if (!m || !trace_dev) return fail(AF_EINVAL, "null argument");
+    m->trace = reinterpret_cast<unsigned long long*>(trace_dev);
+    return AF_OK;
+}
+
+int af_set_decode_mode(af_model* m, int mode) {
+    if (!m) return fail(AF_EINVAL, "null model");
+    if (mode != AF_DECODE_PERSISTENT && mode != AF_DECODE_KERNELS) return fail(AF_EINVAL, "bad decode mode");
+    if (mode == AF_DECODE_PERSISTENT && !m->persistent_ok)
+        return fail(AF_ENOTIMPL, "persistent decode kernel not available for this device/shape");
+    m->decode_mode = mode;
+    return AF_OK;
+}
+
+int af_get_decode_mode(const af_model* m) { return m ? m->decode_mode : -1; }
 
 int af_set_decode_graph(af_model* m, int enable) {
     if (!m) return fail(AF_EINVAL, "null model");
@@ -386,14 +505,6 @@ Epi epi_qkv(af_model* m, int l, float* qout, __half* q16, const int* pos_dev, in
     e.rope = m->rope;
     e.pos_dev = pos_dev;
     e.pos0 = pos0;
-    return e;
-}
-
-Epi epi_simple(int kind, float* out, int ld) {
-    Epi e;
-    e.kind = kind;
-    e.out = out;
-    e.ld = ld;
     return e;
 }
 
@@ -485,8 +596,17 @@ int af_decode_step(af_model* m, int32_t token, int32_t pos, float* logits_dev, i
     if (pos < 0 || pos >= m->c.max_ctx) return fail(AF_ERANGE, "pos %d outside [0, %d)", pos, m->c.max_ctx);
     if (token < -1 || token >= m->c.n_vocab) return fail(AF_ERANGE, "token %d outside [-1, %d)", token, m->c.n_vocab);
     float* logits = logits_dev ? logits_dev : m->logits;
-    CK(launch_step_begin(m->st, token, pos, m->s));
-    if (m->use_graph && !m->capture) {
+    CK(launch_step_begin(m->st, token, pos, m->s, m->dplan.bar_count));
+    if (m->decode_mode == AF_DECODE_PERSISTENT) {
+        DecodePlan P = m->dplan;
+        P.head.epi.out = logits;
+        P.capture = m->capture;
+        P.trace = m->trace;
+        m->capture = nullptr;
+        m->trace = nullptr;
+        CK(launch_decode(P, m->s));
+        CK(launch_step_end(m->st, m->s));
+    } else if (m->use_graph && !m->capture) {
         if (!m->gexec || m->graph_logits != logits) {
             if (m->gexec) {
                 cudaGraphExecDestroy(m->gexec);

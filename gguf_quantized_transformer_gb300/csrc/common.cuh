@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/af.h"
+#include "af.h"  // include/ (passed with -I by the build)
 
 namespace af {
 
@@ -169,6 +169,50 @@ cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, con
                                 int64_t ldo, cudaStream_t s);
 bool attn_supported(int H, int KVH, int D);
 
+// One GEMV of the persistent decode kernel: matrix, input, optional RMSNorm
+// weight, stage shape (R rows per ring slot, WK warps along K) and epilogue.
+struct GemvTask {
+    Planes W;
+    const float* x = nullptr;
+    const float* nw = nullptr;
+    int R = 0, WK = 0;
+    Epi epi;
+};
+
+struct LayerPlan {
+    GemvTask qkv, o, gu, down;
+    void* kc = nullptr;  // this layer's K cache [KVH][max_ctx][D]
+    void* vc = nullptr;
+};
+
+struct StepState;
+
+struct DecodePlan {
+    int wtype = 0, n_layers = 0, H = 0, KVH = 0, D = 0, max_ctx = 0, kv_f16 = 0, attn_splits = 0;
+    float eps = 0.f;
+    const LayerPlan* layers = nullptr;  // device array [n_layers]
+    Planes emb;
+    GemvTask head;
+    float* x = nullptr;
+    float* q = nullptr;
+    float* attn = nullptr;
+    float* attn_part = nullptr;  // [KVH][splits][G][D+2]
+    unsigned* attn_cnt = nullptr;  // [KVH], zero between steps
+    StepState* st = nullptr;
+    unsigned* bar_count = nullptr;  // grid barrier (zero-initialised)
+    unsigned* bar_gen = nullptr;
+    unsigned* abort = nullptr;      // raised by a CTA that timed out
+    unsigned* err = nullptr;        // DEV_* code
+    float* capture = nullptr;       // optional [n_layers+1][E] residual stream after embed / each layer
+    unsigned long long* trace = nullptr;  // optional [2 + 5 n_layers + 1] %globaltimer at phase boundaries (CTA 0)
+};
+
+bool decode_gemv_task(const Planes& W, GemvTask& t);
+int decode_attn_splits(int n_kv_heads);
+int decode_max_cta_rows();
+cudaError_t decode_prepare(const DecodePlan& p);
+cudaError_t launch_decode(const DecodePlan& p, cudaStream_t s);
+
 // Decode-step bookkeeping
 struct StepState {
     int token;  // token of this step
@@ -177,7 +221,7 @@ struct StepState {
     int next_token;
     int pad;
 };
-cudaError_t launch_step_begin(StepState* st, int token, int pos, cudaStream_t s);
+cudaError_t launch_step_begin(StepState* st, int token, int pos, cudaStream_t s, unsigned* bar_count = nullptr);
 cudaError_t launch_step_end(StepState* st, cudaStream_t s);
 
 }  // namespace af

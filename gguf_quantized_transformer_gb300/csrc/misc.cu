@@ -137,10 +137,11 @@ cudaError_t launch_f32_to_f16(const float* x, __half* y, int64_t n, cudaStream_t
     return cudaGetLastError();
 }
 
-__global__ void step_begin_kernel(StepState* st, int token, int pos) {
+__global__ void step_begin_kernel(StepState* st, int token, int pos, unsigned* bar_count) {
     st->token = token >= 0 ? token : st->next_token;
     st->pos = pos;
     st->argmax = 0ull;
+    if (bar_count) *bar_count = 0u;  // grid barrier of the persistent decode kernel starts over
 }
 
 __global__ void step_end_kernel(StepState* st) {
@@ -148,8 +149,8 @@ __global__ void step_end_kernel(StepState* st) {
     st->next_token = st->argmax ? (int)(0xFFFFFFFFu - (unsigned)(st->argmax & 0xFFFFFFFFull)) : 0;
 }
 
-cudaError_t launch_step_begin(StepState* st, int token, int pos, cudaStream_t s) {
-    step_begin_kernel<<<1, 1, 0, s>>>(st, token, pos);
+cudaError_t launch_step_begin(StepState* st, int token, int pos, cudaStream_t s, unsigned* bar_count) {
+    step_begin_kernel<<<1, 1, 0, s>>>(st, token, pos, bar_count);
     return cudaGetLastError();
 }
 

@@ -135,6 +135,11 @@ int af_prefill_dev(af_model* m, const int32_t* tokens_dev, int32_t n, int32_t st
  */
 int af_decode_step(af_model* m, int32_t token, int32_t pos, float* logits_dev, int32_t* next_token_host);
 
+/* Synchronise the model's stream.  Returns AF_ETIMEOUT if a bounded device-side
+ * wait of an earlier call gave up, else AF_OK; if next_token_host is not NULL it
+ * receives the greedy token of the last call that produced logits. */
+int af_model_sync(af_model* m, int32_t* next_token_host);
+
 /* Greedy token of the last af_decode_step / af_prefill with logits (device int32, valid after the stream). */
 const int32_t* af_model_next_token_dev(const af_model* m);
 
@@ -153,8 +158,27 @@ void* af_model_stream(const af_model* m);
  * (n = that call's token count).  One-shot; test instrumentation. */
 int af_debug_capture(af_model* m, float* hidden_dev);
 
-/* Use (1) or stop using (0) a CUDA graph for af_decode_step (default 1). */
+/*
+ * How af_decode_step runs (both are this library's CUDA kernels):
+ *   AF_DECODE_KERNELS (default): one launch per matrix / attention, chained
+ *     with programmatic dependent launch and replayed as a CUDA graph (see
+ *     af_set_decode_graph).
+ *   AF_DECODE_PERSISTENT: one cooperative launch per token, one CTA per SM,
+ *     all layers separated by bounded grid barriers, the weights of the next
+ *     matrix streaming into shared memory while the grid synchronises
+ *     (n_embd <= 4096; AF_ENOTIMPL where it cannot be resident).
+ */
+enum { AF_DECODE_PERSISTENT = 0, AF_DECODE_KERNELS = 1 };
+int af_set_decode_mode(af_model* m, int mode);
+int af_get_decode_mode(const af_model* m);
+
+/* In AF_DECODE_KERNELS mode, use (1) or stop using (0) a CUDA graph (default 1). */
 int af_set_decode_graph(af_model* m, int enable);
+
+/* Trace the next persistent af_decode_step: trace_dev (device, uint64 [5 n_layers + 3])
+ * receives the GPU global timer (ns) at kernel start, after the embedding, after each
+ * of the 5 phases of every layer, and at the end.  One-shot; profiling aid. */
+int af_debug_trace(af_model* m, uint64_t* trace_dev);
 
 void af_model_destroy(af_model* m);
 

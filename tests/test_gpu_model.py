@@ -179,6 +179,7 @@ def test_decode_graph_matches_direct_launch(af, tiny):
     outs = []
     for graph in (True, False):
         m = gpu_model(tiny)
+        af.af_set_decode_mode(m.h, af.AF_DECODE_KERNELS)
         af.af_set_decode_graph(m.h, graph)
         m.prefill(prompt, 0)
         lg = torch.empty(V, device="cuda")
@@ -211,4 +212,61 @@ def test_model_errors(af, tiny):
     # the model still works after rejected calls
     m.prefill(tiny.prompt()[:4], 0)
     assert 0 <= m.decode(0, 4, want_next=True) < cfg.n_vocab
+    m.close()
+
+
+@pytest.mark.parametrize("idx", [0, 2])
+def test_persistent_decode_matches_kernel_mode(af, idx):
+    cfg = synth.CONFIGS[idx]
+    hm = synth.HostModel(cfg, synth.seed_of(idx))
+    prompt = hm.prompt(24)
+    res = {}
+    for mode in (af.AF_DECODE_PERSISTENT, af.AF_DECODE_KERNELS):
+        m = gpu_model(hm)
+        af.af_set_decode_mode(m.h, mode)  # both modes are available for these shapes
+        assert af.af_get_decode_mode(m.h) == mode
+        m.prefill(prompt, 0)
+        lg = torch.empty(cfg.n_vocab, device="cuda")
+        out = []
+        tok = int(prompt[-1])
+        for p in range(24, 32):
+            m.decode(tok, p, lg)
+            out.append(lg.cpu().numpy().copy())
+            tok = int(np.argmax(out[-1]))  # same host-side token sequence for both modes
+        res[mode] = out
+        m.close()
+    for a, b in zip(res[af.AF_DECODE_PERSISTENT], res[af.AF_DECODE_KERNELS]):
+        assert rms_rel_err(a, b) <= 1e-3
+
+
+def test_decode_parity_in_persistent_mode(af):
+    # the per-layer parity run of test_config0_full_workload, through the persistent kernel
+    cfg = synth.CONFIGS[2]
+    hm = synth.HostModel(cfg, synth.seed_of(2))
+    prompt = hm.prompt(20)
+    om = oracle.Model.from_host(hm, kv_slots=32)
+    gm = gpu_model(hm)
+    af.af_set_decode_mode(gm.h, af.AF_DECODE_PERSISTENT)
+    om.forward(prompt, 0, want_logits=False)
+    gm.prefill(prompt, 0)
+    logits = torch.empty(cfg.n_vocab, device="cuda")
+    tok = int(prompt[-1])
+    for p in range(20, 24):
+        ref_logits, ref_cap = om.forward([tok], p, capture=True)
+        cap = torch.empty(cfg.n_layers + 1, 1, cfg.n_embd, device="cuda")
+        af.af_debug_capture(gm.h, cap)
+        gm.decode(tok, p, logits)
+        torch.cuda.synchronize()
+        _check_capture(cap.cpu().numpy(), ref_cap, f"persistent decode pos {p}")
+        _check_logits(logits.cpu().numpy(), ref_logits, f"persistent decode pos {p}")
+        tok = oracle.argmax(ref_logits)
+    gm.close()
+
+
+def test_model_sync_reports_token(af, tiny):
+    m = gpu_model(tiny)
+    lg = torch.empty(tiny.cfg.n_vocab, device="cuda")
+    m.prefill(tiny.prompt()[:8], 0, lg)
+    t = af.af_model_sync(m.h, want_next=True)
+    assert t == int(torch.argmax(lg).item())
     m.close()
