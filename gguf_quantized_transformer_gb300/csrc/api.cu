@@ -61,6 +61,13 @@ struct Allocs {
         p.push_back(q);
         return q;
     }
+    void release(void* q) {
+        for (auto& e : p)
+            if (e == q) {
+                cudaFree(e);
+                e = nullptr;
+            }
+    }
     void free_all() {
         for (void* q : p) cudaFree(q);
         p.clear();
@@ -143,9 +150,9 @@ struct af_model {
     float* q = nullptr;      // [chunk][H*D] rotated q
     float* attn = nullptr;   // [H*D] decode attention output
     float* h = nullptr;      // [F] decode SwiGLU output
-    float* y = nullptr;      // [chunk][E] normalized activations (GEMM operand)
-    float* a = nullptr;      // [chunk][H*D] attention output (GEMM operand)
-    float* hp = nullptr;     // [chunk][F] SwiGLU output (GEMM operand)
+    __half* y16[2] = {};     // [chunk][E] normalized activations, fp16 hi / lo (GEMM operand)
+    __half* a16[2] = {};     // [chunk][H*D] attention output, fp16 hi / lo
+    __half* h16[2] = {};     // [chunk][F] SwiGLU output, fp16 hi / lo
     int* tok = nullptr;      // [chunk]
     float* logits = nullptr; // [V] default logits
     GemvScratch gs;
@@ -191,6 +198,8 @@ struct af_qweight {
     Planes p;
     Allocs A;
     GemvScratch gs;
+    __half* x16[2] = {};  // af_qgemm operand: X as fp16 hi / lo, grown on demand
+    int x16_rows = 0;
 };
 
 extern "C" {
@@ -334,9 +343,11 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     m->q = (float*)A.get((size_t)S * QD * 4);
     m->attn = (float*)A.get((size_t)QD * 4);
     m->h = (float*)A.get((size_t)F * 4);
-    m->y = (float*)A.get((size_t)S * E * 4);
-    m->a = (float*)A.get((size_t)S * QD * 4);
-    m->hp = (float*)A.get((size_t)S * F * 4);
+    for (int i = 0; i < 2; i++) {
+        m->y16[i] = (__half*)A.get((size_t)S * E * 2);
+        m->a16[i] = (__half*)A.get((size_t)S * QD * 2);
+        m->h16[i] = (__half*)A.get((size_t)S * F * 2);
+    }
     m->tok = (int*)A.get((size_t)S * 4);
     m->logits = (float*)A.get((size_t)V * 4);
     m->st = (StepState*)A.get(sizeof(StepState));
@@ -344,7 +355,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     m->as.ns = std::max(attn_decode_splits(c.n_kv_heads), decode_attn_splits(c.n_kv_heads));
     m->as.part = (float*)A.get(attn_decode_part_elems(c.n_heads, D, m->as.ns) * 4);
     m->as.cnt = (unsigned*)A.get((size_t)c.n_kv_heads * 4);
-    if (!m->x || !m->q || !m->attn || !m->h || !m->y || !m->a || !m->hp || !m->tok || !m->logits || !m->st ||
+    if (!m->x || !m->q || !m->attn || !m->h || !m->y16[0] || !m->y16[1] || !m->a16[0] || !m->a16[1] || !m->h16[0] || !m->h16[1] || !m->tok || !m->logits || !m->st ||
         !m->gs.err || !m->as.part || !m->as.cnt)
         return oom("activations");
     // persistent decode plan: per-layer GEMV tasks on the device, barrier words
@@ -411,6 +422,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     }
     {
         cudaError_t e = qgemv_prepare();
+        if (!e) e = qgemm_prepare();
         if (!e) e = cudaMemsetAsync(m->gs.err, 0, sizeof(unsigned), s);
         if (!e) e = cudaMemsetAsync(m->as.cnt, 0, (size_t)c.n_kv_heads * 4, s);
         if (!e) e = cudaMemsetAsync(m->st, 0, sizeof(StepState), s);
@@ -489,11 +501,10 @@ int capture_copy(af_model* m, int slot, int n) {
     return AF_OK;
 }
 
-Epi epi_qkv(af_model* m, int l, float* qout, __half* q16, const int* pos_dev, int pos0) {
+Epi epi_qkv(af_model* m, int l, float* qout, const int* pos_dev, int pos0) {
     Epi e;
     e.kind = EPI_QKV;
     e.out = qout;
-    e.out16 = q16;
     e.ld = m->QD();
     e.qd = m->QD();
     e.kvd = m->KVD();
@@ -518,7 +529,7 @@ int decode_body(af_model* m, float* logits) {
     if (rc) return rc;
     for (int l = 0; l < c.n_layers; l++) {
         const LayerW& lw = m->L[l];
-        CK(launch_qgemv(lw.qkv, m->x, lw.attn_norm, c.rms_eps, epi_qkv(m, l, m->q, nullptr, pos_dev, 0), m->gs, s));
+        CK(launch_qgemv(lw.qkv, m->x, lw.attn_norm, c.rms_eps, epi_qkv(m, l, m->q, pos_dev, 0), m->gs, s));
         CK(launch_attn_decode(m->q, m->kl(l), m->vl(l), c.kv_dtype == AF_F16, c.n_heads, c.n_kv_heads, c.head_dim,
                               c.max_ctx, pos_dev, 0, m->as, m->attn, s));
         CK(launch_qgemv(lw.o, m->attn, nullptr, 0.f, epi_simple(EPI_RESID, m->x, m->E()), m->gs, s));
@@ -543,14 +554,18 @@ int prefill_impl(af_model* m, const int* tok_dev, int n, int start_pos, float* l
     if (rc) return rc;
     for (int l = 0; l < c.n_layers; l++) {
         const LayerW& lw = m->L[l];
-        CK(launch_rmsnorm_rows(m->x, n, E, lw.attn_norm, c.rms_eps, m->y, nullptr, s));
-        CK(launch_qgemm(lw.qkv, m->y, E, n, epi_qkv(m, l, m->q, nullptr, nullptr, start_pos), s));
+        CK(launch_rmsnorm_rows(m->x, n, E, lw.attn_norm, c.rms_eps, m->y16[0], m->y16[1], s));
+        CK(launch_qgemm(lw.qkv, m->y16[0], m->y16[1], E, n, epi_qkv(m, l, m->q, nullptr, start_pos),
+                        m->gs.err, s));
         CK(launch_attn_prefill(m->q, QD, m->kl(l), m->vl(l), c.kv_dtype == AF_F16, c.n_heads, c.n_kv_heads,
-                               c.head_dim, c.max_ctx, start_pos, n, m->a, nullptr, QD, s));
-        CK(launch_qgemm(lw.o, m->a, QD, n, epi_simple(EPI_RESID, m->x, E), s));
-        CK(launch_rmsnorm_rows(m->x, n, E, lw.ffn_norm, c.rms_eps, m->y, nullptr, s));
-        CK(launch_qgemm(lw.gu, m->y, E, n, epi_simple(EPI_SWIGLU, m->hp, F), s));
-        CK(launch_qgemm(lw.down, m->hp, F, n, epi_simple(EPI_RESID, m->x, E), s));
+                               c.head_dim, c.max_ctx, start_pos, n, m->a16[0], m->a16[1], QD, s));
+        CK(launch_qgemm(lw.o, m->a16[0], m->a16[1], QD, n, epi_simple(EPI_RESID, m->x, E), m->gs.err, s));
+        CK(launch_rmsnorm_rows(m->x, n, E, lw.ffn_norm, c.rms_eps, m->y16[0], m->y16[1], s));
+        Epi eg = epi_simple(EPI_SWIGLU, nullptr, F);
+        eg.out16 = m->h16[0];
+        eg.out16_lo = m->h16[1];
+        CK(launch_qgemm(lw.gu, m->y16[0], m->y16[1], E, n, eg, m->gs.err, s));
+        CK(launch_qgemm(lw.down, m->h16[0], m->h16[1], F, n, epi_simple(EPI_RESID, m->x, E), m->gs.err, s));
         rc = capture_copy(m, l + 1, n);
         if (rc) return rc;
     }
@@ -671,6 +686,7 @@ int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t 
         return fail(AF_ENOMEM, "device allocation failed");
     }
     cudaError_t e = qgemv_prepare();
+    if (!e) e = qgemm_prepare();
     if (!e) e = repack_into(w->p, blocks_dev, N, 0, 1, s);
     if (!e) e = cudaMemsetAsync(w->gs.err, 0, sizeof(unsigned), s);
     if (!e) e = cudaStreamSynchronize(s);
@@ -691,7 +707,19 @@ int af_qgemv(const af_qweight* w, const float* x_dev, float* y_dev, void* stream
 int af_qgemm(const af_qweight* wc, const float* X_dev, int32_t M, float* Y_dev, void* stream) {
     if (!wc || !X_dev || !Y_dev) return fail(AF_EINVAL, "null argument");
     if (M < 1) return fail(AF_ERANGE, "M must be >= 1");
-    CK(launch_qgemm(wc->p, X_dev, wc->p.K, M, epi_simple(EPI_STORE, Y_dev, wc->p.N), (cudaStream_t)stream));
+    af_qweight* w = const_cast<af_qweight*>(wc);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (w->x16_rows < M) {  // (re)allocate the operand planes; the old ones may still be in use
+        CK(cudaStreamSynchronize(s));
+        for (int i = 0; i < 2; i++) {
+            w->A.release(w->x16[i]);
+            w->x16[i] = (__half*)w->A.get((size_t)M * w->p.K * 2);
+        }
+        w->x16_rows = (w->x16[0] && w->x16[1]) ? M : 0;
+        if (!w->x16_rows) return fail(AF_ENOMEM, "operand buffer");
+    }
+    CK(launch_split_f16(X_dev, w->x16[0], w->x16[1], (int64_t)M * w->p.K, s));
+    CK(launch_qgemm(w->p, w->x16[0], w->x16[1], w->p.K, M, epi_simple(EPI_STORE, Y_dev, w->p.N), w->gs.err, s));
     return AF_OK;
 }
 

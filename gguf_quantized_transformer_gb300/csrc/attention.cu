@@ -238,7 +238,7 @@ constexpr int kKT = 64;           // keys per tile
 template <int D, int G, typename KT>
 __global__ void __launch_bounds__(kPreThreads)
     attn_prefill_kernel(const float* __restrict__ q, int64_t ldq, const KT* __restrict__ kc, const KT* __restrict__ vc,
-                        int max_ctx, int pos0, int S, float* __restrict__ out, __half* __restrict__ out16,
+                        int max_ctx, int pos0, int S, __half* __restrict__ out_hi, __half* __restrict__ out_lo,
                         int64_t ldo) {
     constexpr int QT = 32 / G;  // query rows per CTA
     constexpr int DP = D + 1;   // padded K row
@@ -348,8 +348,9 @@ __global__ void __launch_bounds__(kPreThreads)
         for (int d = 0; d < DD; d++) {
             const float o = acc[a][d] * inv;
             const int64_t idx = (int64_t)r * ldo + (g * G + h) * D + lane + 32 * d;
-            if (out) out[idx] = o;
-            if (out16) out16[idx] = __float2half_rn(o);
+            const __half oh = __float2half_rn(o);
+            out_hi[idx] = oh;
+            out_lo[idx] = __float2half_rn(o - __half2float(oh));
         }
     }
 }
@@ -377,7 +378,7 @@ cudaError_t dispatch_decode(const float* q, const void* kc, const void* vc, int 
 
 template <int D, int G>
 cudaError_t dispatch_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int KVH,
-                             int max_ctx, int pos0, int S, float* out, __half* out16, int64_t ldo, cudaStream_t s) {
+                             int max_ctx, int pos0, int S, __half* out, __half* out16, int64_t ldo, cudaStream_t s) {
     constexpr int QT = 32 / G;
     const size_t smem = sizeof(float) * (32 * D + kKT * (D + 1) + kKT * D);
     dim3 grid((S + QT - 1) / QT, KVH);
@@ -431,7 +432,7 @@ cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, i
 }
 
 cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int H,
-                                int KVH, int D, int max_ctx, int pos0, int S, float* out, __half* out16,
+                                int KVH, int D, int max_ctx, int pos0, int S, __half* out, __half* out16,
                                 int64_t ldo, cudaStream_t s) {
     const int G = H / KVH;
     AF_ATTN_DISPATCH(dispatch_prefill, q, ldq, kc, vc, kv_f16, KVH, max_ctx, pos0, S, out, out16, ldo, s)

@@ -47,7 +47,8 @@ struct Epi {
     int kind = EPI_STORE;
     float* out = nullptr;  // STORE: Y [M][ld]; RESID: x [M][ld]; QKV: q [M][ld]; SWIGLU: h [M][ld]; LOGITS: [N]
     int ld = 0;
-    __half* out16 = nullptr;  // optional fp16 copy of SWIGLU/QKV-q output (GEMM operand), same ld
+    __half* out16 = nullptr;     // optional fp16 hi part of the SWIGLU output (GEMM operand), same ld
+    __half* out16_lo = nullptr;  // its fp16 lo part: value - hi
     // EPI_QKV: columns [0, qd) are q, [qd, qd+kvd) k, [qd+kvd, qd+2kvd) v
     int qd = 0, kvd = 0, head_dim = 0, max_ctx = 0, kv_f16 = 0;
     void* kcache = nullptr;  // this layer's [KVH][max_ctx][D]
@@ -80,7 +81,11 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, f
         case EPI_SWIGLU: {  // columns (2r, 2r+1) hold (gate_r, up_r)
             float h = silu_f(v0) * v1;
             if (e.out) e.out[(int64_t)m * e.ld + (n >> 1)] = h;
-            if (e.out16) e.out16[(int64_t)m * e.ld + (n >> 1)] = __float2half_rn(h);
+            if (e.out16) {
+                const __half hh = __float2half_rn(h);
+                e.out16[(int64_t)m * e.ld + (n >> 1)] = hh;
+                e.out16_lo[(int64_t)m * e.ld + (n >> 1)] = __float2half_rn(h - __half2float(hh));
+            }
         } break;
         case EPI_LOGITS: {
             e.out[n] = v0;
@@ -102,10 +107,6 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, f
                 if (e.out) {
                     e.out[(int64_t)m * e.ld + n] = v0;
                     e.out[(int64_t)m * e.ld + n + 1] = v1;
-                }
-                if (e.out16) {
-                    e.out16[(int64_t)m * e.ld + n] = __float2half_rn(v0);
-                    e.out16[(int64_t)m * e.ld + n + 1] = __float2half_rn(v1);
                 }
             } else {
                 const bool isk = n < e.qd + e.kvd;
@@ -137,9 +138,11 @@ cudaError_t launch_repack(const uint8_t* src, int wtype, int N, int K, uint8_t* 
 cudaError_t launch_rope_table(float2* tab, int max_ctx, int head_dim, double base, double yarn_scale,
                               cudaStream_t s);
 cudaError_t launch_embed(const Planes& emb, const int* tok_dev, int n, float* x, int64_t ldx, cudaStream_t s);
-cudaError_t launch_rmsnorm_rows(const float* x, int n, int E, const float* w, float eps, float* y, __half* y16,
+// y = RMSNorm(x) per row, written as fp16 hi + lo planes (the tensor-core GEMM operand).
+cudaError_t launch_rmsnorm_rows(const float* x, int n, int E, const float* w, float eps, __half* y_hi, __half* y_lo,
                                 cudaStream_t s);
-cudaError_t launch_f32_to_f16(const float* x, __half* y, int64_t n, cudaStream_t s);
+// x (fp32) -> fp16 hi + lo planes.
+cudaError_t launch_split_f16(const float* x, __half* hi, __half* lo, int64_t n, cudaStream_t s);
 
 // y-part of the decode path: one matrix-vector product with optional RMSNorm
 // prologue (norm_w != nullptr) and a fused epilogue.
@@ -150,8 +153,11 @@ cudaError_t qgemv_prepare();
 // Largest number of K chunks (Kp / chunk_weights) a GEMV supports.
 int qgemv_max_chunks();
 
-// Prefill GEMM: Y = X W^T for M rows with a fused epilogue.  X is fp32 [M][ldx].
-cudaError_t launch_qgemm(const Planes& W, const float* X, int64_t ldx, int M, const Epi& epi, cudaStream_t s);
+// Prefill GEMM on the tensor cores: Y = X W^T for M rows with a fused epilogue.  X is given as fp16
+// hi + lo planes [M][ldx] (ldx % 8 == 0, 16-byte aligned).  err: device error word.
+cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo, int64_t ldx, int M, const Epi& epi,
+                         unsigned* err, cudaStream_t s);
+cudaError_t qgemm_prepare();
 
 // Attention
 struct AttnScratch {
@@ -165,7 +171,7 @@ cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, i
                                int max_ctx, const int* pos_dev, int pos, const AttnScratch& scr, float* out,
                                cudaStream_t s);
 cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int H,
-                                int KVH, int D, int max_ctx, int pos0, int S, float* out, __half* out16,
+                                int KVH, int D, int max_ctx, int pos0, int S, __half* out_hi, __half* out_lo,
                                 int64_t ldo, cudaStream_t s);
 bool attn_supported(int H, int KVH, int D);
 

@@ -102,9 +102,9 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return t;
 }
 
-// y = w * x / sqrt(mean(x^2) + eps) for each of n rows (one CTA per row).
+// y = w * x / sqrt(mean(x^2) + eps) for each of n rows (one CTA per row), as fp16 hi + lo.
 __global__ void rmsnorm_rows_kernel(const float* __restrict__ x, int E, const float* __restrict__ w, float eps,
-                                    float* __restrict__ y, __half* __restrict__ y16) {
+                                    __half* __restrict__ y_hi, __half* __restrict__ y_lo) {
     __shared__ float red[32];
     const float* xr = x + (int64_t)blockIdx.x * E;
     float ss = 0.f;
@@ -113,27 +113,33 @@ __global__ void rmsnorm_rows_kernel(const float* __restrict__ x, int E, const fl
     const float inv = rsqrtf(ss / (float)E + eps);
     for (int k = threadIdx.x; k < E; k += blockDim.x) {
         const float v = w[k] * (xr[k] * inv);
-        if (y) y[(int64_t)blockIdx.x * E + k] = v;
-        if (y16) y16[(int64_t)blockIdx.x * E + k] = __float2half_rn(v);
+        const __half h = __float2half_rn(v);
+        y_hi[(int64_t)blockIdx.x * E + k] = h;
+        y_lo[(int64_t)blockIdx.x * E + k] = __float2half_rn(v - __half2float(h));
     }
 }
 
-cudaError_t launch_rmsnorm_rows(const float* x, int n, int E, const float* w, float eps, float* y, __half* y16,
+cudaError_t launch_rmsnorm_rows(const float* x, int n, int E, const float* w, float eps, __half* y_hi, __half* y_lo,
                                 cudaStream_t s) {
-    rmsnorm_rows_kernel<<<n, 256, 0, s>>>(x, E, w, eps, y, y16);
+    rmsnorm_rows_kernel<<<n, 256, 0, s>>>(x, E, w, eps, y_hi, y_lo);
     return cudaGetLastError();
 }
 
-__global__ void f32_to_f16_kernel(const float* __restrict__ x, __half* __restrict__ y, int64_t n) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        y[i] = __float2half_rn(x[i]);
+__global__ void split_f16_kernel(const float* __restrict__ x, __half* __restrict__ hi, __half* __restrict__ lo,
+                                 int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = x[i];
+        const __half h = __float2half_rn(v);
+        hi[i] = h;
+        lo[i] = __float2half_rn(v - __half2float(h));
+    }
 }
 
-cudaError_t launch_f32_to_f16(const float* x, __half* y, int64_t n, cudaStream_t s) {
+cudaError_t launch_split_f16(const float* x, __half* hi, __half* lo, int64_t n, cudaStream_t s) {
     int64_t blocks = (n + 255) / 256;
     if (blocks > 65535) blocks = 65535;
     if (blocks < 1) blocks = 1;
-    f32_to_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, y, n);
+    split_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>(x, hi, lo, n);
     return cudaGetLastError();
 }
 

@@ -191,7 +191,12 @@ void af_model_destroy(af_model* m);
  *   af_qgemm: Y[m][i] = sum_j X[m][j] W[i][j]     X_dev fp32 [M, K] row-major,
  *                                                 Y_dev fp32 [M, N], M >= 1
  * Calls that share one af_qweight must be ordered on one stream (they share
- * its scratch).  Products accumulate in fp32.
+ * its scratch).  af_qgemv accumulates exact integer products of the weights
+ * with x held in 24-bit fixed point per 32-element block; af_qgemm runs on
+ * the tensor cores with X and W each split into fp16 hi + lo parts (three
+ * fp16 products accumulated in fp32, relative error ~1e-6 per product).
+ * af_qgemm keeps the split X in buffers of the af_qweight: the first call
+ * with a larger M than before synchronises `stream` and grows them.
  */
 int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t K, void* stream, af_qweight** out);
 int af_qgemv(const af_qweight* w, const float* x_dev, float* y_dev, void* stream);

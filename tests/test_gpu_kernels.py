@@ -130,6 +130,25 @@ def test_qgemm_parity(af, wtype, M, N, K):
 
 
 @pytest.mark.parametrize("wtype", ["q8_0", "q4_0"])
+def test_qgemm_near_fp32(af, wtype):
+    """The tensor-core GEMM splits X and W into fp16 hi + lo parts; with all three
+    cross products kept the result is within a few fp32 roundings of the exact sum,
+    far inside the 1e-3 bar (a dropped lo term would show up as ~1e-4)."""
+    M, N, K = 130, 512, 2048
+    W = synth.matrix(wtype, 43, synth.TID_TEST_BASE + 6, N, K)
+    X = synth.normals(43, synth.TID_TEST_BASE + 7, M * K).reshape(M, K)
+    h = _qweight(af, wtype, W, N, K)
+    Y = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    af.af_qgemm(h, _dev(X), M, Y)
+    torch.cuda.synchronize()
+    ref = oracle.qgemm(wtype, W, N, K, X.astype(np.float64))
+    got = Y.cpu().numpy()
+    worst = max(normwise_rel_err(got[m], ref[m]) for m in range(M))
+    assert worst <= 2e-5, worst
+    af.af_qweight_destroy(h)
+
+
+@pytest.mark.parametrize("wtype", ["q8_0", "q4_0"])
 @pytest.mark.parametrize("N,K", [(6144, 4096), (28672, 4096), (4096, 14336)])
 def test_qgemm_full_size_sampled(af, wtype, N, K):
     M = 512
