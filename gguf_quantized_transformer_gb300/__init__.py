@@ -77,6 +77,7 @@ def lib():
         L.af_qweight_destroy.argtypes = [vp]
         L.af_qweight_destroy.restype = None
         L.af_attention_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        L.af_attention_decode_static.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
         _lib = L
     return _lib
 
@@ -218,6 +219,12 @@ def af_attention_decode(q_dev, k_dev, v_dev, kv_dtype: int, n_heads: int, n_kv_h
                         pos: int, out_dev, stream=None):
     return check(lib().af_attention_decode(_ptr(q_dev), _ptr(k_dev), _ptr(v_dev), kv_dtype, n_heads, n_kv_heads,
                                            head_dim, ctx, pos, _ptr(out_dev), _stream(stream)))
+
+
+def af_attention_decode_static(q_dev, k_dev, v_dev, kv_dtype: int, n_heads: int, n_kv_heads: int, head_dim: int,
+                               ctx: int, pos: int, out_dev, stream=None):
+    return check(lib().af_attention_decode_static(_ptr(q_dev), _ptr(k_dev), _ptr(v_dev), kv_dtype, n_heads,
+                                                  n_kv_heads, head_dim, ctx, pos, _ptr(out_dev), _stream(stream)))
 
 
 def af_last_error() -> str:

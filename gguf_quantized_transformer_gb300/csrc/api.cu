@@ -755,4 +755,28 @@ int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev
     return AF_OK;
 }
 
+// Same computation without allocating: the split scratch is a file-scope device
+// array (attn_static.cu).  For callers that cannot allocate mid-step: a serving
+// loop with work queued on other streams cannot take the device-wide
+// synchronisation that cudaFree implies, and a caller that has handed the
+// device's free memory to its own pool has none left to cudaMalloc.
+int af_attention_decode_static(const float* q_dev, const void* k_dev, const void* v_dev, int32_t kv_dtype, int32_t H,
+                               int32_t KVH, int32_t D, int32_t ctx, int32_t pos, float* out_dev, void* stream) {
+    if (!q_dev || !k_dev || !v_dev || !out_dev) return fail(AF_EINVAL, "null argument");
+    if (kv_dtype != AF_F32 && kv_dtype != AF_F16) return fail(AF_EINVAL, "bad kv_dtype");
+    if (H <= 0 || KVH <= 0 || D <= 0 || ctx <= 0) return fail(AF_EINVAL, "sizes must be positive");
+    if (!attn_supported(H, KVH, D)) return fail(AF_ENOTIMPL, "unsupported head_dim / group size");
+    if (pos < 0 || pos >= ctx) return fail(AF_ERANGE, "pos %d outside [0, %d)", pos, ctx);
+    AttnScratch as;
+    as.ns = attn_decode_splits(KVH);
+    if (KVH > kStaticAttnMaxKVH) return fail(AF_ERANGE, "n_kv_heads %d above the fixed scratch (%d)", KVH, kStaticAttnMaxKVH);
+    if (attn_decode_part_elems(H, D, as.ns) > kStaticAttnPartFloats)
+        return fail(AF_ERANGE, "split partials (%zu floats) above the fixed scratch (%zu)",
+                    attn_decode_part_elems(H, D, as.ns), kStaticAttnPartFloats);
+    CK(attn_static_scratch(&as.part, &as.cnt));
+    CK(launch_attn_decode(q_dev, k_dev, v_dev, kv_dtype == AF_F16, H, KVH, D, ctx, nullptr, pos, as, out_dev,
+                          (cudaStream_t)stream));
+    return AF_OK;
+}
+
 }  // extern "C"

@@ -175,6 +175,12 @@ cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, con
                                 int64_t ldo, cudaStream_t s);
 bool attn_supported(int H, int KVH, int D);
 
+// Capacity of the fixed decode-attention scratch (a file-scope device array, no allocation).
+constexpr int kStaticAttnMaxKVH = 1024;                  // arrival counters
+constexpr size_t kStaticAttnPartFloats = (size_t)1 << 20;  // split partials (4 MiB)
+// Device address of that scratch on the current device (looked up once per device).
+cudaError_t attn_static_scratch(float** part, unsigned** cnt);
+
 // One GEMV of the persistent decode kernel: matrix, input, optional RMSNorm
 // weight, stage shape (R rows per ring slot, WK warps along K) and epilogue.
 struct GemvTask {

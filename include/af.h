@@ -216,6 +216,29 @@ void af_qweight_destroy(af_qweight* w);
 int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev, int32_t kv_dtype, int32_t n_heads,
                         int32_t n_kv_heads, int32_t head_dim, int32_t ctx, int32_t pos, float* out_dev, void* stream);
 
+/*
+ * af_attention_decode without any device allocation (no counterpart on the
+ * pages: an interface for callers that cannot allocate mid-step, e.g. a
+ * serving loop that cannot take the device-wide synchronisation of cudaFree,
+ * or one whose memory is all handed to its own pool).  Same arguments, same
+ * kernel and same result as af_attention_decode, but stream-ordered: it does
+ * not synchronise `stream`.
+ * Scratch: one file-scope device array of this library (4 MiB of split
+ * partials + 1024 arrival counters).  Calls with n_kv_heads > 1024 or whose
+ * partials need more than 2^20 floats (n_heads * splits * (head_dim + 2),
+ * splits = ceil(2 * SMs / n_kv_heads)) return AF_ERANGE before launching.
+ * The counters must start at zero: they are zero when the library is loaded
+ * and every call that completes leaves them zero.  All calls on a device
+ * share the one array, so calls that may overlap in time (different streams
+ * without ordering between them) race and give wrong results: order them on
+ * one stream.  The first call on each device looks up the array's address
+ * (cudaGetSymbolAddress, with that device current) and loads the kernels; make
+ * that first call before any stream capture.
+ */
+int af_attention_decode_static(const float* q_dev, const void* k_dev, const void* v_dev, int32_t kv_dtype,
+                               int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t ctx, int32_t pos,
+                               float* out_dev, void* stream);
+
 /* Thread-local message for the last failed call on this thread ("" if none). */
 const char* af_last_error(void);
 

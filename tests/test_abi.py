@@ -78,6 +78,20 @@ def test_validation_errors_without_gpu():
     assert L.af_prefill(None, None, 1, 0, None) == af.AF_EINVAL
     assert L.af_decode_step(None, 0, 0, None, None) == af.AF_EINVAL
     assert L.af_attention_decode(None, None, None, 0, 8, 4, 64, 16, 0, None, None) == af.AF_EINVAL
+    assert L.af_attention_decode_static(None, None, None, 0, 8, 4, 64, 16, 0, None, None) == af.AF_EINVAL
+
+
+def test_static_attention_rejects_oversize():
+    # host-side capacity checks of the fixed scratch; they return before any launch
+    # (the pointers are never dereferenced on the host)
+    af = pytest.importorskip("gguf_quantized_transformer_gb300")
+    L = af.lib()
+    # more kv heads than arrival counters
+    assert L.af_attention_decode_static(1, 1, 1, af.AF_F16, 1028, 1028, 64, 16, 0, 1, None) == af.AF_ERANGE
+    assert "n_kv_heads" in af.af_last_error()
+    # partials: 8192 heads x >= 1 split x 130 floats > 2^20
+    assert L.af_attention_decode_static(1, 1, 1, af.AF_F16, 8192, 1024, 128, 16, 0, 1, None) == af.AF_ERANGE
+    assert "partials" in af.af_last_error()
     assert af.af_kv_bytes(af.af_config()) == 0
 
 
