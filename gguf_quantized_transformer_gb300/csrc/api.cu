@@ -352,7 +352,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     m->logits = (float*)A.get((size_t)V * 4);
     m->st = (StepState*)A.get(sizeof(StepState));
     m->gs.err = (unsigned*)A.get(sizeof(unsigned));
-    m->as.ns = std::max(attn_decode_splits(c.n_kv_heads), decode_attn_splits(c.n_kv_heads));
+    m->as.ns = std::max(attn_decode_splits(c.n_heads, c.n_kv_heads, c.max_ctx), decode_attn_splits(c.n_kv_heads));
     m->as.part = (float*)A.get(attn_decode_part_elems(c.n_heads, D, m->as.ns) * 4);
     m->as.cnt = (unsigned*)A.get((size_t)c.n_kv_heads * 4);
     if (!m->x || !m->q || !m->attn || !m->h || !m->y16[0] || !m->y16[1] || !m->a16[0] || !m->a16[1] || !m->h16[0] || !m->h16[1] || !m->tok || !m->logits || !m->st ||
@@ -734,7 +734,7 @@ int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev
     if (pos < 0 || pos >= ctx) return fail(AF_ERANGE, "pos %d outside [0, %d)", pos, ctx);
     cudaStream_t s = (cudaStream_t)stream;
     AttnScratch as;
-    as.ns = attn_decode_splits(KVH);
+    as.ns = attn_decode_splits(H, KVH, ctx);
     const size_t pe = attn_decode_part_elems(H, D, as.ns);
     if (cudaMalloc(&as.part, pe * 4) != cudaSuccess) {
         cudaGetLastError();
@@ -768,7 +768,7 @@ int af_attention_decode_static(const float* q_dev, const void* k_dev, const void
     if (!attn_supported(H, KVH, D)) return fail(AF_ENOTIMPL, "unsupported head_dim / group size");
     if (pos < 0 || pos >= ctx) return fail(AF_ERANGE, "pos %d outside [0, %d)", pos, ctx);
     AttnScratch as;
-    as.ns = attn_decode_splits(KVH);
+    as.ns = attn_decode_splits(H, KVH, ctx);
     if (KVH > kStaticAttnMaxKVH) return fail(AF_ERANGE, "n_kv_heads %d above the fixed scratch (%d)", KVH, kStaticAttnMaxKVH);
     if (attn_decode_part_elems(H, D, as.ns) > kStaticAttnPartFloats)
         return fail(AF_ERANGE, "split partials (%zu floats) above the fixed scratch (%zu)",

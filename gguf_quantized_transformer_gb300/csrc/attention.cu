@@ -49,138 +49,238 @@ __device__ __forceinline__ void load_vec<__half>(const __half* p, float* out, in
     }
 }
 
-constexpr int kDecThreads = 256;  // 32 position groups x 8 lanes
+constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kMinPerSplit = 64;   // positions per split before another split is used
+constexpr int kMinPerSplit = 64;  // positions per split before another split is used
+constexpr int kTile = 64;         // cache slots per pipeline tile
+constexpr int kRing = 128 * 1024; // tile ring budget (one CTA per SM)
+constexpr int kMaxScores = 64 * 1024;  // score buffer budget: split length x G floats
 
+template <int D, typename KT>
+__host__ __device__ constexpr int dec_stages() {
+    return kRing / (kTile * D * (int)sizeof(KT)) < 8 ? kRing / (kTile * D * (int)sizeof(KT)) : 8;
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// n (2 or 4) consecutive cache values as fp32; p aligned to n elements.
+template <int N>
+__device__ __forceinline__ void load_small(const float* p, float* out) {
+    if (N == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+    } else {
+        const float2 v = *reinterpret_cast<const float2*>(p);
+        out[0] = v.x; out[1] = v.y;
+    }
+}
+template <int N>
+__device__ __forceinline__ void load_small(const __half* p, float* out) {
+    if (N == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(p);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        out[0] = a.x; out[1] = a.y; out[2] = b.x; out[3] = b.y;
+    } else {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(p));
+        out[0] = a.x; out[1] = a.y;
+    }
+}
+
+// Splits of a sequence of n slots: ns_eff non-empty ranges of `chunk` slots (the last may be shorter).
+__device__ __forceinline__ void dec_split(int n, int ns, int& ns_eff, int& chunk) {
+    ns_eff = (n + kMinPerSplit - 1) / kMinPerSplit;
+    ns_eff = ns_eff < ns ? ns_eff : ns;
+    chunk = (n + ns_eff - 1) / ns_eff;
+    ns_eff = (n + chunk - 1) / chunk;
+}
+
+// Decode attention, CTA (s, g): kv head g, slots [s*chunk, ...).  The K tiles
+// and then the V tiles of the range stream through a ring of S shared-memory
+// slots with cp.async (S-1 tiles in flight ahead of the one being used).
+//   pass 1 (K tiles): lanes (LPK per slot, 8 dims each) score 32/LPK slots per
+//                     warp step for all G heads; scores go to shared memory
+//   softmax:          split maximum per head, p = exp(s - max) in place, sum
+//   pass 2 (V tiles): warp w takes slots w, w+8, ..; lane l dims l*DV..; all
+//                     heads per lane; warps are summed at the end
 template <int D, int G, typename KT>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, 1)
     attn_decode_kernel(const float* __restrict__ q, const KT* __restrict__ kc, const KT* __restrict__ vc, int max_ctx,
                        const int* __restrict__ pos_dev, int pos_arg, float* __restrict__ part,
                        unsigned* __restrict__ cnt, float* __restrict__ out) {
-    constexpr int DL = D / 8;  // dims per lane
-    extern __shared__ float sc[];  // [chunk][G] scores; reused for the merge weights [ns][G]
-    __shared__ float red_m[kDecWarps][G], red_l[kDecWarps][G];
-    __shared__ float red_o[kDecWarps][G][D];
-    __shared__ float mh_s[G], inv_den[G];
+    constexpr int TB = kTile * D * (int)sizeof(KT);  // tile bytes
+    constexpr int S = dec_stages<D, KT>();
+    constexpr int LPK = D / 8;    // pass 1: lanes per slot
+    constexpr int KPW = 32 / LPK; // pass 1: slots per warp step
+    constexpr int DV = D / 32;    // pass 2: dims per lane
+    static_assert(S >= 2, "ring too small");
+    extern __shared__ __align__(128) uint8_t dsm[];
+    float* sc = reinterpret_cast<float*>(dsm + S * TB);  // [split length][G] scores, then probabilities
+    __shared__ float red[kDecWarps][G];
+    __shared__ float m_s[G], l_s[G], inv_den[G];
     __shared__ unsigned last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gi = tid >> 3, li = tid & 7;
     const int g = blockIdx.y, s = blockIdx.x, ns = gridDim.x;
     const int pos = pos_dev ? *pos_dev : pos_arg;
     const int n = pos + 1;
-    int ns_eff = (n + kMinPerSplit - 1) / kMinPerSplit;
-    ns_eff = ns_eff < ns ? ns_eff : ns;
-    const int chunk = (n + ns_eff - 1) / ns_eff;
+    int ns_eff, chunk;
+    dec_split(n, ns, ns_eff, chunk);
     const int j0 = s * chunk;
-    const int j1 = min(n, j0 + chunk);
-    const KT* K = kc + (int64_t)g * max_ctx * D;
-    const KT* V = vc + (int64_t)g * max_ctx * D;
+    const int nl = min(n, j0 + chunk) - j0;
+    const KT* K = kc + ((int64_t)g * max_ctx + j0) * D;
+    const KT* V = vc + ((int64_t)g * max_ctx + j0) * D;
     float* my = part + ((int64_t)(g * ns + s) * G) * (D + 2);
 
     if (s < ns_eff) {
+        const int nt = (nl + kTile - 1) / kTile, T = 2 * nt;
+        auto issue = [&](int t) {  // tile t: K tiles 0..nt-1, then V tiles
+            const int tt = t < nt ? t : t - nt;
+            const int keys = min(kTile, nl - tt * kTile);
+            const uint8_t* src = reinterpret_cast<const uint8_t*>((t < nt ? K : V) + (int64_t)tt * kTile * D);
+            uint8_t* dst = dsm + (t % S) * TB;
+            const int n16 = keys * D * (int)sizeof(KT) / 16;
+            for (int c = tid; c < n16; c += kDecThreads) cp_async16(dst + 16 * c, src + 16 * c);
+        };
+#pragma unroll
+        for (int t = 0; t < S - 1; t++) {
+            if (t < T) issue(t);
+            cp_async_commit();
+        }
+        // q of the group's heads, pre-scaled by 1/sqrt(D): lane's 8 dims of each head
+        const int li = lane % LPK, ks = lane / LPK;
+        float qv[G][8];
         const float scale = rsqrtf((float)D);
-        float qv[G][DL];
 #pragma unroll
         for (int h = 0; h < G; h++) {
-            load_vec<float>(q + (int64_t)(g * G + h) * D + li * DL, qv[h], DL);
-#pragma unroll
-            for (int d = 0; d < DL; d++) qv[h][d] *= scale;
+            const float4 a = *reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8);
+            const float4 b = *reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8 + 4);
+            qv[h][0] = a.x * scale; qv[h][1] = a.y * scale; qv[h][2] = a.z * scale; qv[h][3] = a.w * scale;
+            qv[h][4] = b.x * scale; qv[h][5] = b.y * scale; qv[h][6] = b.z * scale; qv[h][7] = b.w * scale;
         }
-        // pass 1: scores of this split's slots into shared memory
-        for (int jb = j0; jb < j1; jb += 32) {  // uniform trip count: every lane reaches the shuffles
-            const int j = jb + gi;
-            const bool ok = j < j1;
-            float kf[DL];
-            if (ok) {
-                load_vec<KT>(K + (int64_t)j * D + li * DL, kf, DL);
+        float mloc[G];
+#pragma unroll
+        for (int h = 0; h < G; h++) mloc[h] = -CUDART_INF_F;
+        float acc[G][DV];
+#pragma unroll
+        for (int h = 0; h < G; h++)
+#pragma unroll
+            for (int e = 0; e < DV; e++) acc[h][e] = 0.f;
+
+        for (int t = 0; t < T; t++) {
+            if (t + S - 1 < T) issue(t + S - 1);
+            cp_async_commit();
+            cp_async_wait<S - 1>();
+            __syncthreads();
+            const uint8_t* tile = dsm + (t % S) * TB;
+            if (t < nt) {
+                // ---- pass 1: scores of this tile's slots
+                const int keys = min(kTile, nl - t * kTile);
+#pragma unroll
+                for (int step = 0; step < kTile / kDecWarps / KPW; step++) {
+                    const int j = warp * (kTile / kDecWarps) + step * KPW + ks;  // slot within the tile
+                    float kf[8];
+                    if (j < keys) {
+                        load_vec<KT>(reinterpret_cast<const KT*>(tile) + j * D + li * 8, kf, 8);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; e++) kf[e] = 0.f;
+                    }
+#pragma unroll
+                    for (int h = 0; h < G; h++) {
+                        float a = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 8; e++) a = fmaf(qv[h][e], kf[e], a);
+#pragma unroll
+                        for (int o = LPK / 2; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+                        if (li == 0 && j < keys) {
+                            sc[(t * kTile + j) * G + h] = a;
+                            mloc[h] = fmaxf(mloc[h], a);
+                        }
+                    }
+                }
             } else {
+                const int tt = t - nt;
+                if (tt == 0) {
+                    // ---- softmax over the split: maximum, probabilities in place, sum
 #pragma unroll
-                for (int d = 0; d < DL; d++) kf[d] = 0.f;
+                    for (int h = 0; h < G; h++) {
+                        float m = mloc[h];
+#pragma unroll
+                        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        if (lane == 0) red[warp][h] = m;
+                    }
+                    __syncthreads();
+                    if (tid < G) {
+                        float m = red[0][tid];
+#pragma unroll
+                        for (int w = 1; w < kDecWarps; w++) m = fmaxf(m, red[w][tid]);
+                        m_s[tid] = m;
+                    }
+                    __syncthreads();
+                    // G divides the block: thread tid always sees head tid % G
+                    const int hh = tid % G;
+                    const float mh = m_s[hh];
+                    float l = 0.f;
+                    for (int i = tid; i < nl * G; i += kDecThreads) {
+                        const float p = __expf(sc[i] - mh);
+                        sc[i] = p;
+                        l += p;
+                    }
+#pragma unroll
+                    for (int o = 16; o >= G; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+                    if (lane < G) red[warp][lane] = l;
+                    __syncthreads();
+                    if (tid < G) {
+                        float a = 0.f;
+#pragma unroll
+                        for (int w = 0; w < kDecWarps; w++) a += red[w][tid];
+                        l_s[tid] = a;
+                    }
+                    __syncthreads();
+                }
+                // ---- pass 2: P V over this tile's slots
+                const int keys = min(kTile, nl - tt * kTile);
+                for (int j = warp; j < keys; j += kDecWarps) {
+                    float vf[DV];
+                    load_small<DV>(reinterpret_cast<const KT*>(tile) + j * D + lane * DV, vf);
+                    const float* pj = sc + (tt * kTile + j) * G;
+#pragma unroll
+                    for (int h = 0; h < G; h++) {
+                        const float p = pj[h];
+#pragma unroll
+                        for (int e = 0; e < DV; e++) acc[h][e] = fmaf(p, vf[e], acc[h][e]);
+                    }
+                }
             }
-#pragma unroll
-            for (int h = 0; h < G; h++) {
-                float a = 0.f;
-#pragma unroll
-                for (int d = 0; d < DL; d++) a = fmaf(qv[h][d], kf[d], a);
-                a += __shfl_xor_sync(0xffffffffu, a, 1);
-                a += __shfl_xor_sync(0xffffffffu, a, 2);
-                a += __shfl_xor_sync(0xffffffffu, a, 4);
-                if (ok && li == 0) sc[(j - j0) * G + h] = a;
-            }
+            __syncthreads();  // the slot of tile t is refilled in the next iteration
         }
+        cp_async_wait<0>();
+        // sum the warps' partial outputs (the ring is free now)
+        float* red_o = reinterpret_cast<float*>(dsm);  // [warp][G][D]
+#pragma unroll
+        for (int h = 0; h < G; h++)
+#pragma unroll
+            for (int e = 0; e < DV; e++) red_o[(warp * G + h) * D + lane * DV + e] = acc[h][e];
         __syncthreads();
-        // split maximum per head
-        float mh[G];
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            float m = -CUDART_INF_F;
-            for (int j = tid; j < j1 - j0; j += kDecThreads) m = fmaxf(m, sc[j * G + h]);
-            for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) red_m[warp][h] = m;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            float m = red_m[0][h];
-#pragma unroll
-            for (int w = 1; w < kDecWarps; w++) m = fmaxf(m, red_m[w][h]);
-            mh[h] = m;
-        }
-        // pass 2: P V
-        float acc[G][DL], lsum[G];
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            lsum[h] = 0.f;
-#pragma unroll
-            for (int d = 0; d < DL; d++) acc[h][d] = 0.f;
-        }
-        for (int j = j0 + gi; j < j1; j += 32) {
-            float vf[DL];
-            load_vec<KT>(V + (int64_t)j * D + li * DL, vf, DL);
-#pragma unroll
-            for (int h = 0; h < G; h++) {
-                const float p = __expf(sc[(j - j0) * G + h] - mh[h]);
-                lsum[h] += p;
-#pragma unroll
-                for (int d = 0; d < DL; d++) acc[h][d] = fmaf(p, vf[d], acc[h][d]);
-            }
-        }
-        // reduce over the 4 position groups of a warp (lanes li, li+8, li+16, li+24)
-#pragma unroll
-        for (int h = 0; h < G; h++) {
-            lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 8);
-            lsum[h] += __shfl_xor_sync(0xffffffffu, lsum[h], 16);
-#pragma unroll
-            for (int d = 0; d < DL; d++) {
-                acc[h][d] += __shfl_xor_sync(0xffffffffu, acc[h][d], 8);
-                acc[h][d] += __shfl_xor_sync(0xffffffffu, acc[h][d], 16);
-            }
-        }
-        if (lane < 8) {
-#pragma unroll
-            for (int h = 0; h < G; h++) {
-#pragma unroll
-                for (int d = 0; d < DL; d++) red_o[warp][h][li * DL + d] = acc[h][d];
-                if (li == 0) red_l[warp][h] = lsum[h];
-            }
-        }
-        __syncthreads();
-        // this split's partial: part[((g*ns + s)*G + h)*(D+2) + {0..D-1: o, D: max, D+1: sum}]
         for (int t = tid; t < G * D; t += kDecThreads) {
-            const int h = t / D, d = t % D;
             float o = 0.f;
 #pragma unroll
-            for (int w = 0; w < kDecWarps; w++) o += red_o[w][h][d];
-            my[h * (D + 2) + d] = o;
+            for (int w = 0; w < kDecWarps; w++) o += red_o[w * G * D + t];
+            my[(t / D) * (D + 2) + t % D] = o;
         }
         if (tid < G) {
-            float l = 0.f;
-#pragma unroll
-            for (int w = 0; w < kDecWarps; w++) l += red_l[w][tid];
-            my[tid * (D + 2) + D] = j1 > j0 ? mh[tid] : -CUDART_INF_F;
-            my[tid * (D + 2) + D + 1] = l;
+            my[tid * (D + 2) + D] = m_s[tid];
+            my[tid * (D + 2) + D + 1] = l_s[tid];
         }
     }
     __threadfence();
@@ -203,16 +303,15 @@ __global__ void __launch_bounds__(kDecThreads)
         float den = 0.f;
         for (int ss = 0; ss < ns_eff; ss++) {
             const float l = __ldcg(pg + ((int64_t)ss * G + tid) * (D + 2) + D + 1);
-            if (l > 0.f) den = fmaf(__expf(wsm[ss * G + tid] - M), l, den);
+            den = fmaf(__expf(wsm[ss * G + tid] - M), l, den);
         }
-        mh_s[tid] = M;
+        m_s[tid] = M;
         inv_den[tid] = 1.f / den;
     }
     __syncthreads();
     for (int t = tid; t < ns_eff * G; t += kDecThreads) {
         const int h = t % G;
-        const float m = wsm[t];
-        wsm[t] = m == -CUDART_INF_F ? 0.f : __expf(m - mh_s[h]) * inv_den[h];
+        wsm[t] = __expf(wsm[t] - m_s[h]) * inv_den[h];
     }
     __syncthreads();
     for (int t = tid; t < G * D; t += kDecThreads) {
@@ -355,25 +454,26 @@ __global__ void __launch_bounds__(kPreThreads)
     }
 }
 
+template <int D, int G, typename KT>
+cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int max_ctx, const int* pos_dev, int pos,
+                            const AttnScratch& scr, int ns, float* out, int KVH, cudaStream_t s) {
+    const int cap = std::max((max_ctx + ns - 1) / ns, std::max(ns, kMinPerSplit));
+    const size_t smem = (size_t)dec_stages<D, KT>() * kTile * D * sizeof(KT) + (size_t)cap * G * sizeof(float);
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    auto k = attn_decode_kernel<D, G, KT>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e) return e;
+    k<<<dim3(ns, KVH), kDecThreads, smem, s>>>(q, (const KT*)kc, (const KT*)vc, max_ctx, pos_dev, pos, scr.part,
+                                               scr.cnt, out);
+    return cudaGetLastError();
+}
+
 template <int D, int G>
 cudaError_t dispatch_decode(const float* q, const void* kc, const void* vc, int kv_f16, int max_ctx,
-                            const int* pos_dev, int pos, const AttnScratch& scr, float* out, int KVH, cudaStream_t s) {
-    const int ns = scr.ns;
-    const int cap = std::max((max_ctx + ns - 1) / ns, std::max(ns, kMinPerSplit));
-    const size_t smem = (size_t)cap * G * sizeof(float);
-    dim3 grid(ns, KVH);
-    if (kv_f16) {
-        auto k = attn_decode_kernel<D, G, __half>;
-        if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, kDecThreads, smem, s>>>(q, (const __half*)kc, (const __half*)vc, max_ctx, pos_dev, pos, scr.part,
-                                          scr.cnt, out);
-    } else {
-        auto k = attn_decode_kernel<D, G, float>;
-        if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, kDecThreads, smem, s>>>(q, (const float*)kc, (const float*)vc, max_ctx, pos_dev, pos, scr.part,
-                                          scr.cnt, out);
-    }
-    return cudaGetLastError();
+                            const int* pos_dev, int pos, const AttnScratch& scr, int ns, float* out, int KVH,
+                            cudaStream_t s) {
+    if (kv_f16) return launch_decode_t<D, G, __half>(q, kc, vc, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
+    return launch_decode_t<D, G, float>(q, kc, vc, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
 }
 
 template <int D, int G>
@@ -404,8 +504,12 @@ bool attn_supported(int H, int KVH, int D) {
     return (D == 64 || D == 128) && (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
-int attn_decode_splits(int n_kv_heads) {
-    int ns = (2 * num_sms() + n_kv_heads - 1) / n_kv_heads;
+int attn_decode_splits(int n_heads, int n_kv_heads, int max_ctx) {
+    // one CTA per SM over all kv heads; more splits only if a split's scores would not fit
+    int ns = num_sms() / n_kv_heads;
+    const int G = n_heads / n_kv_heads;
+    const int need = (int)(((int64_t)max_ctx * G * 4 + kMaxScores - 1) / kMaxScores);
+    if (ns < need) ns = need;
     return ns < 1 ? 1 : ns;
 }
 
@@ -428,7 +532,10 @@ cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, i
                                int max_ctx, const int* pos_dev, int pos, const AttnScratch& scr, float* out,
                                cudaStream_t s) {
     const int G = H / KVH;
-    AF_ATTN_DISPATCH(dispatch_decode, q, kc, vc, kv_f16, max_ctx, pos_dev, pos, scr, out, KVH, s)
+    const int ns = attn_decode_splits(H, KVH, max_ctx);
+    if (scr.ns < ns) return cudaErrorInvalidValue;  // scratch sized for fewer splits
+    if ((reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & 15) return cudaErrorInvalidValue;
+    AF_ATTN_DISPATCH(dispatch_decode, q, kc, vc, kv_f16, max_ctx, pos_dev, pos, scr, ns, out, KVH, s)
 }
 
 cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int H,

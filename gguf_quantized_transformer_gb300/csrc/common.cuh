@@ -162,10 +162,11 @@ cudaError_t qgemm_prepare();
 // Attention
 struct AttnScratch {
     float* part = nullptr;    // [KVH][NS][G][D+2]
-    unsigned* cnt = nullptr;  // [KVH]
-    int ns = 0;
+    unsigned* cnt = nullptr;  // [KVH], zero between launches
+    int ns = 0;               // splits the partials have room for
 };
-int attn_decode_splits(int n_kv_heads);
+// Splits the decode attention launches (grid.x) for this shape.
+int attn_decode_splits(int n_heads, int n_kv_heads, int max_ctx);
 size_t attn_decode_part_elems(int n_heads, int head_dim, int ns);
 cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, int kv_f16, int H, int KVH, int D,
                                int max_ctx, const int* pos_dev, int pos, const AttnScratch& scr, float* out,

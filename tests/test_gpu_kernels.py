@@ -173,6 +173,8 @@ ATTN_CASES = [  # H, KVH, D, ctx, pos, kv dtype
     (8, 4, 64, 64, 0, "f32"), (8, 4, 64, 64, 31, "f32"), (8, 4, 64, 64, 63, "f32"),
     (32, 4, 64, 2048, 2047, "f32"), (32, 8, 64, 4096, 1000, "f16"), (32, 8, 128, 8192, 4351, "f16"),
     (32, 8, 128, 32768, 30720, "f32"), (32, 8, 128, 32768, 30783, "f32"), (16, 16, 128, 300, 299, "f16"),
+    # one kv head: many splits, split length not dividing the sequence; ragged last tile
+    (8, 1, 64, 10000, 9728, "f16"), (8, 1, 128, 4096, 4000, "f32"), (2, 2, 64, 200, 130, "f32"),
 ]
 
 
