@@ -76,12 +76,12 @@ struct Allocs {
 
 Planes make_planes(Allocs& A, int wtype, int N, int K) {
     Planes P;
-    size_t qs_bytes = 0;
-    size_t total = planes_bytes(wtype, N, K, &qs_bytes);
+    size_t sc_off = 0;
+    size_t total = planes_bytes(wtype, N, K, &sc_off);
     uint8_t* buf = (uint8_t*)A.get(total);
     if (!buf) return P;
     P.qs = buf;
-    P.sc = (const __half*)(buf + qs_bytes);
+    P.sc = (const __half*)(buf + sc_off);
     P.N = N;
     P.K = K;
     P.Kp = padded_k(wtype, K);

@@ -18,6 +18,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace af {
 
@@ -53,7 +54,7 @@ constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMinPerSplit = 64;  // positions per split before another split is used
 constexpr int kTile = 64;         // cache slots per pipeline tile
-constexpr int kRing = 128 * 1024; // tile ring budget (one CTA per SM)
+constexpr int kRing = 96 * 1024;  // tile ring budget (leaves room for a GEMV CTA on the same SM)
 constexpr int kMaxScores = 64 * 1024;  // score buffer budget: split length x G floats
 
 template <int D, typename KT>
@@ -131,6 +132,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = blockIdx.y, s = blockIdx.x, ns = gridDim.x;
+    pdl_launch_dependents();
+    // the position word is written before the kernels of a step start; everything else the previous
+    // kernel writes (q, the cache slot at pos) is read after griddepcontrol.wait
     const int pos = pos_dev ? *pos_dev : pos_arg;
     const int n = pos + 1;
     int ns_eff, chunk;
@@ -151,11 +155,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const int n16 = keys * D * (int)sizeof(KT) / 16;
             for (int c = tid; c < n16; c += kDecThreads) cp_async16(dst + 16 * c, src + 16 * c);
         };
+        // tiles without slot pos stream in before waiting for the previous kernel
+        const bool has_pos = j0 + nl == n;
+        bool waited = false;
 #pragma unroll
         for (int t = 0; t < S - 1; t++) {
-            if (t < T) issue(t);
+            if (t < T) {
+                if (has_pos && !waited && (t == nt - 1 || t == T - 1)) {
+                    pdl_wait();
+                    waited = true;
+                }
+                issue(t);
+            }
             cp_async_commit();
         }
+        if (!waited) pdl_wait();
         // q of the group's heads, pre-scaled by 1/sqrt(D): lane's 8 dims of each head
         const int li = lane % LPK, ks = lane / LPK;
         float qv[G][8];
@@ -282,6 +296,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             my[tid * (D + 2) + D] = m_s[tid];
             my[tid * (D + 2) + D + 1] = l_s[tid];
         }
+    } else {
+        pdl_wait();  // the output and the split scratch are in use until the previous kernels finish
     }
     __threadfence();
     __syncthreads();
@@ -463,9 +479,18 @@ cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int 
     auto k = attn_decode_kernel<D, G, KT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e) return e;
-    k<<<dim3(ns, KVH), kDecThreads, smem, s>>>(q, (const KT*)kc, (const KT*)vc, max_ctx, pos_dev, pos, scr.part,
-                                               scr.cnt, out);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ns, KVH);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, q, (const KT*)kc, (const KT*)vc, max_ctx, pos_dev, pos, scr.part, scr.cnt,
+                              out);
 }
 
 template <int D, int G>

@@ -11,9 +11,13 @@ namespace af {
 // ---------------------------------------------------------------------------
 // Repacked weight layout ("planes").
 //
-// A GGUF [N, K] block matrix is split into two 16-byte aligned planes:
-//   qs : N rows x (Kp/32) blocks x QB bytes   (QB = 16 for Q4_0, 32 for Q8_0)
-//   sc : N rows x (Kp/32) fp16 scales
+// A GGUF [N, K] block matrix is stored as
+//   one record per row, qs_pitch() = (Kp/32) * (QB + 2) bytes apart:
+//     [(Kp/32) blocks x QB quant bytes][(Kp/32) fp16 scales]
+//   (QB = 16 for Q4_0, 32 for Q8_0), so R consecutive rows, scales included,
+//   are one contiguous range (one bulk copy per GEMV stage).
+//   qs points at row 0's quants, sc at row 0's scales; both advance by
+//   qs_pitch() bytes (= sc_pitch() halves) per row.
 // Kp = K rounded up to one GEMV chunk (1024 weights for Q4_0, 512 for Q8_0);
 // blocks past K hold zero quants and a zero scale, so they contribute 0.
 // Q4_0 quant bytes keep GGUF's nibble order (byte j: element j low, j+16 high).
@@ -23,18 +27,18 @@ struct Planes {
     const __half* sc = nullptr;
     int N = 0, K = 0, Kp = 0, wtype = 0;
     __host__ __device__ int qb() const { return wtype == AF_Q8_0 ? 32 : 16; }
-    __host__ __device__ int64_t qs_pitch() const { return (int64_t)(Kp / 32) * qb(); }  // bytes per row
-    __host__ __device__ int sc_pitch() const { return Kp / 32; }                          // halves per row
+    __host__ __device__ int64_t qs_pitch() const { return (int64_t)(Kp / 32) * (qb() + 2); }  // bytes per row
+    __host__ __device__ int sc_pitch() const { return (Kp / 32) * (qb() + 2) / 2; }           // halves per row
+    __host__ __device__ int sc_off() const { return (Kp / 32) * qb(); }  // byte offset of the scales in a row
 };
 
 inline int chunk_weights(int wtype) { return wtype == AF_Q8_0 ? 512 : 1024; }
 inline int padded_k(int wtype, int K) { int c = chunk_weights(wtype); return (K + c - 1) / c * c; }
-inline size_t planes_bytes(int wtype, int N, int K, size_t* qs_bytes) {
-    int Kp = padded_k(wtype, K);
-    size_t q = (size_t)N * (Kp / 32) * (wtype == AF_Q8_0 ? 32 : 16);
-    q = (q + 255) & ~(size_t)255;
-    if (qs_bytes) *qs_bytes = q;
-    return q + (((size_t)N * (Kp / 32) * 2 + 255) & ~(size_t)255);
+inline size_t planes_bytes(int wtype, int N, int K, size_t* sc_off) {
+    const int Kp = padded_k(wtype, K);
+    const size_t qb = wtype == AF_Q8_0 ? 32 : 16;
+    if (sc_off) *sc_off = (size_t)(Kp / 32) * qb;
+    return (((size_t)N * (Kp / 32) * (qb + 2)) + 255) & ~(size_t)255;
 }
 
 // ---------------------------------------------------------------------------

@@ -33,11 +33,10 @@ bool decode_gemv_task(const Planes& W, GemvTask& t) {
     t.WK = NC > 8 ? 16 : (NC > 4 ? 8 : (NC > 2 ? 4 : NC));  // 16 warps split long rows: one slot per lane
     if (NC > t.WK * UPL) return false;
     const int RS = kWarpsP / t.WK;
-    const int row_bytes = (int)W.qs_pitch() + W.sc_pitch() * 2;
+    const int row_bytes = (int)W.qs_pitch();  // quants and scales of a row
     t.R = kRWMax * RS < 32 ? kRWMax * RS : 32;
-    while (t.R > RS && t.R * (int)W.qs_pitch() + t.R * W.sc_pitch() * 2 > kSlotBytes) t.R /= 2;
-    (void)row_bytes;
-    if (t.R * (int)W.qs_pitch() + t.R * W.sc_pitch() * 2 > kSlotBytes) return false;
+    while (t.R > RS && t.R * row_bytes > kSlotBytes) t.R /= 2;
+    if (t.R * row_bytes > kSlotBytes) return false;
     if (t.R / RS > kRWMax) return false;
     return true;
 }

@@ -146,10 +146,8 @@ __device__ __forceinline__ RowRange cta_rows(const GemvTask& t) {
 __device__ __forceinline__ void gemv_issue_stage(Shared& sm, uint8_t* ring, const GemvTask& t, const RowRange& rr,
                                                  unsigned base, int st, uint64_t pol) {
     const int64_t pitch = t.W.qs_pitch();
-    const int scp = t.W.sc_pitch();
     const int ra = rr.r0 + st * t.R, nr = min(t.R, rr.r0 + rr.nrows - ra);
-    ring_issue(sm, ring, base + st, t.W.qs + (int64_t)ra * pitch, (unsigned)(nr * pitch), t.W.sc + (int64_t)ra * scp,
-               (unsigned)(nr * scp * 2), (unsigned)(t.R * pitch), pol);
+    ring_issue(sm, ring, base + st, t.W.qs + (int64_t)ra * pitch, (unsigned)(nr * pitch), nullptr, 0u, 0u, pol);
 }
 
 // Issue the first stages of a GEMV phase and the copy of its RMSNorm weight
@@ -190,7 +188,6 @@ __device__ unsigned gemv_run(Shared& sm, uint8_t* ring, const DecodePlan& p, con
     const int rs = warp / WK, wk = warp % WK;
     const int64_t pitch = W.qs_pitch();
     const int scp = W.sc_pitch();
-    const int qstage = t.R * (int)pitch;
     const RowRange rr = cta_rows(t);
     const Epi& epi = t.epi;  // shared memory
 
@@ -266,7 +263,7 @@ __device__ unsigned gemv_run(Shared& sm, uint8_t* ring, const DecodePlan& p, con
         const int slot = (int)(g % kSlots);
         if (!ring_wait(sm, p, g)) break;
         const uint8_t* qsm = ring + slot * kSlotBytes;
-        const unsigned short* ssm = reinterpret_cast<const unsigned short*>(qsm + qstage);
+        const unsigned short* ssm = reinterpret_cast<const unsigned short*>(qsm + W.sc_off());
         const int ra = rr.r0 + st * t.R, nr = min(t.R, rr.r0 + rr.nrows - ra);
         float acc[kRWMax];
 #pragma unroll

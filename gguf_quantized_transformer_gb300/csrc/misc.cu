@@ -17,7 +17,7 @@ int num_sms() {
     return n;
 }
 
-// GGUF AoS blocks -> quant plane + scale plane (see Planes).  One thread per
+// GGUF AoS blocks -> per-row records of quants then scales (see Planes).  One thread per
 // destination block; blocks past K/32 are zero.
 __global__ void repack_kernel(const uint8_t* __restrict__ src, int wtype, int N, int nb, uint8_t* __restrict__ qs,
                               __half* __restrict__ sc, int nbp, int row0, int step) {
@@ -25,15 +25,17 @@ __global__ void repack_kernel(const uint8_t* __restrict__ src, int wtype, int N,
     if (t >= (int64_t)N * nbp) return;
     int r = (int)(t / nbp), b = (int)(t % nbp);
     const int qb = wtype == AF_Q8_0 ? 32 : 16, bb = qb + 2;
+    const int64_t pitch = (int64_t)nbp * bb;  // bytes per destination row (quants, then scales)
     int64_t dr = (int64_t)row0 + (int64_t)r * step;
-    uint8_t* dq = qs + (dr * nbp + b) * qb;
+    uint8_t* dq = qs + dr * pitch + (int64_t)b * qb;
+    __half* dsc = sc + dr * (pitch / 2) + b;
     if (b < nb) {
         const uint8_t* s = src + ((int64_t)r * nb + b) * bb;
         unsigned short bits = (unsigned short)(s[0] | (s[1] << 8));
-        sc[dr * nbp + b] = __ushort_as_half(bits);
+        *dsc = __ushort_as_half(bits);
         for (int j = 0; j < qb; j++) dq[j] = s[2 + j];
     } else {
-        sc[dr * nbp + b] = __ushort_as_half(0);
+        *dsc = __ushort_as_half(0);
         for (int j = 0; j < qb; j++) dq[j] = 0;
     }
 }
