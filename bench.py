@@ -30,6 +30,10 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up GEMV launch, Q4_0 28672 x 4096, from the
+# ncu capture summarised in profiles/qgemv_q4_0_28672x4096.md; valid only for the kernel sources it was taken on.
+GEMV_SOURCES = ["qgemv.cu", "gemv_common.cuh", "tma.cuh", "common.cuh"]
+GEMV_TRAFFIC = {"sources_sha256_16": "23c35e1e6d5755b9", "wtype": "q4_0", "N": 28672, "K": 4096, "bytes": 66189312}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -295,11 +299,11 @@ def run_ours(args, cfg, world, rank, local):
         "prefill_tok_s": prefill_tps, "decode_tok_s": decode_tps,
         "decode_hbm_gbs": dec_gbs, "decode_hbm_frac": dec_gbs / hbm_peak,
         "prefill_tflops": pf_tflops,
-        "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": dec_gbs / hbm_peak, "traffic": None,
-                     "kernel": "decode step (GEMVs + attention + LM head; per-token algorithmic bytes = "
-                               "quantized weights + KV read)", "peak_source": peak_src},
-        "roofline_qgemv": qg,
+        "roofline": dict(qg, peak_source=peak_src),
+        "decode_step_roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
+                                 "frac": dec_gbs / hbm_peak, "traffic": None,
+                                 "kernel": "decode step (GEMVs + attention + LM head; per-token algorithmic bytes = "
+                                           "quantized weights + KV read)", "peak_source": peak_src},
         "cpu_baseline": None,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -345,8 +349,22 @@ def qgemv_roofline(af, cfg, dev, hbm_peak, reps=50):
     ms = float(np.mean(times))
     gbs = nbytes / (ms / 1000) / 1e9
     return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-            "traffic": None, "kernel": f"qgemv {cfg.wtype} [{N}x{K}] (L2 flushed between launches)",
+            "traffic": gemv_traffic(cfg.wtype, N, K),
+            "kernel": f"qgemv {cfg.wtype} [{N}x{K}] gate|up (L2 flushed between launches)",
             "bytes_per_launch": nbytes, "us_per_launch": ms * 1000}
+
+
+def gemv_traffic(wtype, N, K):
+    """ncu DRAM bytes per launch for this shape, or None once the kernel's sources differ from the captured ones."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMV_SOURCES:
+        with open(os.path.join(ROOT, "gguf_quantized_transformer_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    t = GEMV_TRAFFIC
+    if h.hexdigest()[:16] != t["sources_sha256_16"] or (wtype, N, K) != (t["wtype"], t["N"], t["K"]):
+        return None
+    return t["bytes"]
 
 
 def e2e_run(af, m, prompt, cfg, args):
