@@ -558,7 +558,7 @@ int prefill_impl(af_model* m, const int* tok_dev, int n, int start_pos, float* l
         CK(launch_qgemm(lw.qkv, m->y16[0], m->y16[1], E, n, epi_qkv(m, l, m->q, nullptr, start_pos),
                         m->gs.err, s));
         CK(launch_attn_prefill(m->q, QD, m->kl(l), m->vl(l), c.kv_dtype == AF_F16, c.n_heads, c.n_kv_heads,
-                               c.head_dim, c.max_ctx, start_pos, n, m->a16[0], m->a16[1], QD, s));
+                               c.head_dim, c.max_ctx, start_pos, n, m->a16[0], m->a16[1], QD, m->gs.err, s));
         CK(launch_qgemm(lw.o, m->a16[0], m->a16[1], QD, n, epi_simple(EPI_RESID, m->x, E), m->gs.err, s));
         CK(launch_rmsnorm_rows(m->x, n, E, lw.ffn_norm, c.rms_eps, m->y16[0], m->y16[1], s));
         Epi eg = epi_simple(EPI_SWIGLU, nullptr, F);

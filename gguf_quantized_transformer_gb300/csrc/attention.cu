@@ -10,9 +10,7 @@
 // Each CTA stores (o, max, sum) for its range; the last CTA of a kv head to
 // finish (acq_rel counter) merges the splits with the usual max-rescaling.
 //
-// Prefill (S query rows at positions p0..p0+S-1): CTA per (query tile, kv
-// head) with 32 query vectors (QT rows x G heads); K/V tiles of 64 slots in
-// shared memory; online softmax per query vector; causal mask j <= p0 + r.
+// Prefill attention runs on the tensor cores (attn_prefill_tc.cu).
 #include <math_constants.h>
 
 #include <algorithm>
@@ -346,130 +344,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (tid == 0) cnt[g] = 0u;
 }
 
-// ---------------------------------------------------------------- prefill
-constexpr int kPreThreads = 256;  // 8 warps x 4 query vectors
-constexpr int kKT = 64;           // keys per tile
-
-template <int D, int G, typename KT>
-__global__ void __launch_bounds__(kPreThreads)
-    attn_prefill_kernel(const float* __restrict__ q, int64_t ldq, const KT* __restrict__ kc, const KT* __restrict__ vc,
-                        int max_ctx, int pos0, int S, __half* __restrict__ out_hi, __half* __restrict__ out_lo,
-                        int64_t ldo) {
-    constexpr int QT = 32 / G;  // query rows per CTA
-    constexpr int DP = D + 1;   // padded K row
-    extern __shared__ float smem[];
-    float* Qs = smem;                 // [32][D]   query vector v = rr*G + h
-    float* Ks = Qs + 32 * D;          // [kKT][DP]
-    float* Vs = Ks + kKT * DP;        // [kKT][D]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = blockIdx.y, r0 = blockIdx.x * QT;
-    const KT* K = kc + (int64_t)g * max_ctx * D;
-    const KT* V = vc + (int64_t)g * max_ctx * D;
-    const float scale = rsqrtf((float)D);
-
-    for (int t = tid; t < 32 * D; t += kPreThreads) {
-        const int v = t / D, d = t % D, rr = v / G, h = v % G;
-        const int r = min(r0 + rr, S - 1);
-        Qs[t] = q[(int64_t)r * ldq + (g * G + h) * D + d] * scale;
-    }
-    constexpr int DD = D / 32;  // dims per lane in the accumulator
-    float acc[4][DD], mrow[4], lrow[4];
-#pragma unroll
-    for (int a = 0; a < 4; a++) {
-        mrow[a] = -CUDART_INF_F;
-        lrow[a] = 0.f;
-#pragma unroll
-        for (int d = 0; d < DD; d++) acc[a][d] = 0.f;
-    }
-    const int rmax = min(r0 + QT, S) - 1;
-    const int nkeys = pos0 + rmax + 1;
-    for (int kt = 0; kt < nkeys; kt += kKT) {
-        __syncthreads();
-        for (int t = tid; t < kKT * D / 4; t += kPreThreads) {
-            const int j = t / (D / 4), d4 = (t % (D / 4)) * 4;
-            float kf[4], vf[4];
-            if (kt + j < nkeys) {
-                if (sizeof(KT) == 4) {
-                    load_vec<float>(reinterpret_cast<const float*>(K) + (int64_t)(kt + j) * D + d4, kf, 4);
-                    load_vec<float>(reinterpret_cast<const float*>(V) + (int64_t)(kt + j) * D + d4, vf, 4);
-                } else {
-                    const __half* kh = reinterpret_cast<const __half*>(K) + (int64_t)(kt + j) * D + d4;
-                    const __half* vh = reinterpret_cast<const __half*>(V) + (int64_t)(kt + j) * D + d4;
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        kf[e] = __half2float(kh[e]);
-                        vf[e] = __half2float(vh[e]);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; e++) kf[e] = vf[e] = 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                Ks[j * DP + d4 + e] = kf[e];
-                Vs[j * D + d4 + e] = vf[e];
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int a = 0; a < 4; a++) {
-            const int v = warp * 4 + a, rr = v / G;
-            const int r = r0 + rr;
-            if (r >= S) continue;  // warp-uniform
-            const int lim = pos0 + r;  // causal: keys j <= pos0 + r
-            const float* qv = Qs + v * D;
-            float s0 = 0.f, s1 = 0.f;
-            const float* k0 = Ks + lane * DP;
-            const float* k1 = Ks + (lane + 32) * DP;
-#pragma unroll 8
-            for (int d = 0; d < D; d++) {
-                const float qd = qv[d];
-                s0 = fmaf(qd, k0[d], s0);
-                s1 = fmaf(qd, k1[d], s1);
-            }
-            if (kt + lane > lim) s0 = -CUDART_INF_F;
-            if (kt + lane + 32 > lim) s1 = -CUDART_INF_F;
-            float mt = fmaxf(s0, s1);
-            for (int o = 16; o; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-            const float mnew = fmaxf(mrow[a], mt);
-            if (mnew == -CUDART_INF_F) continue;  // whole tile masked (cannot happen for kt <= lim)
-            const float alpha = __expf(mrow[a] - mnew);
-            const float p0 = __expf(s0 - mnew), p1 = __expf(s1 - mnew);
-            float ps = p0 + p1;
-            for (int o = 16; o; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-            lrow[a] = lrow[a] * alpha + ps;
-            mrow[a] = mnew;
-#pragma unroll
-            for (int d = 0; d < DD; d++) acc[a][d] *= alpha;
-            for (int j = 0; j < 32; j++) {
-                const float pj0 = __shfl_sync(0xffffffffu, p0, j);
-                const float pj1 = __shfl_sync(0xffffffffu, p1, j);
-#pragma unroll
-                for (int d = 0; d < DD; d++) {
-                    acc[a][d] = fmaf(pj0, Vs[j * D + lane + 32 * d], acc[a][d]);
-                    acc[a][d] = fmaf(pj1, Vs[(j + 32) * D + lane + 32 * d], acc[a][d]);
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int a = 0; a < 4; a++) {
-        const int v = warp * 4 + a, rr = v / G, h = v % G;
-        const int r = r0 + rr;
-        if (r >= S) continue;
-        const float inv = 1.f / lrow[a];
-#pragma unroll
-        for (int d = 0; d < DD; d++) {
-            const float o = acc[a][d] * inv;
-            const int64_t idx = (int64_t)r * ldo + (g * G + h) * D + lane + 32 * d;
-            const __half oh = __float2half_rn(o);
-            out_hi[idx] = oh;
-            out_lo[idx] = __float2half_rn(o - __half2float(oh));
-        }
-    }
-}
-
 template <int D, int G, typename KT>
 cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int max_ctx, const int* pos_dev, int pos,
                             const AttnScratch& scr, int ns, float* out, int KVH, cudaStream_t s) {
@@ -499,26 +373,6 @@ cudaError_t dispatch_decode(const float* q, const void* kc, const void* vc, int 
                             cudaStream_t s) {
     if (kv_f16) return launch_decode_t<D, G, __half>(q, kc, vc, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
     return launch_decode_t<D, G, float>(q, kc, vc, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
-}
-
-template <int D, int G>
-cudaError_t dispatch_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int KVH,
-                             int max_ctx, int pos0, int S, __half* out, __half* out16, int64_t ldo, cudaStream_t s) {
-    constexpr int QT = 32 / G;
-    const size_t smem = sizeof(float) * (32 * D + kKT * (D + 1) + kKT * D);
-    dim3 grid((S + QT - 1) / QT, KVH);
-    if (kv_f16) {
-        auto k = attn_prefill_kernel<D, G, __half>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, kPreThreads, smem, s>>>(q, ldq, (const __half*)kc, (const __half*)vc, max_ctx, pos0, S, out, out16,
-                                          ldo);
-    } else {
-        auto k = attn_prefill_kernel<D, G, float>;
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        k<<<grid, kPreThreads, smem, s>>>(q, ldq, (const float*)kc, (const float*)vc, max_ctx, pos0, S, out, out16,
-                                          ldo);
-    }
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -561,13 +415,6 @@ cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, i
     if (scr.ns < ns) return cudaErrorInvalidValue;  // scratch sized for fewer splits
     if ((reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & 15) return cudaErrorInvalidValue;
     AF_ATTN_DISPATCH(dispatch_decode, q, kc, vc, kv_f16, max_ctx, pos_dev, pos, scr, ns, out, KVH, s)
-}
-
-cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int H,
-                                int KVH, int D, int max_ctx, int pos0, int S, __half* out, __half* out16,
-                                int64_t ldo, cudaStream_t s) {
-    const int G = H / KVH;
-    AF_ATTN_DISPATCH(dispatch_prefill, q, ldq, kc, vc, kv_f16, KVH, max_ctx, pos0, S, out, out16, ldo, s)
 }
 
 }  // namespace af

@@ -175,9 +175,11 @@ size_t attn_decode_part_elems(int n_heads, int head_dim, int ns);
 cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, int kv_f16, int H, int KVH, int D,
                                int max_ctx, const int* pos_dev, int pos, const AttnScratch& scr, float* out,
                                cudaStream_t s);
+// Causal prefill attention on the tensor cores: S query rows at positions pos0.. (q fp32 [S][ldq], rotated),
+// output as fp16 hi + lo planes [S][ldo].  err: device error word.
 cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int H,
                                 int KVH, int D, int max_ctx, int pos0, int S, __half* out_hi, __half* out_lo,
-                                int64_t ldo, cudaStream_t s);
+                                int64_t ldo, unsigned* err, cudaStream_t s);
 bool attn_supported(int H, int KVH, int D);
 
 // Capacity of the fixed decode-attention scratch (a file-scope device array, no allocation).
