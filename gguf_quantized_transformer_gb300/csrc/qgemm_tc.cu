@@ -11,13 +11,19 @@
 //   X_hi W_hi + X_lo W_hi + X_hi W_lo
 // in fp32 (the dropped X_lo W_lo term is ~2^-22 relative).
 //
-// Tile 128 (rows of X) x 256 (rows of W) x 64 (K), two stages in shared
-// memory, SWIZZLE_128B K-major operand layout:
+// Tile 128 (rows of X) x BN (rows of W: 256, or 128 when N is small so the
+// grid still covers the SMs) x 64 (K), two or three stages in shared memory,
+// SWIZZLE_128B K-major operand layout:
 //   warp 0      : TMA producer for the X_hi / X_lo tiles (cp.async.bulk.tensor.2d)
 //   warp 1      : TMEM allocation; one lane issues the MMAs and commits
-//   warps 2..9  : dequantize the W tile (one weight row per thread) into the
-//                 W_hi / W_lo tiles; warps 2..5 then run the fused epilogue
-//                 from TMEM (tcgen05.ld, 32 columns at a time).
+//   warps 2..9  : dequantize the W tile (256 / BN threads per weight row) into
+//                 the W_hi / W_lo tiles; the raw blocks of the next K step are
+//                 loaded into registers before waiting for a free stage.  The
+//                 split is exact fp16 arithmetic: with c the integer code
+//                 (exact in fp16), w_hi = d * c rounded (HMUL2) and
+//                 w_lo = fma(d, c, -w_hi) (HFMA2, exact);
+//                 warps 2..5 then run the fused epilogue from TMEM
+//                 (tcgen05.ld, 32 columns at a time).
 // Every mbarrier wait is bounded; on a timeout the CTA records DEV_TIMEOUT,
 // drains what it issued and frees its TMEM before returning.
 #include <cuda.h>
@@ -30,20 +36,104 @@ namespace af {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 2;
+constexpr int BM = 128, BK = 64;
 constexpr int kATile = BM * BK * 2;  // 16 KB per fp16 plane
-constexpr int kBTile = BN * BK * 2;  // 32 KB per fp16 plane
-constexpr int kStageBytes = 2 * kATile + 2 * kBTile;
 constexpr int kThreads = 10 * 32;
-constexpr int kDequantThreads = 8 * 32;  // == BN: one weight row per thread
-constexpr int kTmemCols = 256;           // fp32 accumulator, BN columns
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kDequantThreads = 8 * 32;
+constexpr int kMaxStages = 3;
 
-static_assert(kDequantThreads == BN, "one dequant thread per weight row");
+template <int BN>
+struct TcCfg {
+    static constexpr int kBTile = BN * BK * 2;  // one fp16 plane
+    static constexpr int kStageBytes = 2 * kATile + 2 * kBTile;
+    static constexpr int kStages = BN == 256 ? 2 : 3;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+    static constexpr int TPR = kDequantThreads / BN;                // dequant threads per weight row
+    static constexpr int BPT = 2 / TPR;                              // 32-weight blocks per thread per K step
+    static constexpr uint32_t kIdesc = idesc_f16(BM, BN);
+};
 
-// Instruction descriptor of this GEMM's tile.
-constexpr uint32_t kIdesc = idesc_f16(BM, BN);
+// One 32-weight block as loaded from the weight rows: quant bytes and the fp16 scale bits.
+template <int WT>
+struct RawBlk;
+template <>
+struct RawBlk<AF_Q4_0> {
+    uint4 q;
+    unsigned short d;
+};
+template <>
+struct RawBlk<AF_Q8_0> {
+    uint4 q0, q1;
+    unsigned short d;
+};
+
+__device__ __forceinline__ void load_blk(const Planes& W, int n, int blk, RawBlk<AF_Q4_0>& b) {
+    b.q = *reinterpret_cast<const uint4*>(W.qs + (int64_t)n * W.qs_pitch() + (int64_t)blk * 16);
+    b.d = __half_as_ushort(W.sc[(int64_t)n * W.sc_pitch() + blk]);
+}
+__device__ __forceinline__ void load_blk(const Planes& W, int n, int blk, RawBlk<AF_Q8_0>& b) {
+    const uint8_t* q = W.qs + (int64_t)n * W.qs_pitch() + (int64_t)blk * 32;
+    b.q0 = *reinterpret_cast<const uint4*>(q);
+    b.q1 = *reinterpret_cast<const uint4*>(q + 16);
+    b.d = __half_as_ushort(W.sc[(int64_t)n * W.sc_pitch() + blk]);
+}
+__device__ __forceinline__ void zero_blk(RawBlk<AF_Q4_0>& b) { b.q = make_uint4(0, 0, 0, 0); b.d = 0; }
+__device__ __forceinline__ void zero_blk(RawBlk<AF_Q8_0>& b) {
+    b.q0 = make_uint4(0, 0, 0, 0);
+    b.q1 = b.q0;
+    b.d = 0;
+}
+
+__device__ __forceinline__ __half2 u2h(unsigned v) { return *reinterpret_cast<const __half2*>(&v); }
+__device__ __forceinline__ unsigned h2u(__half2 v) { return *reinterpret_cast<const unsigned*>(&v); }
+
+// codes c (fp16, exact) times d -> exact split hi + lo
+__device__ __forceinline__ void split_pair(__half2 c, __half2 d2, unsigned& hi, unsigned& lo) {
+    const __half2 h = __hmul2(c, d2);
+    hi = h2u(h);
+    lo = h2u(__hfma2(c, d2, __hneg2(h)));
+}
+
+// 32 weights of a block -> 4 chunks (8 weights each, block order) of fp16 hi and lo
+__device__ __forceinline__ void deq_blk(const RawBlk<AF_Q4_0>& b, uint4 (&hi)[4], uint4 (&lo)[4]) {
+    const __half2 d2 = __half2half2(__ushort_as_half(b.d));
+    const __half2 k1032 = __float2half2_rn(1032.f);
+    const unsigned w[4] = {b.q.x, b.q.y, b.q.z, b.q.w};
+    unsigned h[16], l[16];  // h[4*i + t]: i = 0,1 low-nibble pairs (x, y), i = 2,3 high-nibble pairs, word t
+#pragma unroll
+    for (int t = 0; t < 4; t++) {
+        const unsigned x = __byte_perm(w[t], 0u, 0x4140);  // bytes b0, 0, b1, 0
+        const unsigned y = __byte_perm(w[t], 0u, 0x4342);  // bytes b2, 0, b3, 0
+        const unsigned c[4] = {(x & 0x000F000Fu) | 0x64006400u, (y & 0x000F000Fu) | 0x64006400u,
+                               ((x >> 4) & 0x000F000Fu) | 0x64006400u, ((y >> 4) & 0x000F000Fu) | 0x64006400u};
+#pragma unroll
+        for (int i = 0; i < 4; i++) split_pair(__hsub2(u2h(c[i]), k1032), d2, h[4 * i + t], l[4 * i + t]);
+    }
+    // chunk 0: elements 0..7 = low nibbles of words 0, 1; chunk 1: words 2, 3; chunks 2, 3: high nibbles
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        const int i0 = q < 2 ? 0 : 2, t0 = (q & 1) * 2;
+        hi[q] = make_uint4(h[4 * i0 + t0], h[4 * (i0 + 1) + t0], h[4 * i0 + t0 + 1], h[4 * (i0 + 1) + t0 + 1]);
+        lo[q] = make_uint4(l[4 * i0 + t0], l[4 * (i0 + 1) + t0], l[4 * i0 + t0 + 1], l[4 * (i0 + 1) + t0 + 1]);
+    }
+}
+__device__ __forceinline__ void deq_blk(const RawBlk<AF_Q8_0>& b, uint4 (&hi)[4], uint4 (&lo)[4]) {
+    const __half2 d2 = __half2half2(__ushort_as_half(b.d));
+    const __half2 k1152 = __float2half2_rn(1152.f);
+    const unsigned w[8] = {b.q0.x, b.q0.y, b.q0.z, b.q0.w, b.q1.x, b.q1.y, b.q1.z, b.q1.w};
+    unsigned h[16], l[16];
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        const unsigned u = w[t] ^ 0x80808080u;  // q + 128 in 0..255
+        split_pair(__hsub2(u2h(__byte_perm(u, 0x64646464u, 0x5140)), k1152), d2, h[2 * t], l[2 * t]);
+        split_pair(__hsub2(u2h(__byte_perm(u, 0x64646464u, 0x5342)), k1152), d2, h[2 * t + 1], l[2 * t + 1]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+        hi[q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+        lo[q] = make_uint4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+    }
+}
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
@@ -54,10 +144,10 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 }
 
 struct TcSmem {
-    uint64_t full_a[kStages];  // X tiles landed (TMA transaction bytes)
-    uint64_t full_b[kStages];  // W tiles written (kDequantThreads arrivals)
-    uint64_t empty[kStages];   // MMAs reading the stage finished (commit)
-    uint64_t done;             // all MMAs finished (commit)
+    uint64_t full_a[kMaxStages];  // X tiles landed (TMA transaction bytes)
+    uint64_t full_b[kMaxStages];  // W tiles written (kDequantThreads arrivals)
+    uint64_t empty[kMaxStages];   // MMAs reading the stage finished (commit)
+    uint64_t done;                // all MMAs finished (commit)
     uint32_t tmem_base;
     volatile int abort;
     int issued_a;  // X tile loads issued so far
@@ -73,10 +163,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, unsigned parity, Tc
     return false;
 }
 
-template <int WT>
+template <int WT, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo, Planes W,
                     int M, Epi epi, unsigned* err) {
+    using C = TcCfg<BN>;
+    constexpr int kStages = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     __shared__ TcSmem sm;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -95,21 +187,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.issued_a = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {  // TMEM accumulator (whole warp)
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm.tmem_base)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1) tmem_alloc(&sm.tmem_base, BN);  // fp32 accumulator, BN columns
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    auto a_hi = [&](int s) { return smem + s * kStageBytes; };
-    auto a_lo = [&](int s) { return smem + s * kStageBytes + kATile; };
-    auto b_hi = [&](int s) { return smem + s * kStageBytes + 2 * kATile; };
-    auto b_lo = [&](int s) { return smem + s * kStageBytes + 2 * kATile + kBTile; };
+    auto a_hi = [&](int s) { return smem + s * C::kStageBytes; };
+    auto a_lo = [&](int s) { return smem + s * C::kStageBytes + kATile; };
+    auto b_hi = [&](int s) { return smem + s * C::kStageBytes + 2 * kATile; };
+    auto b_lo = [&](int s) { return smem + s * C::kStageBytes + 2 * kATile + C::kBTile; };
 
     if (warp == 0) {
         // ---------------- TMA producer: X_hi, X_lo tiles
@@ -137,9 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < BK / 16; kk++) {  // 16 fp16 = 32 bytes along K per MMA
                     const uint32_t off = kk * 32;
                     const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
-                    mma_f16(tmem, umma_desc_sw128(ah + off), umma_desc_sw128(bh + off), kIdesc, acc);
-                    mma_f16(tmem, umma_desc_sw128(al + off), umma_desc_sw128(bh + off), kIdesc, 1u);
-                    mma_f16(tmem, umma_desc_sw128(ah + off), umma_desc_sw128(bl + off), kIdesc, 1u);
+                    mma_f16(tmem, umma_desc_sw128(ah + off), umma_desc_sw128(bh + off), C::kIdesc, acc);
+                    mma_f16(tmem, umma_desc_sw128(al + off), umma_desc_sw128(bh + off), C::kIdesc, 1u);
+                    mma_f16(tmem, umma_desc_sw128(ah + off), umma_desc_sw128(bl + off), C::kIdesc, 1u);
                 }
                 mma_commit(&sm.empty[s]);  // frees the stage when these MMAs complete
             }
@@ -147,53 +234,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- dequantize W rows into the fp16 hi / lo tiles
-        const int r = tid - 64;  // 0..255: weight row n0 + r
+        const int dt = tid - 64;                // 0..255
+        const int r = dt / C::TPR;              // weight row n0 + r of the tile
+        const int bsel = dt % C::TPR;           // which block of a K step (two threads per row)
         const int n = n0 + r;
-        const int64_t pitch = W.qs_pitch();
-        const int scp = W.sc_pitch();
+        const bool valid = n < W.N;
+        RawBlk<WT> cur[C::BPT], nxt[C::BPT];
+        auto fetch = [&](int ks, RawBlk<WT> (&b)[C::BPT]) {
+#pragma unroll
+            for (int i = 0; i < C::BPT; i++) {
+                if (valid) load_blk(W, n, ks * 2 + (C::TPR == 1 ? i : bsel), b[i]);
+                else zero_blk(b[i]);
+            }
+        };
+        fetch(0, cur);
         for (int ks = 0; ks < nk; ks++) {
             const int s = ks % kStages, u = ks / kStages;
+            if (ks + 1 < nk) fetch(ks + 1, nxt);  // next K step's blocks in flight while this one is converted
             if (u > 0 && !wait_or_abort(&sm.empty[s], (u - 1) & 1, sm, err)) break;
-            float w[64];
-            if (n < W.N) {
-                const int kb = ks * 2;  // two 32-weight blocks per K step
 #pragma unroll
-                for (int b = 0; b < 2; b++) {
-                    const float d = __half2float(W.sc[(int64_t)n * scp + kb + b]);
-                    const uint8_t* q = W.qs + (int64_t)n * pitch + (int64_t)(kb + b) * W.qb();
-                    if (WT == AF_Q8_0) {
-                        const uint4 q0 = *reinterpret_cast<const uint4*>(q);
-                        const uint4 q1 = *reinterpret_cast<const uint4*>(q + 16);
-                        const uint32_t ws[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            for (int i = 0; i < C::BPT; i++) {
+                uint4 hi[4], lo[4];
+                deq_blk(cur[i], hi, lo);
+                const int c0 = 4 * (C::TPR == 1 ? i : bsel);  // first 16-byte chunk of this block in the row
 #pragma unroll
-                        for (int j = 0; j < 32; j++) w[b * 32 + j] = d * (float)(int8_t)((ws[j >> 2] >> (8 * (j & 3))) & 0xFF);
-                    } else {
-                        const uint4 q0 = *reinterpret_cast<const uint4*>(q);
-                        const uint32_t ws[4] = {q0.x, q0.y, q0.z, q0.w};
-#pragma unroll
-                        for (int j = 0; j < 16; j++) {
-                            const uint32_t byte = (ws[j >> 2] >> (8 * (j & 3))) & 0xFF;
-                            w[b * 32 + j] = d * (float)((int)(byte & 15) - 8);
-                            w[b * 32 + 16 + j] = d * (float)((int)(byte >> 4) - 8);
-                        }
-                    }
+                for (int q = 0; q < 4; q++) {
+                    *reinterpret_cast<uint4*>(b_hi(s) + sw128(r, c0 + q)) = hi[q];
+                    *reinterpret_cast<uint4*>(b_lo(s) + sw128(r, c0 + q)) = lo[q];
                 }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 64; j++) w[j] = 0.f;
-            }
-#pragma unroll
-            for (int c = 0; c < 8; c++) {
-                float w8[8];
-#pragma unroll
-                for (int e = 0; e < 8; e++) w8[e] = w[8 * c + e];
-                uint4 hi, lo;
-                split8(w8, hi, lo);
-                *reinterpret_cast<uint4*>(b_hi(s) + sw128(r, c)) = hi;
-                *reinterpret_cast<uint4*>(b_lo(s) + sw128(r, c)) = lo;
             }
             fence_proxy_async_shared();  // generic-proxy writes -> visible to the tensor core
             mbar_arrive(&sm.full_b[s]);
+#pragma unroll
+            for (int i = 0; i < C::BPT; i++) cur[i] = nxt[i];
         }
         // ---------------- epilogue (warps 2..5: TMEM lane quadrant = warp % 4)
         if (warp < 6) {
@@ -227,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+        tmem_free(tmem, BN);
     }
 }
 
@@ -264,10 +337,15 @@ bool make_map(CUtensorMap* map, const __half* base, int rows, int cols, int64_t 
 }  // namespace
 
 cudaError_t qgemm_prepare() {
-    cudaError_t e = cudaFuncSetAttribute(qgemm_tc_kernel<AF_Q4_0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
-    if (!e)
-        e = cudaFuncSetAttribute(qgemm_tc_kernel<AF_Q8_0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaSuccess;
+#define AF_QGEMM_ATTR(WT, BN)                                                                                  \
+    if (!e) e = cudaFuncSetAttribute(qgemm_tc_kernel<WT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                     TcCfg<BN>::kSmemBytes);
+    AF_QGEMM_ATTR(AF_Q4_0, 256)
+    AF_QGEMM_ATTR(AF_Q4_0, 128)
+    AF_QGEMM_ATTR(AF_Q8_0, 256)
+    AF_QGEMM_ATTR(AF_Q8_0, 128)
+#undef AF_QGEMM_ATTR
     return e;
 }
 
@@ -278,11 +356,22 @@ cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo
         return cudaErrorInvalidValue;  // TMA: 16-byte aligned base and row stride
     CUtensorMap mh, ml;
     if (!make_map(&mh, X_hi, M, W.K, ldx) || !make_map(&ml, X_lo, M, W.K, ldx)) return cudaErrorInvalidValue;
-    dim3 grid((W.N + BN - 1) / BN, (M + BM - 1) / BM);
-    if (W.wtype == AF_Q4_0)
-        qgemm_tc_kernel<AF_Q4_0><<<grid, kThreads, kSmemBytes, s>>>(mh, ml, W, M, epi, err);
-    else
-        qgemm_tc_kernel<AF_Q8_0><<<grid, kThreads, kSmemBytes, s>>>(mh, ml, W, M, epi, err);
+    const int mt = (M + BM - 1) / BM;
+    // 256-wide tiles unless that leaves a third or more of the SMs without a tile
+    const bool narrow = (int64_t)((W.N + 255) / 256) * mt * 3 < (int64_t)num_sms() * 2;
+    if (narrow) {
+        dim3 grid((W.N + 127) / 128, mt);
+        if (W.wtype == AF_Q4_0)
+            qgemm_tc_kernel<AF_Q4_0, 128><<<grid, kThreads, TcCfg<128>::kSmemBytes, s>>>(mh, ml, W, M, epi, err);
+        else
+            qgemm_tc_kernel<AF_Q8_0, 128><<<grid, kThreads, TcCfg<128>::kSmemBytes, s>>>(mh, ml, W, M, epi, err);
+    } else {
+        dim3 grid((W.N + 255) / 256, mt);
+        if (W.wtype == AF_Q4_0)
+            qgemm_tc_kernel<AF_Q4_0, 256><<<grid, kThreads, TcCfg<256>::kSmemBytes, s>>>(mh, ml, W, M, epi, err);
+        else
+            qgemm_tc_kernel<AF_Q8_0, 256><<<grid, kThreads, TcCfg<256>::kSmemBytes, s>>>(mh, ml, W, M, epi, err);
+    }
     return cudaGetLastError();
 }
 
