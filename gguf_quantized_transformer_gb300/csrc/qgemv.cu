@@ -11,8 +11,10 @@
 // griddepcontrol.wait (weights do not depend on the previous kernel), so the
 // ring (up to 192 KB) fills while the prologue runs.
 //
-// Activations.  The prologue (all threads) reduces sum(x^2) for the optional
-// RMSNorm and converts x, 32 elements at a time, to 16-bit fixed point with a
+// Activations.  The prologue (all threads) reads x once: it reduces sum(x^2)
+// for the optional RMSNorm and converts w (.) x (the norm weight times x; the
+// scalar RMS factor is applied to each row's result), 32 elements at a time,
+// to 16-bit fixed point with a
 // power-of-two scale per block: x_j ~= s * xi_j, |xi_j| <= 32767 (relative
 // error <= 2^-16 of the block maximum).  The integers are stored in shared
 // memory as two byte planes (high byte signed, low byte unsigned; four
@@ -52,6 +54,7 @@ constexpr int kMaxCtaRows = 512;        // residual rows a CTA may own (preloade
 constexpr int kMaxRing = 12;
 constexpr int kRingBudget = 192 * 1024;  // ring, x images inside (one CTA per SM)
 constexpr int kMinStage = 24 * 1024;     // stage size target: enough work per warp between waits
+constexpr int kMaxStage = 64 * 1024;     // largest stage that still leaves three in the ring
 constexpr int kXBlkBytes = 80;          // shared image of one 32-element x block
 constexpr int kMaxGemvSmem = 208 * 1024;
 
@@ -132,9 +135,12 @@ __host__ __device__ constexpr int units_per_lane() { return WT == AF_Q4_0 ? 4 : 
 
 // Convert x (optionally RMS-normalized) to the fixed-point block images.
 // Eight lanes per block, lane g of the group holds elements 4g..4g+3.
+// With NORM the images hold w (.) x (the RMS factor is a scalar, applied to each row's dot product in the
+// epilogue) and the return value is this thread's part of sum(x^2), from the same loads.
 template <bool NORM>
-__device__ __forceinline__ void quantize_x(const float* __restrict__ x, const float* __restrict__ nw, float rstd,
-                                           int K, int nblk, XBlk* xb, int tid) {
+__device__ __forceinline__ float quantize_x(const float* __restrict__ x, const float* __restrict__ nw, int K,
+                                            int nblk, XBlk* xb, int tid) {
+    float ss = 0.f;
     constexpr int kBlkPerRound = kThreads / 8;
     constexpr int kBatch = 4;  // rounds whose global loads are in flight together
     const int g = tid & 7;
@@ -150,9 +156,9 @@ __device__ __forceinline__ void quantize_x(const float* __restrict__ x, const fl
                 const float4 xv = *reinterpret_cast<const float4*>(x + k);
                 v[i][0] = xv.x; v[i][1] = xv.y; v[i][2] = xv.z; v[i][3] = xv.w;
                 if (NORM) {
+                    ss = fmaf(xv.x, xv.x, fmaf(xv.y, xv.y, fmaf(xv.z, xv.z, fmaf(xv.w, xv.w, ss))));
                     const float4 w = *reinterpret_cast<const float4*>(nw + k);
-                    v[i][0] = w.x * (v[i][0] * rstd); v[i][1] = w.y * (v[i][1] * rstd);
-                    v[i][2] = w.z * (v[i][2] * rstd); v[i][3] = w.w * (v[i][3] * rstd);
+                    v[i][0] *= w.x; v[i][1] *= w.y; v[i][2] *= w.z; v[i][3] *= w.w;
                 }
             }
         }
@@ -193,6 +199,7 @@ __device__ __forceinline__ void quantize_x(const float* __restrict__ x, const fl
             }
         }
     }
+    return ss;
 }
 
 template <int WT, bool NORM, int WK, int PPW>
@@ -257,23 +264,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     pdl_wait();  // x (and the residual rows) are written by the previous kernel
 
-    float rstd = 1.f;
-    if (NORM) {  // RMSNorm prologue: every CTA reduces sum(x^2) over the whole input
-        float ss = 0.f;
-        const float4* x4 = reinterpret_cast<const float4*>(x);
-        for (int k4 = tid; k4 < K / 4; k4 += kThreads) {
-            const float4 v = x4[k4];
-            ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-        }
+    // RMSNorm prologue: every CTA reduces sum(x^2) over the whole input while it converts w (.) x
+    float ss = quantize_x<NORM>(x, nw, K, W.Kp / 32, xb, tid);
+    if (NORM) {
         for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         if (lane == 0) ssum[warp] = ss;
-        __syncthreads();
-        float t = 0.f;
-#pragma unroll
-        for (int i = 0; i < kWarps; i++) t += ssum[i];
-        rstd = rsqrtf(t / (float)K + eps);
     }
-    quantize_x<NORM>(x, nw, rstd, K, W.Kp / 32, xb, tid);
     // epilogue inputs into shared memory
     if (epi.kind == EPI_RESID)
         for (int i = tid; i < nrows; i += kThreads) xres[i] = epi.out[r0 + i];
@@ -290,6 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
+    float rstd = 1.f;  // applied to each row's dot product (the images hold w (.) x)
+    if (NORM) {
+        float t = 0.f;
+#pragma unroll
+        for (int i = 0; i < kWarps; i++) t += ssum[i];
+        rstd = rsqrtf(t / (float)K + eps);
+    }
     // this lane's x units: chunk wk + WK*u, unit lane
     Unit<WT> xr[UPL];
 #pragma unroll
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float r1 = __shfl_down_sync(0xffffffffu, r, 32 / RW);
             if (lane % (64 / RW) == 0) {
                 const int p = lane / (64 / RW), j0 = 2 * (rs + RS * p);
-                if (j0 < nr) gemv_epi(epi, ectx, ra + j0, r, r1);
+                if (j0 < nr) gemv_epi(epi, ectx, ra + j0, r * rstd, r1 * rstd);
             }
         } else {
             if ((lane & (32 / RW - 1)) == 0) red[slot][warp][lane / (32 / RW)] = r;
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int w = 0; w < WK; w++) a += red[slot][prs * WK + w][2 * pp + h];
                     y[h] = a;
                 }
-                gemv_epi(epi, ectx, ra + 2 * lane, y[0], y[1]);
+                gemv_epi(epi, ectx, ra + 2 * lane, y[0] * rstd, y[1] * rstd);
             }
             __syncwarp();
             if (lane == 0) {
@@ -413,6 +416,7 @@ Shape pick_shape(const Planes& W) {
     while (wk_min < kWarps && NC > wk_min * UPL) wk_min *= 2;
     int RS = 1;
     while (RS < pairs && RS < kWarps / wk_min) RS *= 2;
+    if (2 * (kWarps / wk_min) * row_bytes <= kMaxStage) RS = kWarps / wk_min;  // more work per warp per stage
     Shape s;
     s.WK = kWarps / RS;
     s.PPW = 1;
