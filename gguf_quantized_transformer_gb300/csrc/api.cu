@@ -355,6 +355,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     m->as.ns = std::max(attn_decode_splits(c.n_heads, c.n_kv_heads, c.max_ctx), decode_attn_splits(c.n_kv_heads));
     m->as.part = (float*)A.get(attn_decode_part_elems(c.n_heads, D, m->as.ns) * 4);
     m->as.cnt = (unsigned*)A.get((size_t)c.n_kv_heads * 4);
+    m->as.err = m->gs.err;
     if (!m->x || !m->q || !m->attn || !m->h || !m->y16[0] || !m->y16[1] || !m->a16[0] || !m->a16[1] || !m->h16[0] || !m->h16[1] || !m->tok || !m->logits || !m->st ||
         !m->gs.err || !m->as.part || !m->as.cnt)
         return oom("activations");
@@ -740,18 +741,22 @@ int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev
         cudaGetLastError();
         return fail(AF_ENOMEM, "scratch");
     }
-    if (cudaMalloc(&as.cnt, (size_t)KVH * 4) != cudaSuccess) {
+    if (cudaMalloc(&as.cnt, (size_t)(KVH + 1) * 4) != cudaSuccess) {  // counters, then the error word
         cudaGetLastError();
         cudaFree(as.part);
         return fail(AF_ENOMEM, "scratch");
     }
-    cudaError_t e = cudaMemsetAsync(as.cnt, 0, (size_t)KVH * 4, s);
+    as.err = as.cnt + KVH;
+    unsigned err_host = 0;
+    cudaError_t e = cudaMemsetAsync(as.cnt, 0, (size_t)(KVH + 1) * 4, s);
     if (!e) e = launch_attn_decode(q_dev, k_dev, v_dev, kv_dtype == AF_F16, H, KVH, D, ctx, nullptr, pos, as, out_dev, s);
+    if (!e) e = cudaMemcpyAsync(&err_host, as.err, 4, cudaMemcpyDeviceToHost, s);
     cudaError_t e2 = cudaStreamSynchronize(s);
     cudaFree(as.part);
     cudaFree(as.cnt);
     if (e) return fail(AF_ECUDA, "attention: %s", cudaGetErrorString(e));
     if (e2) return fail(AF_ECUDA, "attention sync: %s", cudaGetErrorString(e2));
+    if (err_host) return fail(AF_ETIMEOUT, "a bounded device-side wait gave up (code %u)", err_host);
     return AF_OK;
 }
 
@@ -773,7 +778,7 @@ int af_attention_decode_static(const float* q_dev, const void* k_dev, const void
     if (attn_decode_part_elems(H, D, as.ns) > kStaticAttnPartFloats)
         return fail(AF_ERANGE, "split partials (%zu floats) above the fixed scratch (%zu)",
                     attn_decode_part_elems(H, D, as.ns), kStaticAttnPartFloats);
-    CK(attn_static_scratch(&as.part, &as.cnt));
+    CK(attn_static_scratch(&as.part, &as.cnt, &as.err));
     CK(launch_attn_decode(q_dev, k_dev, v_dev, kv_dtype == AF_F16, H, KVH, D, ctx, nullptr, pos, as, out_dev,
                           (cudaStream_t)stream));
     return AF_OK;

@@ -51,24 +51,18 @@ __device__ __forceinline__ void load_vec<__half>(const __half* p, float* out, in
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMinPerSplit = 64;  // positions per split before another split is used
-constexpr int kTile = 64;         // cache slots per pipeline tile
-constexpr int kRing = 96 * 1024;  // tile ring budget (leaves room for a GEMV CTA on the same SM)
+constexpr int kRing = 96 * 1024;  // tile ring budget
 constexpr int kMaxScores = 64 * 1024;  // score buffer budget: split length x G floats
 
+// cache slots per pipeline tile: at least 64 and at least 16 KB (one bulk copy each)
+template <int D, typename KT>
+__host__ __device__ constexpr int dec_tile() {
+    return 16384 / (D * (int)sizeof(KT)) > 64 ? 16384 / (D * (int)sizeof(KT)) : 64;
+}
 template <int D, typename KT>
 __host__ __device__ constexpr int dec_stages() {
-    return kRing / (kTile * D * (int)sizeof(KT)) < 8 ? kRing / (kTile * D * (int)sizeof(KT)) : 8;
-}
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
-                 "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+    return kRing / (dec_tile<D, KT>() * D * (int)sizeof(KT)) < 8 ? kRing / (dec_tile<D, KT>() * D * (int)sizeof(KT))
+                                                                  : 8;
 }
 
 // n (2 or 4) consecutive cache values as fp32; p aligned to n elements.
@@ -104,8 +98,9 @@ __device__ __forceinline__ void dec_split(int n, int ns, int& ns_eff, int& chunk
 }
 
 // Decode attention, CTA (s, g): kv head g, slots [s*chunk, ...).  The K tiles
-// and then the V tiles of the range stream through a ring of S shared-memory
-// slots with cp.async (S-1 tiles in flight ahead of the one being used).
+// and then the V tiles of the range (contiguous in the cache) stream through a
+// ring of S shared-memory slots, one bulk copy (cp.async.bulk, mbarrier
+// completion) per tile; every wait is bounded.
 //   pass 1 (K tiles): lanes (LPK per slot, 8 dims each) score 32/LPK slots per
 //                     warp step for all G heads; scores go to shared memory
 //   softmax:          split maximum per head, p = exp(s - max) in place, sum
@@ -115,7 +110,8 @@ template <int D, int G, typename KT>
 __global__ void __launch_bounds__(kDecThreads, 1)
     attn_decode_kernel(const float* __restrict__ q, const KT* __restrict__ kc, const KT* __restrict__ vc, int max_ctx,
                        const int* __restrict__ pos_dev, int pos_arg, float* __restrict__ part,
-                       unsigned* __restrict__ cnt, float* __restrict__ out) {
+                       unsigned* __restrict__ cnt, float* __restrict__ out, unsigned* __restrict__ err) {
+    constexpr int kTile = dec_tile<D, KT>();
     constexpr int TB = kTile * D * (int)sizeof(KT);  // tile bytes
     constexpr int S = dec_stages<D, KT>();
     constexpr int LPK = D / 8;    // pass 1: lanes per slot
@@ -127,6 +123,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __shared__ float red[kDecWarps][G];
     __shared__ float m_s[G], l_s[G], inv_den[G];
     __shared__ unsigned last;
+    __shared__ uint64_t full[8];    // tile landed in slot (transaction bytes)
+    __shared__ unsigned issues[8];  // copies issued into the slot so far
+    __shared__ volatile int abort_f;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = blockIdx.y, s = blockIdx.x, ns = gridDim.x;
@@ -141,33 +140,43 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int nl = min(n, j0 + chunk) - j0;
     const KT* K = kc + ((int64_t)g * max_ctx + j0) * D;
     const KT* V = vc + ((int64_t)g * max_ctx + j0) * D;
-    float* my = part + ((int64_t)(g * ns + s) * G) * (D + 2);
+    constexpr int PST = D + 4;  // partial row: o[0..D-1], max, sum, 2 pad (16-byte rows)
+    float* my = part + ((int64_t)(g * ns + s) * G) * PST;
 
+    if (tid == 0) {
+        for (int i = 0; i < S; i++) {
+            mbar_init(&full[i], 1);
+            issues[i] = 0;
+        }
+        abort_f = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
     if (s < ns_eff) {
         const int nt = (nl + kTile - 1) / kTile, T = 2 * nt;
-        auto issue = [&](int t) {  // tile t: K tiles 0..nt-1, then V tiles
+        auto issue = [&](int t) {  // one thread: tile t (K tiles 0..nt-1, then V tiles) into slot t % S
             const int tt = t < nt ? t : t - nt;
             const int keys = min(kTile, nl - tt * kTile);
-            const uint8_t* src = reinterpret_cast<const uint8_t*>((t < nt ? K : V) + (int64_t)tt * kTile * D);
-            uint8_t* dst = dsm + (t % S) * TB;
-            const int n16 = keys * D * (int)sizeof(KT) / 16;
-            for (int c = tid; c < n16; c += kDecThreads) cp_async16(dst + 16 * c, src + 16 * c);
+            const KT* src = (t < nt ? K : V) + (int64_t)tt * kTile * D;
+            const int slot = t % S;
+            const unsigned bytes = (unsigned)(keys * D * (int)sizeof(KT));
+            issues[slot]++;
+            mbar_arrive_expect_tx(&full[slot], bytes);
+            bulk_g2s(dsm + slot * TB, src, bytes, &full[slot]);
         };
         // tiles without slot pos stream in before waiting for the previous kernel
-        const bool has_pos = j0 + nl == n;
-        bool waited = false;
-#pragma unroll
-        for (int t = 0; t < S - 1; t++) {
-            if (t < T) {
+        if (tid == 0) {
+            const bool has_pos = j0 + nl == n;
+            bool waited = false;
+            for (int t = 0; t < min(S, T); t++) {
                 if (has_pos && !waited && (t == nt - 1 || t == T - 1)) {
                     pdl_wait();
                     waited = true;
                 }
                 issue(t);
             }
-            cp_async_commit();
         }
-        if (!waited) pdl_wait();
+        pdl_wait();
         // q of the group's heads, pre-scaled by 1/sqrt(D): lane's 8 dims of each head
         const int li = lane % LPK, ks = lane / LPK;
         float qv[G][8];
@@ -189,10 +198,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             for (int e = 0; e < DV; e++) acc[h][e] = 0.f;
 
         for (int t = 0; t < T; t++) {
-            if (t + S - 1 < T) issue(t + S - 1);
-            cp_async_commit();
-            cp_async_wait<S - 1>();
+            bool ok = false;
+            for (unsigned it = 0; it < kWaitLimit && !ok; it++) {
+                ok = mbar_try_wait(&full[t % S], (unsigned)((t / S) & 1));
+                if (!ok && abort_f) break;
+            }
+            if (!ok) {
+                abort_f = 1;
+                atomicExch(err, (unsigned)DEV_TIMEOUT);
+            }
             __syncthreads();
+            if (abort_f) break;  // uniform: read after the barrier
             const uint8_t* tile = dsm + (t % S) * TB;
             if (t < nt) {
                 // ---- pass 1: scores of this tile's slots
@@ -274,9 +290,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     }
                 }
             }
-            __syncthreads();  // the slot of tile t is refilled in the next iteration
+            __syncthreads();  // every thread is done with slot t % S
+            if (tid == 0 && t + S < T) {
+                fence_proxy_async_shared();
+                issue(t + S);
+            }
         }
-        cp_async_wait<0>();
+        if (abort_f) {  // drain the copies still in flight before the ring is reused or the CTA exits
+            if (tid == 0)
+                for (int i = 0; i < S; i++)
+                    if (issues[i]) mbar_wait_bounded(&full[i], (issues[i] - 1u) & 1u);
+            __syncthreads();
+        }
         // sum the warps' partial outputs (the ring is free now)
         float* red_o = reinterpret_cast<float*>(dsm);  // [warp][G][D]
 #pragma unroll
@@ -288,11 +313,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             float o = 0.f;
 #pragma unroll
             for (int w = 0; w < kDecWarps; w++) o += red_o[w * G * D + t];
-            my[(t / D) * (D + 2) + t % D] = o;
+            my[(t / D) * PST + t % D] = o;
         }
         if (tid < G) {
-            my[tid * (D + 2) + D] = m_s[tid];
-            my[tid * (D + 2) + D + 1] = l_s[tid];
+            my[tid * PST + D] = m_s[tid];
+            my[tid * PST + D + 1] = l_s[tid];
         }
     } else {
         pdl_wait();  // the output and the split scratch are in use until the previous kernels finish
@@ -306,40 +331,61 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __syncthreads();
     if (!last) return;
     __threadfence();
-    // merge the ns_eff partials of this kv head: weights exp(m_s - M) / sum_s exp(m_s - M) l_s
-    const float* pg = part + ((int64_t)g * ns * G) * (D + 2);
-    float* wsm = sc;  // [ns_eff][G]
-    for (int t = tid; t < ns_eff * G; t += kDecThreads) wsm[t] = __ldcg(pg + (int64_t)t * (D + 2) + D);
+    // merge the ns_eff partials of this kv head: weights exp(m_s - M) / sum_s exp(m_s - M) l_s.
+    // Every load below is independent of the others, so the partials arrive in about one L2 round trip.
+    const float* pg = part + ((int64_t)g * ns * G) * PST;
+    float* wm = sc;                // [ns_eff][G] split maxima, then merge weights
+    float* wl = sc + ns_eff * G;   // [ns_eff][G] split sums
+    for (int t = tid; t < ns_eff * G; t += kDecThreads) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(pg + (int64_t)t * PST + D));
+        wm[t] = ml.x;
+        wl[t] = ml.y;
+    }
     __syncthreads();
     if (tid < G) {
         float M = -CUDART_INF_F;
-        for (int ss = 0; ss < ns_eff; ss++) M = fmaxf(M, wsm[ss * G + tid]);
+        for (int ss = 0; ss < ns_eff; ss++) M = fmaxf(M, wm[ss * G + tid]);
         float den = 0.f;
-        for (int ss = 0; ss < ns_eff; ss++) {
-            const float l = __ldcg(pg + ((int64_t)ss * G + tid) * (D + 2) + D + 1);
-            den = fmaf(__expf(wsm[ss * G + tid] - M), l, den);
-        }
+        for (int ss = 0; ss < ns_eff; ss++) den = fmaf(__expf(wm[ss * G + tid] - M), wl[ss * G + tid], den);
         m_s[tid] = M;
         inv_den[tid] = 1.f / den;
     }
     __syncthreads();
     for (int t = tid; t < ns_eff * G; t += kDecThreads) {
         const int h = t % G;
-        wsm[t] = __expf(wsm[t] - m_s[h]) * inv_den[h];
+        wm[t] = __expf(wm[t] - m_s[h]) * inv_den[h];
     }
-    __syncthreads();
-    for (int t = tid; t < G * D; t += kDecThreads) {
-        const int h = t / D, d = t % D;
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        int ss = 0;
-        for (; ss + 4 <= ns_eff; ss += 4) {
-            a0 = fmaf(wsm[(ss + 0) * G + h], __ldcg(pg + ((int64_t)(ss + 0) * G + h) * (D + 2) + d), a0);
-            a1 = fmaf(wsm[(ss + 1) * G + h], __ldcg(pg + ((int64_t)(ss + 1) * G + h) * (D + 2) + d), a1);
-            a2 = fmaf(wsm[(ss + 2) * G + h], __ldcg(pg + ((int64_t)(ss + 2) * G + h) * (D + 2) + d), a2);
-            a3 = fmaf(wsm[(ss + 3) * G + h], __ldcg(pg + ((int64_t)(ss + 3) * G + h) * (D + 2) + d), a3);
+    // the partial rows, a chunk of splits at a time, into the (free) tile ring
+    constexpr int kOut = (G * D + kDecThreads - 1) / kDecThreads;  // outputs per thread
+    constexpr int SC = S * TB / (G * PST * 4);                      // splits per chunk
+    static_assert(SC >= 1, "ring too small for one split's partials");
+    float* buf = reinterpret_cast<float*>(dsm);
+    float accm[kOut];
+#pragma unroll
+    for (int i = 0; i < kOut; i++) accm[i] = 0.f;
+    for (int c0 = 0; c0 < ns_eff; c0 += SC) {
+        const int nsc = min(SC, ns_eff - c0);
+        const int n4 = nsc * G * PST / 4;
+        const float4* src = reinterpret_cast<const float4*>(pg + (int64_t)c0 * G * PST);
+        __syncthreads();  // weights written / previous chunk consumed
+#pragma unroll 4
+        for (int i = tid; i < n4; i += kDecThreads) reinterpret_cast<float4*>(buf)[i] = __ldcg(src + i);
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kOut; i++) {
+            const int o = tid + i * kDecThreads;
+            if (o < G * D) {
+                const int h = o / D, d = o % D;
+                float a = accm[i];
+                for (int ss = 0; ss < nsc; ss++) a = fmaf(wm[(c0 + ss) * G + h], buf[(ss * G + h) * PST + d], a);
+                accm[i] = a;
+            }
         }
-        for (; ss < ns_eff; ss++) a0 = fmaf(wsm[ss * G + h], __ldcg(pg + ((int64_t)ss * G + h) * (D + 2) + d), a0);
-        out[(int64_t)(g * G + h) * D + d] = (a0 + a1) + (a2 + a3);
+    }
+#pragma unroll
+    for (int i = 0; i < kOut; i++) {
+        const int o = tid + i * kDecThreads;
+        if (o < G * D) out[(int64_t)(g * G + o / D) * D + o % D] = accm[i];
     }
     if (tid == 0) cnt[g] = 0u;
 }
@@ -347,8 +393,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 template <int D, int G, typename KT>
 cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int max_ctx, const int* pos_dev, int pos,
                             const AttnScratch& scr, int ns, float* out, int KVH, cudaStream_t s) {
-    const int cap = std::max((max_ctx + ns - 1) / ns, std::max(ns, kMinPerSplit));
-    const size_t smem = (size_t)dec_stages<D, KT>() * kTile * D * sizeof(KT) + (size_t)cap * G * sizeof(float);
+    const int cap = std::max((max_ctx + ns - 1) / ns, std::max(2 * ns, kMinPerSplit));  // scores, or 2 merge words per split
+    const size_t smem =
+        (size_t)dec_stages<D, KT>() * dec_tile<D, KT>() * D * sizeof(KT) + (size_t)cap * G * sizeof(float);
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     auto k = attn_decode_kernel<D, G, KT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -364,7 +411,7 @@ cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k, q, (const KT*)kc, (const KT*)vc, max_ctx, pos_dev, pos, scr.part, scr.cnt,
-                              out);
+                              out, scr.err);
 }
 
 template <int D, int G>
@@ -392,7 +439,7 @@ int attn_decode_splits(int n_heads, int n_kv_heads, int max_ctx) {
     return ns < 1 ? 1 : ns;
 }
 
-size_t attn_decode_part_elems(int n_heads, int head_dim, int ns) { return (size_t)ns * n_heads * (head_dim + 2); }
+size_t attn_decode_part_elems(int n_heads, int head_dim, int ns) { return (size_t)ns * n_heads * (head_dim + 4); }
 
 #define AF_ATTN_DISPATCH(FN, ...)                                          \
     switch (D * 100 + G) {                                                 \

@@ -8,6 +8,7 @@
 //
 // Layout of g_attn_static:
 //   [0, kStaticAttnMaxKVH * 4)          arrival counters (unsigned)
+//   word kStaticAttnMaxKVH              error word (a bounded device wait gave up)
 //   [kStaticAttnCntBytes, end)          split partials (float)
 // The counters are zero when the module is loaded and every call that runs
 // to completion leaves them zero again (the last CTA of each kv head resets
@@ -21,7 +22,7 @@ namespace af {
 
 namespace {
 
-constexpr size_t kStaticAttnCntBytes = (size_t)kStaticAttnMaxKVH * sizeof(unsigned);
+constexpr size_t kStaticAttnCntBytes = ((size_t)kStaticAttnMaxKVH + 64) * sizeof(unsigned);
 constexpr size_t kStaticAttnBytes = kStaticAttnCntBytes + kStaticAttnPartFloats * sizeof(float);
 static_assert(kStaticAttnCntBytes % 256 == 0, "partials start 256-byte aligned");
 
@@ -33,7 +34,7 @@ void* g_addr[kMaxDevices] = {};
 
 }  // namespace
 
-cudaError_t attn_static_scratch(float** part, unsigned** cnt) {
+cudaError_t attn_static_scratch(float** part, unsigned** cnt, unsigned** err) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e) return e;
@@ -46,6 +47,7 @@ cudaError_t attn_static_scratch(float** part, unsigned** cnt) {
         g_addr[dev] = p;
     }
     *cnt = reinterpret_cast<unsigned*>(g_addr[dev]);
+    *err = *cnt + kStaticAttnMaxKVH;
     *part = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(g_addr[dev]) + kStaticAttnCntBytes);
     return cudaSuccess;
 }

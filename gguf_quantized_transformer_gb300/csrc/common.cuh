@@ -167,6 +167,7 @@ cudaError_t qgemm_prepare();
 struct AttnScratch {
     float* part = nullptr;    // [KVH][NS][G][D+2]
     unsigned* cnt = nullptr;  // [KVH], zero between launches
+    unsigned* err = nullptr;  // device error word (a bounded wait gave up)
     int ns = 0;               // splits the partials have room for
 };
 // Splits the decode attention launches (grid.x) for this shape.
@@ -183,10 +184,10 @@ cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, con
 bool attn_supported(int H, int KVH, int D);
 
 // Capacity of the fixed decode-attention scratch (a file-scope device array, no allocation).
-constexpr int kStaticAttnMaxKVH = 1024;                  // arrival counters
+constexpr int kStaticAttnMaxKVH = 1024;                  // arrival counters (plus one error word)
 constexpr size_t kStaticAttnPartFloats = (size_t)1 << 20;  // split partials (4 MiB)
 // Device address of that scratch on the current device (looked up once per device).
-cudaError_t attn_static_scratch(float** part, unsigned** cnt);
+cudaError_t attn_static_scratch(float** part, unsigned** cnt, unsigned** err);
 
 // One GEMV of the persistent decode kernel: matrix, input, optional RMSNorm
 // weight, stage shape (R rows per ring slot, WK warps along K) and epilogue.

@@ -224,8 +224,9 @@ int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev
  * kernel and same result as af_attention_decode, but stream-ordered: it does
  * not synchronise `stream`.
  * Scratch: one file-scope device array of this library (4 MiB of split
- * partials + 1024 arrival counters).  Calls with n_kv_heads > 1024 or whose
- * partials need more than 2^20 floats (n_heads * splits * (head_dim + 2),
+ * partials + 1024 arrival counters + an error word that a device-side wait
+ * timeout sets; this call does not read it back).  Calls with n_kv_heads > 1024 or whose
+ * partials need more than 2^20 floats (n_heads * splits * (head_dim + 4),
  * splits = ceil(2 * SMs / n_kv_heads)) return AF_ERANGE before launching.
  * The counters must start at zero: they are zero when the library is loaded
  * and every call that completes leaves them zero.  All calls on a device
