@@ -107,7 +107,7 @@ __device__ __forceinline__ void dec_split(int n, int ns, int& ns_eff, int& chunk
 //   pass 2 (V tiles): warp w takes slots w, w+8, ..; lane l dims l*DV..; all
 //                     heads per lane; warps are summed at the end
 template <int D, int G, typename KT>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(kDecThreads, G <= 4 ? 2 : 1)  // two CTAs per SM where the registers allow
     attn_decode_kernel(const float* __restrict__ q, const KT* __restrict__ kc, const KT* __restrict__ vc, int max_ctx,
                        const int* __restrict__ pos_dev, int pos_arg, float* __restrict__ part,
                        unsigned* __restrict__ cnt, float* __restrict__ out, unsigned* __restrict__ err) {
@@ -431,8 +431,9 @@ bool attn_supported(int H, int KVH, int D) {
 }
 
 int attn_decode_splits(int n_heads, int n_kv_heads, int max_ctx) {
-    // one CTA per SM over all kv heads; more splits only if a split's scores would not fit
-    int ns = num_sms() / n_kv_heads;
+    // two CTAs per SM over all kv heads (their serial per-tile work overlaps); more splits only if a
+    // split's scores would not fit
+    int ns = 2 * num_sms() / n_kv_heads;
     const int G = n_heads / n_kv_heads;
     const int need = (int)(((int64_t)max_ctx * G * 4 + kMaxScores - 1) / kMaxScores);
     if (ns < need) ns = need;
