@@ -80,6 +80,8 @@ def lib():
             L.orc_model_destroy.argtypes = [vp]
             L.orc_model_destroy.restype = None
             L.orc_argmax.argtypes = [vp, i64]
+            L.orc_sample.argtypes = [vp, i64, vp, i64, dbl, dbl, dbl, dbl, vp, vp]
+            L.orc_sample.restype = i64
             L.orc_argmax.restype = i64
             _lib = L
     return _lib
@@ -176,6 +178,16 @@ def attention(q, kc, vc, n_heads: int, n_kv_heads: int, head_dim: int, n_keys: i
     lib().orc_attention(_p(q), n_heads, n_kv_heads, head_dim, _p(kc), _p(vc), kc.shape[1] * head_dim, n_keys,
                         _p(out))
     return out
+
+
+def sample(logits, recent, repeat_penalty: float, temperature: float, top_p: float, u: float):
+    """Sampler chain; returns (token, lo, hi): the token's cumulative-mass interval within the nucleus."""
+    v = np.ascontiguousarray(logits, dtype=np.float64)
+    r = np.ascontiguousarray(recent, dtype=np.int32)
+    lo, hi = ctypes.c_double(), ctypes.c_double()
+    t = lib().orc_sample(_p(v), v.size, _p(r) if r.size else None, r.size, repeat_penalty, temperature, top_p, u,
+                         ctypes.byref(lo), ctypes.byref(hi))
+    return int(t), lo.value, hi.value
 
 
 def argmax(v) -> int:

@@ -4,6 +4,7 @@
 // summation order unchanged (so results do not depend on the thread count).
 #include "oracle.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <thread>
@@ -288,6 +289,76 @@ int64_t orc_argmax(const double* v, int64_t n) {
     for (int64_t i = 1; i < n; i++)
         if (v[i] > v[best]) best = i;
     return best;
+}
+
+// Sampler chain (Airframe GPU pipeline, "sampling applies these transformations
+// in order"): repetition penalty, temperature, softmax, top-p, sample.  Readings:
+// the penalty divides each distinct recent token's logit once; temperature 0 is
+// greedy (argmax, lowest index on ties); the nucleus is the shortest prefix of
+// the tokens sorted by (probability descending, index ascending) whose sum
+// reaches top_p, extended by every token tied with its last one (top_p >= 1
+// keeps everything); the sample is the first token of that order whose
+// cumulative mass reaches u times the nucleus mass (u in [0, 1) is the caller's
+// uniform draw).  *lo / *hi receive the token's cumulative mass interval
+// (before, after) as a fraction of the nucleus mass.
+int64_t orc_sample(const double* logits, int64_t V, const int32_t* recent, int64_t n_recent, double repeat_penalty,
+                   double temperature, double top_p, double u, double* lo, double* hi) {
+    std::vector<double> l(logits, logits + V);
+    if (repeat_penalty > 1.0) {
+        for (int64_t i = 0; i < n_recent; i++) {
+            const int32_t t = recent[i];
+            if (t < 0 || t >= V) continue;
+            bool seen = false;
+            for (int64_t j = 0; j < i; j++) seen = seen || recent[j] == t;
+            if (!seen) l[t] /= repeat_penalty;
+        }
+    }
+    if (temperature <= 0.0) {
+        if (lo) *lo = 0.0;
+        if (hi) *hi = 1.0;
+        return orc_argmax(l.data(), V);
+    }
+    double mx = -INFINITY;
+    for (int64_t i = 0; i < V; i++) {
+        l[i] /= temperature;
+        mx = std::fmax(mx, l[i]);
+    }
+    std::vector<double> p(V);
+    double z = 0.0;
+    for (int64_t i = 0; i < V; i++) {
+        p[i] = std::exp(l[i] - mx);
+        z += p[i];
+    }
+    for (int64_t i = 0; i < V; i++) p[i] /= z;
+    std::vector<int64_t> order(V);
+    for (int64_t i = 0; i < V; i++) order[i] = i;
+    std::sort(order.begin(), order.end(), [&](int64_t a, int64_t b) { return p[a] > p[b] || (p[a] == p[b] && a < b); });
+    int64_t kept = V;
+    if (top_p < 1.0) {
+        double c = 0.0;
+        for (int64_t k = 0; k < V; k++) {
+            c += p[order[k]];
+            if (c >= top_p) {
+                kept = k + 1;
+                break;
+            }
+        }
+        while (kept < V && p[order[kept]] == p[order[kept - 1]]) kept++;
+    }
+    double zk = 0.0;
+    for (int64_t k = 0; k < kept; k++) zk += p[order[k]];
+    const double target = u * zk;
+    double c = 0.0;
+    for (int64_t k = 0; k < kept; k++) {
+        const double before = c;
+        c += p[order[k]];
+        if (c >= target || k == kept - 1) {
+            if (lo) *lo = before / zk;
+            if (hi) *hi = c / zk;
+            return order[k];
+        }
+    }
+    return order[0];
 }
 
 // Forward pass over n tokens at positions start_pos.. (Airframe per-layer op

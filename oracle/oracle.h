@@ -100,6 +100,10 @@ int orc_kv_read(const orc_model* m, int32_t layer, int32_t kvh, int64_t pos, dou
 void orc_model_destroy(orc_model* m);
 /* Greedy token: argmax, lowest index on ties. */
 int64_t orc_argmax(const double* v, int64_t n);
+// Sampler chain: repetition penalty -> temperature -> softmax -> top-p -> sample with uniform u.
+// Returns the token; lo / hi (nullable) get its cumulative-mass interval within the nucleus.
+int64_t orc_sample(const double* logits, int64_t V, const int32_t* recent, int64_t n_recent, double repeat_penalty,
+                   double temperature, double top_p, double u, double* lo, double* hi);
 
 #ifdef __cplusplus
 }

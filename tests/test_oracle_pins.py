@@ -376,3 +376,50 @@ def test_dispatch_count_arithmetic():
     g = GOLD["dispatch_count_tinyllama"]
     assert g["n_layers"] * 6 == g["matmul_dispatches"]
     assert g["matmul_dispatches"] + 4 * g["n_layers"] == g["total_dispatches"]
+
+
+# ---------------------------------------------------------------- sampler chain (Airframe GPU pipeline)
+
+def test_sample_uniform_logits_picks_floor_u_v():
+    # equal logits, no nucleus cut: the order is by index and each token has mass 1/V
+    V = 10
+    for u, want in [(0.0, 0), (0.05, 0), (0.15, 1), (0.47, 4), (0.999, 9)]:
+        t, lo, hi = oracle.sample(np.zeros(V), [], 1.0, 1.0, 1.0, u)
+        assert t == want, (u, t)
+        assert lo <= u <= hi
+
+
+def test_sample_greedy_at_zero_temperature_with_penalty():
+    logits = np.arange(10, dtype=np.float64)
+    assert oracle.sample(logits, [], 1.0, 0.0, 1.0, 0.7)[0] == 9
+    # token 9 divided by 2 -> 4.5: token 8 wins; duplicates in the recent list divide once
+    assert oracle.sample(logits, [9], 2.0, 0.0, 1.0, 0.7)[0] == 8
+    assert oracle.sample(logits, [9, 9, 9, 8], 2.0, 0.0, 1.0, 0.7)[0] == 7  # 9 -> 4.5, 8 -> 4, 7 wins
+    # penalty <= 1 is off
+    assert oracle.sample(logits, [9], 1.0, 0.0, 1.0, 0.7)[0] == 9
+
+
+def test_sample_two_tokens_closed_form():
+    a, b, T = 1.3, 0.4, 0.7
+    p0 = 1.0 / (1.0 + np.exp((b - a) / T))  # token 0 is the more probable one
+    assert oracle.sample(np.array([a, b]), [], 1.0, T, 1.0, p0 - 1e-9)[0] == 0
+    assert oracle.sample(np.array([a, b]), [], 1.0, T, 1.0, p0 + 1e-9)[0] == 1
+
+
+def test_sample_nucleus_cut_and_renormalization():
+    probs = np.array([0.2, 0.5, 0.3])
+    logits = np.log(probs)
+    # sorted: 1 (0.5), 2 (0.3), 0 (0.2); top_p 0.75 keeps {1, 2} (0.5 < 0.75 <= 0.8), mass 0.8
+    assert oracle.sample(logits, [], 1.0, 1.0, 0.75, 0.6)[0] == 1   # target 0.48 <= 0.5
+    assert oracle.sample(logits, [], 1.0, 1.0, 0.75, 0.7)[0] == 2   # target 0.56 in (0.5, 0.8]
+    assert oracle.sample(logits, [], 1.0, 1.0, 0.75, 0.999)[0] == 2  # token 0 is never drawn
+    # a tiny top_p keeps only the most probable token
+    for u in (0.0, 0.5, 0.999):
+        assert oracle.sample(logits, [], 1.0, 1.0, 1e-9, u)[0] == 1
+
+
+def test_sample_high_temperature_approaches_uniform():
+    logits = np.array([3.0, 0.0, -2.0, 1.0])
+    t, lo, hi = oracle.sample(logits, [], 1.0, 1e6, 1.0, 0.6)
+    # near-equal masses, still ordered by probability: 0, 3, 1, 2 -> the third one
+    assert t == 1 and abs(lo - 0.5) < 1e-5 and abs(hi - 0.75) < 1e-5
