@@ -33,7 +33,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up GEMV launch, Q4_0 28672 x 4096, from the
 # ncu capture summarised in profiles/qgemv_q4_0_28672x4096.md; valid only for the kernel sources it was taken on.
 GEMV_SOURCES = ["qgemv.cu", "gemv_common.cuh", "tma.cuh", "common.cuh"]
-GEMV_TRAFFIC = {"sources_sha256_16": "6cd7195d1715e15a", "wtype": "q4_0", "N": 28672, "K": 4096, "bytes": 66204160}
+GEMV_TRAFFIC = {"sources_sha256_16": "a99ba43fd54077f8", "wtype": "q4_0", "N": 28672, "K": 4096, "bytes": 66124800}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -286,6 +286,9 @@ def run_ours(args, cfg, world, rank, local):
     # per-kernel: the decode GEMV alone, at this model's largest per-layer matrix (gate|up), CUDA events
     qg = qgemv_roofline(af, cfg, dev, hbm_peak)
 
+    # the sampler chain over this vocabulary (typical settings), CUDA events
+    samp_us = sampler_time(af, cfg, dev)
+
     # end to end through the host API: host token ids in, greedy token ids out, one sync per decode step
     e2e = e2e_run(af, m, prompt, cfg, args)
 
@@ -299,6 +302,7 @@ def run_ours(args, cfg, world, rank, local):
         "prefill_tok_s": prefill_tps, "decode_tok_s": decode_tps,
         "decode_hbm_gbs": dec_gbs, "decode_hbm_frac": dec_gbs / hbm_peak,
         "prefill_tflops": pf_tflops,
+        "sampler_us": samp_us,
         "roofline": dict(qg, peak_source=peak_src),
         "decode_step_roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
                                  "frac": dec_gbs / hbm_peak, "traffic": None,
@@ -352,6 +356,31 @@ def qgemv_roofline(af, cfg, dev, hbm_peak, reps=50):
             "traffic": gemv_traffic(cfg.wtype, N, K),
             "kernel": f"qgemv {cfg.wtype} [{N}x{K}] gate|up (L2 flushed between launches)",
             "bytes_per_launch": nbytes, "us_per_launch": ms * 1000}
+
+
+def sampler_time(af, cfg, dev, reps=20):
+    """Device time of one af_sample over a vocabulary-sized logits vector (penalty 1.1 on 64 recent ids,
+    temperature 0.8, top-p 0.95), from a CUDA graph of `reps` calls with distinct draws u: a host loop of
+    single calls would time the host, not the kernel."""
+    import torch
+    logits = torch.randn(cfg.n_vocab, device=dev) * 3
+    recent = torch.randint(0, cfg.n_vocab, (64,), dtype=torch.int32, device=dev)
+    tok = torch.empty(1, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        af.af_sample(logits, cfg.n_vocab, recent, 64, 1.1, 0.8, 0.95, 0.37, tok)
+    torch.cuda.synchronize()
+    g, s = torch.cuda.CUDAGraph(), torch.cuda.Stream()
+    with torch.cuda.stream(s), torch.cuda.graph(g, stream=s):
+        for i in range(reps):
+            af.af_sample(logits, cfg.n_vocab, recent, 64, 1.1, 0.8, 0.95, (i + 0.5) / reps, tok)
+    g.replay()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(5):
+        g.replay()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) * 1000 / (5 * reps)
 
 
 def gemv_traffic(wtype, N, K):

@@ -78,6 +78,8 @@ def lib():
         L.af_qweight_destroy.restype = None
         L.af_attention_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
         L.af_attention_decode_static.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        f32 = ctypes.c_float
+        L.af_sample.argtypes = [vp, i32, vp, i32, f32, f32, f32, f32, vp, vp]
         _lib = L
     return _lib
 
@@ -225,6 +227,12 @@ def af_attention_decode_static(q_dev, k_dev, v_dev, kv_dtype: int, n_heads: int,
                                ctx: int, pos: int, out_dev, stream=None):
     return check(lib().af_attention_decode_static(_ptr(q_dev), _ptr(k_dev), _ptr(v_dev), kv_dtype, n_heads,
                                                   n_kv_heads, head_dim, ctx, pos, _ptr(out_dev), _stream(stream)))
+
+
+def af_sample(logits_dev, n_vocab: int, recent_dev, n_recent: int, repeat_penalty: float, temperature: float,
+              top_p: float, u: float, token_dev, stream=None):
+    return check(lib().af_sample(_ptr(logits_dev), n_vocab, _ptr(recent_dev), n_recent, repeat_penalty, temperature,
+                                 top_p, u, _ptr(token_dev), _stream(stream)))
 
 
 def af_last_error() -> str:

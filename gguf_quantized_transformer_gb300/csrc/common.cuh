@@ -183,6 +183,11 @@ cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, con
                                 int64_t ldo, unsigned* err, cudaStream_t s);
 bool attn_supported(int H, int KVH, int D);
 
+// Sampler chain over the logits (one CTA): penalty, temperature, softmax, top-p, draw with uniform u.
+int sampler_max_vocab();
+cudaError_t launch_sample(const float* logits, int V, const int* recent, int n_recent, float penalty,
+                          float temperature, float top_p, float u, int* token_out, cudaStream_t s);
+
 // Capacity of the fixed decode-attention scratch (a file-scope device array, no allocation).
 constexpr int kStaticAttnMaxKVH = 1024;                  // arrival counters (plus one error word)
 constexpr size_t kStaticAttnPartFloats = (size_t)1 << 20;  // split partials (4 MiB)

@@ -240,6 +240,29 @@ int af_attention_decode_static(const float* q_dev, const void* k_dev, const void
                                int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t ctx, int32_t pos,
                                float* out_dev, void* stream);
 
+/*
+ * Sampler chain on the device (Airframe GPU pipeline, sampler: "repetition
+ * penalty -> temperature -> softmax -> top-p -> sample"): one kernel launch
+ * of one 8-CTA thread-block cluster that keeps the logits in shared memory; no
+ * device scratch and no allocation, so calls on different streams are
+ * independent.  Asynchronous on `stream`:
+ *   logits_dev  fp32 [n_vocab] (not modified), n_vocab <= 262144
+ *   recent_dev  int32 [n_recent] recent token ids (device; NULL when n_recent = 0);
+ *               each distinct id in [0, n_vocab) has its logit divided by
+ *               repeat_penalty once (only when repeat_penalty > 1)
+ *   temperature 0 -> greedy (argmax, lowest index on ties); > 0 divides the logits
+ *   top_p       nucleus: the shortest prefix of the tokens sorted by
+ *               (probability descending, index ascending) whose mass reaches
+ *               top_p, plus every token tied with its last one; >= 1 keeps all
+ *   u           the caller's uniform draw in [0, 1): the token returned is the
+ *               first of that order whose cumulative mass reaches u times the
+ *               nucleus mass
+ *   token_dev   int32 [1] result
+ * AF_EINVAL / AF_ERANGE for bad arguments (checked on the host).
+ */
+int af_sample(const float* logits_dev, int32_t n_vocab, const int32_t* recent_dev, int32_t n_recent,
+              float repeat_penalty, float temperature, float top_p, float u, int32_t* token_dev, void* stream);
+
 /* Thread-local message for the last failed call on this thread ("" if none). */
 const char* af_last_error(void);
 

@@ -82,6 +82,7 @@ def lib():
             L.orc_argmax.argtypes = [vp, i64]
             L.orc_sample.argtypes = [vp, i64, vp, i64, dbl, dbl, dbl, dbl, vp, vp]
             L.orc_sample.restype = i64
+            L.orc_sample_interval.argtypes = [vp, i64, vp, i64, dbl, dbl, dbl, i64, vp, vp, vp, vp]
             L.orc_argmax.restype = i64
             _lib = L
     return _lib
@@ -188,6 +189,18 @@ def sample(logits, recent, repeat_penalty: float, temperature: float, top_p: flo
     t = lib().orc_sample(_p(v), v.size, _p(r) if r.size else None, r.size, repeat_penalty, temperature, top_p, u,
                          ctypes.byref(lo), ctypes.byref(hi))
     return int(t), lo.value, hi.value
+
+
+def sample_interval(logits, recent, repeat_penalty: float, temperature: float, top_p: float, token: int):
+    """(in_nucleus, lo, hi, p_token, p_boundary) of `token` under the sampler's distribution (temperature > 0)."""
+    v = np.ascontiguousarray(logits, dtype=np.float64)
+    r = np.ascontiguousarray(recent, dtype=np.int32)
+    out = [ctypes.c_double() for _ in range(4)]
+    rc = lib().orc_sample_interval(_p(v), v.size, _p(r) if r.size else None, r.size, repeat_penalty, temperature,
+                                   top_p, token, *[ctypes.byref(o) for o in out])
+    if rc < 0:
+        raise ValueError("bad arguments")
+    return bool(rc), out[0].value, out[1].value, out[2].value, out[3].value
 
 
 def argmax(v) -> int:

@@ -301,8 +301,19 @@ int64_t orc_argmax(const double* v, int64_t n) {
 // cumulative mass reaches u times the nucleus mass (u in [0, 1) is the caller's
 // uniform draw).  *lo / *hi receive the token's cumulative mass interval
 // (before, after) as a fraction of the nucleus mass.
-int64_t orc_sample(const double* logits, int64_t V, const int32_t* recent, int64_t n_recent, double repeat_penalty,
-                   double temperature, double top_p, double u, double* lo, double* hi) {
+namespace {
+
+// The sampler's distribution: penalized, temperature-scaled softmax probabilities p, the order
+// (probability descending, index ascending) and the nucleus length.  temperature > 0.
+struct SampleDist {
+    std::vector<double> p;
+    std::vector<int64_t> order;
+    int64_t kept = 0;
+    double zk = 0.0;
+};
+
+std::vector<double> penalized(const double* logits, int64_t V, const int32_t* recent, int64_t n_recent,
+                              double repeat_penalty) {
     std::vector<double> l(logits, logits + V);
     if (repeat_penalty > 1.0) {
         for (int64_t i = 0; i < n_recent; i++) {
@@ -313,52 +324,90 @@ int64_t orc_sample(const double* logits, int64_t V, const int32_t* recent, int64
             if (!seen) l[t] /= repeat_penalty;
         }
     }
-    if (temperature <= 0.0) {
-        if (lo) *lo = 0.0;
-        if (hi) *hi = 1.0;
-        return orc_argmax(l.data(), V);
-    }
+    return l;
+}
+
+SampleDist sample_dist(std::vector<double> l, double temperature, double top_p) {
+    const int64_t V = (int64_t)l.size();
+    SampleDist d;
     double mx = -INFINITY;
     for (int64_t i = 0; i < V; i++) {
         l[i] /= temperature;
         mx = std::fmax(mx, l[i]);
     }
-    std::vector<double> p(V);
+    d.p.resize(V);
     double z = 0.0;
     for (int64_t i = 0; i < V; i++) {
-        p[i] = std::exp(l[i] - mx);
-        z += p[i];
+        d.p[i] = std::exp(l[i] - mx);
+        z += d.p[i];
     }
-    for (int64_t i = 0; i < V; i++) p[i] /= z;
-    std::vector<int64_t> order(V);
-    for (int64_t i = 0; i < V; i++) order[i] = i;
-    std::sort(order.begin(), order.end(), [&](int64_t a, int64_t b) { return p[a] > p[b] || (p[a] == p[b] && a < b); });
-    int64_t kept = V;
+    for (int64_t i = 0; i < V; i++) d.p[i] /= z;
+    d.order.resize(V);
+    for (int64_t i = 0; i < V; i++) d.order[i] = i;
+    const std::vector<double>& p = d.p;
+    std::sort(d.order.begin(), d.order.end(),
+              [&](int64_t a, int64_t b) { return p[a] > p[b] || (p[a] == p[b] && a < b); });
+    d.kept = V;
     if (top_p < 1.0) {
         double c = 0.0;
         for (int64_t k = 0; k < V; k++) {
-            c += p[order[k]];
+            c += p[d.order[k]];
             if (c >= top_p) {
-                kept = k + 1;
+                d.kept = k + 1;
                 break;
             }
         }
-        while (kept < V && p[order[kept]] == p[order[kept - 1]]) kept++;
+        while (d.kept < V && p[d.order[d.kept]] == p[d.order[d.kept - 1]]) d.kept++;
     }
-    double zk = 0.0;
-    for (int64_t k = 0; k < kept; k++) zk += p[order[k]];
-    const double target = u * zk;
+    for (int64_t k = 0; k < d.kept; k++) d.zk += p[d.order[k]];
+    return d;
+}
+
+}  // namespace
+
+int64_t orc_sample(const double* logits, int64_t V, const int32_t* recent, int64_t n_recent, double repeat_penalty,
+                   double temperature, double top_p, double u, double* lo, double* hi) {
+    std::vector<double> l = penalized(logits, V, recent, n_recent, repeat_penalty);
+    if (temperature <= 0.0) {
+        if (lo) *lo = 0.0;
+        if (hi) *hi = 1.0;
+        return orc_argmax(l.data(), V);
+    }
+    const SampleDist d = sample_dist(std::move(l), temperature, top_p);
+    const double target = u * d.zk;
     double c = 0.0;
-    for (int64_t k = 0; k < kept; k++) {
+    for (int64_t k = 0; k < d.kept; k++) {
         const double before = c;
-        c += p[order[k]];
-        if (c >= target || k == kept - 1) {
-            if (lo) *lo = before / zk;
-            if (hi) *hi = c / zk;
-            return order[k];
+        c += d.p[d.order[k]];
+        if (c >= target || k == d.kept - 1) {
+            if (lo) *lo = before / d.zk;
+            if (hi) *hi = c / d.zk;
+            return d.order[k];
         }
     }
-    return order[0];
+    return d.order[0];
+}
+
+int orc_sample_interval(const double* logits, int64_t V, const int32_t* recent, int64_t n_recent,
+                        double repeat_penalty, double temperature, double top_p, int64_t token, double* lo,
+                        double* hi, double* p_token, double* p_boundary) {
+    if (token < 0 || token >= V || temperature <= 0.0) return -1;
+    const SampleDist d = sample_dist(penalized(logits, V, recent, n_recent, repeat_penalty), temperature, top_p);
+    double c = 0.0;
+    int in_nucleus = 0;
+    for (int64_t k = 0; k < V; k++) {
+        const double before = c;
+        c += d.p[d.order[k]];
+        if (d.order[k] == token) {
+            *lo = before / d.zk;
+            *hi = c / d.zk;
+            in_nucleus = k < d.kept;
+            break;
+        }
+    }
+    *p_token = d.p[token];
+    *p_boundary = d.p[d.order[d.kept - 1]];
+    return in_nucleus;
 }
 
 // Forward pass over n tokens at positions start_pos.. (Airframe per-layer op

@@ -104,6 +104,12 @@ int64_t orc_argmax(const double* v, int64_t n);
 // Returns the token; lo / hi (nullable) get its cumulative-mass interval within the nucleus.
 int64_t orc_sample(const double* logits, int64_t V, const int32_t* recent, int64_t n_recent, double repeat_penalty,
                    double temperature, double top_p, double u, double* lo, double* hi);
+// For a given token (temperature > 0): its cumulative-mass interval [lo, hi] in the sampling order as a
+// fraction of the nucleus mass, its probability and the nucleus' smallest probability.  Returns 1 if the
+// token is in the nucleus, 0 if not, -1 on bad arguments.
+int orc_sample_interval(const double* logits, int64_t V, const int32_t* recent, int64_t n_recent,
+                        double repeat_penalty, double temperature, double top_p, int64_t token, double* lo,
+                        double* hi, double* p_token, double* p_boundary);
 
 #ifdef __cplusplus
 }

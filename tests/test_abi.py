@@ -81,6 +81,19 @@ def test_validation_errors_without_gpu():
     assert L.af_attention_decode_static(None, None, None, 0, 8, 4, 64, 16, 0, None, None) == af.AF_EINVAL
 
 
+def test_sampler_validation():
+    # host-side checks only (no launch)
+    af = pytest.importorskip("gguf_quantized_transformer_gb300")
+    L = af.lib()
+    assert L.af_sample(None, 10, None, 0, 1.0, 1.0, 1.0, 0.5, 1, None) == af.AF_EINVAL
+    assert L.af_sample(1, 0, None, 0, 1.0, 1.0, 1.0, 0.5, 1, None) == af.AF_ERANGE
+    assert L.af_sample(1, 300000, None, 0, 1.0, 1.0, 1.0, 0.5, 1, None) == af.AF_ERANGE
+    assert L.af_sample(1, 10, None, 3, 1.0, 1.0, 1.0, 0.5, 1, None) == af.AF_EINVAL
+    assert L.af_sample(1, 10, None, 0, 1.0, -1.0, 1.0, 0.5, 1, None) == af.AF_EINVAL
+    assert L.af_sample(1, 10, None, 0, 1.0, 1.0, 1.0, 1.0, 1, None) == af.AF_ERANGE
+    assert L.af_sample(1, 10, None, 0, 1.0, 1.0, 1.0, -0.1, 1, None) == af.AF_ERANGE
+
+
 def test_static_attention_rejects_oversize():
     # host-side capacity checks of the fixed scratch; they return before any launch
     # (the pointers are never dereferenced on the host)

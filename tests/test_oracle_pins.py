@@ -423,3 +423,12 @@ def test_sample_high_temperature_approaches_uniform():
     t, lo, hi = oracle.sample(logits, [], 1.0, 1e6, 1.0, 0.6)
     # near-equal masses, still ordered by probability: 0, 3, 1, 2 -> the third one
     assert t == 1 and abs(lo - 0.5) < 1e-5 and abs(hi - 0.75) < 1e-5
+
+
+def test_sample_interval_contains_the_draw():
+    logits = synth.normals(9, synth.TID_TEST_BASE + 32, 500) * 2.0
+    for top_p in (1.0, 0.9, 0.3):
+        for u in (0.0, 0.2, 0.61, 0.97):
+            t, lo, hi = oracle.sample(logits, [3, 4], 1.2, 0.9, top_p, u)
+            inn, lo2, hi2, pt, pb = oracle.sample_interval(logits, [3, 4], 1.2, 0.9, top_p, t)
+            assert inn and (lo2, hi2) == (lo, hi) and lo <= u <= hi and pt >= pb
