@@ -20,13 +20,13 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-WTYPE_ID = {"q8_0": 8, "q4_0": 2}
+WTYPE_ID = {"q8_0": 8, "q4_0": 2, "q4_k": 12, "q6_k": 14}
 
 
 class OrcConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n_layers", "n_embd", "n_heads", "n_kv_heads", "head_dim", "n_ff",
                                                "n_vocab", "wtype", "kv_f16", "max_ctx", "native_ctx")] + \
-               [("rms_eps", ctypes.c_double), ("rope_base", ctypes.c_double)]
+               [("rms_eps", ctypes.c_double), ("rope_base", ctypes.c_double), ("out_wtype", ctypes.c_int32)]
 
 
 def build(force: bool = False) -> str:
@@ -212,7 +212,7 @@ def config_of(cfg) -> OrcConfig:
     """OrcConfig from a synth.ModelConfig-like object."""
     return OrcConfig(cfg.n_layers, cfg.n_embd, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.n_ff, cfg.n_vocab,
                      WTYPE_ID[cfg.wtype], 1 if cfg.kv_dtype == "f16" else 0, cfg.max_ctx, cfg.native_ctx,
-                     cfg.rms_eps, cfg.rope_base)
+                     cfg.rms_eps, cfg.rope_base, WTYPE_ID[getattr(cfg, "out_wtype", "") or cfg.wtype])
 
 
 def layer_offsets(cfg):

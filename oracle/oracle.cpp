@@ -44,7 +44,71 @@ double round_f32(double x) { return (double)(float)x; }
 
 // ---- GGUF blocks (Shimmy v2.0 Architecture, "Quantization") --------------
 
-size_t block_bytes(int32_t wtype) { return wtype == ORC_Q8_0 ? 34 : (wtype == ORC_Q4_0 ? 18 : 0); }
+size_t block_bytes(int32_t wtype) {
+    switch (wtype) {
+        case ORC_Q8_0: return 34;
+        case ORC_Q4_0: return 18;
+        case ORC_Q4_K: return 144;
+        case ORC_Q6_K: return 210;
+        default: return 0;
+    }
+}
+
+// elements per block: 32, or 256 for the K-quant super-blocks
+int64_t block_elems(int32_t wtype) { return (wtype == ORC_Q4_K || wtype == ORC_Q6_K) ? 256 : 32; }
+
+// bytes of one row of k elements
+size_t row_bytes_of(int32_t wtype, int64_t k) { return (size_t)(k / block_elems(wtype)) * block_bytes(wtype); }
+
+// K-quant super-blocks (Shimmy v2.0 Architecture, "Quantization": "Q4_K_M super-block with row scales",
+// "Q6_K super-block, 6-bit"; GPU Inference - dotLLM, "Weight Strategy": Q4_K at about 4.5 bits per weight).
+// The pages leave the byte layout to another document, so the published GGUF layout is taken.
+//
+// Q4_K (144 B per 256 elements): fp16 d, fp16 dmin, 12 bytes holding eight 6-bit scales s_j and eight 6-bit
+// mins m_j of the 32-element sub-blocks, then 128 bytes of 4-bit codes.  Element e: sub-block j = e / 32,
+// value = d s_j n_e - dmin m_j.
+void q4_k_scale_min(const uint8_t* sc, int j, int* s, int* m) {
+    if (j < 4) {  // low six bits of bytes j and j + 4
+        *s = sc[j] & 63;
+        *m = sc[j + 4] & 63;
+    } else {  // low four bits from byte j + 4 (s: low nibble, m: high nibble), top two bits from bytes j - 4 / j
+        *s = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
+        *m = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
+    }
+}
+
+void dequant_q4_k(const uint8_t* b, double* out) {
+    const double d = f16_to_double((uint16_t)(b[0] | (b[1] << 8)));
+    const double dmin = f16_to_double((uint16_t)(b[2] | (b[3] << 8)));
+    const uint8_t* sc = b + 4;
+    const uint8_t* qs = b + 16;
+    for (int e = 0; e < 256; e++) {
+        int s = 0, m = 0;
+        q4_k_scale_min(sc, e / 32, &s, &m);
+        // 64-element group c shares 32 bytes: the low nibbles are its first 32 elements, the high its last 32
+        const int c = e / 64, r = e % 64;
+        const uint8_t byte = qs[32 * c + r % 32];
+        const int n = r < 32 ? (byte & 15) : (byte >> 4);
+        out[e] = d * (double)s * (double)n - dmin * (double)m;
+    }
+}
+
+// Q6_K (210 B per 256 elements): 128 bytes of low 4-bit parts, 64 bytes of high 2-bit parts, sixteen int8
+// scales of the 16-element sub-blocks, fp16 d.  Element e: value = d * scale[e / 16] * (q_e - 32).
+void dequant_q6_k(const uint8_t* b, double* out) {
+    const uint8_t* ql = b;
+    const uint8_t* qh = b + 128;
+    const int8_t* scale = reinterpret_cast<const int8_t*>(b + 192);
+    const double d = f16_to_double((uint16_t)(b[208] | (b[209] << 8)));
+    for (int e = 0; e < 256; e++) {
+        // half h of 128 elements uses ql[64h ..] and qh[32h ..]; its quarter k (32 elements) takes the low
+        // (k < 2) or high (k >= 2) nibbles of ql[64h + 32 (k & 1) ..] and bits 2k, 2k+1 of qh[32h ..]
+        const int h = e / 128, k = (e % 128) / 32, l = e % 32;
+        const uint8_t lo = ql[64 * h + 32 * (k & 1) + l];
+        const int q = (k < 2 ? (lo & 15) : (lo >> 4)) | (((qh[32 * h + l] >> (2 * k)) & 3) << 4);
+        out[e] = d * (double)scale[e / 16] * (double)(q - 32);
+    }
+}
 
 // Q8_0: fp16 scale d, then 32 signed bytes q; element j = d * q_j.
 // Q4_0: fp16 scale d, then 16 bytes; element j uses the low nibble of byte j
@@ -63,8 +127,16 @@ void dequant_block(int32_t wtype, const uint8_t* b, double* out) {
 }
 
 void dequant_row(int32_t wtype, const uint8_t* blocks, int64_t k, double* out) {
-    size_t bb = block_bytes(wtype);
-    for (int64_t b = 0; b < k / 32; b++) dequant_block(wtype, blocks + b * bb, out + b * 32);
+    const size_t bb = block_bytes(wtype);
+    const int64_t be = block_elems(wtype);
+    for (int64_t b = 0; b < k / be; b++) {
+        if (wtype == ORC_Q4_K)
+            dequant_q4_k(blocks + b * bb, out + b * be);
+        else if (wtype == ORC_Q6_K)
+            dequant_q6_k(blocks + b * bb, out + b * be);
+        else
+            dequant_block(wtype, blocks + b * bb, out + b * be);
+    }
 }
 
 // Run f(i) for i in [0, n) over n_threads threads (contiguous ranges).
@@ -92,7 +164,7 @@ double dot(const double* a, const double* b, int64_t n) {
 // Y[m][i] = W_i . X_m : dequantize weight row i once, then dot it with every input row.
 void qgemm(int32_t wtype, const uint8_t* W, int64_t n, int64_t k, const double* X, int64_t M, double* Y,
            int n_threads) {
-    size_t row_bytes = (size_t)(k / 32) * block_bytes(wtype);
+    const size_t row_bytes = row_bytes_of(wtype, k);
     parallel_for(n, n_threads, [&](int64_t i) {
         std::vector<double> w(k);
         dequant_row(wtype, W + (size_t)i * row_bytes, k, w.data());
@@ -187,7 +259,7 @@ double orc_round_f16(double x) { return round_f16(x); }
 double orc_round_f32(double x) { return round_f32(x); }
 
 int orc_dequant_row(int32_t wtype, const uint8_t* blocks, int64_t k, double* out) {
-    if (!block_bytes(wtype) || k % 32) return -1;
+    if (!block_bytes(wtype) || k % block_elems(wtype)) return -1;
     dequant_row(wtype, blocks, k, out);
     return 0;
 }
@@ -198,8 +270,8 @@ int orc_qgemv(int32_t wtype, const uint8_t* W, int64_t n, int64_t k, const doubl
 
 int orc_qgemv_rows(int32_t wtype, const uint8_t* W, int64_t k, const int64_t* rows, int64_t n_rows, const double* x,
                    double* y, int n_threads) {
-    if (!block_bytes(wtype) || k % 32) return -1;
-    size_t row_bytes = (size_t)(k / 32) * block_bytes(wtype);
+    if (!block_bytes(wtype) || k % block_elems(wtype)) return -1;
+    const size_t row_bytes = row_bytes_of(wtype, k);
     parallel_for(n_rows, n_threads, [&](int64_t r) {
         std::vector<double> w(k);
         dequant_row(wtype, W + (size_t)rows[r] * row_bytes, k, w.data());
@@ -210,7 +282,7 @@ int orc_qgemv_rows(int32_t wtype, const uint8_t* W, int64_t k, const int64_t* ro
 
 int orc_qgemm(int32_t wtype, const uint8_t* W, int64_t n, int64_t k, const double* X, int64_t M, double* Y,
               int n_threads) {
-    if (!block_bytes(wtype) || k % 32) return -1;
+    if (!block_bytes(wtype) || k % block_elems(wtype)) return -1;
     qgemm(wtype, W, n, k, X, M, Y, n_threads);
     return 0;
 }
@@ -231,13 +303,16 @@ void orc_attention(const double* q, int32_t H, int32_t KVH, int32_t D, const dou
 }
 
 int orc_layer_offsets(const orc_config* c, uint64_t off[10]) {
-    size_t bb = block_bytes(c->wtype);
-    if (!bb || c->n_embd % 32 || c->n_ff % 32 || (c->n_heads * c->head_dim) % 32) return -1;
+    const int32_t w = c->wtype;
+    const int64_t be = block_elems(w);
+    if (!block_bytes(w) || c->n_embd % be || c->n_ff % be || (c->n_heads * c->head_dim) % be) return -1;
+    if (c->out_wtype && (!block_bytes(c->out_wtype) || c->n_embd % block_elems(c->out_wtype))) return -1;
     size_t E = c->n_embd, QD = (size_t)c->n_heads * c->head_dim, KVD = (size_t)c->n_kv_heads * c->head_dim;
     size_t F = c->n_ff;
     // attn_norm, attn_q, attn_k, attn_v, attn_o, ffn_norm, ffn_gate, ffn_up, ffn_down
-    size_t sz[9] = {E * 4, QD * (E / 32) * bb, KVD * (E / 32) * bb, KVD * (E / 32) * bb, E * (QD / 32) * bb,
-                    E * 4, F * (E / 32) * bb, F * (E / 32) * bb, E * (F / 32) * bb};
+    size_t sz[9] = {E * 4, QD * row_bytes_of(w, E), KVD * row_bytes_of(w, E), KVD * row_bytes_of(w, E),
+                    E * row_bytes_of(w, QD), E * 4, F * row_bytes_of(w, E), F * row_bytes_of(w, E),
+                    E * row_bytes_of(w, F)};
     size_t o = 0;
     for (int i = 0; i < 9; i++) {
         off[i] = o;
@@ -421,14 +496,14 @@ int orc_forward(orc_model* m, const int32_t* tokens, int64_t n, int64_t start_po
         if (tokens[r] < 0 || tokens[r] >= c.n_vocab) return -2;
     const int64_t E = c.n_embd, H = c.n_heads, KVH = c.n_kv_heads, D = c.head_dim, F = c.n_ff;
     const int64_t QD = H * D, KVD = KVH * D;
-    const size_t bb = block_bytes(c.wtype);
+    const int32_t head_wtype = c.out_wtype ? c.out_wtype : c.wtype;
 
     std::vector<double> X(n * E), Y(n * E), Q(n * QD), K(n * KVD), V(n * KVD), A(n * QD), O(n * E);
     std::vector<double> G(n * F), U(n * F), Hh(n * F);
 
     // embedding lookup: dequantized row of token_embd
     for (int64_t r = 0; r < n; r++)
-        dequant_row(c.wtype, m->token_embd + (size_t)tokens[r] * (E / 32) * bb, E, &X[r * E]);
+        dequant_row(c.wtype, m->token_embd + (size_t)tokens[r] * row_bytes_of(c.wtype, E), E, &X[r * E]);
     if (capture) std::memcpy(capture, X.data(), sizeof(double) * n * E);
 
     for (int32_t l = 0; l < c.n_layers; l++) {
@@ -481,7 +556,7 @@ int orc_forward(orc_model* m, const int32_t* tokens, int64_t n, int64_t start_po
         // final RMS norm on the last position only, then the LM head
         std::vector<double> last(E);
         rmsnorm(&X[(n - 1) * E], m->output_norm, E, c.rms_eps, last.data());
-        qgemm(c.wtype, m->output, c.n_vocab, E, last.data(), 1, logits, n_threads);
+        qgemm(head_wtype, m->output, c.n_vocab, E, last.data(), 1, logits, n_threads);
     }
     return 0;
 }

@@ -15,7 +15,9 @@
  *    "Decode" step; "Output head" (LM head on the last position); "Sampler"
  *    (greedy = temperature 0).
  *  - "Shimmy v2.0 Architecture": "Quantization" table (Q4_0, Q8_0 32-element
- *    blocks), "Extended Context (YaRN)" (scale applied to all positions).
+ *    blocks; Q4_K and Q6_K super-blocks, whose byte layout the pages leave to
+ *    another document: the published GGUF layout is taken), "Extended Context
+ *    (YaRN)" (scale applied to all positions).
  *  - "GPU Inference — dotLLM": "Forward Pass" steps (final RmsNorm on the last
  *    token, LM head), "Attention on GPU" (causal mask, GQA group = H / KVH).
  *
@@ -34,14 +36,15 @@
 extern "C" {
 #endif
 
-enum { ORC_Q4_0 = 2, ORC_Q8_0 = 8 };
+enum { ORC_Q4_0 = 2, ORC_Q8_0 = 8, ORC_Q4_K = 12, ORC_Q6_K = 14 };
 
 typedef struct orc_config {
     int32_t n_layers, n_embd, n_heads, n_kv_heads, head_dim, n_ff, n_vocab;
-    int32_t wtype;      /* ORC_Q8_0 | ORC_Q4_0 */
+    int32_t wtype;      /* ORC_Q8_0 | ORC_Q4_0 | ORC_Q4_K | ORC_Q6_K: layer matrices and token_embd */
     int32_t kv_f16;     /* 0: f32 cache, 1: f16 cache */
     int32_t max_ctx, native_ctx;
     double rms_eps, rope_base;
+    int32_t out_wtype;  /* block type of the LM head (0 = wtype) */
 } orc_config;
 
 typedef struct orc_model orc_model;
@@ -53,7 +56,8 @@ double orc_round_f16(double x);
 /* double -> nearest binary32 value, returned as double. */
 double orc_round_f32(double x);
 
-/* Decode k elements (k % 32 == 0) of GGUF blocks into exact doubles. */
+/* Decode k elements (a whole number of blocks: 32 elements, 256 for Q4_K / Q6_K) of GGUF blocks into exact
+ * doubles. */
 int orc_dequant_row(int32_t wtype, const uint8_t* blocks, int64_t k, double* out);
 
 /* y[i] = sum_j W[i][j] x[j] for the n rows of W (k columns, GGUF blocks). */

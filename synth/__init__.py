@@ -1,7 +1,7 @@
 """Seeded synthetic inputs shared by the CUDA path and the CPU oracle.
 
-A thin ctypes wrapper over ``synth.c`` (counter-based normals, GGUF Q8_0/Q4_0
-block encoder, layer-blob packer).  It holds input generation only: nothing in
+A thin ctypes wrapper over ``synth.c`` (counter-based normals, GGUF Q8_0/Q4_0/
+Q4_K/Q6_K block encoder, layer-blob packer).  It holds input generation only: nothing in
 this package decodes a block or computes any step of the forward pass.
 """
 import ctypes
@@ -11,7 +11,8 @@ import threading
 
 import numpy as np
 
-from .configs import CONFIGS, ModelConfig, Q4_0, Q8_0, BASE_SEED, seed_of  # noqa: F401
+from .configs import (CONFIGS, KQUANT_CONFIGS, ModelConfig, Q4_0, Q8_0, Q4_K, Q6_K, BASE_SEED,  # noqa: F401
+                      seed_of, kquant_seed_of)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "synth.c")
@@ -19,8 +20,9 @@ _LIB = os.path.join(_HERE, "libsynth.so")
 _lock = threading.Lock()
 _lib = None
 
-WTYPE_ID = {Q8_0: 8, Q4_0: 2}
-BLOCK_BYTES = {Q8_0: 34, Q4_0: 18}
+WTYPE_ID = {Q8_0: 8, Q4_0: 2, Q4_K: 12, Q6_K: 14}
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_K: 144, Q6_K: 210}
+BLOCK_ELEMS = {Q8_0: 32, Q4_0: 32, Q4_K: 256, Q6_K: 256}
 
 # tensor ids outside the per-layer range 1 + 16*layer + section
 TID_TOKEN_EMBD = 0x100000
@@ -69,18 +71,20 @@ def layer_offsets(cfg: ModelConfig):
     rc = _load().syn_layer_offsets(cfg.n_embd, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.n_ff,
                                    WTYPE_ID[cfg.wtype], off)
     if rc:
-        raise ValueError("shape not blockable by 32")
+        raise ValueError(f"shape not blockable by {BLOCK_ELEMS[cfg.wtype]}")
     return [int(v) for v in off]
 
 
 def matrix(wtype: str, seed: int, tid: int, n: int, k: int, sigma: float = 0.02, mean: float = 0.0,
            threads: int = 0) -> np.ndarray:
-    """Random [n, k] matrix encoded as GGUF blocks: uint8 array of n*(k/32)*block bytes."""
-    out = np.empty(n * (k // 32) * BLOCK_BYTES[wtype], dtype=np.uint8)
+    """Random [n, k] matrix encoded as GGUF blocks: uint8 array of n*(k/block elements)*block bytes."""
+    if k % BLOCK_ELEMS[wtype]:
+        raise ValueError(f"k must be a multiple of {BLOCK_ELEMS[wtype]}")
+    out = np.empty(n * (k // BLOCK_ELEMS[wtype]) * BLOCK_BYTES[wtype], dtype=np.uint8)
     rc = _load().syn_gen_matrix(WTYPE_ID[wtype], seed, tid, n, k, mean, sigma, out.ctypes.data,
                                 threads or default_threads())
     if rc:
-        raise ValueError("k must be a multiple of 32")
+        raise ValueError("bad matrix shape")
     return out
 
 
@@ -121,7 +125,8 @@ class HostModel:
         self.token_embd = matrix(cfg.wtype, seed, TID_TOKEN_EMBD, cfg.n_vocab, cfg.n_embd, cfg.w_sigma,
                                  threads=threads)
         self.output_norm = normals(seed, TID_OUTPUT_NORM, cfg.n_embd, 1.0, cfg.norm_sigma)
-        self.output = matrix(cfg.wtype, seed, TID_OUTPUT, cfg.n_vocab, cfg.n_embd, cfg.w_sigma, threads=threads)
+        self.output = matrix(cfg.head_wtype, seed, TID_OUTPUT, cfg.n_vocab, cfg.n_embd, cfg.w_sigma,
+                             threads=threads)
 
     def prompt(self, n: int = 0) -> np.ndarray:
         return tokens(self.seed, n or self.cfg.prompt_len, self.cfg.n_vocab)

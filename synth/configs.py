@@ -12,6 +12,8 @@ from dataclasses import dataclass, asdict, replace
 
 Q8_0 = "q8_0"
 Q4_0 = "q4_0"
+Q4_K = "q4_k"
+Q6_K = "q6_k"
 BASE_SEED = 20261202
 
 
@@ -25,7 +27,7 @@ class ModelConfig:
     head_dim: int
     n_ff: int
     n_vocab: int
-    wtype: str          # "q8_0" | "q4_0"
+    wtype: str          # "q8_0" | "q4_0" | "q4_k" | "q6_k": every layer matrix and token_embd
     kv_dtype: str       # "f32" | "f16"
     max_ctx: int
     native_ctx: int     # == max_ctx means no YaRN scaling
@@ -37,6 +39,11 @@ class ModelConfig:
     n_decode: int = 0
     w_sigma: float = 0.02
     norm_sigma: float = 0.1
+    out_wtype: str = ""  # the LM head's block type ("" = wtype)
+
+    @property
+    def head_wtype(self) -> str:
+        return self.out_wtype or self.wtype
 
     def as_dict(self):
         return asdict(self)
@@ -59,5 +66,19 @@ CONFIGS = [
 ]
 
 
+# K-quant models in the Q4_K_M mix the pages run (dotLLM, VRAM Estimation: "Llama 3 8B, Q4_K_M"): Q4_K
+# layer matrices and embedding, a Q6_K LM head (Airframe GPU pipeline, output head stored as Q6_K).
+KQUANT_CONFIGS = [
+    ModelConfig("tiny-2L-q4_k_m", 2, 512, 8, 4, 64, 1536, 2048, Q4_K, "f32", 64, 64, 10000.0,
+                prompt_len=32, chunk=512, n_decode=16, out_wtype=Q6_K),
+    ModelConfig("llama-3-8b-shape-q4_k_m", 32, 4096, 32, 8, 128, 14336, 128256, Q4_K, "f16", 8192, 8192, 500000.0,
+                prompt_len=4096, chunk=512, n_decode=256, out_wtype=Q6_K),
+]
+
+
 def seed_of(index: int) -> int:
     return BASE_SEED + index
+
+
+def kquant_seed_of(index: int) -> int:
+    return BASE_SEED + 100 + index
