@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) forward pass of a GGUF Q8_0/Q4_0 Llama-style decoder.
+"""GB300 (sm_103a) forward pass of a GGUF (Q8_0 / Q4_0 / Q4_K / Q6_K) Llama-style decoder.
 
 Thin ctypes binding over ``libaf.so`` (C ABI in ``include/af.h``): the
 functions below only marshal arguments; every step of the forward pass runs in
@@ -11,9 +11,9 @@ import os
 from ._build import LIB_PATH, build  # noqa: F401
 
 AF_OK, AF_EINVAL, AF_ERANGE, AF_ENOMEM, AF_ECUDA, AF_ETIMEOUT, AF_ENOTIMPL = range(7)
-AF_Q4_0, AF_Q8_0 = 2, 8
+AF_Q4_0, AF_Q8_0, AF_Q4_K, AF_Q6_K = 2, 8, 12, 14
 AF_F32, AF_F16 = 0, 1
-WTYPE = {"q4_0": AF_Q4_0, "q8_0": AF_Q8_0}
+WTYPE = {"q4_0": AF_Q4_0, "q8_0": AF_Q8_0, "q4_k": AF_Q4_K, "q6_k": AF_Q6_K}
 KVTYPE = {"f32": AF_F32, "f16": AF_F16}
 STATUS_NAMES = {0: "AF_OK", 1: "AF_EINVAL", 2: "AF_ERANGE", 3: "AF_ENOMEM", 4: "AF_ECUDA", 5: "AF_ETIMEOUT",
                 6: "AF_ENOTIMPL"}
@@ -29,7 +29,7 @@ class af_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n_layers", "n_embd", "n_heads", "n_kv_heads", "head_dim", "n_ff",
                                                "n_vocab", "wtype", "kv_dtype", "max_ctx", "native_ctx",
                                                "max_chunk")] + \
-               [("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float)]
+               [("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("out_wtype", ctypes.c_int32)]
 
 
 class af_weights(ctypes.Structure):
@@ -109,7 +109,7 @@ def make_config(cfg, max_chunk: int = 512) -> af_config:
     """af_config from a ModelConfig-like object (fields as in synth.configs)."""
     return af_config(cfg.n_layers, cfg.n_embd, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.n_ff, cfg.n_vocab,
                      WTYPE[cfg.wtype], KVTYPE[cfg.kv_dtype], cfg.max_ctx, cfg.native_ctx, max_chunk, cfg.rms_eps,
-                     cfg.rope_base)
+                     cfg.rope_base, WTYPE[getattr(cfg, "out_wtype", "") or cfg.wtype])
 
 
 # ---------------------------------------------------------------- same-name entry points

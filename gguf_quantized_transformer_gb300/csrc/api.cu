@@ -47,7 +47,20 @@ int fail(int code, const char* fmt, ...) {
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-size_t block_bytes(int wtype) { return wtype == AF_Q8_0 ? 34 : (wtype == AF_Q4_0 ? 18 : 0); }
+size_t block_bytes(int wtype) {
+    switch (wtype) {
+        case AF_Q8_0: return 34;
+        case AF_Q4_0: return 18;
+        case AF_Q4_K: return 144;
+        case AF_Q6_K: return 210;
+        default: return 0;
+    }
+}
+
+// bytes of one GGUF row of k weights
+size_t row_bytes(int wtype, size_t k) { return k / (size_t)block_elems(wtype) * block_bytes(wtype); }
+
+int head_wtype(const af_config* c) { return c->out_wtype ? c->out_wtype : c->wtype; }
 
 // Tracks device allocations of one object so a failed create frees everything.
 struct Allocs {
@@ -90,7 +103,7 @@ Planes make_planes(Allocs& A, int wtype, int N, int K) {
 }
 
 cudaError_t repack_into(const Planes& P, const void* src, int N, int row0, int step, cudaStream_t s) {
-    return launch_repack((const uint8_t*)src, P.wtype, N, P.K, (uint8_t*)P.qs, (__half*)P.sc, P.Kp, row0, step, s);
+    return launch_repack((const uint8_t*)src, P, N, row0, step, s);
 }
 
 struct LayerW {
@@ -109,14 +122,18 @@ Epi epi_simple(int kind, float* out, int ld) {
 
 int check_config(const af_config* c) {
     if (!c) return fail(AF_EINVAL, "null config");
-    if (c->wtype != AF_Q4_0 && c->wtype != AF_Q8_0) return fail(AF_EINVAL, "wtype must be AF_Q4_0 or AF_Q8_0");
+    if (!block_bytes(c->wtype)) return fail(AF_EINVAL, "wtype must be AF_Q4_0, AF_Q8_0, AF_Q4_K or AF_Q6_K");
+    if (!block_bytes(head_wtype(c))) return fail(AF_EINVAL, "bad out_wtype");
     if (c->kv_dtype != AF_F32 && c->kv_dtype != AF_F16) return fail(AF_EINVAL, "kv_dtype must be AF_F32 or AF_F16");
     if (c->n_layers <= 0 || c->n_embd <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
         c->n_ff <= 0 || c->n_vocab <= 0 || c->max_ctx <= 0)
         return fail(AF_EINVAL, "all sizes must be positive");
     if (c->max_chunk < 0 || c->native_ctx < 0) return fail(AF_EINVAL, "negative max_chunk / native_ctx");
-    if (c->n_embd % 32 || c->n_ff % 32 || (c->n_heads * c->head_dim) % 32)
-        return fail(AF_EINVAL, "n_embd, n_ff and n_heads*head_dim must be multiples of 32 (GGUF block)");
+    {
+        const int be = std::max(block_elems(c->wtype), block_elems(head_wtype(c)));
+        if (c->n_embd % be || c->n_ff % block_elems(c->wtype) || (c->n_heads * c->head_dim) % block_elems(c->wtype))
+            return fail(AF_EINVAL, "n_embd, n_ff and n_heads*head_dim must be whole GGUF blocks (%d weights)", be);
+    }
     if (c->n_heads % c->n_kv_heads) return fail(AF_EINVAL, "n_heads must be a multiple of n_kv_heads");
     if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return fail(AF_EINVAL, "bad rms_eps / rope_base");
     if (!attn_supported(c->n_heads, c->n_kv_heads, c->head_dim))
@@ -127,6 +144,9 @@ int check_config(const af_config* c) {
         const int kmax = std::max(std::max(c->n_embd, c->n_ff), c->n_heads * c->head_dim);
         if (padded_k(c->wtype, kmax) / chunk_weights(c->wtype) > qgemv_max_chunks())
             return fail(AF_ENOTIMPL, "matrix rows longer than %d weights", qgemv_max_chunks() * chunk_weights(c->wtype));
+        if (padded_k(head_wtype(c), c->n_embd) / chunk_weights(head_wtype(c)) > qgemv_max_chunks())
+            return fail(AF_ENOTIMPL, "LM head rows longer than %d weights",
+                        qgemv_max_chunks() * chunk_weights(head_wtype(c)));
     }
     return AF_OK;
 }
@@ -208,15 +228,17 @@ const char* af_last_error(void) { return g_err.c_str(); }
 
 int af_layer_offsets(const af_config* c, uint64_t off[10]) {
     if (!c || !off) return fail(AF_EINVAL, "null argument");
-    size_t bb = block_bytes(c->wtype);
-    if (!bb) return fail(AF_EINVAL, "bad wtype");
+    const int wt = c->wtype;
+    if (!block_bytes(wt)) return fail(AF_EINVAL, "bad wtype");
+    const int be = block_elems(wt);
     if (c->n_embd <= 0 || c->n_ff <= 0 || c->n_heads <= 0 || c->head_dim <= 0 || c->n_kv_heads <= 0 ||
-        c->n_embd % 32 || c->n_ff % 32 || (c->n_heads * c->head_dim) % 32)
+        c->n_embd % be || c->n_ff % be || (c->n_heads * c->head_dim) % be)
         return fail(AF_EINVAL, "bad shape");
     const size_t E = c->n_embd, QD = (size_t)c->n_heads * c->head_dim, KVD = (size_t)c->n_kv_heads * c->head_dim;
     const size_t F = c->n_ff;
-    const size_t sz[9] = {E * 4, QD * (E / 32) * bb, KVD * (E / 32) * bb, KVD * (E / 32) * bb, E * (QD / 32) * bb,
-                          E * 4, F * (E / 32) * bb, F * (E / 32) * bb, E * (F / 32) * bb};
+    const size_t sz[9] = {E * 4, QD * row_bytes(wt, E), KVD * row_bytes(wt, E), KVD * row_bytes(wt, E),
+                          E * row_bytes(wt, QD), E * 4, F * row_bytes(wt, E), F * row_bytes(wt, E),
+                          E * row_bytes(wt, F)};
     size_t o = 0;
     for (int i = 0; i < 9; i++) {
         off[i] = o;
@@ -311,7 +333,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
         if (e) return cuda_fail(e, "weight repack");
     }
     m->emb = make_planes(A, wt, V, E);
-    m->out = make_planes(A, wt, V, E);
+    m->out = make_planes(A, head_wtype(&c), V, E);
     float* onorm = (float*)A.get((size_t)E * 4);
     if (!m->emb.qs || !m->out.qs || !onorm) return oom("embedding / output");
     m->out_norm = onorm;
@@ -387,7 +409,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
         P.abort = words + 2;
         P.err = m->gs.err;
         std::vector<LayerPlan> lp(c.n_layers);
-        bool ok = true;
+        bool ok = head_wtype(&c) == wt;  // the persistent kernel decodes every matrix as one type
         for (int l = 0; l < c.n_layers; l++) {
             const LayerW& lw = m->L[l];
             LayerPlan& L = lp[l];
@@ -671,9 +693,10 @@ void af_qweight_destroy(af_qweight* w) {
 int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t K, void* stream, af_qweight** out) {
     if (!out) return fail(AF_EINVAL, "null out");
     *out = nullptr;
-    if (wtype != AF_Q4_0 && wtype != AF_Q8_0) return fail(AF_EINVAL, "bad wtype");
+    if (!block_bytes(wtype)) return fail(AF_EINVAL, "bad wtype");
     if (!blocks_dev) return fail(AF_EINVAL, "null blocks");
-    if (N <= 0 || K <= 0 || K % 32) return fail(AF_EINVAL, "need N > 0 and K a positive multiple of 32");
+    if (N <= 0 || K <= 0 || K % block_elems(wtype))
+        return fail(AF_EINVAL, "need N > 0 and K a positive multiple of %d", block_elems(wtype));
     if (N % 2) return fail(AF_ENOTIMPL, "N must be even");
     if (padded_k(wtype, K) / chunk_weights(wtype) > qgemv_max_chunks())
         return fail(AF_ENOTIMPL, "K above %d", qgemv_max_chunks() * chunk_weights(wtype));

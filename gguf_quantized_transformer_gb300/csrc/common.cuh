@@ -11,34 +11,61 @@ namespace af {
 // ---------------------------------------------------------------------------
 // Repacked weight layout ("planes").
 //
-// A GGUF [N, K] block matrix is stored as
-//   one record per row, qs_pitch() = (Kp/32) * (QB + 2) bytes apart:
-//     [(Kp/32) blocks x QB quant bytes][(Kp/32) fp16 scales]
-//   (QB = 16 for Q4_0, 32 for Q8_0), so R consecutive rows, scales included,
-//   are one contiguous range (one bulk copy per GEMV stage).
-//   qs points at row 0's quants, sc at row 0's scales; both advance by
-//   qs_pitch() bytes (= sc_pitch() halves) per row.
-// Kp = K rounded up to one GEMV chunk (1024 weights for Q4_0, 512 for Q8_0);
-// blocks past K hold zero quants and a zero scale, so they contribute 0.
-// Q4_0 quant bytes keep GGUF's nibble order (byte j: element j low, j+16 high).
+// A GGUF [N, K] block matrix is stored as one record per row, pitch() bytes
+// apart (a multiple of 16), so R consecutive rows, scales included, are one
+// contiguous range (one bulk copy per GEMV stage).  K is padded to Kp, a whole
+// GEMV chunk (1024 weights; 512 for Q8_0); padding holds zero codes and zero
+// scales, so it contributes 0.  The unit of the kernels is 32 weights whose
+// 4-bit codes sit in 16 bytes in GGUF's Q4_0 nibble order (byte j: element j
+// low, element j + 16 high); Q8_0 units are 16 weights in 16 bytes.
+//   Q4_0 / Q8_0: [(Kp/32) x QB code bytes][(Kp/32) fp16 scales]  (QB = 16 / 32)
+//   Q4_K: [(Kp/32) x 16 code bytes][(Kp/256) super-block records of 20 B:
+//          fp16 d, fp16 dmin, then (s_j, m_j) byte pairs of its 8 sub-blocks,
+//          the 6-bit scales and mins already unpacked]
+//   Q6_K: [(Kp/32) x 16 bytes: low 4 bits of the codes][(Kp/32) x 8 bytes: the
+//          high 2 bits, two words per unit, element 4t + i of a 16-element half
+//          at bits 8i + 2t][(Kp/256) records of 18 B: fp16 d, 16 int8 scales]
+//          (+ padding of the row to 16 bytes)
+// qs points at row 0; sc at row 0's fp16 scales (Q4_0 / Q8_0; sc_pitch()
+// halves per row).  sc_off() is the byte offset of the scales or records in a
+// row, hb_off() that of the Q6_K high-bit plane.
 // ---------------------------------------------------------------------------
+constexpr int kQ4KRec = 20;
+constexpr int kQ6KRec = 18;
+
+__host__ __device__ inline bool is_kquant(int wtype) { return wtype == AF_Q4_K || wtype == AF_Q6_K; }
+
 struct Planes {
     const uint8_t* qs = nullptr;
     const __half* sc = nullptr;
     int N = 0, K = 0, Kp = 0, wtype = 0;
-    __host__ __device__ int qb() const { return wtype == AF_Q8_0 ? 32 : 16; }
-    __host__ __device__ int64_t qs_pitch() const { return (int64_t)(Kp / 32) * (qb() + 2); }  // bytes per row
-    __host__ __device__ int sc_pitch() const { return (Kp / 32) * (qb() + 2) / 2; }           // halves per row
-    __host__ __device__ int sc_off() const { return (Kp / 32) * qb(); }  // byte offset of the scales in a row
+    __host__ __device__ int qb() const { return wtype == AF_Q8_0 ? 32 : 16; }  // code bytes per 32 weights
+    __host__ __device__ int sc_off() const {
+        return wtype == AF_Q6_K ? (Kp / 32) * 24 : (Kp / 32) * qb();
+    }
+    __host__ __device__ int hb_off() const { return (Kp / 32) * 16; }
+    __host__ __device__ int64_t qs_pitch() const {  // bytes per row
+        int64_t b;
+        if (wtype == AF_Q4_K)
+            b = (int64_t)(Kp / 32) * 16 + (int64_t)(Kp / 256) * kQ4KRec;
+        else if (wtype == AF_Q6_K)
+            b = (int64_t)(Kp / 32) * 24 + (int64_t)(Kp / 256) * kQ6KRec;
+        else
+            b = (int64_t)(Kp / 32) * (qb() + 2);
+        return (b + 15) & ~(int64_t)15;
+    }
+    __host__ __device__ int sc_pitch() const { return (int)(qs_pitch() / 2); }  // halves per row
 };
 
 inline int chunk_weights(int wtype) { return wtype == AF_Q8_0 ? 512 : 1024; }
 inline int padded_k(int wtype, int K) { int c = chunk_weights(wtype); return (K + c - 1) / c * c; }
+inline int block_elems(int wtype) { return is_kquant(wtype) ? 256 : 32; }
 inline size_t planes_bytes(int wtype, int N, int K, size_t* sc_off) {
-    const int Kp = padded_k(wtype, K);
-    const size_t qb = wtype == AF_Q8_0 ? 32 : 16;
-    if (sc_off) *sc_off = (size_t)(Kp / 32) * qb;
-    return (((size_t)N * (Kp / 32) * (qb + 2)) + 255) & ~(size_t)255;
+    Planes p;
+    p.wtype = wtype;
+    p.Kp = padded_k(wtype, K);
+    if (sc_off) *sc_off = (size_t)p.sc_off();
+    return ((size_t)N * (size_t)p.qs_pitch() + 255) & ~(size_t)255;
 }
 
 // ---------------------------------------------------------------------------
@@ -137,8 +164,7 @@ struct GemvScratch {
 
 int num_sms();
 
-cudaError_t launch_repack(const uint8_t* src, int wtype, int N, int K, uint8_t* qs, __half* sc, int Kp,
-                          int dst_row0, int dst_row_step, cudaStream_t s);
+cudaError_t launch_repack(const uint8_t* src, const Planes& P, int N, int row0, int step, cudaStream_t s);
 cudaError_t launch_rope_table(float2* tab, int max_ctx, int head_dim, double base, double yarn_scale,
                               cudaStream_t s);
 cudaError_t launch_embed(const Planes& emb, const int* tok_dev, int n, float* x, int64_t ldx, cudaStream_t s);

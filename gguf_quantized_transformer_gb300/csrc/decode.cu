@@ -26,6 +26,7 @@ cudaError_t dispatch(const DecodePlan& p, cudaStream_t s, bool prepare) {
 
 // Shapes of a GEMV phase: R rows per stage within one ring slot, WK chunk warps.
 bool decode_gemv_task(const Planes& W, GemvTask& t) {
+    if (is_kquant(W.wtype)) return false;  // the persistent kernel is built for Q4_0 / Q8_0 only
     const int UW = W.wtype == AF_Q8_0 ? 16 : 32;
     const int NC = W.Kp / (32 * UW);
     const int UPL = 2;  // x slots per lane the kernel is instantiated for

@@ -17,18 +17,88 @@ int num_sms() {
     return n;
 }
 
-// GGUF AoS blocks -> per-row records of quants then scales (see Planes).  One thread per
-// destination block; blocks past K/32 are zero.
-__global__ void repack_kernel(const uint8_t* __restrict__ src, int wtype, int N, int nb, uint8_t* __restrict__ qs,
-                              __half* __restrict__ sc, int nbp, int row0, int step) {
+// GGUF AoS blocks -> per-row records (see Planes).  One thread per destination 32-weight unit (per 32-weight
+// block for Q4_0 / Q8_0); units past K are zero.  The first unit of a K-quant super-block also writes the
+// super-block's record.  Source row r goes to destination row row0 + r * step.
+__device__ void repack_q4_k_unit(const uint8_t* blk, int j, uint8_t* dq, uint8_t* rec) {
+    // codes of sub-block j: elements 32 j + i live in qs[32 (j / 2) + i], low nibble for even j
+    const uint8_t* qs = blk + 16 + 32 * (j >> 1);
+    const int sh = (j & 1) * 4;
+    for (int t = 0; t < 16; t++)
+        dq[t] = (uint8_t)(((qs[t] >> sh) & 15) | (((qs[t + 16] >> sh) & 15) << 4));
+    if (j == 0) {  // record: d, dmin, then the unpacked (scale, min) of every sub-block
+        for (int i = 0; i < 4; i++) rec[i] = blk[i];
+        const uint8_t* sc = blk + 4;
+        for (int k = 0; k < 8; k++) {
+            int sk, mk;
+            if (k < 4) {
+                sk = sc[k] & 63;
+                mk = sc[k + 4] & 63;
+            } else {
+                sk = (sc[k + 4] & 15) | ((sc[k - 4] >> 6) << 4);
+                mk = (sc[k + 4] >> 4) | ((sc[k] >> 6) << 4);
+            }
+            rec[4 + 2 * k] = (uint8_t)sk;
+            rec[5 + 2 * k] = (uint8_t)mk;
+        }
+    }
+}
+
+__device__ void repack_q6_k_unit(const uint8_t* blk, int g, uint8_t* dq, uint8_t* dh, uint8_t* rec) {
+    // code of element e = 32 g + i of the super-block: low 4 bits in ql, high 2 bits in qh
+    auto code = [&](int e) {
+        const int h = e >> 7, k = (e & 127) >> 5, l = e & 31;
+        const uint8_t lo = blk[64 * h + 32 * (k & 1) + l];
+        return ((k < 2 ? lo : lo >> 4) & 15) | (((blk[128 + 32 * h + l] >> (2 * k)) & 3) << 4);
+    };
+    uint32_t hw[2] = {0u, 0u};
+    for (int t = 0; t < 16; t++) {
+        const int c0 = code(32 * g + t), c1 = code(32 * g + t + 16);
+        dq[t] = (uint8_t)((c0 & 15) | ((c1 & 15) << 4));
+        // element 4 tt + i of a half at bits 8 i + 2 tt of that half's word
+        const int tt = t >> 2, i = t & 3;
+        hw[0] |= (uint32_t)(c0 >> 4) << (8 * i + 2 * tt);
+        hw[1] |= (uint32_t)(c1 >> 4) << (8 * i + 2 * tt);
+    }
+    for (int b = 0; b < 8; b++) dh[b] = (uint8_t)(hw[b >> 2] >> (8 * (b & 3)));
+    if (g == 0) {  // record: d, then the 16 scales
+        rec[0] = blk[208];
+        rec[1] = blk[209];
+        for (int k = 0; k < 16; k++) rec[2 + k] = blk[192 + k];
+    }
+}
+
+__global__ void repack_kernel(const uint8_t* __restrict__ src, Planes P, int N, int row0, int step) {
+    const int nbp = P.Kp / 32, nb = P.K / 32;  // destination units per row, source units per row
     int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= (int64_t)N * nbp) return;
-    int r = (int)(t / nbp), b = (int)(t % nbp);
-    const int qb = wtype == AF_Q8_0 ? 32 : 16, bb = qb + 2;
-    const int64_t pitch = (int64_t)nbp * bb;  // bytes per destination row (quants, then scales)
-    int64_t dr = (int64_t)row0 + (int64_t)r * step;
-    uint8_t* dq = qs + dr * pitch + (int64_t)b * qb;
-    __half* dsc = sc + dr * (pitch / 2) + b;
+    const int r = (int)(t / nbp), b = (int)(t % nbp);
+    const int64_t pitch = P.qs_pitch();
+    uint8_t* row = const_cast<uint8_t*>(P.qs) + ((int64_t)row0 + (int64_t)r * step) * pitch;
+    if (P.wtype == AF_Q4_K || P.wtype == AF_Q6_K) {
+        const int sb = b / 8, u = b % 8;
+        const int bb = P.wtype == AF_Q4_K ? 144 : 210, rec_bytes = P.wtype == AF_Q4_K ? kQ4KRec : kQ6KRec;
+        uint8_t* dq = row + (int64_t)b * 16;
+        uint8_t* rec = row + P.sc_off() + (int64_t)sb * rec_bytes;
+        uint8_t* dh = row + P.hb_off() + (int64_t)b * 8;
+        if (b < nb) {
+            const uint8_t* blk = src + ((int64_t)r * (nb / 8) + sb) * bb;
+            if (P.wtype == AF_Q4_K) repack_q4_k_unit(blk, u, dq, rec);
+            else repack_q6_k_unit(blk, u, dq, dh, rec);
+        } else {
+            for (int j = 0; j < 16; j++) dq[j] = 0;
+            if (P.wtype == AF_Q6_K)
+                for (int j = 0; j < 8; j++) dh[j] = 0;
+            if (u == 0)
+                for (int j = 0; j < rec_bytes; j++) rec[j] = 0;
+        }
+        if (b == nbp - 1)  // the row's padding up to its 16-byte pitch
+            for (int64_t j = P.sc_off() + (int64_t)(nbp / 8) * rec_bytes; j < pitch; j++) row[j] = 0;
+        return;
+    }
+    const int qb = P.qb(), bb = qb + 2;
+    uint8_t* dq = row + (int64_t)b * qb;
+    __half* dsc = reinterpret_cast<__half*>(row + P.sc_off()) + b;
     if (b < nb) {
         const uint8_t* s = src + ((int64_t)r * nb + b) * bb;
         unsigned short bits = (unsigned short)(s[0] | (s[1] << 8));
@@ -40,12 +110,11 @@ __global__ void repack_kernel(const uint8_t* __restrict__ src, int wtype, int N,
     }
 }
 
-cudaError_t launch_repack(const uint8_t* src, int wtype, int N, int K, uint8_t* qs, __half* sc, int Kp, int row0,
-                          int step, cudaStream_t s) {
-    int64_t n = (int64_t)N * (Kp / 32);
+cudaError_t launch_repack(const uint8_t* src, const Planes& P, int N, int row0, int step, cudaStream_t s) {
+    int64_t n = (int64_t)N * (P.Kp / 32);
     int threads = 256;
     int64_t blocks = (n + threads - 1) / threads;
-    repack_kernel<<<(unsigned)blocks, threads, 0, s>>>(src, wtype, N, K / 32, qs, sc, Kp / 32, row0, step);
+    repack_kernel<<<(unsigned)blocks, threads, 0, s>>>(src, P, N, row0, step);
     return cudaGetLastError();
 }
 
@@ -67,24 +136,43 @@ cudaError_t launch_rope_table(float2* tab, int max_ctx, int head_dim, double bas
     return cudaGetLastError();
 }
 
+// Value of weight k of row `row` of repacked planes (the embedding table), in fp32.
+__device__ float plane_weight(const Planes& P, int row, int k) {
+    const uint8_t* base = P.qs + (int64_t)row * P.qs_pitch();
+    const int u = k >> 5, e = k & 31;
+    if (P.wtype == AF_Q4_K || P.wtype == AF_Q6_K) {
+        const uint8_t byte = base[(int64_t)u * 16 + (e & 15)];
+        const int lo4 = e < 16 ? (byte & 15) : (byte >> 4);
+        if (P.wtype == AF_Q4_K) {
+            const uint8_t* rec = base + P.sc_off() + (int64_t)(u >> 3) * kQ4KRec;
+            const float d = __half2float(__ushort_as_half((unsigned short)(rec[0] | (rec[1] << 8))));
+            const float dmin = __half2float(__ushort_as_half((unsigned short)(rec[2] | (rec[3] << 8))));
+            const int j = u & 7;
+            return d * (float)rec[4 + 2 * j] * (float)lo4 - dmin * (float)rec[5 + 2 * j];
+        }
+        const uint8_t* hb = base + P.hb_off() + (int64_t)u * 8 + (e >> 4) * 4;
+        const uint32_t hw = (uint32_t)hb[0] | ((uint32_t)hb[1] << 8) | ((uint32_t)hb[2] << 16) | ((uint32_t)hb[3] << 24);
+        const int i = e & 15;
+        const int q = lo4 | (int)((hw >> (8 * (i & 3) + 2 * (i >> 2))) & 3u) << 4;
+        const uint8_t* rec = base + P.sc_off() + (int64_t)(u >> 3) * kQ6KRec;
+        const float d = __half2float(__ushort_as_half((unsigned short)(rec[0] | (rec[1] << 8))));
+        const int sc = (int8_t)rec[2 + 2 * (u & 7) + (e >> 4)];
+        return d * (float)sc * (float)(q - 32);
+    }
+    const float d = __half2float(P.sc[(int64_t)row * P.sc_pitch() + u]);
+    const uint8_t* q = base + (int64_t)u * P.qb();
+    if (P.wtype == AF_Q8_0) return d * (float)(int8_t)q[e];
+    const uint8_t byte = q[e & 15];
+    return d * (float)((e < 16 ? (byte & 15) : (byte >> 4)) - 8);
+}
+
 // x[r][:] = dequantized row tok[r] of the embedding table.
 __global__ void embed_kernel(Planes emb, const int* __restrict__ tok, int E, float* __restrict__ x, int64_t ldx) {
     const int r = blockIdx.y;
     int row = tok[r];
     if (row < 0 || row >= emb.N) row = 0;  // ids are validated on the host; never read outside the table
-    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < E; k += gridDim.x * blockDim.x) {
-        const int b = k >> 5, e = k & 31;
-        const float d = __half2float(emb.sc[(int64_t)row * emb.sc_pitch() + b]);
-        const uint8_t* q = emb.qs + (int64_t)row * emb.qs_pitch() + (int64_t)b * emb.qb();
-        float v;
-        if (emb.wtype == AF_Q8_0) {
-            v = d * (float)(int8_t)q[e];
-        } else {
-            const uint8_t byte = q[e & 15];
-            v = d * (float)((e < 16 ? (byte & 15) : (byte >> 4)) - 8);
-        }
-        x[(int64_t)r * ldx + k] = v;
-    }
+    for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < E; k += gridDim.x * blockDim.x)
+        x[(int64_t)r * ldx + k] = plane_weight(emb, row, k);
 }
 
 cudaError_t launch_embed(const Planes& emb, const int* tok_dev, int n, float* x, int64_t ldx, cudaStream_t s) {

@@ -1,5 +1,5 @@
 // Prefill GEMM on the 5th-generation tensor cores: Y[m][n] = sum_k X[m][k] W[n][k]
-// with W in Q4_0 / Q8_0 planes, dequantized tile by tile into shared memory
+// with W in Q4_0 / Q8_0 / Q4_K / Q6_K planes, dequantized tile by tile into shared memory
 // and multiplied with tcgen05.mma into a TMEM accumulator (dotLLM "GPU
 // Inference", "Weight Strategy", approach 1: fused dequantize-in-kernel feeding
 // the tensor cores; dequantized values never touch device memory).
@@ -21,7 +21,9 @@
 //                 loaded into registers before waiting for a free stage.  The
 //                 split is exact fp16 arithmetic: with c the integer code
 //                 (exact in fp16), w_hi = d * c rounded (HMUL2) and
-//                 w_lo = fma(d, c, -w_hi) (HFMA2, exact);
+//                 w_lo = fma(d, c, -w_hi) (HFMA2, exact); K-quant weights
+//                 are formed in fp32 from the unpacked sub-block scale and
+//                 min, then split into fp16 hi and the rounded remainder;
 //                 warps 2..5 then run the fused epilogue from TMEM
 //                 (tcgen05.ld, 32 columns at a time).
 // Every mbarrier wait is bounded; on a timeout the CTA records DEV_TIMEOUT,
@@ -66,6 +68,47 @@ struct RawBlk<AF_Q8_0> {
     uint4 q0, q1;
     unsigned short d;
 };
+
+template <>
+struct RawBlk<AF_Q4_K> {
+    uint4 q;
+    unsigned dm;         // fp16 d, dmin of the super-block
+    unsigned short smj;  // unpacked (s_j, m_j) of this sub-block
+};
+template <>
+struct RawBlk<AF_Q6_K> {
+    uint4 q;             // low 4 bits of the codes
+    uint2 h;             // high 2 bits (element 4t + i of a half at bits 8i + 2t of that half's word)
+    unsigned short d;    // fp16 d of the super-block
+    unsigned short sc;   // int8 scales of the two 16-weight halves
+};
+
+__device__ __forceinline__ void load_blk(const Planes& W, int n, int blk, RawBlk<AF_Q4_K>& b) {
+    const uint8_t* row = W.qs + (int64_t)n * W.qs_pitch();
+    b.q = *reinterpret_cast<const uint4*>(row + (int64_t)blk * 16);
+    const uint8_t* rec = row + W.sc_off() + (int64_t)(blk >> 3) * kQ4KRec;
+    b.dm = *reinterpret_cast<const unsigned*>(rec);
+    b.smj = *reinterpret_cast<const unsigned short*>(rec + 4 + (blk & 7) * 2);
+}
+__device__ __forceinline__ void load_blk(const Planes& W, int n, int blk, RawBlk<AF_Q6_K>& b) {
+    const uint8_t* row = W.qs + (int64_t)n * W.qs_pitch();
+    b.q = *reinterpret_cast<const uint4*>(row + (int64_t)blk * 16);
+    b.h = *reinterpret_cast<const uint2*>(row + W.hb_off() + (int64_t)blk * 8);
+    const uint8_t* rec = row + W.sc_off() + (int64_t)(blk >> 3) * kQ6KRec;
+    b.d = *reinterpret_cast<const unsigned short*>(rec);
+    b.sc = *reinterpret_cast<const unsigned short*>(rec + 2 + (blk & 7) * 2);
+}
+__device__ __forceinline__ void zero_blk(RawBlk<AF_Q4_K>& b) {
+    b.q = make_uint4(0, 0, 0, 0);
+    b.dm = 0;
+    b.smj = 0;
+}
+__device__ __forceinline__ void zero_blk(RawBlk<AF_Q6_K>& b) {
+    b.q = make_uint4(0, 0, 0, 0);
+    b.h = make_uint2(0, 0);
+    b.d = 0;
+    b.sc = 0;
+}
 
 __device__ __forceinline__ void load_blk(const Planes& W, int n, int blk, RawBlk<AF_Q4_0>& b) {
     b.q = *reinterpret_cast<const uint4*>(W.qs + (int64_t)n * W.qs_pitch() + (int64_t)blk * 16);
@@ -132,6 +175,66 @@ __device__ __forceinline__ void deq_blk(const RawBlk<AF_Q8_0>& b, uint4 (&hi)[4]
     for (int q = 0; q < 4; q++) {
         hi[q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
         lo[q] = make_uint4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+    }
+}
+
+// fp32 weights (w0, w1) -> fp16 hi pair and the fp16 rounding of the remainders (relative error ~2^-22)
+__device__ __forceinline__ void split_f32_pair(float w0, float w1, unsigned& hi, unsigned& lo) {
+    const __half2 h = __floats2half2_rn(w0, w1);
+    const float2 hf = __half22float2(h);
+    hi = h2u(h);
+    lo = h2u(__floats2half2_rn(w0 - hf.x, w1 - hf.y));
+}
+
+// exact float of a small unsigned integer v < 2^23
+__device__ __forceinline__ float u2f_small(unsigned v) { return __uint_as_float(0x4B000000u | v) - 8388608.f; }
+
+// Q4_K: w_e = (d s_j) n_e - dmin m_j, formed in fp32 (d s_j and dmin m_j are exact products), then split.
+// Chunk c holds elements 8c..8c+7: low nibbles of bytes 8c.. (c < 2), high nibbles of bytes 8(c-2).. (c >= 2).
+__device__ __forceinline__ void deq_blk(const RawBlk<AF_Q4_K>& b, uint4 (&hi)[4], uint4 (&lo)[4]) {
+    const float2 dm = __half22float2(u2h(b.dm));
+    const float A = dm.x * (float)(b.smj & 255u), B = dm.y * (float)(b.smj >> 8);
+    const unsigned w[4] = {b.q.x, b.q.y, b.q.z, b.q.w};
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        unsigned hv[4], lv[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {  // elements 8c + 2k, 8c + 2k + 1
+            const unsigned word = w[2 * (c & 1) + (k >> 1)] >> (c < 2 ? 0 : 4);
+            const int sh = 16 * (k & 1);
+            const float n0 = u2f_small((word >> sh) & 15u), n1 = u2f_small((word >> (sh + 8)) & 15u);
+            split_f32_pair(fmaf(A, n0, -B), fmaf(A, n1, -B), hv[k], lv[k]);
+        }
+        hi[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        lo[c] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+    }
+}
+
+// Q6_K: w_e = (d c_half) (q_e - 32), exact in fp32 (at most 24 significant bits), then split.
+__device__ __forceinline__ void deq_blk(const RawBlk<AF_Q6_K>& b, uint4 (&hi)[4], uint4 (&lo)[4]) {
+    const float d = __half2float(__ushort_as_half(b.d));
+    const float da = d * (float)(int)(signed char)(b.sc & 255u), db = d * (float)(int)(signed char)(b.sc >> 8);
+    const unsigned w[4] = {b.q.x, b.q.y, b.q.z, b.q.w};
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        // elements 8c..8c+7 lie in half c / 2; their index within the half is i = 8 (c & 1) + ..
+        const unsigned hw = c < 2 ? b.h.x : b.h.y;
+        const float dh = c < 2 ? da : db;
+        unsigned hv[4], lv[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            float v[2];
+#pragma unroll
+            for (int e2 = 0; e2 < 2; e2++) {
+                const int i = 8 * (c & 1) + 2 * k + e2;  // index within the half, 0..15
+                const unsigned nib = (w[i >> 2] >> (8 * (i & 3) + (c < 2 ? 0 : 4))) & 15u;
+                const unsigned h2 = (hw >> (8 * (i & 3) + 2 * (i >> 2))) & 3u;
+                v[e2] = dh * (u2f_small(nib | (h2 << 4)) - 32.f);
+            }
+            split_f32_pair(v[0], v[1], hv[k], lv[k]);
+        }
+        hi[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        lo[c] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
     }
 }
 
@@ -345,6 +448,10 @@ cudaError_t qgemm_prepare() {
     AF_QGEMM_ATTR(AF_Q4_0, 128)
     AF_QGEMM_ATTR(AF_Q8_0, 256)
     AF_QGEMM_ATTR(AF_Q8_0, 128)
+    AF_QGEMM_ATTR(AF_Q4_K, 256)
+    AF_QGEMM_ATTR(AF_Q4_K, 128)
+    AF_QGEMM_ATTR(AF_Q6_K, 256)
+    AF_QGEMM_ATTR(AF_Q6_K, 128)
 #undef AF_QGEMM_ATTR
     return e;
 }
@@ -359,19 +466,24 @@ cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo
     const int mt = (M + BM - 1) / BM;
     // 256-wide tiles unless that leaves a third or more of the SMs without a tile
     const bool narrow = (int64_t)((W.N + 255) / 256) * mt * 3 < (int64_t)num_sms() * 2;
-    if (narrow) {
-        dim3 grid((W.N + 127) / 128, mt);
-        if (W.wtype == AF_Q4_0)
-            qgemm_tc_kernel<AF_Q4_0, 128><<<grid, kThreads, TcCfg<128>::kSmemBytes, s>>>(mh, ml, W, M, epi, err);
-        else
-            qgemm_tc_kernel<AF_Q8_0, 128><<<grid, kThreads, TcCfg<128>::kSmemBytes, s>>>(mh, ml, W, M, epi, err);
-    } else {
-        dim3 grid((W.N + 255) / 256, mt);
-        if (W.wtype == AF_Q4_0)
-            qgemm_tc_kernel<AF_Q4_0, 256><<<grid, kThreads, TcCfg<256>::kSmemBytes, s>>>(mh, ml, W, M, epi, err);
-        else
-            qgemm_tc_kernel<AF_Q8_0, 256><<<grid, kThreads, TcCfg<256>::kSmemBytes, s>>>(mh, ml, W, M, epi, err);
+#define AF_QGEMM_LAUNCH(WT, BN)                                                                                   \
+    qgemm_tc_kernel<WT, BN><<<dim3((W.N + BN - 1) / BN, mt), kThreads, TcCfg<BN>::kSmemBytes, s>>>(mh, ml, W, M, epi, \
+                                                                                                 err)
+#define AF_QGEMM_TYPES(BN)                                          \
+    switch (W.wtype) {                                              \
+        case AF_Q4_0: AF_QGEMM_LAUNCH(AF_Q4_0, BN); break;          \
+        case AF_Q8_0: AF_QGEMM_LAUNCH(AF_Q8_0, BN); break;          \
+        case AF_Q4_K: AF_QGEMM_LAUNCH(AF_Q4_K, BN); break;          \
+        case AF_Q6_K: AF_QGEMM_LAUNCH(AF_Q6_K, BN); break;          \
+        default: return cudaErrorInvalidValue;                      \
     }
+    if (narrow) {
+        AF_QGEMM_TYPES(128)
+    } else {
+        AF_QGEMM_TYPES(256)
+    }
+#undef AF_QGEMM_TYPES
+#undef AF_QGEMM_LAUNCH
     return cudaGetLastError();
 }
 

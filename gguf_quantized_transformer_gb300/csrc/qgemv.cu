@@ -1,489 +1,17 @@
-// Decode GEMV: y = W x over repacked Q4_0 / Q8_0 planes, with an optional
-// RMSNorm prologue and a fused epilogue (Airframe "GPU_PIPELINE.md" per-layer
-// ops: dequantization happens inside the matmul, no separate dequantize pass;
-// decode is bound by reading the weights, "Decode loop").
-//
-// Streaming.  One CTA of 16 warps per SM owns a contiguous, even-aligned range
-// of rows.  Rows are contiguous in the quant and scale planes, so a stage of R
-// whole rows (scales included) is one bulk asynchronous copy (cp.async.bulk, mbarrier
-// completion, L2 evict-first) into a shared-memory ring; the warp that
-// finishes a stage last refills its slot.  The first stages are issued before
-// griddepcontrol.wait (weights do not depend on the previous kernel), so the
-// ring (up to 192 KB) fills while the prologue runs.
-//
-// Activations.  The prologue (all threads) reads x once: it reduces sum(x^2)
-// for the optional RMSNorm and converts w (.) x (the norm weight times x; the
-// scalar RMS factor is applied to each row's result), 32 elements at a time,
-// to 16-bit fixed point with a
-// power-of-two scale per block: x_j ~= s * xi_j, |xi_j| <= 32767 (relative
-// error <= 2^-16 of the block maximum).  The integers are stored in shared
-// memory as two byte planes (high byte signed, low byte unsigned; four
-// elements per word), and each lane copies the planes of the units it owns
-// into registers once.
-//
-// Compute.  The K axis of a row is NC chunks of 32 sixteen-byte units; all 16
-// warps work on every stage: warp (rs, wk) owns chunks wk, wk+WK, ... of the
-// row pairs rs, rs+RS, ... (RS x WK = 16), lane l unit l of each chunk.
-// Products with the weight codes are dp4a instructions:
-//   Q4_0: code n in 0..15; lo = w & 0x0F0F0F0F, hi = w & 0xF0F0F0F0 (= 16 n),
-//         sum_j n_j xi_j = (4096 A + 256 C + 16 B + D) / 16 over the byte planes,
-//         sum_j (n_j - 8) x_j = s * that - 8 s sum_j xi_j
-//   Q8_0: code q in -127..127, sum_j q_j x_j = s * (256 A + B)
-// accumulated exactly in int32 per unit; the unit value times the block's
-// fp16 scale d is accumulated in fp32 per row.  Row partials are reduced over
-// the lanes with a transpose-reduce; with WK > 1 the WK partials of a row are
-// summed in a fixed order (deterministic) by the last warp of the stage.
-//
-// Shared memory.  Stages of about 24 KB (the rows that make it), several in
-// flight; the x images live in the last ring slots, which are filled only
-// after every lane has copied its x units into registers.
-//
-// Every mbarrier wait is bounded; on a timeout the kernel records DEV_TIMEOUT
-// in its error word, drains its outstanding copies (bounded) and returns.
-#include "common.cuh"
-#include "gemv_common.cuh"
-#include "tma.cuh"
+// Decode GEMV entry points: the kernel is in qgemv_impl.cuh and each weight type's instantiations live in
+// their own translation unit (qgemv_<type>.cu), so they compile in parallel.
+#include "qgemv_impl.cuh"
 
 namespace af {
 
-namespace {
-
-constexpr int kWarps = 16;
-constexpr int kThreads = kWarps * 32;
-constexpr int kMaxCtaRows = 512;        // residual rows a CTA may own (preloaded to shared memory)
-constexpr int kMaxRing = 12;
-constexpr int kRingBudget = 192 * 1024;  // ring, x images inside (one CTA per SM)
-constexpr int kMinStage = 24 * 1024;     // stage size target: enough work per warp between waits
-constexpr int kMaxStage = 64 * 1024;     // largest stage that still leaves three in the ring
-constexpr int kXBlkBytes = 80;          // shared image of one 32-element x block
-constexpr int kMaxGemvSmem = 208 * 1024;
-
-// Shared-memory image of 32 x values in 16-bit fixed point: hi[g] / lo[g] hold
-// the high (signed) / low bytes of elements 4g..4g+3.
-struct __align__(16) XBlk {
-    unsigned hi[8];
-    unsigned lo[8];
-    float s;    // scale: x ~= s * xi
-    float sx8;  // -8 * s * sum_j xi_j (the Q4_0 code offset)
-    float pad[2];
-};
-static_assert(sizeof(XBlk) == kXBlkBytes, "x block image size");
-
-template <int WT>
-struct Unit;
-// One lane's x for one 16-byte Q4_0 unit (= one block of 32 weights).
-template <>
-struct Unit<AF_Q4_0> {
-    unsigned hi[8], lo[8];
-    float s16, sx8;
-    __device__ __forceinline__ void load(const XBlk* xb, int unit) {
-        const XBlk& b = xb[unit];
-        const uint4 h0 = *reinterpret_cast<const uint4*>(&b.hi[0]), h1 = *reinterpret_cast<const uint4*>(&b.hi[4]);
-        const uint4 l0 = *reinterpret_cast<const uint4*>(&b.lo[0]), l1 = *reinterpret_cast<const uint4*>(&b.lo[4]);
-        hi[0] = h0.x; hi[1] = h0.y; hi[2] = h0.z; hi[3] = h0.w; hi[4] = h1.x; hi[5] = h1.y; hi[6] = h1.z; hi[7] = h1.w;
-        lo[0] = l0.x; lo[1] = l0.y; lo[2] = l0.z; lo[3] = l0.w; lo[4] = l1.x; lo[5] = l1.y; lo[6] = l1.z; lo[7] = l1.w;
-        const float2 sv = *reinterpret_cast<const float2*>(&b.s);
-        s16 = sv.x * (1.f / 16.f);
-        sx8 = sv.y;
-    }
-    // sum_j (n_j - 8) x_j over the block; byte j of the unit holds n_j (low nibble) and n_{j+16} (high)
-    __device__ __forceinline__ float dot(const uint4 q) const {
-        const unsigned w[4] = {q.x, q.y, q.z, q.w};
-        int A = 0, B = 0, C = 0, D = 0;
-#pragma unroll
-        for (int t = 0; t < 4; t++) {
-            const unsigned l = w[t] & 0x0F0F0F0Fu, h = w[t] & 0xF0F0F0F0u;
-            A = dp4a_us(l, hi[t], A);
-            B = dp4a_uu(l, lo[t], B);
-            C = dp4a_us(h, hi[4 + t], C);
-            D = dp4a_uu(h, lo[4 + t], D);
-        }
-        // |16 A + C| < 2^20 and |16 B + D| < 2^21: the int32 sum is exact
-        const int v = ((A * 16 + C) << 8) + (B * 16 + D);
-        return fmaf(s16, (float)v, sx8);
-    }
-};
-// One lane's x for one 16-byte Q8_0 unit (= half a block: 16 weights).
-template <>
-struct Unit<AF_Q8_0> {
-    unsigned hi[4], lo[4];
-    float s;
-    __device__ __forceinline__ void load(const XBlk* xb, int unit) {
-        const XBlk& b = xb[unit >> 1];
-        const int g = (unit & 1) * 4;
-        const uint4 h = *reinterpret_cast<const uint4*>(&b.hi[g]);
-        const uint4 l = *reinterpret_cast<const uint4*>(&b.lo[g]);
-        hi[0] = h.x; hi[1] = h.y; hi[2] = h.z; hi[3] = h.w;
-        lo[0] = l.x; lo[1] = l.y; lo[2] = l.z; lo[3] = l.w;
-        s = b.s;
-    }
-    // sum_j q_j x_j over the half block
-    __device__ __forceinline__ float dot(const uint4 q) const {
-        const unsigned w[4] = {q.x, q.y, q.z, q.w};
-        int A = 0, B = 0;
-#pragma unroll
-        for (int t = 0; t < 4; t++) {
-            A = dp4a_ss(w[t], hi[t], A);
-            B = dp4a_su(w[t], lo[t], B);
-        }
-        return s * (float)(A * 256 + B);  // |256 A + B| < 2^25: exact in int32
-    }
-};
-
-template <int WT>
-__host__ __device__ constexpr int units_per_lane() { return WT == AF_Q4_0 ? 4 : 8; }
-
-// Convert x (optionally RMS-normalized) to the fixed-point block images.
-// Eight lanes per block, lane g of the group holds elements 4g..4g+3.
-// With NORM the images hold w (.) x (the RMS factor is a scalar, applied to each row's dot product in the
-// epilogue) and the return value is this thread's part of sum(x^2), from the same loads.
-template <bool NORM>
-__device__ __forceinline__ float quantize_x(const float* __restrict__ x, const float* __restrict__ nw, int K,
-                                            int nblk, XBlk* xb, int tid) {
-    float ss = 0.f;
-    constexpr int kBlkPerRound = kThreads / 8;
-    constexpr int kBatch = 4;  // rounds whose global loads are in flight together
-    const int g = tid & 7;
-    const int nround = (nblk + kBlkPerRound - 1) / kBlkPerRound;
-    for (int r0 = 0; r0 < nround; r0 += kBatch) {
-        float v[kBatch][4];
-#pragma unroll
-        for (int i = 0; i < kBatch; i++) {
-            const int b = (r0 + i) * kBlkPerRound + (tid >> 3);
-            const int k = b * 32 + g * 4;
-            v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
-            if (r0 + i < nround && b < nblk && k < K) {  // K % 32 == 0: the 4 elements are all in range
-                const float4 xv = *reinterpret_cast<const float4*>(x + k);
-                v[i][0] = xv.x; v[i][1] = xv.y; v[i][2] = xv.z; v[i][3] = xv.w;
-                if (NORM) {
-                    ss = fmaf(xv.x, xv.x, fmaf(xv.y, xv.y, fmaf(xv.z, xv.z, fmaf(xv.w, xv.w, ss))));
-                    const float4 w = *reinterpret_cast<const float4*>(nw + k);
-                    v[i][0] *= w.x; v[i][1] *= w.y; v[i][2] *= w.z; v[i][3] *= w.w;
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kBatch; i++) {
-            // uniform per warp: every lane takes part in the shuffles
-            if (r0 + i >= nround) break;
-            const int b = (r0 + i) * kBlkPerRound + (tid >> 3);
-            float m = fmaxf(fmaxf(fabsf(v[i][0]), fabsf(v[i][1])), fmaxf(fabsf(v[i][2]), fabsf(v[i][3])));
-#pragma unroll
-            for (int o = 4; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            // power-of-two scale: m = f 2^E with f in [0.5, 1) gives |x| / s <= 2^15 and s * xi exact
-            int E = 0;
-            frexpf(m, &E);
-            const float inv = m > 0.f ? ldexpf(1.f, 15 - E) : 0.f;
-            const float sc = m > 0.f ? ldexpf(1.f, E - 15) : 0.f;
-            int xi[4];
-            int sum = 0;
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                xi[e] = max(-32767, min(32767, __float2int_rn(v[i][e] * inv)));
-                sum += xi[e];
-            }
-#pragma unroll
-            for (int o = 4; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            // byte planes: lo = byte 0 of each element, hi = byte 1
-            const unsigned a01 = __byte_perm((unsigned)xi[0], (unsigned)xi[1], 0x5410);  // (x0.lo16, x1.lo16)
-            const unsigned a23 = __byte_perm((unsigned)xi[2], (unsigned)xi[3], 0x5410);
-            const unsigned lo = __byte_perm(a01, a23, 0x6420);  // bytes 0 of x0, x1, x2, x3
-            const unsigned hi = __byte_perm(a01, a23, 0x7531);  // bytes 1
-            if (b < nblk) {
-                xb[b].hi[g] = hi;
-                xb[b].lo[g] = lo;
-                if (g == 0) {
-                    xb[b].s = sc;
-                    xb[b].sx8 = -8.f * sc * (float)sum;
-                }
-            }
-        }
-    }
-    return ss;
-}
-
-template <int WT, bool NORM, int WK, int PPW>
-__global__ void __launch_bounds__(kThreads, 1)
-    qgemv_kernel(Planes W, const float* __restrict__ x, const float* __restrict__ nw, float eps, Epi epi, int ring,
-                 int xslot, unsigned* __restrict__ err) {
-    constexpr int UPL = units_per_lane<WT>();
-    constexpr int RS = kWarps / WK;  // row-pair streams
-    constexpr int RW = 2 * PPW;      // rows per warp per stage (PPW row pairs)
-    constexpr int R = RS * RW;       // rows per stage
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ uint64_t full[kMaxRing];
-    __shared__ unsigned done_cnt[kMaxRing];  // warps finished with the slot's current stage
-    __shared__ unsigned issues[kMaxRing];    // copies issued into the slot so far
-    __shared__ float red[kMaxRing][kWarps][RW];
-    __shared__ float ssum[kWarps];
-    __shared__ float xres[kMaxCtaRows];
-    __shared__ float2 rope_s[64];
-    __shared__ unsigned long long amax_s;
-    __shared__ volatile int abort_flag;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int rs = warp / WK, wk = warp % WK;
-    const int N = W.N, K = W.K;
-    const int UW = WT == AF_Q4_0 ? 32 : 16;  // weights per unit
-    const int NC = W.Kp / (32 * UW);
-    const int64_t pitch = W.qs_pitch();
-    const int scp = W.sc_pitch();
-    const int stage_bytes = (R * (int)pitch + 127) & ~127;
-    // x images at the end of the ring: slots xslot.. are filled after the prologue
-    const int xbytes = (W.Kp / 32) * kXBlkBytes;
-    XBlk* xb = reinterpret_cast<XBlk*>(smem + ((ring * stage_bytes - xbytes) & ~127));
-    const int np = N / 2;
-    const int pa = (int)((int64_t)np * blockIdx.x / gridDim.x), pb = (int)((int64_t)np * (blockIdx.x + 1) / gridDim.x);
-    const int r0 = 2 * pa, nrows = 2 * (pb - pa);
-    const int nst = (nrows + R - 1) / R;
-
-    pdl_launch_dependents();
-    if (tid == 0) {
-        for (int s = 0; s < ring; s++) {
-            mbar_init(&full[s], 1);
-            done_cnt[s] = 0;
-            issues[s] = 0;
-        }
-        abort_flag = 0;
-        amax_s = 0ull;
-        fence_mbar_init();
-    }
-    __syncthreads();
-    const uint64_t pol = policy_evict_first();
-    auto issue = [&](int st) {  // one thread: stage st (rows r0 + st*R ..) into its slot
-        const int slot = st % ring;
-        const int ra = r0 + st * R, nr = min(R, r0 + nrows - ra);
-        const unsigned bytes = (unsigned)(nr * pitch);  // rows ra.. with their scales: one range
-        uint8_t* dst = smem + slot * stage_bytes;
-        issues[slot]++;
-        mbar_arrive_expect_tx(&full[slot], bytes);
-        bulk_g2s_evict_first(dst, W.qs + (int64_t)ra * pitch, bytes, &full[slot], pol);
-    };
-    if (tid == 0)
-        for (int st = 0; st < min(nst, xslot); st++) issue(st);
-
-    pdl_wait();  // x (and the residual rows) are written by the previous kernel
-
-    // RMSNorm prologue: every CTA reduces sum(x^2) over the whole input while it converts w (.) x
-    float ss = quantize_x<NORM>(x, nw, K, W.Kp / 32, xb, tid);
-    if (NORM) {
-        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) ssum[warp] = ss;
-    }
-    // epilogue inputs into shared memory
-    if (epi.kind == EPI_RESID)
-        for (int i = tid; i < nrows; i += kThreads) xres[i] = epi.out[r0 + i];
-    GemvEpiCtx ectx;
-    ectx.xres = xres;
-    ectx.rope = rope_s;
-    ectx.amax = &amax_s;
-    ectx.r0 = r0;
-    ectx.pos = 0;
-    if (epi.kind == EPI_QKV) {
-        ectx.pos = epi.pos_dev ? *epi.pos_dev : epi.pos0;
-        for (int i = tid; i < epi.head_dim / 2; i += kThreads)
-            rope_s[i] = epi.rope[(int64_t)ectx.pos * (epi.head_dim / 2) + i];
-    }
-    __syncthreads();
-
-    float rstd = 1.f;  // applied to each row's dot product (the images hold w (.) x)
-    if (NORM) {
-        float t = 0.f;
-#pragma unroll
-        for (int i = 0; i < kWarps; i++) t += ssum[i];
-        rstd = rsqrtf(t / (float)K + eps);
-    }
-    // this lane's x units: chunk wk + WK*u, unit lane
-    Unit<WT> xr[UPL];
-#pragma unroll
-    for (int u = 0; u < UPL; u++) {
-        const int c = wk + WK * u;
-        if (c < NC) xr[u].load(xb, c * 32 + lane);
-    }
-    __syncthreads();  // the x images are dead: their slots take stages now
-    if (tid == 0) {
-        fence_proxy_async_shared();  // generic-proxy accesses of those bytes before the copies overwrite them
-        for (int st = xslot; st < min(nst, ring); st++) issue(st);
-    }
-
-    for (int st = 0; st < nst; st++) {
-        const int slot = st % ring;
-        const unsigned par = (unsigned)((st / ring) & 1);
-        bool ok = false;
-        for (unsigned it = 0; it < kWaitLimit && !ok; it++) {
-            ok = mbar_try_wait(&full[slot], par);
-            if (!ok && abort_flag) break;
-        }
-        if (!ok) {
-            if (lane == 0) {
-                abort_flag = 1;
-                atomicExch(err, (unsigned)DEV_TIMEOUT);
-            }
-            break;
-        }
-        const uint8_t* qsm = smem + slot * stage_bytes;
-        const unsigned short* ssm = reinterpret_cast<const unsigned short*>(qsm + W.sc_off());
-        const int ra = r0 + st * R, nr = min(R, r0 + nrows - ra);
-        float acc[RW];
-#pragma unroll
-        for (int t = 0; t < RW; t++) acc[t] = 0.f;
-#pragma unroll
-        for (int p = 0; p < PPW; p++) {
-            const int j0 = 2 * (rs + RS * p);  // rows j0, j0 + 1 of the stage
-            if (j0 < nr) {
-#pragma unroll
-                for (int u = 0; u < UPL; u++) {
-                    const int c = wk + WK * u;
-                    if (c < NC) {
-                        const int unit = c * 32 + lane;
-                        const int sidx = WT == AF_Q8_0 ? unit >> 1 : unit;
-#pragma unroll
-                        for (int h = 0; h < 2; h++) {
-                            const int j = j0 + h;
-                            const uint4 q = *reinterpret_cast<const uint4*>(qsm + j * pitch + unit * 16);
-                            const float d = __half2float(__ushort_as_half(ssm[j * scp + sidx]));
-                            acc[2 * p + h] = fmaf(d, xr[u].dot(q), acc[2 * p + h]);
-                        }
-                    }
-                }
-            }
-        }
-        // lanes (32/RW)*t .. hold the sum of acc[t]
-        const float r = transpose_reduce<RW>(acc, lane);
-        if (WK == 1) {
-            const float r1 = __shfl_down_sync(0xffffffffu, r, 32 / RW);
-            if (lane % (64 / RW) == 0) {
-                const int p = lane / (64 / RW), j0 = 2 * (rs + RS * p);
-                if (j0 < nr) gemv_epi(epi, ectx, ra + j0, r * rstd, r1 * rstd);
-            }
-        } else {
-            if ((lane & (32 / RW - 1)) == 0) red[slot][warp][lane / (32 / RW)] = r;
-        }
-        __syncwarp();
-        unsigned last = 0;
-        if (lane == 0) {
-            __threadfence_block();
-            last = atomicAdd(&done_cnt[slot], 1u) == (unsigned)kWarps - 1u;
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {  // every warp is done with this slot
-            __threadfence_block();
-            if (WK > 1 && lane < nr / 2) {  // row pair `lane` of the stage
-                const int prs = lane % RS, pp = lane / RS;
-                float y[2];
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    float a = 0.f;
-#pragma unroll
-                    for (int w = 0; w < WK; w++) a += red[slot][prs * WK + w][2 * pp + h];
-                    y[h] = a;
-                }
-                gemv_epi(epi, ectx, ra + 2 * lane, y[0] * rstd, y[1] * rstd);
-            }
-            __syncwarp();
-            if (lane == 0) {
-                done_cnt[slot] = 0;
-                if (st + ring < nst) {
-                    fence_proxy_async_shared();
-                    issue(st + ring);
-                }
-            }
-        }
-    }
-    __syncthreads();
-    if (abort_flag) {  // drain every copy still in flight before the CTA exits
-        if (tid == 0)
-            for (int s = 0; s < ring; s++)
-                if (issues[s]) mbar_wait_bounded(&full[s], (issues[s] - 1u) & 1u);
-        __syncthreads();
-        return;
-    }
-    if (epi.kind == EPI_LOGITS && tid == 0 && amax_s) atomicMax(epi.argmax, amax_s);
-}
-
-struct Shape {
-    int WK, PPW, ring, xslot, stage_bytes, smem;
-};
-
-Shape pick_shape(const Planes& W) {
-    const int UW = W.wtype == AF_Q8_0 ? 16 : 32;
-    const int UPL = W.wtype == AF_Q8_0 ? units_per_lane<AF_Q8_0>() : units_per_lane<AF_Q4_0>();
-    const int NC = W.Kp / (32 * UW);
-    const int row_bytes = (int)W.qs_pitch();
-    const int pairs = (kMinStage + 2 * row_bytes - 1) / (2 * row_bytes);  // row pairs for a >= kMinStage stage
-    const int xbytes = (W.Kp / 32) * kXBlkBytes;
-    int wk_min = 1;  // fewest warps per row that keep a lane's x units within UPL
-    while (wk_min < kWarps && NC > wk_min * UPL) wk_min *= 2;
-    int RS = 1;
-    while (RS < pairs && RS < kWarps / wk_min) RS *= 2;
-    if (2 * (kWarps / wk_min) * row_bytes <= kMaxStage) RS = kWarps / wk_min;  // more work per warp per stage
-    Shape s;
-    s.WK = kWarps / RS;
-    s.PPW = 1;
-    while (s.PPW < 4 && RS == kWarps && RS * s.PPW < pairs) s.PPW *= 2;
-    const int R = 2 * RS * s.PPW;
-    s.stage_bytes = (R * row_bytes + 127) & ~127;
-    s.ring = kRingBudget / s.stage_bytes;
-    s.ring = s.ring > kMaxRing ? kMaxRing : (s.ring < 2 ? 2 : s.ring);
-    // at least one slot before the x images (they may push the ring above the budget)
-    while (((s.ring * s.stage_bytes - xbytes) & ~127) < s.stage_bytes) s.ring++;
-    s.xslot = ((s.ring * s.stage_bytes - xbytes) & ~127) / s.stage_bytes;
-    s.smem = s.ring * s.stage_bytes;
-    return s;
-}
-
-template <int WT, bool NORM, int WK, int PPW>
-cudaError_t launch_t(const Planes& W, const float* x, const float* nw, float eps, const Epi& epi, const Shape& sh,
-                     unsigned* err, cudaStream_t s) {
-    auto kern = qgemv_kernel<WT, NORM, WK, PPW>;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_sms());
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = sh.smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, W, x, nw, eps, epi, sh.ring, sh.xslot, err);
-}
-
-// (WK, PPW) shapes pick_shape can return (row-pair streams RS = 16 / WK; PPW > 1 only with WK = 1)
-#define AF_GEMV_SHAPES(X) X(1, 1) X(1, 2) X(1, 4) X(2, 1) X(4, 1) X(8, 1) X(16, 1)
-
-template <int WT, bool NORM>
-cudaError_t dispatch(const Planes& W, const float* x, const float* nw, float eps, const Epi& epi, unsigned* err,
-                     cudaStream_t s) {
-    const Shape sh = pick_shape(W);
-    if (sh.smem > kMaxGemvSmem || sh.ring > kMaxRing) return cudaErrorInvalidValue;
-#define AF_GEMV_CASE(WW, PP) \
-    if (sh.WK == WW && sh.PPW == PP) return launch_t<WT, NORM, WW, PP>(W, x, nw, eps, epi, sh, err, s);
-    AF_GEMV_SHAPES(AF_GEMV_CASE)
-#undef AF_GEMV_CASE
-    return cudaErrorInvalidValue;
-}
-
-}  // namespace
-
 cudaError_t qgemv_prepare() {
-    // every instantiation may use up to kMaxGemvSmem of dynamic shared memory; done once, outside any
-    // stream capture
+    // done once, outside any stream capture
     static bool done = false;
     if (done) return cudaSuccess;
-    cudaError_t e = cudaSuccess;
-#define AF_GEMV_ATTR(WT, NORM, WW, PP)                                                                   \
-    if (!e)                                                                                               \
-        e = cudaFuncSetAttribute(qgemv_kernel<WT, NORM, WW, PP>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                 kMaxGemvSmem);
-#define AF_GEMV_ATTR4(WW, PP)                 \
-    AF_GEMV_ATTR(AF_Q4_0, true, WW, PP)       \
-    AF_GEMV_ATTR(AF_Q4_0, false, WW, PP)      \
-    AF_GEMV_ATTR(AF_Q8_0, true, WW, PP)       \
-    AF_GEMV_ATTR(AF_Q8_0, false, WW, PP)
-    AF_GEMV_SHAPES(AF_GEMV_ATTR4)
-#undef AF_GEMV_ATTR4
-#undef AF_GEMV_ATTR
+    cudaError_t e = qgemv_set_attrs<AF_Q4_0>();
+    if (!e) e = qgemv_set_attrs<AF_Q8_0>();
+    if (!e) e = qgemv_set_attrs<AF_Q4_K>();
+    if (!e) e = qgemv_set_attrs<AF_Q6_K>();
     if (!e) done = true;
     return e;
 }
@@ -492,11 +20,13 @@ int qgemv_max_chunks() { return 32; }
 
 cudaError_t launch_qgemv(const Planes& W, const float* x, const float* norm_w, float eps, const Epi& epi,
                          const GemvScratch& scr, cudaStream_t s) {
-    if (W.wtype == AF_Q4_0)
-        return norm_w ? dispatch<AF_Q4_0, true>(W, x, norm_w, eps, epi, scr.err, s)
-                      : dispatch<AF_Q4_0, false>(W, x, norm_w, eps, epi, scr.err, s);
-    return norm_w ? dispatch<AF_Q8_0, true>(W, x, norm_w, eps, epi, scr.err, s)
-                  : dispatch<AF_Q8_0, false>(W, x, norm_w, eps, epi, scr.err, s);
+    switch (W.wtype) {
+        case AF_Q4_0: return qgemv_dispatch<AF_Q4_0>(W, x, norm_w, eps, epi, scr.err, s);
+        case AF_Q8_0: return qgemv_dispatch<AF_Q8_0>(W, x, norm_w, eps, epi, scr.err, s);
+        case AF_Q4_K: return qgemv_dispatch<AF_Q4_K>(W, x, norm_w, eps, epi, scr.err, s);
+        case AF_Q6_K: return qgemv_dispatch<AF_Q6_K>(W, x, norm_w, eps, epi, scr.err, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace af

@@ -37,7 +37,21 @@
  *      Q8_0 (34 B): fp16 d, int8 q[32];             w_j = d * q_j
  *      Q4_0 (18 B): fp16 d, uint8 qs[16];            w_j = d * (n_j - 8),
  *                   n_j = qs[j] & 15 (j < 16), qs[j - 16] >> 4 (j >= 16)
- *    A matrix [N, K] is N rows of K/32 blocks each (K % 32 == 0).
+ *      Q4_K (144 B per 256 weights): fp16 d, fp16 dmin, uint8 scales[12],
+ *                   uint8 qs[128]; 6-bit scale s_j and min m_j of sub-block
+ *                   j = e / 32 (j < 4: scales[j] & 63, scales[j + 4] & 63;
+ *                   j >= 4: (scales[j + 4] & 15) | (scales[j - 4] >> 6) << 4,
+ *                   (scales[j + 4] >> 4) | (scales[j] >> 6) << 4); code n_e in
+ *                   the low (e % 64 < 32) or high nibble of qs[32 (e / 64) + e % 32];
+ *                   w_e = d s_j n_e - dmin m_j
+ *      Q6_K (210 B per 256 weights): uint8 ql[128], uint8 qh[64], int8
+ *                   scales[16], fp16 d; with h = e / 128, k = (e % 128) / 32,
+ *                   l = e % 32 the code q_e has its low 4 bits in the low (k < 2)
+ *                   or high nibble of ql[64 h + 32 (k & 1) + l] and its high 2 bits
+ *                   at bits 2k of qh[32 h + l]; w_e = d scales[e / 16] (q_e - 32)
+ *    (Shimmy v2.0 Architecture, "Quantization": the K-quant super-blocks; their
+ *    byte layout is GGUF's.)  A matrix [N, K] is N rows of K / 32 blocks each
+ *    (K / 256 super-blocks for Q4_K and Q6_K; K must be a whole number of blocks).
  */
 #ifndef AF_H
 #define AF_H
@@ -58,7 +72,7 @@ typedef enum af_status {
     AF_ENOTIMPL = 6  /* valid request this build does not implement */
 } af_status;
 
-typedef enum af_wtype { AF_Q4_0 = 2, AF_Q8_0 = 8 } af_wtype; /* own ids, not GGUF's */
+typedef enum af_wtype { AF_Q4_0 = 2, AF_Q8_0 = 8, AF_Q4_K = 12, AF_Q6_K = 14 } af_wtype; /* GGUF's type numbers */
 typedef enum af_dtype { AF_F32 = 0, AF_F16 = 1 } af_dtype;
 
 typedef struct af_config {
@@ -70,6 +84,8 @@ typedef struct af_config {
     int32_t max_chunk;  /* largest n accepted by af_prefill (0 = 512) */
     float rms_eps;      /* RMSNorm epsilon */
     float rope_base;    /* RoPE base */
+    int32_t out_wtype;  /* af_wtype of the LM head (output.weight); 0 = wtype (a Q4_K_M model: Q4_K layers and
+                           embedding with a Q6_K head) */
 } af_config;
 
 /*
@@ -84,7 +100,7 @@ typedef struct af_weights {
     const void* const* layer_blob; /* host array of n_layers device pointers */
     const void* token_embd;        /* device, [n_vocab, n_embd] blocks */
     const float* output_norm;      /* device, f32 [n_embd] */
-    const void* output;            /* device, [n_vocab, n_embd] blocks (LM head, not tied) */
+    const void* output;            /* device, [n_vocab, n_embd] blocks of out_wtype (LM head, not tied) */
 } af_weights;
 
 typedef struct af_model af_model;
@@ -184,17 +200,20 @@ void af_model_destroy(af_model* m);
 
 /*
  * Standalone quantized matmuls.
- * af_qweight_create repacks a [N, K] block matrix (N even, K % 32 == 0,
- * K <= 32768 for Q4_0 and <= 16384 for Q8_0, else AF_ENOTIMPL) into
- * its own device memory (and scratch for the GEMV); synchronises `stream`.
+ * af_qweight_create repacks a [N, K] block matrix (N even, K a whole number
+ * of blocks: K % 32 == 0, K % 256 == 0 for Q4_K / Q6_K; K <= 32768, or
+ * <= 16384 for Q8_0, else AF_ENOTIMPL) into its own device memory (and
+ * scratch for the GEMV); synchronises `stream`.
  *   af_qgemv: y[i]    = sum_j W[i][j] x[j]        x_dev fp32 [K], y_dev fp32 [N]
  *   af_qgemm: Y[m][i] = sum_j X[m][j] W[i][j]     X_dev fp32 [M, K] row-major,
  *                                                 Y_dev fp32 [M, N], M >= 1
  * Calls that share one af_qweight must be ordered on one stream (they share
- * its scratch).  af_qgemv accumulates exact integer products of the weights
- * with x held in 24-bit fixed point per 32-element block; af_qgemm runs on
- * the tensor cores with X and W each split into fp16 hi + lo parts (three
- * fp16 products accumulated in fp32, relative error ~1e-6 per product).
+ * its scratch).  af_qgemv accumulates exact integer products of the weight
+ * codes with x held in 16-bit fixed point per 32-element block (K-quant
+ * sub-block scales and mins applied per 32 or 16 elements in fp32); af_qgemm
+ * runs on the tensor cores with X and W each split into fp16 hi + lo parts
+ * (three fp16 products accumulated in fp32, relative error ~1e-6 per product;
+ * K-quant weights are formed in fp32 before their split).
  * af_qgemm keeps the split X in buffers of the af_qweight: the first call
  * with a larger M than before synchronises `stream` and grows them.
  */

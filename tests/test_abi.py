@@ -50,6 +50,33 @@ def test_layer_offsets_and_kv_bytes_match_oracle(idx):
     assert af.af_kv_bytes(c) == oracle.kv_bytes(cfg)
 
 
+@pytest.mark.parametrize("idx", range(2))
+def test_kquant_layer_offsets_match_oracle(idx):
+    af = _af()
+    cfg = synth.KQUANT_CONFIGS[idx]
+    c = af.make_config(cfg)
+    assert c.out_wtype == af.AF_Q6_K
+    assert af.af_layer_offsets(c) == oracle.layer_offsets(cfg) == synth.layer_offsets(cfg)
+
+
+def test_kquant_config_validation_without_gpu():
+    af = _af()
+    L = af.lib()
+    out = ctypes.c_void_p()
+    c = af.make_config(synth.KQUANT_CONFIGS[0])
+    c.n_ff = 1408  # not a whole number of 256-weight super-blocks
+    assert L.af_model_create(ctypes.byref(c), None, None, ctypes.byref(out)) == af.AF_EINVAL
+    c = af.make_config(synth.KQUANT_CONFIGS[0])
+    c.out_wtype = 7
+    assert L.af_model_create(ctypes.byref(c), None, None, ctypes.byref(out)) == af.AF_EINVAL
+    assert "out_wtype" in af.af_last_error()
+    c = af.make_config(synth.CONFIGS[0])  # a Q8_0 body with a Q6_K head: n_embd 512 is whole super-blocks
+    c.out_wtype = af.AF_Q6_K
+    c.n_embd = 500
+    assert L.af_model_create(ctypes.byref(c), None, None, ctypes.byref(out)) == af.AF_EINVAL
+    assert out.value is None
+
+
 def test_tinyllama_kv_bytes_worked_example():
     af = _af()
     assert af.af_kv_bytes(af.make_config(synth.CONFIGS[1])) == 92274688

@@ -95,6 +95,18 @@ def test_large_configs_short_prompt(af, idx, chunks, n_decode):
     run_parity(af, cfg, synth.seed_of(idx), chunks, n_decode, sum(chunks) + n_decode)
 
 
+@pytest.mark.parametrize("chunks,n_decode", [([32], 16), ([13, 16, 3], 4)])
+def test_q4_k_m_tiny(af, chunks, n_decode):
+    """Q4_K layers and embedding with a Q6_K LM head (the Q4_K_M mix)."""
+    cfg = synth.KQUANT_CONFIGS[0]
+    run_parity(af, cfg, synth.kquant_seed_of(0), chunks, n_decode, 0)
+
+
+def test_q4_k_m_8b_shape_short_prompt(af):
+    cfg = synth.KQUANT_CONFIGS[1]
+    run_parity(af, cfg, synth.kquant_seed_of(1), [12, 5], 2, 12 + 5 + 2)
+
+
 @pytest.fixture(scope="module")
 def tiny(af):
     cfg = synth.CONFIGS[0]
