@@ -48,11 +48,12 @@ def peaks():
 
 def decode_bytes_per_token(cfg, pos):
     """Algorithmic HBM bytes of one decode step at position pos."""
-    bpe = 34 / 32 if cfg.wtype == "q8_0" else 18 / 32
+    bpe = synth.BLOCK_BYTES[cfg.wtype] / synth.BLOCK_ELEMS[cfg.wtype]  # GGUF bytes per weight
+    hbpe = synth.BLOCK_BYTES[cfg.head_wtype] / synth.BLOCK_ELEMS[cfg.head_wtype]
     E, QD, KVD, F, V, L = (cfg.n_embd, cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim, cfg.n_ff,
                            cfg.n_vocab, cfg.n_layers)
     layer_w = (E * (QD + 2 * KVD) + QD * E + 2 * F * E + F * E) * bpe + 2 * E * 4
-    head = V * E * bpe + E * 4 + E * bpe  # LM head + final norm + one embedding row
+    head = V * E * hbpe + E * 4 + E * bpe  # LM head + final norm + one embedding row
     kvb = 2 if cfg.kv_dtype == "f16" else 4
     kv = 2 * L * KVD * (pos + 1) * kvb
     return L * layer_w + head + kv
@@ -291,6 +292,12 @@ def run_ours(args, cfg, world, rank, local):
 
     # end to end through the host API: host token ids in, greedy token ids out, one sync per decode step
     e2e = e2e_run(af, m, prompt, cfg, args)
+    m.close()
+    del m
+    torch.cuda.empty_cache()
+
+    # the same workload on the 8B shape in the Q4_K_M mix (Q4_K layers, Q6_K LM head): a secondary line
+    kq = None if args.no_kquant else kquant_run(af, args, dev, hbm_peak)
 
     launches_per_step = (P + C - 1) // C * (1 + 7 * cfg.n_layers) + 3 + ND * (3 + 5 * cfg.n_layers + 1)
 
@@ -303,6 +310,7 @@ def run_ours(args, cfg, world, rank, local):
         "decode_hbm_gbs": dec_gbs, "decode_hbm_frac": dec_gbs / hbm_peak,
         "prefill_tflops": pf_tflops,
         "sampler_us": samp_us,
+        "q4_k_m": kq,
         "roofline": dict(qg, peak_source=peak_src),
         "decode_step_roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
                                  "frac": dec_gbs / hbm_peak, "traffic": None,
@@ -322,7 +330,48 @@ def run_ours(args, cfg, world, rank, local):
                                           f"({dt:.1f} s, fp64, {threads} threads)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def kquant_run(af, args, dev, hbm_peak, steps=2, warmup=1):
+    """Prefill + greedy decode of the 8B shape with Q4_K layers and a Q6_K head, timed like the main line."""
+    import torch
+    cfg = synth.KQUANT_CONFIGS[1]
+    hm = synth.HostModel(cfg, synth.kquant_seed_of(1))
+    m = af.Model(cfg, [torch.from_numpy(b).to(dev) for b in hm.layers], torch.from_numpy(hm.token_embd).to(dev),
+                 torch.from_numpy(hm.output_norm).to(dev), torch.from_numpy(hm.output).to(dev),
+                 max_chunk=args.chunk)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    stream = torch.cuda.ExternalStream(af.af_model_stream(m.h))
+    P, ND, C = args.prompt, args.decode, args.chunk
+    prompt_dev = torch.from_numpy(hm.prompt(P)).to(dev)
+    logits = torch.empty(cfg.n_vocab, dtype=torch.float32, device=dev)
+
+    def one_step(ev):
+        ev[0].record(stream)
+        for p in range(0, P, C):
+            n = min(C, P - p)
+            af.af_prefill_dev(m.h, prompt_dev[p:p + n], n, p, logits if p + n >= P else None)
+        ev[1].record(stream)
+        for i in range(ND):
+            af.af_decode_step(m.h, -1, P + i, logits)
+        ev[2].record(stream)
+
+    for _ in range(warmup):
+        one_step([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for k in range(steps):
+        one_step(evs[k])
+    torch.cuda.synchronize()
+    pre_s = sum(e[0].elapsed_time(e[1]) for e in evs) / 1000
+    dec_s = sum(e[1].elapsed_time(e[2]) for e in evs) / 1000
     m.close()
+    dec_gbs = sum(decode_bytes_per_token(cfg, P + i) for i in range(ND)) * steps / dec_s / 1e9
+    return {"workload": f"{cfg.name}: {P}-token prompt in {C}-token chunks + {ND} greedy decode steps, "
+                        f"KV {cfg.kv_dtype} max_ctx {cfg.max_ctx}", "weights": f"{cfg.wtype} + {cfg.head_wtype} head",
+            "steps": steps, "warmup": warmup, "decode_tok_s": ND * steps / dec_s, "prefill_tok_s": P * steps / pre_s,
+            "decode_hbm_gbs": dec_gbs, "decode_hbm_frac": dec_gbs / hbm_peak,
+            "prefill_tflops": prefill_flops(cfg, P, C)[0] * steps / pre_s / 1e12}
 
 
 def qgemv_roofline(af, cfg, dev, hbm_peak, reps=50):
@@ -432,6 +481,7 @@ def main():
     ap.add_argument("--chunk", type=int, default=512)
     ap.add_argument("--ref-decode", type=int, default=2, help="oracle decode steps per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kquant", action="store_true", help="skip the secondary Q4_K_M line")
     args = ap.parse_args()
     cfg = synth.CONFIGS[args.config]
     args.prompt = args.prompt or cfg.prompt_len
