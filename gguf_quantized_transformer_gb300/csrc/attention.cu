@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kDecThreads, G <= 4 ? 2 : 1)  // two CTAs per 
     extern __shared__ __align__(128) uint8_t dsm[];
     float* sc = reinterpret_cast<float*>(dsm + S * TB);  // [split length][G] scores, then probabilities
     __shared__ float red[kDecWarps][G];
-    __shared__ float m_s[G], l_s[G], inv_den[G];
+    __shared__ float m_s[G], l_s[G];
     __shared__ unsigned last;
     __shared__ uint64_t full[8];    // tile landed in slot (transaction bytes)
     __shared__ unsigned issues[8];  // copies issued into the slot so far
@@ -331,61 +331,82 @@ __global__ void __launch_bounds__(kDecThreads, G <= 4 ? 2 : 1)  // two CTAs per 
     __syncthreads();
     if (!last) return;
     __threadfence();
-    // merge the ns_eff partials of this kv head: weights exp(m_s - M) / sum_s exp(m_s - M) l_s.
-    // Every load below is independent of the others, so the partials arrive in about one L2 round trip.
+    // Merge the ns_eff partials of this kv head: o_h = sum_s exp(m_s - M) o_s / sum_s exp(m_s - M) l_s.
+    // Each thread owns float4 f of the group's G x D outputs and the splits ph, ph + P, ..; it issues a
+    // batch of those partial-row loads into registers first, while warp h forms head h's weights with its
+    // lanes over the splits, so the partials and the weights arrive in about one L2 round trip.
+    constexpr int NF = G * D / 4;                // float4 outputs of the group
+    constexpr int P = kDecThreads / NF;          // threads per output float4
+    constexpr int kBatch = 16;                   // partial loads in flight per thread
+    static_assert(P >= 1 && P * NF == kDecThreads, "merge mapping");
     const float* pg = part + ((int64_t)g * ns * G) * PST;
     float* wm = sc;                // [ns_eff][G] split maxima, then merge weights
     float* wl = sc + ns_eff * G;   // [ns_eff][G] split sums
-    for (int t = tid; t < ns_eff * G; t += kDecThreads) {
-        const float2 ml = __ldcg(reinterpret_cast<const float2*>(pg + (int64_t)t * PST + D));
-        wm[t] = ml.x;
-        wl[t] = ml.y;
-    }
-    __syncthreads();
-    if (tid < G) {
+    const int f = tid % NF, ph = tid / NF, hf = (4 * f) / D, df = (4 * f) % D;
+    float4 v[kBatch];
+    auto load_batch = [&](int s0) {
+#pragma unroll
+        for (int i = 0; i < kBatch; i++) {
+            const int ss = s0 + i * P;
+            v[i] = ss < ns_eff ? __ldcg(reinterpret_cast<const float4*>(pg + ((int64_t)ss * G + hf) * PST + df))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    load_batch(ph);
+    if (warp < G) {
+        const int h = warp;
         float M = -CUDART_INF_F;
-        for (int ss = 0; ss < ns_eff; ss++) M = fmaxf(M, wm[ss * G + tid]);
+        for (int ss = lane; ss < ns_eff; ss += 32) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(pg + ((int64_t)ss * G + h) * PST + D));
+            wm[ss * G + h] = ml.x;
+            wl[ss * G + h] = ml.y;
+            M = fmaxf(M, ml.x);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float den = 0.f;
-        for (int ss = 0; ss < ns_eff; ss++) den = fmaf(__expf(wm[ss * G + tid] - M), wl[ss * G + tid], den);
-        m_s[tid] = M;
-        inv_den[tid] = 1.f / den;
+        for (int ss = lane; ss < ns_eff; ss += 32) den = fmaf(__expf(wm[ss * G + h] - M), wl[ss * G + h], den);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        const float inv = 1.f / den;
+        for (int ss = lane; ss < ns_eff; ss += 32) wm[ss * G + h] = __expf(wm[ss * G + h] - M) * inv;
     }
     __syncthreads();
-    for (int t = tid; t < ns_eff * G; t += kDecThreads) {
-        const int h = t % G;
-        wm[t] = __expf(wm[t] - m_s[h]) * inv_den[h];
-    }
-    // the partial rows, a chunk of splits at a time, into the (free) tile ring
-    constexpr int kOut = (G * D + kDecThreads - 1) / kDecThreads;  // outputs per thread
-    constexpr int SC = S * TB / (G * PST * 4);                      // splits per chunk
-    static_assert(SC >= 1, "ring too small for one split's partials");
-    float* buf = reinterpret_cast<float*>(dsm);
-    float accm[kOut];
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = ph; s0 < ns_eff; s0 += kBatch * P) {
+        if (s0 != ph) load_batch(s0);
 #pragma unroll
-    for (int i = 0; i < kOut; i++) accm[i] = 0.f;
-    for (int c0 = 0; c0 < ns_eff; c0 += SC) {
-        const int nsc = min(SC, ns_eff - c0);
-        const int n4 = nsc * G * PST / 4;
-        const float4* src = reinterpret_cast<const float4*>(pg + (int64_t)c0 * G * PST);
-        __syncthreads();  // weights written / previous chunk consumed
-#pragma unroll 4
-        for (int i = tid; i < n4; i += kDecThreads) reinterpret_cast<float4*>(buf)[i] = __ldcg(src + i);
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < kOut; i++) {
-            const int o = tid + i * kDecThreads;
-            if (o < G * D) {
-                const int h = o / D, d = o % D;
-                float a = accm[i];
-                for (int ss = 0; ss < nsc; ss++) a = fmaf(wm[(c0 + ss) * G + h], buf[(ss * G + h) * PST + d], a);
-                accm[i] = a;
+        for (int i = 0; i < kBatch; i++) {
+            const int ss = s0 + i * P;
+            if (ss < ns_eff) {
+                const float w = wm[ss * G + hf];
+                a.x = fmaf(w, v[i].x, a.x);
+                a.y = fmaf(w, v[i].y, a.y);
+                a.z = fmaf(w, v[i].z, a.z);
+                a.w = fmaf(w, v[i].w, a.w);
             }
         }
     }
-#pragma unroll
-    for (int i = 0; i < kOut; i++) {
-        const int o = tid + i * kDecThreads;
-        if (o < G * D) out[(int64_t)(g * G + o / D) * D + o % D] = accm[i];
+    // the P phases of an output, summed in a fixed order (the ring is free)
+    float4* red4 = reinterpret_cast<float4*>(dsm);
+    if (P > 1) {
+        red4[ph * NF + f] = a;
+        __syncthreads();
+        if (ph == 0)
+            for (int pp = 1; pp < P; pp++) {
+                const float4 b = red4[pp * NF + f];
+                a.x += b.x;
+                a.y += b.y;
+                a.z += b.z;
+                a.w += b.w;
+            }
+    }
+    if (ph == 0) {
+        float* o = out + (int64_t)(g * G + hf) * D + df;
+        o[0] = a.x;
+        o[1] = a.y;
+        o[2] = a.z;
+        o[3] = a.w;
     }
     if (tid == 0) cnt[g] = 0u;
 }
