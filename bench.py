@@ -33,7 +33,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up GEMV launch, Q4_0 28672 x 4096, from the
 # ncu capture summarised in profiles/qgemv_q4_0_28672x4096.md; valid only for the kernel sources it was taken on.
 GEMV_SOURCES = ["qgemv_impl.cuh", "qgemv_q4_0.cu", "gemv_common.cuh", "tma.cuh", "common.cuh"]
-GEMV_TRAFFIC = {"sources_sha256_16": "a99ba43fd54077f8", "wtype": "q4_0", "N": 28672, "K": 4096, "bytes": 66124800}
+GEMV_TRAFFIC = {"sources_sha256_16": "12e1327c6e7a187a", "wtype": "q4_0", "N": 28672, "K": 4096, "bytes": 66143232}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -374,37 +374,64 @@ def kquant_run(af, args, dev, hbm_peak, steps=2, warmup=1):
             "prefill_tflops": prefill_flops(cfg, P, C)[0] * steps / pre_s / 1e12}
 
 
-def qgemv_roofline(af, cfg, dev, hbm_peak, reps=50):
-    """Standalone af_qgemv on the model's gate|up shape [2F, E]: algorithmic bytes / event time."""
+def qgemv_roofline(af, cfg, dev, hbm_peak, reps=20, copies=8):
+    """af_qgemv on the model's gate|up shape [2F, E]: algorithmic bytes / CUDA-event time per launch.
+
+    As in the decode step: a CUDA graph of `copies` back-to-back launches (programmatic dependent launch), each
+    over its own copy of the weights (copies x 66 MB, far larger than L2, so no launch finds its weights in L2),
+    replayed `reps` times on the launching stream.  A single launch after an L2 flush is reported beside it
+    (cold: it also pays the launch and ramp that back-to-back launches overlap)."""
     import torch
     N, K = 2 * cfg.n_ff, cfg.n_embd
     W = synth.matrix(cfg.wtype, 7, synth.TID_TEST_BASE + 99, N, K)
     Wd = torch.from_numpy(W).to(dev)
-    h = af.af_qweight_create(af.WTYPE[cfg.wtype], Wd, N, K)
+    hs = [af.af_qweight_create(af.WTYPE[cfg.wtype], Wd, N, K) for _ in range(copies)]
     del Wd
     x = torch.randn(K, device=dev)
     y = torch.empty(N, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
-    s = torch.cuda.current_stream()
-    times = []
+    s = torch.cuda.Stream()
+    for h in hs:
+        af.af_qgemv(h, x, y)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s), torch.cuda.graph(g, stream=s):
+        for h in hs:
+            af.af_qgemv(h, x, y)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):  # replays run on the current stream
+        a.record(s)
+        for _ in range(reps):
+            g.replay()
+        b.record(s)
+    b.synchronize()
+    ms = a.elapsed_time(b) / (reps * copies)
+    # cold: one launch after writing a buffer larger than L2
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cur = torch.cuda.current_stream()
+    cold = []
     for i in range(reps + 3):
         flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s)
-        af.af_qgemv(h, x, y)
-        b.record(s)
-        b.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        af.af_qgemv(hs[0], x, y)
+        e1.record(cur)
+        e1.synchronize()
         if i >= 3:
-            times.append(a.elapsed_time(b))
-    af.af_qweight_destroy(h)
-    bpe = 34 / 32 if cfg.wtype == "q8_0" else 18 / 32
+            cold.append(e0.elapsed_time(e1))
+    for h in hs:
+        af.af_qweight_destroy(h)
+    bpe = synth.BLOCK_BYTES[cfg.wtype] / synth.BLOCK_ELEMS[cfg.wtype]
     nbytes = N * K * bpe + K * 4 + N * 4
-    ms = float(np.mean(times))
     gbs = nbytes / (ms / 1000) / 1e9
+    cold_ms = float(np.mean(cold))
     return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
             "traffic": gemv_traffic(cfg.wtype, N, K),
-            "kernel": f"qgemv {cfg.wtype} [{N}x{K}] gate|up (L2 flushed between launches)",
-            "bytes_per_launch": nbytes, "us_per_launch": ms * 1000}
+            "kernel": f"qgemv {cfg.wtype} [{N}x{K}] gate|up: graph of {copies} back-to-back launches over "
+                      f"{copies} weight copies ({copies * N * K * bpe / 1e6:.0f} MB > L2)",
+            "bytes_per_launch": nbytes, "us_per_launch": ms * 1000,
+            "cold_us_per_launch": cold_ms * 1000, "cold_frac": nbytes / (cold_ms / 1000) / 1e9 / hbm_peak}
 
 
 def sampler_time(af, cfg, dev, reps=20):
