@@ -292,6 +292,9 @@ def run_ours(args, cfg, world, rank, local):
 
     # end to end through the host API: host token ids in, greedy token ids out, one sync per decode step
     e2e = e2e_run(af, m, prompt, cfg, args)
+
+    # decode with the sampler chain between steps, all on the device (no logits read back)
+    sampled_tps = sampled_decode(af, m, prompt_dev, cfg, args, stream)
     m.close()
     del m
     torch.cuda.empty_cache()
@@ -310,6 +313,7 @@ def run_ours(args, cfg, world, rank, local):
         "decode_hbm_gbs": dec_gbs, "decode_hbm_frac": dec_gbs / hbm_peak,
         "prefill_tflops": pf_tflops,
         "sampler_us": samp_us,
+        "decode_sampled_tok_s": sampled_tps,
         "q4_k_m": kq,
         "roofline": dict(qg, peak_source=peak_src),
         "decode_step_roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
@@ -330,6 +334,31 @@ def run_ours(args, cfg, world, rank, local):
                                           f"({dt:.1f} s, fp64, {threads} threads)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def sampled_decode(af, m, prompt_dev, cfg, args, stream):
+    """The workload's decode phase with af_model_sample (penalty 1.1 on the prompt's last 64 ids, temperature 0.8,
+    top-p 0.95, seeded uniforms) between the steps; each step reads the drawn token from the device."""
+    import torch
+    P, ND, C = args.prompt, args.decode, args.chunk
+    if P + 1 + ND > cfg.max_ctx or P < 64:
+        return None
+    recent = prompt_dev[-64:].contiguous()
+    us = np.random.default_rng(1).random(ND).astype(np.float32) * 0.999
+    for p in range(0, P, C):
+        n = min(C, P - p)
+        af.af_prefill_dev(m.h, prompt_dev[p:p + n], n, p, None)
+    af.af_model_sample(m.h, None, recent, 64, 1.1, 0.8, 0.95, float(us[0]))
+    af.af_decode_step(m.h, -1, P, None)  # untimed: the step's graph for the model's own logits buffer is built here
+    af.af_model_sample(m.h, None, recent, 64, 1.1, 0.8, 0.95, float(us[0]))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(ND):
+        af.af_decode_step(m.h, -1, P + 1 + i, None)
+        af.af_model_sample(m.h, None, recent, 64, 1.1, 0.8, 0.95, float(us[i]))
+    b.record(stream)
+    b.synchronize()
+    return ND / (a.elapsed_time(b) / 1000)
 
 
 def kquant_run(af, args, dev, hbm_peak, steps=2, warmup=1):

@@ -80,6 +80,7 @@ def lib():
         L.af_attention_decode_static.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
         f32 = ctypes.c_float
         L.af_sample.argtypes = [vp, i32, vp, i32, f32, f32, f32, f32, vp, vp]
+        L.af_model_sample.argtypes = [vp, vp, vp, i32, f32, f32, f32, f32, vp]
         _lib = L
     return _lib
 
@@ -233,6 +234,15 @@ def af_sample(logits_dev, n_vocab: int, recent_dev, n_recent: int, repeat_penalt
               top_p: float, u: float, token_dev, stream=None):
     return check(lib().af_sample(_ptr(logits_dev), n_vocab, _ptr(recent_dev), n_recent, repeat_penalty, temperature,
                                  top_p, u, _ptr(token_dev), _stream(stream)))
+
+
+def af_model_sample(m, logits_dev, recent_dev, n_recent: int, repeat_penalty: float, temperature: float,
+                    top_p: float, u: float, want_token: bool = False):
+    """Sampler chain over the model's logits into its next-token word; returns the token if want_token."""
+    out = ctypes.c_int32(-1)
+    check(lib().af_model_sample(m, _ptr(logits_dev), _ptr(recent_dev), n_recent, repeat_penalty, temperature, top_p,
+                                u, ctypes.byref(out) if want_token else None))
+    return out.value if want_token else None
 
 
 def af_last_error() -> str:

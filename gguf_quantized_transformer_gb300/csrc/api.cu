@@ -809,17 +809,44 @@ int af_attention_decode_static(const float* q_dev, const void* k_dev, const void
 
 // ---------------------------------------------------------------- sampler chain
 
-int af_sample(const float* logits_dev, int32_t n_vocab, const int32_t* recent_dev, int32_t n_recent,
-              float repeat_penalty, float temperature, float top_p, float u, int32_t* token_dev, void* stream) {
-    if (!logits_dev || !token_dev) return fail(AF_EINVAL, "null argument");
+}  // extern "C"
+
+namespace {
+int check_sample_args(int32_t n_vocab, const int32_t* recent_dev, int32_t n_recent, float repeat_penalty,
+                      float temperature, float top_p, float u) {
     if (n_recent < 0 || (n_recent > 0 && !recent_dev)) return fail(AF_EINVAL, "bad recent-token list");
     if (n_vocab < 1 || n_vocab > sampler_max_vocab())
         return fail(AF_ERANGE, "n_vocab %d outside [1, %d]", n_vocab, sampler_max_vocab());
     if (!(repeat_penalty > 0.f) || !(temperature >= 0.f) || !(top_p == top_p))
         return fail(AF_EINVAL, "repeat_penalty must be > 0, temperature >= 0, top_p a number");
     if (!(u >= 0.f && u < 1.f)) return fail(AF_ERANGE, "u must be in [0, 1)");
+    return AF_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int af_sample(const float* logits_dev, int32_t n_vocab, const int32_t* recent_dev, int32_t n_recent,
+              float repeat_penalty, float temperature, float top_p, float u, int32_t* token_dev, void* stream) {
+    if (!logits_dev || !token_dev) return fail(AF_EINVAL, "null argument");
+    if (int rc = check_sample_args(n_vocab, recent_dev, n_recent, repeat_penalty, temperature, top_p, u)) return rc;
     CK(launch_sample(logits_dev, n_vocab, recent_dev, n_recent, repeat_penalty, temperature, top_p, u, token_dev,
                      (cudaStream_t)stream));
+    return AF_OK;
+}
+
+int af_model_sample(af_model* m, const float* logits_dev, const int32_t* recent_dev, int32_t n_recent,
+                    float repeat_penalty, float temperature, float top_p, float u, int32_t* token_host) {
+    if (!m) return fail(AF_EINVAL, "null model");
+    if (int rc = check_sample_args(m->c.n_vocab, recent_dev, n_recent, repeat_penalty, temperature, top_p, u))
+        return rc;
+    const float* logits = logits_dev ? logits_dev : m->logits;
+    CK(launch_sample(logits, m->c.n_vocab, recent_dev, n_recent, repeat_penalty, temperature, top_p, u,
+                     &m->st->next_token, m->s));
+    if (token_host) {
+        CK(cudaMemcpyAsync(token_host, &m->st->next_token, 4, cudaMemcpyDeviceToHost, m->s));
+        CK(cudaStreamSynchronize(m->s));
+    }
     return AF_OK;
 }
 

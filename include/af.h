@@ -282,6 +282,22 @@ int af_attention_decode_static(const float* q_dev, const void* k_dev, const void
 int af_sample(const float* logits_dev, int32_t n_vocab, const int32_t* recent_dev, int32_t n_recent,
               float repeat_penalty, float temperature, float top_p, float u, int32_t* token_dev, void* stream);
 
+/*
+ * The sampler chain (as af_sample) over a model's logits, on the model's stream:
+ * the token drawn replaces the model's next-token word (af_model_next_token_dev),
+ * so a following af_decode_step(m, -1, ...) feeds it.  A decode loop that
+ * alternates af_decode_step(m, -1, pos, NULL, NULL) and af_model_sample(...)
+ * samples on the device with no logits read back.
+ *   logits_dev  the logits to sample (n_vocab fp32); NULL = the model's own
+ *               buffer, which steps called with logits_dev = NULL write
+ *   recent_dev, n_recent, repeat_penalty, temperature, top_p, u: as af_sample
+ *   token_host  if not NULL: synchronises the model's stream once and stores
+ *               the token drawn; otherwise the call only enqueues
+ * AF_EINVAL / AF_ERANGE for bad arguments (checked on the host).
+ */
+int af_model_sample(af_model* m, const float* logits_dev, const int32_t* recent_dev, int32_t n_recent,
+                    float repeat_penalty, float temperature, float top_p, float u, int32_t* token_host);
+
 /* Thread-local message for the last failed call on this thread ("" if none). */
 const char* af_last_error(void);
 

@@ -102,3 +102,32 @@ def test_vocab_sizes_and_ragged_slices(af, V):
         want = max(0, int(np.ceil(float(np.float32(u)) * V)) - 1)
         got = _run(af, np.zeros(V), [], 1.0, 1.0, 1.0, u)
         assert abs(got - want) <= max(1, V // 100000), (V, u, got, want)
+
+
+def test_on_device_sampled_decode_loop(af):
+    """Prefill, then decode steps fed by af_model_sample: the drawn token goes into the model's next-token word
+    and af_decode_step(-1) consumes it from the device.  Each token is a valid draw from that step's logits,
+    and every step's logits match the oracle fed the same tokens."""
+    from helpers import LAYER_TOL, gpu_model, rms_rel_err
+    cfg = synth.CONFIGS[0]
+    hm = synth.HostModel(cfg, synth.seed_of(0))
+    gm = gpu_model(hm)
+    om = oracle.Model.from_host(hm)
+    prompt = hm.prompt()
+    logits = torch.empty(cfg.n_vocab, dtype=torch.float32, device="cuda")
+    gm.prefill(prompt, 0, logits)
+    ref, _ = om.forward(prompt, 0)
+    p = len(prompt)
+    rec = prompt[-8:].astype(np.int32)
+    recent = torch.from_numpy(rec).cuda()
+    for u in (0.1, 0.5, 0.9, 0.33, 0.77, 0.05):
+        tok = af.af_model_sample(gm.h, logits, recent, 8, 1.1, 0.8, 0.95, u, want_token=True)
+        got = logits.cpu().numpy().astype(np.float64)
+        assert rms_rel_err(got, ref) <= LAYER_TOL
+        inn, lo, hi, _, _ = oracle.sample_interval(got, rec, 1.1, 0.8, 0.95, tok)
+        assert lo - 1e-4 <= u <= hi + 1e-4, (u, tok, lo, hi)
+        assert inn or oracle.sample_interval(got, rec, 1.1, 0.8, 0.95 + 1e-4, tok)[0]
+        gm.decode(-1, p, logits)  # the drawn token, fed from the device
+        ref, _ = om.forward([tok], p)
+        p += 1
+    gm.close()
