@@ -500,8 +500,17 @@ cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int 
         (size_t)dec_stages<D, KT, CL>() * dec_tile<D, KT>() * D * sizeof(KT) + (size_t)cap * G * sizeof(float);
     if (smem > 222 * 1024) return cudaErrorInvalidValue;  // with the static shared memory, within 227 KB
     auto k = attn_decode_kernel<D, G, KT, CL>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // the largest dynamic shared memory this instantiation was opened to, per device (set before a launch
+    // that needs more; launches inside a stream capture reuse what was set before it)
+    static int opened[16] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e) return e;
+    if (dev < 0 || dev >= 16 || opened[dev] < (int)smem) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e) return e;
+        if (dev >= 0 && dev < 16) opened[dev] = (int)smem;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ns, KVH);
     cfg.blockDim = dim3(kDecThreads);

@@ -182,7 +182,8 @@ int af_debug_capture(af_model* m, float* hidden_dev);
  *   AF_DECODE_PERSISTENT: one cooperative launch per token, one CTA per SM,
  *     all layers separated by bounded grid barriers, the weights of the next
  *     matrix streaming into shared memory while the grid synchronises
- *     (n_embd <= 4096; AF_ENOTIMPL where it cannot be resident).
+ *     (n_embd <= 4096, Q4_0 or Q8_0 for every matrix including the LM head;
+ *     AF_ENOTIMPL otherwise or where it cannot be resident).
  */
 enum { AF_DECODE_PERSISTENT = 0, AF_DECODE_KERNELS = 1 };
 int af_set_decode_mode(af_model* m, int mode);

@@ -286,3 +286,16 @@ def test_model_sync_reports_token(af, tiny):
     t = af.af_model_sync(m.h, want_next=True)
     assert t == int(torch.argmax(lg).item())
     m.close()
+
+
+def test_q4_k_m_model_refuses_persistent_mode(af):
+    """The persistent decode kernel is built for Q4_0 / Q8_0 rows of one block type; a K-quant model keeps the
+    per-kernel decode and says so."""
+    cfg = synth.KQUANT_CONFIGS[0]
+    hm = synth.HostModel(cfg, synth.kquant_seed_of(0))
+    gm = gpu_model(hm)
+    with pytest.raises(af.AfError) as ei:
+        af.af_set_decode_mode(gm.h, af.AF_DECODE_PERSISTENT)
+    assert ei.value.code == af.AF_ENOTIMPL
+    assert af.af_get_decode_mode(gm.h) == af.AF_DECODE_KERNELS
+    gm.close()
