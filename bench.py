@@ -198,7 +198,8 @@ def run_reference(args, cfg, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_obj(cfg, args),
-            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "cpu": cpu_name(),
+                             "sample": sample},
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -312,6 +313,12 @@ def run_ours(args, cfg, world, rank, local):
         "prefill_tok_s": prefill_tps, "decode_tok_s": decode_tps,
         "decode_hbm_gbs": dec_gbs, "decode_hbm_frac": dec_gbs / hbm_peak,
         "prefill_tflops": pf_tflops,
+        # the prefill is seconds of back-to-back GEMMs: the sustained dense bf16 figure is its denominator (the
+        # same rate as fp16).  Each product runs as three MMAs (hi/lo split), so the tensor pipe does 3x this work.
+        "prefill_roofline": {"bound": "tensor", "achieved": pf_tflops, "peak": bf16_sust or bf16_peak,
+                             "unit": "TFLOP/s", "frac": pf_tflops / (bf16_sust or bf16_peak),
+                             "pipe_work_factor": 3, "kind": "algorithmic flops (GEMMs + causal attention) / prefill time",
+                             "peak_source": peak_src + (" sustained" if bf16_sust else " burst")},
         "sampler_us": samp_us,
         "decode_sampled_tok_s": sampled_tps,
         "q4_k_m": kq,
@@ -329,7 +336,7 @@ def run_ours(args, cfg, world, rank, local):
     if rank == 0 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         v, dt = oracle_sample(hm, cfg, args.ref_decode, threads)
-        line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle",
+        line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "cpu": cpu_name(),
                                 "sample": f"{args.ref_decode} decode steps after a 4-token prefill "
                                           f"({dt:.1f} s, fp64, {threads} threads)"}
     if rank == 0:
@@ -359,6 +366,21 @@ def sampled_decode(af, m, prompt_dev, cfg, args, stream):
     b.record(stream)
     b.synchronize()
     return ND / (a.elapsed_time(b) / 1000)
+
+
+def cpu_name():
+    """The host CPU, as far as /proc/cpuinfo names it (x86: model name; Arm: implementer and part)."""
+    import platform
+    fields = {}
+    try:
+        for line in open("/proc/cpuinfo"):
+            k, _, v = line.partition(":")
+            fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    name = fields.get("model name") or " ".join(
+        f"{k} {fields[k]}" for k in ("CPU implementer", "CPU part") if k in fields)
+    return f"{platform.machine()} {name}".strip()
 
 
 def kquant_run(af, args, dev, hbm_peak, steps=2, warmup=1):
