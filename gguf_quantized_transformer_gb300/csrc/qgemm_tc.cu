@@ -6,24 +6,23 @@
 //
 // Precision.  A single fp16 product would round X and W to 11 significant
 // bits.  X arrives split as X_hi + X_lo (two fp16 planes written by the
-// producing kernel) and each weight w = d * (n - 8) (or d * q) is split as
-// w_hi + w_lo in fp16 while dequantizing; three MMAs per K step accumulate
+// producing kernel) and each weight is split as w_hi + w_lo in fp16 while
+// dequantizing: exactly for Q4_0 / Q8_0 (w_hi = d * c by HMUL2 on the exact
+// integer code c, w_lo = fma(d, c, -w_hi) by HFMA2), and from an fp32 value
+// for the K-quants (formed from the unpacked sub-block scale and min).  Three
+// MMAs per K step accumulate
 //   X_hi W_hi + X_lo W_hi + X_hi W_lo
-// in fp32 (the dropped X_lo W_lo term is ~2^-22 relative).
+// in fp32 (the dropped X_lo W_lo term is ~2^-22 relative); see TcCfg for the
+// measured cost of dropping X_hi W_lo.
 //
 // Tile 128 (rows of X) x BN (rows of W: 256, or 128 when N is small so the
-// grid still covers the SMs) x 64 (K), two or three stages in shared memory,
-// SWIZZLE_128B K-major operand layout:
+// grid still covers the SMs) x 64 (K), two to four stages (192 KB) in shared
+// memory, SWIZZLE_128B K-major operand layout:
 //   warp 0      : TMA producer for the X_hi / X_lo tiles (cp.async.bulk.tensor.2d)
 //   warp 1      : TMEM allocation; one lane issues the MMAs and commits
 //   warps 2..9  : dequantize the W tile (256 / BN threads per weight row) into
-//                 the W_hi / W_lo tiles; the raw blocks of the next K step are
-//                 loaded into registers before waiting for a free stage.  The
-//                 split is exact fp16 arithmetic: with c the integer code
-//                 (exact in fp16), w_hi = d * c rounded (HMUL2) and
-//                 w_lo = fma(d, c, -w_hi) (HFMA2, exact); K-quant weights
-//                 are formed in fp32 from the unpacked sub-block scale and
-//                 min, then split into fp16 hi and the rounded remainder;
+//                 the W_hi (and W_lo) tiles; the raw blocks of the next K step
+//                 are loaded into registers before waiting for a free stage;
 //                 warps 2..5 then run the fused epilogue from TMEM
 //                 (tcgen05.ld, 32 columns at a time).
 // Every mbarrier wait is bounded; on a timeout the CTA records DEV_TIMEOUT,
@@ -42,13 +41,19 @@ constexpr int BM = 128, BK = 64;
 constexpr int kATile = BM * BK * 2;  // 16 KB per fp16 plane
 constexpr int kThreads = 10 * 32;
 constexpr int kDequantThreads = 8 * 32;
-constexpr int kMaxStages = 3;
+constexpr int kMaxStages = 4;
 
-template <int BN>
+// Every weight keeps its fp16 remainder W_lo as a third product X_hi W_lo.  Rounding W to fp16 alone (two MMAs,
+// one stage more in the same shared memory) measured 17.3k against 15.4k prefill tok/s on the 8B Q4_0 shape, but
+// its worst layer error on a 17-token prompt was 1.67e-2 of the 2e-2 RMS bar (5.6e-3 with the third product), and
+// the bar is a maximum over all elements: a 4096-token prompt has ~240x more of them, which puts the expected
+// maximum near 2.05e-2.  The 8B Q4_K_M model reached 2.05e-2 already on the short prompt.
+template <int WT, int BN>
 struct TcCfg {
+    static constexpr bool kWLo = true;  // W_lo tile and third MMA
     static constexpr int kBTile = BN * BK * 2;  // one fp16 plane
-    static constexpr int kStageBytes = 2 * kATile + 2 * kBTile;
-    static constexpr int kStages = BN == 256 ? 2 : 3;
+    static constexpr int kStageBytes = 2 * kATile + (kWLo ? 2 : 1) * kBTile;
+    static constexpr int kStages = kWLo ? (BN == 256 ? 2 : 3) : (BN == 256 ? 3 : 4);  // 192 KB of stages
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
     static constexpr int TPR = kDequantThreads / BN;                // dequant threads per weight row
     static constexpr int BPT = 2 / TPR;                              // 32-weight blocks per thread per K step
@@ -270,7 +275,7 @@ template <int WT, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo, Planes W,
                     int M, Epi epi, unsigned* err) {
-    using C = TcCfg<BN>;
+    using C = TcCfg<WT, BN>;
     constexpr int kStages = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     __shared__ TcSmem sm;
@@ -329,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
                     mma_f16(tmem, umma_desc_sw128(ah + off), umma_desc_sw128(bh + off), C::kIdesc, acc);
                     mma_f16(tmem, umma_desc_sw128(al + off), umma_desc_sw128(bh + off), C::kIdesc, 1u);
-                    mma_f16(tmem, umma_desc_sw128(ah + off), umma_desc_sw128(bl + off), C::kIdesc, 1u);
+                    if (C::kWLo) mma_f16(tmem, umma_desc_sw128(ah + off), umma_desc_sw128(bl + off), C::kIdesc, 1u);
                 }
                 mma_commit(&sm.empty[s]);  // frees the stage when these MMAs complete
             }
@@ -363,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
                     *reinterpret_cast<uint4*>(b_hi(s) + sw128(r, c0 + q)) = hi[q];
-                    *reinterpret_cast<uint4*>(b_lo(s) + sw128(r, c0 + q)) = lo[q];
+                    if (C::kWLo) *reinterpret_cast<uint4*>(b_lo(s) + sw128(r, c0 + q)) = lo[q];
                 }
             }
             fence_proxy_async_shared();  // generic-proxy writes -> visible to the tensor core
@@ -443,7 +448,7 @@ cudaError_t qgemm_prepare() {
     cudaError_t e = cudaSuccess;
 #define AF_QGEMM_ATTR(WT, BN)                                                                                  \
     if (!e) e = cudaFuncSetAttribute(qgemm_tc_kernel<WT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                     TcCfg<BN>::kSmemBytes);
+                                     TcCfg<WT, BN>::kSmemBytes);
     AF_QGEMM_ATTR(AF_Q4_0, 256)
     AF_QGEMM_ATTR(AF_Q4_0, 128)
     AF_QGEMM_ATTR(AF_Q8_0, 256)
@@ -467,7 +472,7 @@ cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo
     // 256-wide tiles unless that leaves a third or more of the SMs without a tile
     const bool narrow = (int64_t)((W.N + 255) / 256) * mt * 3 < (int64_t)num_sms() * 2;
 #define AF_QGEMM_LAUNCH(WT, BN)                                                                                   \
-    qgemm_tc_kernel<WT, BN><<<dim3((W.N + BN - 1) / BN, mt), kThreads, TcCfg<BN>::kSmemBytes, s>>>(mh, ml, W, M, epi, \
+    qgemm_tc_kernel<WT, BN><<<dim3((W.N + BN - 1) / BN, mt), kThreads, TcCfg<WT, BN>::kSmemBytes, s>>>(mh, ml, W, M, epi, \
                                                                                                  err)
 #define AF_QGEMM_TYPES(BN)                                          \
     switch (W.wtype) {                                              \
