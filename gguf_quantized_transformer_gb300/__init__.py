@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) forward pass of a GGUF (Q8_0 / Q4_0 / Q4_K / Q6_K) Llama-style decoder.
+"""GB300 (sm_103a) forward pass of a GGUF (Q8_0 / Q4_0 / Q4_K / Q5_K / Q6_K) Llama-style decoder.
 
 Thin ctypes binding over ``libaf.so`` (C ABI in ``include/af.h``): the
 functions below only marshal arguments; every step of the forward pass runs in
@@ -11,9 +11,9 @@ import os
 from ._build import LIB_PATH, build  # noqa: F401
 
 AF_OK, AF_EINVAL, AF_ERANGE, AF_ENOMEM, AF_ECUDA, AF_ETIMEOUT, AF_ENOTIMPL = range(7)
-AF_Q4_0, AF_Q8_0, AF_Q4_K, AF_Q6_K = 2, 8, 12, 14
+AF_Q4_0, AF_Q8_0, AF_Q4_K, AF_Q5_K, AF_Q6_K = 2, 8, 12, 13, 14
 AF_F32, AF_F16 = 0, 1
-WTYPE = {"q4_0": AF_Q4_0, "q8_0": AF_Q8_0, "q4_k": AF_Q4_K, "q6_k": AF_Q6_K}
+WTYPE = {"q4_0": AF_Q4_0, "q8_0": AF_Q8_0, "q4_k": AF_Q4_K, "q5_k": AF_Q5_K, "q6_k": AF_Q6_K}
 KVTYPE = {"f32": AF_F32, "f16": AF_F16}
 STATUS_NAMES = {0: "AF_OK", 1: "AF_EINVAL", 2: "AF_ERANGE", 3: "AF_ENOMEM", 4: "AF_ECUDA", 5: "AF_ETIMEOUT",
                 6: "AF_ENOTIMPL"}

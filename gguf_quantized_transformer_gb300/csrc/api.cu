@@ -52,6 +52,7 @@ size_t block_bytes(int wtype) {
         case AF_Q8_0: return 34;
         case AF_Q4_0: return 18;
         case AF_Q4_K: return 144;
+        case AF_Q5_K: return 176;
         case AF_Q6_K: return 210;
         default: return 0;
     }
@@ -122,7 +123,7 @@ Epi epi_simple(int kind, float* out, int ld) {
 
 int check_config(const af_config* c) {
     if (!c) return fail(AF_EINVAL, "null config");
-    if (!block_bytes(c->wtype)) return fail(AF_EINVAL, "wtype must be AF_Q4_0, AF_Q8_0, AF_Q4_K or AF_Q6_K");
+    if (!block_bytes(c->wtype)) return fail(AF_EINVAL, "wtype must be AF_Q4_0, AF_Q8_0, AF_Q4_K, AF_Q5_K or AF_Q6_K");
     if (!block_bytes(head_wtype(c))) return fail(AF_EINVAL, "bad out_wtype");
     if (c->kv_dtype != AF_F32 && c->kv_dtype != AF_F16) return fail(AF_EINVAL, "kv_dtype must be AF_F32 or AF_F16");
     if (c->n_layers <= 0 || c->n_embd <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||

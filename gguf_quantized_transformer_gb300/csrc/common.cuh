@@ -22,18 +22,22 @@ namespace af {
 //   Q4_K: [(Kp/32) x 16 code bytes][(Kp/256) super-block records of 20 B:
 //          fp16 d, fp16 dmin, then (s_j, m_j) byte pairs of its 8 sub-blocks,
 //          the 6-bit scales and mins already unpacked]
+//   Q5_K: as Q4_K, with a plane of the codes' high bits after the units: one word
+//          per unit, element 4t + i of half h (16 elements) at bit 8i + 4h + t
 //   Q6_K: [(Kp/32) x 16 bytes: low 4 bits of the codes][(Kp/32) x 8 bytes: the
 //          high 2 bits, two words per unit, element 4t + i of a 16-element half
 //          at bits 8i + 2t][(Kp/256) records of 18 B: fp16 d, 16 int8 scales]
 //          (+ padding of the row to 16 bytes)
 // qs points at row 0; sc at row 0's fp16 scales (Q4_0 / Q8_0; sc_pitch()
 // halves per row).  sc_off() is the byte offset of the scales or records in a
-// row, hb_off() that of the Q6_K high-bit plane.
+// row, hb_off() that of the Q5_K / Q6_K high-bit plane.
 // ---------------------------------------------------------------------------
-constexpr int kQ4KRec = 20;
+constexpr int kQ4KRec = 20;  // also Q5_K's record
 constexpr int kQ6KRec = 18;
 
-__host__ __device__ inline bool is_kquant(int wtype) { return wtype == AF_Q4_K || wtype == AF_Q6_K; }
+__host__ __device__ inline bool is_kquant(int wtype) {
+    return wtype == AF_Q4_K || wtype == AF_Q5_K || wtype == AF_Q6_K;
+}
 
 struct Planes {
     const uint8_t* qs = nullptr;
@@ -41,13 +45,15 @@ struct Planes {
     int N = 0, K = 0, Kp = 0, wtype = 0;
     __host__ __device__ int qb() const { return wtype == AF_Q8_0 ? 32 : 16; }  // code bytes per 32 weights
     __host__ __device__ int sc_off() const {
-        return wtype == AF_Q6_K ? (Kp / 32) * 24 : (Kp / 32) * qb();
+        return wtype == AF_Q6_K ? (Kp / 32) * 24 : wtype == AF_Q5_K ? (Kp / 32) * 20 : (Kp / 32) * qb();
     }
     __host__ __device__ int hb_off() const { return (Kp / 32) * 16; }
     __host__ __device__ int64_t qs_pitch() const {  // bytes per row
         int64_t b;
         if (wtype == AF_Q4_K)
             b = (int64_t)(Kp / 32) * 16 + (int64_t)(Kp / 256) * kQ4KRec;
+        else if (wtype == AF_Q5_K)
+            b = (int64_t)(Kp / 32) * 20 + (int64_t)(Kp / 256) * kQ4KRec;
         else if (wtype == AF_Q6_K)
             b = (int64_t)(Kp / 32) * 24 + (int64_t)(Kp / 256) * kQ6KRec;
         else

@@ -20,9 +20,10 @@ int num_sms() {
 // GGUF AoS blocks -> per-row records (see Planes).  One thread per destination 32-weight unit (per 32-weight
 // block for Q4_0 / Q8_0); units past K are zero.  The first unit of a K-quant super-block also writes the
 // super-block's record.  Source row r goes to destination row row0 + r * step.
-__device__ void repack_q4_k_unit(const uint8_t* blk, int j, uint8_t* dq, uint8_t* rec) {
+// qs_off: byte offset of the nibbles in the source block (16 for Q4_K, 48 for Q5_K)
+__device__ void repack_q4_k_unit(const uint8_t* blk, int j, uint8_t* dq, uint8_t* rec, int qs_off = 16) {
     // codes of sub-block j: elements 32 j + i live in qs[32 (j / 2) + i], low nibble for even j
-    const uint8_t* qs = blk + 16 + 32 * (j >> 1);
+    const uint8_t* qs = blk + qs_off + 32 * (j >> 1);
     const int sh = (j & 1) * 4;
     for (int t = 0; t < 16; t++)
         dq[t] = (uint8_t)(((qs[t] >> sh) & 15) | (((qs[t + 16] >> sh) & 15) << 4));
@@ -42,6 +43,19 @@ __device__ void repack_q4_k_unit(const uint8_t* blk, int j, uint8_t* dq, uint8_t
             rec[5 + 2 * k] = (uint8_t)mk;
         }
     }
+}
+
+// Q5_K: Q4_K's nibbles and record, plus the high bits of sub-block j (bit j of qh[i] for element i) as one
+// word: element 4t + b of half h at bit 8b + 4h + t
+__device__ void repack_q5_k_unit(const uint8_t* blk, int j, uint8_t* dq, uint8_t* dh, uint8_t* rec) {
+    repack_q4_k_unit(blk, j, dq, rec, 48);
+    const uint8_t* qh = blk + 16;
+    uint32_t hw = 0u;
+    for (int e = 0; e < 32; e++) {
+        const int h = e >> 4, i = e & 15;
+        hw |= (uint32_t)((qh[e] >> j) & 1) << (8 * (i & 3) + 4 * h + (i >> 2));
+    }
+    for (int b = 0; b < 4; b++) dh[b] = (uint8_t)(hw >> (8 * b));
 }
 
 __device__ void repack_q6_k_unit(const uint8_t* blk, int g, uint8_t* dq, uint8_t* dh, uint8_t* rec) {
@@ -75,20 +89,23 @@ __global__ void repack_kernel(const uint8_t* __restrict__ src, Planes P, int N, 
     const int r = (int)(t / nbp), b = (int)(t % nbp);
     const int64_t pitch = P.qs_pitch();
     uint8_t* row = const_cast<uint8_t*>(P.qs) + ((int64_t)row0 + (int64_t)r * step) * pitch;
-    if (P.wtype == AF_Q4_K || P.wtype == AF_Q6_K) {
+    if (is_kquant(P.wtype)) {
         const int sb = b / 8, u = b % 8;
-        const int bb = P.wtype == AF_Q4_K ? 144 : 210, rec_bytes = P.wtype == AF_Q4_K ? kQ4KRec : kQ6KRec;
+        const int bb = P.wtype == AF_Q4_K ? 144 : P.wtype == AF_Q5_K ? 176 : 210;
+        const int rec_bytes = P.wtype == AF_Q6_K ? kQ6KRec : kQ4KRec;
+        const int hbu = P.wtype == AF_Q6_K ? 8 : 4;  // high-bit bytes per unit (Q5_K, Q6_K)
         uint8_t* dq = row + (int64_t)b * 16;
         uint8_t* rec = row + P.sc_off() + (int64_t)sb * rec_bytes;
-        uint8_t* dh = row + P.hb_off() + (int64_t)b * 8;
+        uint8_t* dh = row + P.hb_off() + (int64_t)b * hbu;
         if (b < nb) {
             const uint8_t* blk = src + ((int64_t)r * (nb / 8) + sb) * bb;
             if (P.wtype == AF_Q4_K) repack_q4_k_unit(blk, u, dq, rec);
+            else if (P.wtype == AF_Q5_K) repack_q5_k_unit(blk, u, dq, dh, rec);
             else repack_q6_k_unit(blk, u, dq, dh, rec);
         } else {
             for (int j = 0; j < 16; j++) dq[j] = 0;
-            if (P.wtype == AF_Q6_K)
-                for (int j = 0; j < 8; j++) dh[j] = 0;
+            if (P.wtype != AF_Q4_K)
+                for (int j = 0; j < hbu; j++) dh[j] = 0;
             if (u == 0)
                 for (int j = 0; j < rec_bytes; j++) rec[j] = 0;
         }
@@ -140,15 +157,22 @@ cudaError_t launch_rope_table(float2* tab, int max_ctx, int head_dim, double bas
 __device__ float plane_weight(const Planes& P, int row, int k) {
     const uint8_t* base = P.qs + (int64_t)row * P.qs_pitch();
     const int u = k >> 5, e = k & 31;
-    if (P.wtype == AF_Q4_K || P.wtype == AF_Q6_K) {
+    if (is_kquant(P.wtype)) {
         const uint8_t byte = base[(int64_t)u * 16 + (e & 15)];
         const int lo4 = e < 16 ? (byte & 15) : (byte >> 4);
-        if (P.wtype == AF_Q4_K) {
+        if (P.wtype != AF_Q6_K) {
+            int q = lo4;
+            if (P.wtype == AF_Q5_K) {  // high bit: element 4t + b of half h at bit 8b + 4h + t of the unit's word
+                const uint8_t* hb = base + P.hb_off() + (int64_t)u * 4;
+                const uint32_t hw = (uint32_t)hb[0] | ((uint32_t)hb[1] << 8) | ((uint32_t)hb[2] << 16) | ((uint32_t)hb[3] << 24);
+                const int i = e & 15;
+                q |= (int)((hw >> (8 * (i & 3) + 4 * (e >> 4) + (i >> 2))) & 1u) << 4;
+            }
             const uint8_t* rec = base + P.sc_off() + (int64_t)(u >> 3) * kQ4KRec;
             const float d = __half2float(__ushort_as_half((unsigned short)(rec[0] | (rec[1] << 8))));
             const float dmin = __half2float(__ushort_as_half((unsigned short)(rec[2] | (rec[3] << 8))));
             const int j = u & 7;
-            return d * (float)rec[4 + 2 * j] * (float)lo4 - dmin * (float)rec[5 + 2 * j];
+            return d * (float)rec[4 + 2 * j] * (float)q - dmin * (float)rec[5 + 2 * j];
         }
         const uint8_t* hb = base + P.hb_off() + (int64_t)u * 8 + (e >> 4) * 4;
         const uint32_t hw = (uint32_t)hb[0] | ((uint32_t)hb[1] << 8) | ((uint32_t)hb[2] << 16) | ((uint32_t)hb[3] << 24);

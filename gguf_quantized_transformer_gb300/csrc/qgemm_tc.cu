@@ -1,5 +1,5 @@
 // Prefill GEMM on the 5th-generation tensor cores: Y[m][n] = sum_k X[m][k] W[n][k]
-// with W in Q4_0 / Q8_0 / Q4_K / Q6_K planes, dequantized tile by tile into shared memory
+// with W in Q4_0 / Q8_0 / Q4_K / Q5_K / Q6_K planes, dequantized tile by tile into shared memory
 // and multiplied with tcgen05.mma into a TMEM accumulator (dotLLM "GPU
 // Inference", "Weight Strategy", approach 1: fused dequantize-in-kernel feeding
 // the tensor cores; dequantized values never touch device memory).
@@ -81,6 +81,13 @@ struct RawBlk<AF_Q4_K> {
     unsigned short smj;  // unpacked (s_j, m_j) of this sub-block
 };
 template <>
+struct RawBlk<AF_Q5_K> {
+    uint4 q;
+    unsigned h;          // high bits: element 4t + i of half hh at bit 8i + 4hh + t
+    unsigned dm;
+    unsigned short smj;
+};
+template <>
 struct RawBlk<AF_Q6_K> {
     uint4 q;             // low 4 bits of the codes
     uint2 h;             // high 2 bits (element 4t + i of a half at bits 8i + 2t of that half's word)
@@ -94,6 +101,20 @@ __device__ __forceinline__ void load_blk(const Planes& W, int n, int blk, RawBlk
     const uint8_t* rec = row + W.sc_off() + (int64_t)(blk >> 3) * kQ4KRec;
     b.dm = *reinterpret_cast<const unsigned*>(rec);
     b.smj = *reinterpret_cast<const unsigned short*>(rec + 4 + (blk & 7) * 2);
+}
+__device__ __forceinline__ void load_blk(const Planes& W, int n, int blk, RawBlk<AF_Q5_K>& b) {
+    const uint8_t* row = W.qs + (int64_t)n * W.qs_pitch();
+    b.q = *reinterpret_cast<const uint4*>(row + (int64_t)blk * 16);
+    b.h = *reinterpret_cast<const unsigned*>(row + W.hb_off() + (int64_t)blk * 4);
+    const uint8_t* rec = row + W.sc_off() + (int64_t)(blk >> 3) * kQ4KRec;
+    b.dm = *reinterpret_cast<const unsigned*>(rec);
+    b.smj = *reinterpret_cast<const unsigned short*>(rec + 4 + (blk & 7) * 2);
+}
+__device__ __forceinline__ void zero_blk(RawBlk<AF_Q5_K>& b) {
+    b.q = make_uint4(0, 0, 0, 0);
+    b.h = 0;
+    b.dm = 0;
+    b.smj = 0;
 }
 __device__ __forceinline__ void load_blk(const Planes& W, int n, int blk, RawBlk<AF_Q6_K>& b) {
     const uint8_t* row = W.qs + (int64_t)n * W.qs_pitch();
@@ -209,6 +230,31 @@ __device__ __forceinline__ void deq_blk(const RawBlk<AF_Q4_K>& b, uint4 (&hi)[4]
             const int sh = 16 * (k & 1);
             const float n0 = u2f_small((word >> sh) & 15u), n1 = u2f_small((word >> (sh + 8)) & 15u);
             split_f32_pair(fmaf(A, n0, -B), fmaf(A, n1, -B), hv[k], lv[k]);
+        }
+        hi[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        lo[c] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+    }
+}
+
+// Q5_K: as Q4_K with the 5-bit code nibble + 16 * high bit.
+__device__ __forceinline__ void deq_blk(const RawBlk<AF_Q5_K>& b, uint4 (&hi)[4], uint4 (&lo)[4]) {
+    const float2 dm = __half22float2(u2h(b.dm));
+    const float A = dm.x * (float)(b.smj & 255u), B = dm.y * (float)(b.smj >> 8);
+    const unsigned w[4] = {b.q.x, b.q.y, b.q.z, b.q.w};
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+        unsigned hv[4], lv[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            float v[2];
+#pragma unroll
+            for (int e2 = 0; e2 < 2; e2++) {
+                const int i = 8 * (c & 1) + 2 * k + e2;  // index within the half c / 2
+                const unsigned nib = (w[i >> 2] >> (8 * (i & 3) + (c < 2 ? 0 : 4))) & 15u;
+                const unsigned h1 = (b.h >> (8 * (i & 3) + 4 * (c >> 1) + (i >> 2))) & 1u;
+                v[e2] = fmaf(A, u2f_small(nib | (h1 << 4)), -B);
+            }
+            split_f32_pair(v[0], v[1], hv[k], lv[k]);
         }
         hi[c] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
         lo[c] = make_uint4(lv[0], lv[1], lv[2], lv[3]);
@@ -455,6 +501,8 @@ cudaError_t qgemm_prepare() {
     AF_QGEMM_ATTR(AF_Q8_0, 128)
     AF_QGEMM_ATTR(AF_Q4_K, 256)
     AF_QGEMM_ATTR(AF_Q4_K, 128)
+    AF_QGEMM_ATTR(AF_Q5_K, 256)
+    AF_QGEMM_ATTR(AF_Q5_K, 128)
     AF_QGEMM_ATTR(AF_Q6_K, 256)
     AF_QGEMM_ATTR(AF_Q6_K, 128)
 #undef AF_QGEMM_ATTR
@@ -479,6 +527,7 @@ cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo
         case AF_Q4_0: AF_QGEMM_LAUNCH(AF_Q4_0, BN); break;          \
         case AF_Q8_0: AF_QGEMM_LAUNCH(AF_Q8_0, BN); break;          \
         case AF_Q4_K: AF_QGEMM_LAUNCH(AF_Q4_K, BN); break;          \
+        case AF_Q5_K: AF_QGEMM_LAUNCH(AF_Q5_K, BN); break;          \
         case AF_Q6_K: AF_QGEMM_LAUNCH(AF_Q6_K, BN); break;          \
         default: return cudaErrorInvalidValue;                      \
     }

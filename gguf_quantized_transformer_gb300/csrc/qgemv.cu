@@ -11,6 +11,7 @@ cudaError_t qgemv_prepare() {
     cudaError_t e = qgemv_set_attrs<AF_Q4_0>();
     if (!e) e = qgemv_set_attrs<AF_Q8_0>();
     if (!e) e = qgemv_set_attrs<AF_Q4_K>();
+    if (!e) e = qgemv_set_attrs<AF_Q5_K>();
     if (!e) e = qgemv_set_attrs<AF_Q6_K>();
     if (!e) done = true;
     return e;
@@ -24,6 +25,7 @@ cudaError_t launch_qgemv(const Planes& W, const float* x, const float* norm_w, f
         case AF_Q4_0: return qgemv_dispatch<AF_Q4_0>(W, x, norm_w, eps, epi, scr.err, s);
         case AF_Q8_0: return qgemv_dispatch<AF_Q8_0>(W, x, norm_w, eps, epi, scr.err, s);
         case AF_Q4_K: return qgemv_dispatch<AF_Q4_K>(W, x, norm_w, eps, epi, scr.err, s);
+        case AF_Q5_K: return qgemv_dispatch<AF_Q5_K>(W, x, norm_w, eps, epi, scr.err, s);
         case AF_Q6_K: return qgemv_dispatch<AF_Q6_K>(W, x, norm_w, eps, epi, scr.err, s);
         default: return cudaErrorInvalidValue;
     }

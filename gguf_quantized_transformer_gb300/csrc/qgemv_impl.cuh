@@ -195,6 +195,43 @@ struct Unit<AF_Q4_K> {
     }
 };
 
+// One lane's x for one Q5_K unit (32 weights = sub-block j): 5-bit codes, nibble | high bit << 4, with the
+// high bits in one word per unit (element 4t + i of half h at bit 8i + 4h + t).  Row value as Q4_K's:
+//   d s_j sum_e q_e x_e - dmin m_j sum_e x_e
+template <>
+struct Unit<AF_Q5_K> {
+    XPlanes x;
+    float s, sx;  // s; s * sum of the 32 xi
+    __device__ __forceinline__ void load(const XBlk* xb, int unit) {
+        const XBlk& b = xb[unit];
+        x.load(b);
+        s = b.s;
+        sx = b.sxa + b.sxb;
+    }
+    __device__ __forceinline__ float accumulate(const uint8_t* row, int sc_off, int hb_off, int unit,
+                                                float acc) const {
+        const uint4 q = *reinterpret_cast<const uint4*>(row + unit * 16);
+        const unsigned hw = *reinterpret_cast<const unsigned*>(row + hb_off + unit * 4);
+        const unsigned w[4] = {q.x, q.y, q.z, q.w};
+        int A = 0, B = 0, C = 0, D = 0;
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+            const unsigned qa = (w[t] & 0x0F0F0F0Fu) | ((hw >> t) << 4 & 0x10101010u);
+            const unsigned qb = ((w[t] >> 4) & 0x0F0F0F0Fu) | ((hw >> t) & 0x10101010u);
+            A = dp4a_us(qa, x.hi[t], A);
+            B = dp4a_uu(qa, x.lo[t], B);
+            C = dp4a_us(qb, x.hi[4 + t], C);
+            D = dp4a_uu(qb, x.lo[4 + t], D);
+        }
+        const int v = (A + C) * 256 + (B + D);  // sum_e q_e xi_e, |.| < 2^26: exact
+        const uint8_t* rec = row + sc_off + (unit >> 3) * kQ4KRec;
+        const float2 dm = __half22float2(*reinterpret_cast<const __half2*>(rec));
+        const unsigned smj = *reinterpret_cast<const unsigned short*>(rec + 4 + (unit & 7) * 2);
+        const float ds = dm.x * (float)(smj & 255u), dmm = dm.y * (float)(smj >> 8);
+        return fmaf(ds, s * (float)v, fmaf(-dmm, sx, acc));
+    }
+};
+
 // One lane's x for one Q6_K unit (32 weights = sub-blocks 2g, 2g+1 of 16 weights).  Codes q in 0..63 are
 // rebuilt from the low nibbles and the high-bit words (element 4t + i of a half at bits 8i + 2t); the value
 // of a half with int8 scale c is d c (s sum_e q_e xi_e - 32 s sum_e xi_e).
@@ -455,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int h = 0; h < 2; h++) {
                             const uint8_t* row = qsm + (j0 + h) * pitch;
-                            if constexpr (WT == AF_Q6_K)
+                            if constexpr (WT == AF_Q5_K || WT == AF_Q6_K)
                                 acc[2 * p + h] = xr[u].accumulate(row, sc_off, hb_off, unit, acc[2 * p + h]);
                             else
                                 acc[2 * p + h] = xr[u].accumulate(row, sc_off, unit, acc[2 * p + h]);

@@ -44,6 +44,10 @@
  *                   (scales[j + 4] >> 4) | (scales[j] >> 6) << 4); code n_e in
  *                   the low (e % 64 < 32) or high nibble of qs[32 (e / 64) + e % 32];
  *                   w_e = d s_j n_e - dmin m_j
+ *      Q5_K (176 B per 256 weights): fp16 d, fp16 dmin, uint8 scales[12] (as
+ *                   Q4_K), uint8 qh[32], uint8 qs[128] (nibbles placed as Q4_K's);
+ *                   the 5-bit code q_e = nibble + 16 * (bit 2 (e / 64) + (e % 64 >= 32)
+ *                   of qh[e % 32]); w_e = d s_j q_e - dmin m_j
  *      Q6_K (210 B per 256 weights): uint8 ql[128], uint8 qh[64], int8
  *                   scales[16], fp16 d; with h = e / 128, k = (e % 128) / 32,
  *                   l = e % 32 the code q_e has its low 4 bits in the low (k < 2)
@@ -51,7 +55,7 @@
  *                   at bits 2k of qh[32 h + l]; w_e = d scales[e / 16] (q_e - 32)
  *    (Shimmy v2.0 Architecture, "Quantization": the K-quant super-blocks; their
  *    byte layout is GGUF's.)  A matrix [N, K] is N rows of K / 32 blocks each
- *    (K / 256 super-blocks for Q4_K and Q6_K; K must be a whole number of blocks).
+ *    (K / 256 super-blocks for Q4_K, Q5_K and Q6_K; K must be a whole number of blocks).
  */
 #ifndef AF_H
 #define AF_H
@@ -72,7 +76,7 @@ typedef enum af_status {
     AF_ENOTIMPL = 6  /* valid request this build does not implement */
 } af_status;
 
-typedef enum af_wtype { AF_Q4_0 = 2, AF_Q8_0 = 8, AF_Q4_K = 12, AF_Q6_K = 14 } af_wtype; /* GGUF's type numbers */
+typedef enum af_wtype { AF_Q4_0 = 2, AF_Q8_0 = 8, AF_Q4_K = 12, AF_Q5_K = 13, AF_Q6_K = 14 } af_wtype; /* GGUF's type numbers */
 typedef enum af_dtype { AF_F32 = 0, AF_F16 = 1 } af_dtype;
 
 typedef struct af_config {
@@ -202,7 +206,7 @@ void af_model_destroy(af_model* m);
 /*
  * Standalone quantized matmuls.
  * af_qweight_create repacks a [N, K] block matrix (N even, K a whole number
- * of blocks: K % 32 == 0, K % 256 == 0 for Q4_K / Q6_K; K <= 32768, or
+ * of blocks: K % 32 == 0, K % 256 == 0 for Q4_K / Q5_K / Q6_K; K <= 32768, or
  * <= 16384 for Q8_0, else AF_ENOTIMPL) into its own device memory (and
  * scratch for the GEMV); synchronises `stream`.
  *   af_qgemv: y[i]    = sum_j W[i][j] x[j]        x_dev fp32 [K], y_dev fp32 [N]

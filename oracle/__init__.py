@@ -20,7 +20,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-WTYPE_ID = {"q8_0": 8, "q4_0": 2, "q4_k": 12, "q6_k": 14}
+WTYPE_ID = {"q8_0": 8, "q4_0": 2, "q4_k": 12, "q5_k": 13, "q6_k": 14}
 
 
 class OrcConfig(ctypes.Structure):

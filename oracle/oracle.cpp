@@ -49,13 +49,14 @@ size_t block_bytes(int32_t wtype) {
         case ORC_Q8_0: return 34;
         case ORC_Q4_0: return 18;
         case ORC_Q4_K: return 144;
+        case ORC_Q5_K: return 176;
         case ORC_Q6_K: return 210;
         default: return 0;
     }
 }
 
 // elements per block: 32, or 256 for the K-quant super-blocks
-int64_t block_elems(int32_t wtype) { return (wtype == ORC_Q4_K || wtype == ORC_Q6_K) ? 256 : 32; }
+int64_t block_elems(int32_t wtype) { return (wtype == ORC_Q4_K || wtype == ORC_Q5_K || wtype == ORC_Q6_K) ? 256 : 32; }
 
 // bytes of one row of k elements
 size_t row_bytes_of(int32_t wtype, int64_t k) { return (size_t)(k / block_elems(wtype)) * block_bytes(wtype); }
@@ -90,6 +91,27 @@ void dequant_q4_k(const uint8_t* b, double* out) {
         const uint8_t byte = qs[32 * c + r % 32];
         const int n = r < 32 ? (byte & 15) : (byte >> 4);
         out[e] = d * (double)s * (double)n - dmin * (double)m;
+    }
+}
+
+// Q5_K (176 B per 256 elements; Shimmy v2.0 Architecture: "Q5_K_M super-block, 5-bit with high-bit plane"):
+// fp16 d, fp16 dmin, the 12 bytes of 6-bit scales and mins as in Q4_K, 32 bytes of high bits, 128 bytes of
+// low nibbles (placed as Q4_K's).  The high bit of element e (c = e / 64, r = e % 64) is bit 2c + (r >= 32) of
+// byte r % 32 of the high-bit plane; the 5-bit code is nibble + 16 * high bit; value = d s_j q_e - dmin m_j.
+void dequant_q5_k(const uint8_t* b, double* out) {
+    const double d = f16_to_double((uint16_t)(b[0] | (b[1] << 8)));
+    const double dmin = f16_to_double((uint16_t)(b[2] | (b[3] << 8)));
+    const uint8_t* sc = b + 4;
+    const uint8_t* qh = b + 16;
+    const uint8_t* qs = b + 48;
+    for (int e = 0; e < 256; e++) {
+        int s = 0, m = 0;
+        q4_k_scale_min(sc, e / 32, &s, &m);
+        const int c = e / 64, r = e % 64;
+        const uint8_t byte = qs[32 * c + r % 32];
+        const int nib = r < 32 ? (byte & 15) : (byte >> 4);
+        const int hb = (qh[r % 32] >> (2 * c + (r >= 32 ? 1 : 0))) & 1;
+        out[e] = d * (double)s * (double)(nib + 16 * hb) - dmin * (double)m;
     }
 }
 
@@ -132,6 +154,8 @@ void dequant_row(int32_t wtype, const uint8_t* blocks, int64_t k, double* out) {
     for (int64_t b = 0; b < k / be; b++) {
         if (wtype == ORC_Q4_K)
             dequant_q4_k(blocks + b * bb, out + b * be);
+        else if (wtype == ORC_Q5_K)
+            dequant_q5_k(blocks + b * bb, out + b * be);
         else if (wtype == ORC_Q6_K)
             dequant_q6_k(blocks + b * bb, out + b * be);
         else

@@ -15,7 +15,7 @@
  *    "Decode" step; "Output head" (LM head on the last position); "Sampler"
  *    (greedy = temperature 0).
  *  - "Shimmy v2.0 Architecture": "Quantization" table (Q4_0, Q8_0 32-element
- *    blocks; Q4_K and Q6_K super-blocks, whose byte layout the pages leave to
+ *    blocks; Q4_K, Q5_K and Q6_K super-blocks, whose byte layout the pages leave to
  *    another document: the published GGUF layout is taken), "Extended Context
  *    (YaRN)" (scale applied to all positions).
  *  - "GPU Inference — dotLLM": "Forward Pass" steps (final RmsNorm on the last
@@ -36,11 +36,11 @@
 extern "C" {
 #endif
 
-enum { ORC_Q4_0 = 2, ORC_Q8_0 = 8, ORC_Q4_K = 12, ORC_Q6_K = 14 };
+enum { ORC_Q4_0 = 2, ORC_Q8_0 = 8, ORC_Q4_K = 12, ORC_Q5_K = 13, ORC_Q6_K = 14 };
 
 typedef struct orc_config {
     int32_t n_layers, n_embd, n_heads, n_kv_heads, head_dim, n_ff, n_vocab;
-    int32_t wtype;      /* ORC_Q8_0 | ORC_Q4_0 | ORC_Q4_K | ORC_Q6_K: layer matrices and token_embd */
+    int32_t wtype;      /* ORC_Q8_0 | ORC_Q4_0 | ORC_Q4_K | ORC_Q5_K | ORC_Q6_K: layer matrices and token_embd */
     int32_t kv_f16;     /* 0: f32 cache, 1: f16 cache */
     int32_t max_ctx, native_ctx;
     double rms_eps, rope_base;

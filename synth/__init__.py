@@ -11,7 +11,7 @@ import threading
 
 import numpy as np
 
-from .configs import (CONFIGS, KQUANT_CONFIGS, ModelConfig, Q4_0, Q8_0, Q4_K, Q6_K, BASE_SEED,  # noqa: F401
+from .configs import (CONFIGS, KQUANT_CONFIGS, ModelConfig, Q4_0, Q8_0, Q4_K, Q5_K, Q6_K, BASE_SEED,  # noqa: F401
                       seed_of, kquant_seed_of)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -20,9 +20,9 @@ _LIB = os.path.join(_HERE, "libsynth.so")
 _lock = threading.Lock()
 _lib = None
 
-WTYPE_ID = {Q8_0: 8, Q4_0: 2, Q4_K: 12, Q6_K: 14}
-BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_K: 144, Q6_K: 210}
-BLOCK_ELEMS = {Q8_0: 32, Q4_0: 32, Q4_K: 256, Q6_K: 256}
+WTYPE_ID = {Q8_0: 8, Q4_0: 2, Q4_K: 12, Q5_K: 13, Q6_K: 14}
+BLOCK_BYTES = {Q8_0: 34, Q4_0: 18, Q4_K: 144, Q5_K: 176, Q6_K: 210}
+BLOCK_ELEMS = {Q8_0: 32, Q4_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256}
 
 # tensor ids outside the per-layer range 1 + 16*layer + section
 TID_TOKEN_EMBD = 0x100000

@@ -13,6 +13,7 @@ from dataclasses import dataclass, asdict, replace
 Q8_0 = "q8_0"
 Q4_0 = "q4_0"
 Q4_K = "q4_k"
+Q5_K = "q5_k"
 Q6_K = "q6_k"
 BASE_SEED = 20261202
 
@@ -27,7 +28,7 @@ class ModelConfig:
     head_dim: int
     n_ff: int
     n_vocab: int
-    wtype: str          # "q8_0" | "q4_0" | "q4_k" | "q6_k": every layer matrix and token_embd
+    wtype: str          # "q8_0" | "q4_0" | "q4_k" | "q5_k" | "q6_k": every layer matrix and token_embd
     kv_dtype: str       # "f32" | "f16"
     max_ctx: int
     native_ctx: int     # == max_ctx means no YaRN scaling
@@ -73,6 +74,9 @@ KQUANT_CONFIGS = [
                 prompt_len=32, chunk=512, n_decode=16, out_wtype=Q6_K),
     ModelConfig("llama-3-8b-shape-q4_k_m", 32, 4096, 32, 8, 128, 14336, 128256, Q4_K, "f16", 8192, 8192, 500000.0,
                 prompt_len=4096, chunk=512, n_decode=256, out_wtype=Q6_K),
+    # the Q5_K_M mix (Shimmy v2.0 Architecture, Quantization: "Q5_K_M super-block, 5-bit with high-bit plane")
+    ModelConfig("tiny-2L-q5_k_m", 2, 512, 8, 4, 64, 1536, 2048, Q5_K, "f16", 64, 64, 10000.0,
+                prompt_len=32, chunk=512, n_decode=16, out_wtype=Q6_K),
 ]
 
 

@@ -50,7 +50,7 @@ def test_layer_offsets_and_kv_bytes_match_oracle(idx):
     assert af.af_kv_bytes(c) == oracle.kv_bytes(cfg)
 
 
-@pytest.mark.parametrize("idx", range(2))
+@pytest.mark.parametrize("idx", range(len(synth.KQUANT_CONFIGS)))
 def test_kquant_layer_offsets_match_oracle(idx):
     af = _af()
     cfg = synth.KQUANT_CONFIGS[idx]

@@ -1,4 +1,4 @@
-"""K-quant (Q4_K, Q6_K) kernels through the C ABI against the fp64 oracle.
+"""K-quant (Q4_K, Q5_K, Q6_K) kernels through the C ABI against the fp64 oracle.
 
 Same bars as the Q4_0 / Q8_0 kernels: the GEMV's decode of a weight is bit-exact (a one-hot x extracts
 a weight column exactly, since d s_j n - dmin m_j and d c (q - 32) are formed with one rounding); qgemv
@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-KTYPES = ["q4_k", "q6_k"]
+KTYPES = ["q4_k", "q5_k", "q6_k"]
 
 
 @pytest.fixture(scope="module")
@@ -49,9 +49,10 @@ def test_kquant_decode_bit_exact_via_onehot(af, wtype):
     N, K = 64, 1280  # five super-blocks: the row is padded to 2048 weights
     W = synth.matrix(wtype, 61, synth.TID_TEST_BASE + 20, N, K)
     # hand-edited first super-block of row 0: a negative d; of row 1: zero d (and dmin)
-    if wtype == "q4_k":
+    if wtype in ("q4_k", "q5_k"):
+        bb = synth.BLOCK_BYTES[wtype]
         W[0:2] = np.frombuffer(np.uint16(0xBC00).tobytes(), np.uint8)
-        W[144:148] = 0
+        W[bb:bb + 4] = 0
     else:
         W[208:210] = np.frombuffer(np.uint16(0xBC00).tobytes(), np.uint8)
         W[(K // 256) * 210 + 208:(K // 256) * 210 + 210] = 0
@@ -90,7 +91,8 @@ def test_kquant_qgemv_parity(af, wtype, N, K):
 
 
 @pytest.mark.parametrize("wtype,N,K", [("q4_k", 6144, 4096), ("q4_k", 28672, 4096), ("q4_k", 4096, 14336),
-                                       ("q4_k", 128256, 4096), ("q6_k", 128256, 4096), ("q6_k", 4096, 14336)])
+                                       ("q4_k", 128256, 4096), ("q6_k", 128256, 4096), ("q6_k", 4096, 14336),
+                                       ("q5_k", 28672, 4096), ("q5_k", 4096, 14336)])
 def test_kquant_qgemv_full_size_sampled_rows(af, wtype, N, K):
     W = synth.matrix(wtype, 81, synth.TID_TEST_BASE + 23, N, K)
     x = synth.normals(81, synth.TID_TEST_BASE + 24, K)

@@ -102,6 +102,13 @@ def test_q4_k_m_tiny(af, chunks, n_decode):
     run_parity(af, cfg, synth.kquant_seed_of(0), chunks, n_decode, 0)
 
 
+@pytest.mark.parametrize("chunks,n_decode", [([32], 16), ([13, 16, 3], 4)])
+def test_q5_k_m_tiny(af, chunks, n_decode):
+    """Q5_K layers and embedding with a Q6_K LM head, f16 cache."""
+    cfg = synth.KQUANT_CONFIGS[2]
+    run_parity(af, cfg, synth.kquant_seed_of(2), chunks, n_decode, 0)
+
+
 def test_q4_k_m_8b_shape_short_prompt(af):
     cfg = synth.KQUANT_CONFIGS[1]
     run_parity(af, cfg, synth.kquant_seed_of(1), [12, 5], 2, 12 + 5 + 2)

@@ -1,4 +1,4 @@
-"""Pins of the oracle's K-quant decoders (Q4_K, Q6_K super-blocks of 256 elements).
+"""Pins of the oracle's K-quant decoders (Q4_K, Q5_K, Q6_K super-blocks of 256 elements).
 
 The pages name these formats (Shimmy v2.0 Architecture, "Quantization": "Q4_K_M super-block with row scales",
 "Q6_K super-block, 6-bit"; the Airframe GPU pipeline's output head stored as Q6_K; dotLLM's Q4_K at about 4.5
@@ -81,6 +81,43 @@ def test_q4_k_nibble_locality(c, l):
     assert np.array_equal(v, want)
 
 
+# ---------------------------------------------------------------- Q5_K
+
+def _q5k_block(d, dmin, s, m, codes):
+    """One Q5_K block: Q4_K's header and nibble placement for the low 4 bits, the high bits in their plane."""
+    codes = np.asarray(codes, np.int64)
+    b4 = _q4k_block(d, dmin, s, m, codes & 15)
+    qh = np.zeros(32, np.int64)
+    for e in range(256):
+        c, r = e // 64, e % 64
+        qh[r % 32] += (codes[e] >> 4) << (2 * c + (1 if r >= 32 else 0))
+    return np.concatenate([b4[:16], qh.astype(np.uint8), b4[16:]])
+
+
+def test_q5_k_size_is_5_5_bits():
+    assert synth.BLOCK_BYTES["q5_k"] * 8 / 256 == 5.5
+    assert synth.matrix("q5_k", 1, synth.TID_TEST_BASE, 2, 512).nbytes == 2 * 2 * 176
+
+
+def test_q5_k_scales_mins_and_codes():
+    # codes 17 everywhere (nibble 1, high bit 1): value = 17 s_j - m_j with d = dmin = 1
+    v = oracle.dequant_row("q5_k", _q5k_block(ONE, ONE, S, M, [17] * 256), 256)
+    for j in range(8):
+        assert np.all(v[32 * j:32 * j + 32] == 17 * S[j] - M[j])
+
+
+@pytest.mark.parametrize("e", [0, 31, 32, 63, 64, 100, 150, 191, 192, 255])
+def test_q5_k_high_bit_locality(e):
+    # one element's high bit set (code 16): exactly that element changes (d = 1, dmin = 0, scales 1)
+    codes = [0] * 256
+    codes[e] = 16
+    blk = _q5k_block(ONE, ZERO, [1] * 8, [0] * 8, codes)
+    assert np.count_nonzero(blk[16:48]) == 1 and np.count_nonzero(blk[48:]) == 0
+    want = np.zeros(256)
+    want[e] = 16
+    assert np.array_equal(oracle.dequant_row("q5_k", blk, 256), want)
+
+
 # ---------------------------------------------------------------- Q6_K
 
 def _q6k_block(d, scales, q):
@@ -130,16 +167,19 @@ def _int_matrix_blocks(wtype, Wi):
             v = Wi[r, 256 * b:256 * b + 256]
             if wtype == "q4_k":
                 out.append(_q4k_block(ONE, ZERO, [1] * 8, [0] * 8, v))
+            elif wtype == "q5_k":
+                out.append(_q5k_block(ONE, ZERO, [1] * 8, [0] * 8, v))
             else:
                 out.append(_q6k_block(ONE, [1] * 16, v + 32))
     return np.concatenate(out)
 
 
-@pytest.mark.parametrize("wtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("wtype", ["q4_k", "q5_k", "q6_k"])
 @pytest.mark.parametrize("N,K,M", [(1, 256, 1), (3, 512, 2)])
 def test_kquant_qgemm_brute_force_integers(wtype, N, K, M):
     rng = np.random.default_rng(N * 10 + K + M)
-    Wi = rng.integers(0, 16, size=(N, K)) if wtype == "q4_k" else rng.integers(-32, 32, size=(N, K))
+    lim = {"q4_k": (0, 16), "q5_k": (0, 32), "q6_k": (-32, 32)}[wtype]
+    Wi = rng.integers(*lim, size=(N, K))
     X = rng.integers(-50, 51, size=(M, K)).astype(np.float64)
     blocks = _int_matrix_blocks(wtype, Wi)
     want = np.array([[sum(int(X[m, j]) * int(Wi[i, j]) for j in range(K)) for i in range(N)] for m in range(M)])
@@ -147,7 +187,7 @@ def test_kquant_qgemm_brute_force_integers(wtype, N, K, M):
     assert np.array_equal(oracle.qgemv(wtype, blocks, N, K, X[0]), want[0].astype(np.float64))
 
 
-@pytest.mark.parametrize("wtype", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("wtype", ["q4_k", "q5_k", "q6_k"])
 def test_kquant_encoder_decoder_roundtrip(wtype):
     # the generator's encoder and the oracle's decoder were written separately: each decoded element lies within
     # two quantisation steps of its source (half a step of code rounding plus the rounding of the 6- or 8-bit
@@ -161,14 +201,14 @@ def test_kquant_encoder_decoder_roundtrip(wtype):
         row = oracle.dequant_row(wtype, W[r * rb:(r + 1) * rb], K)
         for sb in range(K // 32):
             w = src[r, 32 * sb:32 * sb + 32]
-            if wtype == "q4_k":
-                step = (w.max() - min(0.0, w.min())) / 15
+            if wtype in ("q4_k", "q5_k"):
+                step = (w.max() - min(0.0, w.min())) / (15 if wtype == "q4_k" else 31)
             else:
                 step = np.max(np.abs(w)) / 32
             assert np.max(np.abs(row[32 * sb:32 * sb + 32] - w)) <= 2 * step + 1e-7, (r, sb)
         err.append(row - src[r])
     rel_rms = np.sqrt(np.mean(np.square(err))) / sigma
-    assert rel_rms < (0.15 if wtype == "q4_k" else 0.05)
+    assert rel_rms < {"q4_k": 0.15, "q5_k": 0.08, "q6_k": 0.05}[wtype]
 
 
 def test_kquant_layer_offsets_agree_with_generator():
@@ -176,9 +216,10 @@ def test_kquant_layer_offsets_agree_with_generator():
         assert oracle.layer_offsets(cfg) == synth.layer_offsets(cfg)
 
 
-def test_kquant_model_chunked_prefill_equals_unchunked():
-    cfg = synth.KQUANT_CONFIGS[0]
-    host = synth.HostModel(cfg, synth.kquant_seed_of(0))
+@pytest.mark.parametrize("idx", [0, 2])
+def test_kquant_model_chunked_prefill_equals_unchunked(idx):
+    cfg = synth.KQUANT_CONFIGS[idx]
+    host = synth.HostModel(cfg, synth.kquant_seed_of(idx))
     assert host.output.nbytes == cfg.n_vocab * (cfg.n_embd // 256) * 210  # the Q6_K head
     toks = host.prompt()
     lf, _ = oracle.Model.from_host(host).forward(toks, 0)
