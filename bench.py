@@ -20,6 +20,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -88,7 +89,8 @@ class ClockSampler:
         self.path = None
 
     def start(self):
-        out_dir = os.path.join(ROOT, "gpurun_out")
+        # raw samples in a temporary file (the summary goes into the JSON line); AF_CLOCKS_DIR keeps them
+        out_dir = os.environ.get("AF_CLOCKS_DIR") or tempfile.gettempdir()
         os.makedirs(out_dir, exist_ok=True)
         self.path = os.path.join(out_dir, f"clocks_bench_{os.getpid()}.csv")
         try:
