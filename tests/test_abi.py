@@ -121,6 +121,14 @@ def test_sampler_validation():
     assert L.af_sample(1, 10, None, 0, 1.0, 1.0, 1.0, -0.1, 1, None) == af.AF_ERANGE
 
 
+def test_model_sample_validation():
+    # host-side checks only: a null model and bad arguments return before any launch
+    af = pytest.importorskip("gguf_quantized_transformer_gb300")
+    L = af.lib()
+    assert L.af_model_sample(None, None, None, 0, 1.0, 0.8, 0.9, 0.5, None) == af.AF_EINVAL
+    assert "null model" in af.af_last_error()
+
+
 def test_static_attention_rejects_oversize():
     # host-side capacity checks of the fixed scratch; they return before any launch
     # (the pointers are never dereferenced on the host)
