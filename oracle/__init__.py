@@ -21,12 +21,14 @@ _lock = threading.Lock()
 _lib = None
 
 WTYPE_ID = {"q8_0": 8, "q4_0": 2, "q4_k": 12, "q5_k": 13, "q6_k": 14}
+KV_ID = {"f32": 0, "f16": 1, "q8_0": 2, "q4_0": 3}
 
 
 class OrcConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n_layers", "n_embd", "n_heads", "n_kv_heads", "head_dim", "n_ff",
                                                "n_vocab", "wtype", "kv_f16", "max_ctx", "native_ctx")] + \
-               [("rms_eps", ctypes.c_double), ("rope_base", ctypes.c_double), ("out_wtype", ctypes.c_int32)]
+               [("rms_eps", ctypes.c_double), ("rope_base", ctypes.c_double), ("out_wtype", ctypes.c_int32),
+                ("kv_window", ctypes.c_int32)]
 
 
 def build(force: bool = False) -> str:
@@ -84,6 +86,7 @@ def lib():
             L.orc_sample.restype = i64
             L.orc_sample_interval.argtypes = [vp, i64, vp, i64, dbl, dbl, dbl, i64, vp, vp, vp, vp]
             L.orc_argmax.restype = i64
+            L.orc_quant_kv_row.argtypes = [i32, vp, i64]
             _lib = L
     return _lib
 
@@ -102,6 +105,14 @@ def f16_to_double(bits: int) -> float:
 
 def round_f16(x: float) -> float:
     return lib().orc_round_f16(x)
+
+
+def quant_kv_row(kv_dtype: str, v) -> np.ndarray:
+    """A quantized cache's Q8_0 / Q4_0 replacement of one row of fp16 values."""
+    out = np.array(v, dtype=np.float64)
+    if lib().orc_quant_kv_row(KV_ID[kv_dtype], _p(out), out.size):
+        raise ValueError("bad kv dtype or row length")
+    return out
 
 
 def dequant_row(wtype: str, blocks: np.ndarray, k: int) -> np.ndarray:
@@ -211,8 +222,9 @@ def argmax(v) -> int:
 def config_of(cfg) -> OrcConfig:
     """OrcConfig from a synth.ModelConfig-like object."""
     return OrcConfig(cfg.n_layers, cfg.n_embd, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.n_ff, cfg.n_vocab,
-                     WTYPE_ID[cfg.wtype], 1 if cfg.kv_dtype == "f16" else 0, cfg.max_ctx, cfg.native_ctx,
-                     cfg.rms_eps, cfg.rope_base, WTYPE_ID[getattr(cfg, "out_wtype", "") or cfg.wtype])
+                     WTYPE_ID[cfg.wtype], KV_ID[cfg.kv_dtype], cfg.max_ctx, cfg.native_ctx,
+                     cfg.rms_eps, cfg.rope_base, WTYPE_ID[getattr(cfg, "out_wtype", "") or cfg.wtype],
+                     getattr(cfg, "kv_window", 0))
 
 
 def layer_offsets(cfg):

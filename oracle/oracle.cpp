@@ -264,6 +264,56 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
+// ---- quantized KV cache ---------------------------------------------------
+// dotLLM, "CUDA components": a quantized KV cache, "Q8_0/Q4_0 + FP16 window".  The pages name the parts only.
+// Reading: a slot is written in fp16; once it lies outside the step's window (slot <= b - W, b = the step's
+// last position, W = kv_window) it is replaced by the Q8_0 / Q4_0 quantization of its fp16 values, per
+// 32-element block along head_dim.  The quantizer takes its decisions in fp32 on those fp16 values:
+//   Q8_0: d = fp16(max|v| / 127), q = clamp(round-half-away(v / d), -127, 127)  (floor(r + 0.5) in fp32), v' = d q
+//   Q4_0: m = the element of largest |v| (first on ties), d = fp16(m / -8),
+//         n = clamp(floor(v / d + 8.5), 0, 15), v' = d (n - 8)
+// (a zero scale gives zero values).  Every query of the step sees the same representation of a slot.
+enum { KV_F32 = 0, KV_F16 = 1, KV_Q8_0 = 2, KV_Q4_0 = 3 };
+
+void quant_kv_row(int32_t kvt, double* v, int64_t D) {
+    for (int64_t b0 = 0; b0 < D; b0 += 32) {
+        float x[32];
+        for (int j = 0; j < 32; j++) x[j] = (float)v[b0 + j];  // fp16 values: exact in fp32
+        if (kvt == KV_Q8_0) {
+            float amax = 0.f;
+            for (int j = 0; j < 32; j++) amax = std::fmax(amax, std::fabs(x[j]));
+            const double d = round_f16((double)(amax / 127.f));
+            const float df = (float)d;
+            for (int j = 0; j < 32; j++) {
+                int q = 0;
+                if (df != 0.f) {
+                    const float r = x[j] / df;
+                    q = (int)(r >= 0.f ? std::floor(r + 0.5f) : -std::floor(-r + 0.5f));
+                    q = q < -127 ? -127 : (q > 127 ? 127 : q);
+                }
+                v[b0 + j] = d * (double)q;
+            }
+        } else {
+            float mx = 0.f, amax = 0.f;
+            for (int j = 0; j < 32; j++)
+                if (std::fabs(x[j]) > amax) {
+                    amax = std::fabs(x[j]);
+                    mx = x[j];
+                }
+            const double d = round_f16((double)(mx / -8.f));
+            const float df = (float)d;
+            for (int j = 0; j < 32; j++) {
+                int q = 8;
+                if (df != 0.f) {
+                    q = (int)std::floor(x[j] / df + 8.5f);
+                    q = q < 0 ? 0 : (q > 15 ? 15 : q);
+                }
+                v[b0 + j] = d * (double)(q - 8);
+            }
+        }
+    }
+}
+
 struct orc_model {
     orc_config c;
     std::vector<const uint8_t*> layers;
@@ -273,6 +323,7 @@ struct orc_model {
     uint64_t off[10];
     int64_t slots;
     std::vector<double> kcache, vcache;  // [L][KVH][slots][D], values rounded to the cache dtype
+    int64_t kv_quantized = 0;            // quantized KV: slots [0, kv_quantized) hold their quantized values
     double ys;
 };
 
@@ -281,6 +332,12 @@ extern "C" {
 double orc_f16_to_double(uint16_t h) { return f16_to_double(h); }
 double orc_round_f16(double x) { return round_f16(x); }
 double orc_round_f32(double x) { return round_f32(x); }
+
+int orc_quant_kv_row(int32_t kv_dtype, double* v, int64_t D) {
+    if ((kv_dtype != KV_Q8_0 && kv_dtype != KV_Q4_0) || D % 32) return -1;
+    quant_kv_row(kv_dtype, v, D);
+    return 0;
+}
 
 int orc_dequant_row(int32_t wtype, const uint8_t* blocks, int64_t k, double* out) {
     if (!block_bytes(wtype) || k % block_elems(wtype)) return -1;
@@ -348,7 +405,11 @@ int orc_layer_offsets(const orc_config* c, uint64_t off[10]) {
 
 // Airframe GPU_PIPELINE.md, "KV cache": L * KVH * max_ctx * head_dim * elem, times 2 (K and V).
 uint64_t orc_kv_bytes(const orc_config* c) {
-    return (uint64_t)c->n_layers * c->n_kv_heads * c->max_ctx * c->head_dim * (c->kv_f16 ? 2 : 4) * 2;
+    const uint64_t rows = (uint64_t)c->n_layers * c->n_kv_heads * 2;  // K and V
+    if (c->kv_f16 == KV_Q8_0 || c->kv_f16 == KV_Q4_0)  // quantized store of every slot + fp16 window of kv_window slots
+        return rows * ((uint64_t)c->max_ctx * (c->head_dim / 32) * (c->kv_f16 == KV_Q8_0 ? 34 : 18) +
+                       (uint64_t)c->kv_window * c->head_dim * 2);
+    return rows * c->max_ctx * c->head_dim * (c->kv_f16 ? 2 : 4);
 }
 
 orc_model* orc_model_create(const orc_config* c, const uint8_t* const* layer_blobs, const uint8_t* token_embd,
@@ -521,6 +582,8 @@ int orc_forward(orc_model* m, const int32_t* tokens, int64_t n, int64_t start_po
     const int64_t E = c.n_embd, H = c.n_heads, KVH = c.n_kv_heads, D = c.head_dim, F = c.n_ff;
     const int64_t QD = H * D, KVD = KVH * D;
     const int32_t head_wtype = c.out_wtype ? c.out_wtype : c.wtype;
+    const bool quantized_kv = c.kv_f16 == KV_Q8_0 || c.kv_f16 == KV_Q4_0;
+    const int64_t retire_to = start_pos + n - 1 - c.kv_window;  // last slot outside this step's window
 
     std::vector<double> X(n * E), Y(n * E), Q(n * QD), K(n * KVD), V(n * KVD), A(n * QD), O(n * E);
     std::vector<double> G(n * F), U(n * F), Hh(n * F);
@@ -556,8 +619,15 @@ int orc_forward(orc_model* m, const int32_t* tokens, int64_t n, int64_t start_po
                 for (int64_t d = 0; d < D; d++) {
                     size_t idx = (((size_t)l * KVH + g) * m->slots + start_pos + r) * D + d;
                     double kv = K[r * KVD + g * D + d], vv = V[r * KVD + g * D + d];
-                    m->kcache[idx] = c.kv_f16 ? round_f16(kv) : round_f32(kv);
+                    m->kcache[idx] = c.kv_f16 ? round_f16(kv) : round_f32(kv);  // quantized caches: fp16 first
                     m->vcache[idx] = c.kv_f16 ? round_f16(vv) : round_f32(vv);
+                }
+        if (quantized_kv)  // slots that left this step's window take their quantized values
+            for (int64_t sl = m->kv_quantized; sl <= retire_to; sl++)
+                for (int64_t g = 0; g < KVH; g++) {
+                    const size_t row = (((size_t)l * KVH + g) * m->slots + sl) * D;
+                    quant_kv_row(c.kv_f16, &m->kcache[row], D);
+                    quant_kv_row(c.kv_f16, &m->vcache[row], D);
                 }
         const double* kc = &m->kcache[(size_t)l * KVH * m->slots * D];
         const double* vc = &m->vcache[(size_t)l * KVH * m->slots * D];
@@ -582,6 +652,7 @@ int orc_forward(orc_model* m, const int32_t* tokens, int64_t n, int64_t start_po
         rmsnorm(&X[(n - 1) * E], m->output_norm, E, c.rms_eps, last.data());
         qgemm(head_wtype, m->output, c.n_vocab, E, last.data(), 1, logits, n_threads);
     }
+    if (quantized_kv && retire_to + 1 > m->kv_quantized) m->kv_quantized = retire_to + 1;
     return 0;
 }
 

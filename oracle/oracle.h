@@ -41,10 +41,11 @@ enum { ORC_Q4_0 = 2, ORC_Q8_0 = 8, ORC_Q4_K = 12, ORC_Q5_K = 13, ORC_Q6_K = 14 }
 typedef struct orc_config {
     int32_t n_layers, n_embd, n_heads, n_kv_heads, head_dim, n_ff, n_vocab;
     int32_t wtype;      /* ORC_Q8_0 | ORC_Q4_0 | ORC_Q4_K | ORC_Q5_K | ORC_Q6_K: layer matrices and token_embd */
-    int32_t kv_f16;     /* 0: f32 cache, 1: f16 cache */
+    int32_t kv_f16;     /* 0: f32 cache, 1: f16 cache, 2: Q8_0, 3: Q4_0 (quantized, with an fp16 window) */
     int32_t max_ctx, native_ctx;
     double rms_eps, rope_base;
     int32_t out_wtype;  /* block type of the LM head (0 = wtype) */
+    int32_t kv_window;  /* quantized caches: slots within this many positions of a step's last one stay fp16 */
 } orc_config;
 
 typedef struct orc_model orc_model;
@@ -59,6 +60,10 @@ double orc_round_f32(double x);
 /* Decode k elements (a whole number of blocks: 32 elements, 256 for Q4_K / Q6_K) of GGUF blocks into exact
  * doubles. */
 int orc_dequant_row(int32_t wtype, const uint8_t* blocks, int64_t k, double* out);
+
+/* A quantized cache's replacement of one K or V row (D % 32 == 0, fp16 values) by its Q8_0 (kv_dtype 2) or Q4_0
+ * (3) quantization, in place (see the quantized KV reading in oracle.cpp). */
+int orc_quant_kv_row(int32_t kv_dtype, double* v, int64_t D);
 
 /* y[i] = sum_j W[i][j] x[j] for the n rows of W (k columns, GGUF blocks). */
 int orc_qgemv(int32_t wtype, const uint8_t* W, int64_t n, int64_t k, const double* x, double* y, int n_threads);

@@ -29,7 +29,7 @@ class ModelConfig:
     n_ff: int
     n_vocab: int
     wtype: str          # "q8_0" | "q4_0" | "q4_k" | "q5_k" | "q6_k": every layer matrix and token_embd
-    kv_dtype: str       # "f32" | "f16"
+    kv_dtype: str       # "f32" | "f16" (and, for the oracle, "q8_0" | "q4_0": quantized with an fp16 window)
     max_ctx: int
     native_ctx: int     # == max_ctx means no YaRN scaling
     rope_base: float
@@ -41,6 +41,7 @@ class ModelConfig:
     w_sigma: float = 0.02
     norm_sigma: float = 0.1
     out_wtype: str = ""  # the LM head's block type ("" = wtype)
+    kv_window: int = 0   # quantized caches: slots kept fp16 behind a step's last position
 
     @property
     def head_wtype(self) -> str:
