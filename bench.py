@@ -419,26 +419,34 @@ def kquant_run(af, args, dev, hbm_peak, steps=2, warmup=1):
     pre_s = sum(e[0].elapsed_time(e[1]) for e in evs) / 1000
     dec_s = sum(e[1].elapsed_time(e[2]) for e in evs) / 1000
     m.close()
+    del m
+    torch.cuda.empty_cache()
+    gu = qgemv_roofline(af, cfg, dev, hbm_peak)
+    head = qgemv_roofline(af, cfg, dev, hbm_peak, wtype=cfg.head_wtype, shape=(cfg.n_vocab, cfg.n_embd),
+                          label="LM head")
     dec_gbs = sum(decode_bytes_per_token(cfg, P + i) for i in range(ND)) * steps / dec_s / 1e9
     return {"workload": f"{cfg.name}: {P}-token prompt in {C}-token chunks + {ND} greedy decode steps, "
                         f"KV {cfg.kv_dtype} max_ctx {cfg.max_ctx}", "weights": f"{cfg.wtype} + {cfg.head_wtype} head",
             "steps": steps, "warmup": warmup, "decode_tok_s": ND * steps / dec_s, "prefill_tok_s": P * steps / pre_s,
             "decode_hbm_gbs": dec_gbs, "decode_hbm_frac": dec_gbs / hbm_peak,
-            "prefill_tflops": prefill_flops(cfg, P, C)[0] * steps / pre_s / 1e12}
+            "prefill_tflops": prefill_flops(cfg, P, C)[0] * steps / pre_s / 1e12,
+            "gemv_rooflines": [gu, head]}
 
 
-def qgemv_roofline(af, cfg, dev, hbm_peak, reps=20, copies=8):
-    """af_qgemv on the model's gate|up shape [2F, E]: algorithmic bytes / CUDA-event time per launch.
+def qgemv_roofline(af, cfg, dev, hbm_peak, reps=20, copies=8, wtype=None, shape=None, label="gate|up"):
+    """af_qgemv on the model's gate|up shape [2F, E] (or `shape` in `wtype`): algorithmic bytes / CUDA-event time
+    per launch.
 
     As in the decode step: a CUDA graph of `copies` back-to-back launches (programmatic dependent launch), each
     over its own copy of the weights (copies x 66 MB, far larger than L2, so no launch finds its weights in L2),
     replayed `reps` times on the launching stream.  A single launch after an L2 flush is reported beside it
     (cold: it also pays the launch and ramp that back-to-back launches overlap)."""
     import torch
-    N, K = 2 * cfg.n_ff, cfg.n_embd
-    W = synth.matrix(cfg.wtype, 7, synth.TID_TEST_BASE + 99, N, K)
+    wt = wtype or cfg.wtype
+    N, K = shape or (2 * cfg.n_ff, cfg.n_embd)
+    W = synth.matrix(wt, 7, synth.TID_TEST_BASE + 99, N, K)
     Wd = torch.from_numpy(W).to(dev)
-    hs = [af.af_qweight_create(af.WTYPE[cfg.wtype], Wd, N, K) for _ in range(copies)]
+    hs = [af.af_qweight_create(af.WTYPE[wt], Wd, N, K) for _ in range(copies)]
     del Wd
     x = torch.randn(K, device=dev)
     y = torch.empty(N, device=dev)
@@ -475,13 +483,13 @@ def qgemv_roofline(af, cfg, dev, hbm_peak, reps=20, copies=8):
             cold.append(e0.elapsed_time(e1))
     for h in hs:
         af.af_qweight_destroy(h)
-    bpe = synth.BLOCK_BYTES[cfg.wtype] / synth.BLOCK_ELEMS[cfg.wtype]
+    bpe = synth.BLOCK_BYTES[wt] / synth.BLOCK_ELEMS[wt]
     nbytes = N * K * bpe + K * 4 + N * 4
     gbs = nbytes / (ms / 1000) / 1e9
     cold_ms = float(np.mean(cold))
     return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-            "traffic": gemv_traffic(cfg.wtype, N, K),
-            "kernel": f"qgemv {cfg.wtype} [{N}x{K}] gate|up: graph of {copies} back-to-back launches over "
+            "traffic": gemv_traffic(wt, N, K),
+            "kernel": f"qgemv {wt} [{N}x{K}] {label}: graph of {copies} back-to-back launches over "
                       f"{copies} weight copies ({copies * N * K * bpe / 1e6:.0f} MB > L2)",
             "bytes_per_launch": nbytes, "us_per_launch": ms * 1000,
             "cold_us_per_launch": cold_ms * 1000, "cold_frac": nbytes / (cold_ms / 1000) / 1e9 / hbm_peak}
