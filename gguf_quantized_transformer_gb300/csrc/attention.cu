@@ -9,6 +9,9 @@
 // memory, pass 2 exponentiates against the CTA maximum and accumulates P V.
 // Each CTA stores (o, max, sum) for its range; the last CTA of a kv head to
 // finish (acq_rel counter) merges the splits with the usual max-rescaling.
+// For caches of up to kC * kClMaxSplit slots the kC splits of a kv head form a
+// thread-block cluster instead and merge through distributed shared memory
+// (attn_decode_kernel's CL path).
 //
 // Prefill attention runs on the tensor cores (attn_prefill_tc.cu).
 #include <math_constants.h>
