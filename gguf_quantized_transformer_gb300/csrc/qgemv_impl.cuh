@@ -1,4 +1,4 @@
-// Decode GEMV: y = W x over repacked Q4_0 / Q8_0 planes, with an optional
+// Decode GEMV: y = W x over repacked Q4_0 / Q8_0 / Q4_K / Q5_K / Q6_K rows, with an optional
 // RMSNorm prologue and a fused epilogue (Airframe "GPU_PIPELINE.md" per-layer
 // ops: dequantization happens inside the matmul, no separate dequantize pass;
 // decode is bound by reading the weights, "Decode loop").
@@ -29,8 +29,11 @@
 //         sum_j n_j xi_j = (4096 A + 256 C + 16 B + D) / 16 over the byte planes,
 //         sum_j (n_j - 8) x_j = s * that - 8 s sum_j xi_j
 //   Q8_0: code q in -127..127, sum_j q_j x_j = s * (256 A + B)
+//   Q4_K / Q5_K / Q6_K: 4-, 5- or 6-bit codes (nibble, or nibble | high bits << 4)
+//         per 32-weight unit, with the sub-block scale (and min) from the row's
+//         super-block record applied in fp32 (the Unit specializations below)
 // accumulated exactly in int32 per unit; the unit value times the block's
-// fp16 scale d is accumulated in fp32 per row.  Row partials are reduced over
+// scale is accumulated in fp32 per row.  Row partials are reduced over
 // the lanes with a transpose-reduce; with WK > 1 the WK partials of a row are
 // summed in a fixed order (deterministic) by the last warp of the stage.
 //
