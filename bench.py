@@ -31,8 +31,8 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up GEMV launch, Q4_0 28672 x 4096, from the
-# ncu capture summarised in profiles/qgemv_q4_0_28672x4096.md; valid only for the kernel sources it was taken on.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gate/up GEMV launch, Q4_0 28672 x 4096, from one
+# ncu capture of the kernel built from these sources (identified by their hash); reported only while they match.
 GEMV_SOURCES = ["qgemv_impl.cuh", "qgemv_q4_0.cu", "gemv_common.cuh", "tma.cuh", "common.cuh"]
 GEMV_TRAFFIC = {"sources_sha256_16": "dc018336c89c5737", "wtype": "q4_0", "N": 28672, "K": 4096, "bytes": 66131456}
 FALLBACK_HBM_GBS = 6800.0
@@ -180,6 +180,34 @@ def oracle_sample(hm, cfg, n_decode, threads):
     return n_decode / dt, dt
 
 
+def oracle_timing(hm, cfg, threads, n_prefill, n_decode):
+    """The oracle on `threads` host threads: an n_prefill-token prefill chunk at position 0, then n_decode decode
+    steps.  Returns a cpu-baseline record with both rates."""
+    import oracle
+    om = oracle.Model.from_host(hm, kv_slots=n_prefill + n_decode + 1)
+    prompt = hm.prompt(n_prefill)
+    t0 = time.perf_counter()
+    logits, _ = om.forward(prompt, 0, nthreads=threads)
+    t1 = time.perf_counter()
+    tok = oracle.argmax(logits)
+    for i in range(n_decode):
+        logits, _ = om.forward([tok], n_prefill + i, nthreads=threads)
+        tok = oracle.argmax(logits)
+    t2 = time.perf_counter()
+    return {"threads": threads, "prefill_tok_s": n_prefill / (t1 - t0), "decode_tok_s": n_decode / (t2 - t1),
+            "sample": f"{n_prefill}-token prefill chunk then {n_decode} decode steps ({t2 - t0:.1f} s, fp64)"}
+
+
+def oracle_baselines(hm, cfg):
+    """Per-config CPU baseline: all host threads on a 4-token chunk + 2 decode steps; one thread as well where the
+    model is small enough for that to take seconds (the full 64-token chunk would take minutes per config)."""
+    T = os.cpu_count() or 1
+    out = {"threaded": oracle_timing(hm, cfg, T, 4, 2)}
+    if decode_bytes_per_token(cfg, 0) < 1.5e9:  # up to ~1.5 G weights: a few seconds single-threaded
+        out["single_thread"] = oracle_timing(hm, cfg, 1, 2, 1)
+    return out
+
+
 def run_reference(args, cfg, world, rank):
     """The reference arm: the CPU oracle on the host cores, bounded sample per step."""
     if rank != 0:
@@ -303,7 +331,9 @@ def run_ours(args, cfg, world, rank, local):
     torch.cuda.empty_cache()
 
     # the same workload on the 8B shape in the Q4_K_M mix (Q4_K layers, Q6_K LM head): a secondary line
-    kq = None if args.no_kquant else kquant_run(af, args, dev, hbm_peak)
+    tc_peak = bf16_sust or bf16_peak
+    kq = None if args.no_kquant else kquant_run(af, args, dev, hbm_peak, tc_peak)
+    others = config_runs(af, args, dev, hbm_peak, tc_peak)
 
     launches_per_step = (P + C - 1) // C * (1 + 7 * cfg.n_layers) + 3 + ND * (3 + 5 * cfg.n_layers + 1)
 
@@ -324,6 +354,7 @@ def run_ours(args, cfg, world, rank, local):
         "sampler_us": samp_us,
         "decode_sampled_tok_s": sampled_tps,
         "q4_k_m": kq,
+        "configs": others,
         "roofline": dict(qg, peak_source=peak_src),
         "decode_step_roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
                                  "frac": dec_gbs / hbm_peak, "traffic": None,
@@ -340,7 +371,10 @@ def run_ours(args, cfg, world, rank, local):
         v, dt = oracle_sample(hm, cfg, args.ref_decode, threads)
         line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "cpu": cpu_name(),
                                 "sample": f"{args.ref_decode} decode steps after a 4-token prefill "
-                                          f"({dt:.1f} s, fp64, {threads} threads)"}
+                                          f"({dt:.1f} s, fp64, {threads} threads)",
+                                "per_config": {f"config{args.config}": oracle_baselines(hm, cfg),
+                                               **{k: v.get("cpu_baseline") for k, v in others.items()
+                                                  if isinstance(v, dict)}}}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -385,18 +419,16 @@ def cpu_name():
     return f"{platform.machine()} {name}".strip()
 
 
-def kquant_run(af, args, dev, hbm_peak, steps=2, warmup=1):
-    """Prefill + greedy decode of the 8B shape with Q4_K layers and a Q6_K head, timed like the main line."""
+def workload_run(af, cfg, seed, P, ND, C, dev, hbm_peak, tc_peak, steps=2, warmup=1, cpu=False):
+    """Prefill of a P-token prompt in C-token chunks + ND greedy decode steps of one synthetic model, timed like the
+    headline line (CUDA events on the model stream, inputs resident).  Returns the model's throughput keys."""
     import torch
-    cfg = synth.KQUANT_CONFIGS[1]
-    hm = synth.HostModel(cfg, synth.kquant_seed_of(1))
+    hm = synth.HostModel(cfg, seed)
     m = af.Model(cfg, [torch.from_numpy(b).to(dev) for b in hm.layers], torch.from_numpy(hm.token_embd).to(dev),
-                 torch.from_numpy(hm.output_norm).to(dev), torch.from_numpy(hm.output).to(dev),
-                 max_chunk=args.chunk)
+                 torch.from_numpy(hm.output_norm).to(dev), torch.from_numpy(hm.output).to(dev), max_chunk=C)
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     stream = torch.cuda.ExternalStream(af.af_model_stream(m.h))
-    P, ND, C = args.prompt, args.decode, args.chunk
     prompt_dev = torch.from_numpy(hm.prompt(P)).to(dev)
     logits = torch.empty(cfg.n_vocab, dtype=torch.float32, device=dev)
 
@@ -421,16 +453,90 @@ def kquant_run(af, args, dev, hbm_peak, steps=2, warmup=1):
     m.close()
     del m
     torch.cuda.empty_cache()
+    dec_gbs = sum(decode_bytes_per_token(cfg, P + i) for i in range(ND)) * steps / dec_s / 1e9
+    pf_tflops = prefill_flops(cfg, P, C)[0] * steps / pre_s / 1e12
+    cpu_line = oracle_baselines(hm, cfg) if cpu else None
+    del hm
+    return {"cpu_baseline": cpu_line, "workload": f"{cfg.name}: {P}-token prompt in {C}-token chunks + {ND} greedy decode steps "
+                        f"from position {P}, KV {cfg.kv_dtype} max_ctx {cfg.max_ctx}",
+            "weights": cfg.wtype + (f" + {cfg.head_wtype} head" if cfg.head_wtype != cfg.wtype else ""),
+            "seed": seed, "steps": steps, "warmup": warmup,
+            "decode_tok_s": ND * steps / dec_s, "prefill_tok_s": P * steps / pre_s,
+            "decode_hbm_gbs": dec_gbs, "decode_hbm_frac": dec_gbs / hbm_peak,
+            "prefill_tflops": pf_tflops, "prefill_tc_frac": pf_tflops / tc_peak}
+
+
+def kquant_run(af, args, dev, hbm_peak, tc_peak, steps=2, warmup=1):
+    """Prefill + greedy decode of the 8B shape with Q4_K layers and a Q6_K head, timed like the main line."""
+    cfg = synth.KQUANT_CONFIGS[1]
+    out = workload_run(af, cfg, synth.kquant_seed_of(1), args.prompt, args.decode, args.chunk, dev, hbm_peak,
+                       tc_peak, steps, warmup)
     gu = qgemv_roofline(af, cfg, dev, hbm_peak)
     head = qgemv_roofline(af, cfg, dev, hbm_peak, wtype=cfg.head_wtype, shape=(cfg.n_vocab, cfg.n_embd),
                           label="LM head")
-    dec_gbs = sum(decode_bytes_per_token(cfg, P + i) for i in range(ND)) * steps / dec_s / 1e9
-    return {"workload": f"{cfg.name}: {P}-token prompt in {C}-token chunks + {ND} greedy decode steps, "
-                        f"KV {cfg.kv_dtype} max_ctx {cfg.max_ctx}", "weights": f"{cfg.wtype} + {cfg.head_wtype} head",
-            "steps": steps, "warmup": warmup, "decode_tok_s": ND * steps / dec_s, "prefill_tok_s": P * steps / pre_s,
-            "decode_hbm_gbs": dec_gbs, "decode_hbm_frac": dec_gbs / hbm_peak,
-            "prefill_tflops": prefill_flops(cfg, P, C)[0] * steps / pre_s / 1e12,
-            "gemv_rooflines": [gu, head]}
+    out["gemv_rooflines"] = [gu, head]
+    return out
+
+
+def config_runs(af, args, dev, hbm_peak, tc_peak):
+    """Every other full-size config over its own workload (the headline config is the main line)."""
+    out = {}
+    for idx in [int(x) for x in args.configs.split(",") if x.strip()]:
+        if idx == args.config:
+            continue
+        cfg = synth.CONFIGS[idx]
+        try:
+            line = workload_run(af, cfg, synth.seed_of(idx), cfg.prompt_len, cfg.n_decode, cfg.chunk, dev, hbm_peak,
+                                tc_peak, steps=1, warmup=1, cpu=args.rank == 0 and not args.no_cpu_baseline)
+            if cfg.max_ctx > 8192:  # long context: decode attention is half the bytes of a token; its roofline
+                line["attn_roofline"] = attn_roofline(af, cfg, cfg.prompt_len, dev, hbm_peak)
+            out[f"config{idx}"] = line
+        except Exception as e:  # a failed secondary line must not take the headline with it
+            out[f"config{idx}"] = {"error": f"{type(e).__name__}: {e}"}
+    return out
+
+
+def attn_roofline(af, cfg, pos, dev, hbm_peak, copies=4, reps=10):
+    """Decode attention of one layer at position pos (the config's KV shape and dtype): algorithmic bytes
+    2 * KVH * D * (pos + 1) * elem per launch over CUDA-event time, from a CUDA graph of `copies` back-to-back launches
+    of af_attention_decode_static over `copies` separate caches (each larger than L2)."""
+    import torch
+    H, KVH, D, ctx = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.max_ctx
+    dt = torch.float16 if cfg.kv_dtype == "f16" else torch.float32
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    caches = [(torch.randn(KVH, ctx, D, device=dev, generator=g).to(dt),
+               torch.randn(KVH, ctx, D, device=dev, generator=g).to(dt)) for _ in range(copies)]
+    q = torch.randn(H * D, device=dev, generator=g)
+    out = torch.empty(H * D, device=dev)
+    kvt = af.KVTYPE[cfg.kv_dtype]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for k, v in caches:  # first call per device: address lookup, outside capture
+            af.af_attention_decode_static(q, k, v, kvt, H, KVH, D, ctx, pos, out, s)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s), torch.cuda.graph(gr, stream=s):
+        for k, v in caches:
+            af.af_attention_decode_static(q, k, v, kvt, H, KVH, D, ctx, pos, out, s)
+    gr.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        a.record(s)
+        for _ in range(reps):
+            gr.replay()
+        b.record(s)
+    b.synchronize()
+    ms = a.elapsed_time(b) / (reps * copies)
+    nbytes = 2 * KVH * D * (pos + 1) * (2 if cfg.kv_dtype == "f16" else 4)
+    gbs = nbytes / (ms / 1000) / 1e9
+    del caches
+    torch.cuda.empty_cache()
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+            "traffic": None, "kernel": f"decode attention {H}/{KVH}x{D} {cfg.kv_dtype} at position {pos}: graph of "
+                                       f"{copies} back-to-back launches over {copies} caches",
+            "bytes_per_launch": nbytes, "us_per_launch": ms * 1000}
 
 
 def qgemv_roofline(af, cfg, dev, hbm_peak, reps=20, copies=8, wtype=None, shape=None, label="gate|up"):
@@ -487,8 +593,12 @@ def qgemv_roofline(af, cfg, dev, hbm_peak, reps=20, copies=8, wtype=None, shape=
     nbytes = N * K * bpe + K * 4 + N * 4
     gbs = nbytes / (ms / 1000) / 1e9
     cold_ms = float(np.mean(cold))
+    traffic = gemv_traffic(wt, N, K)
     return {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-            "traffic": gemv_traffic(wt, N, K),
+            "traffic": traffic,
+            "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, captured on the "
+                               "same kernel sources (hash " + GEMV_TRAFFIC["sources_sha256_16"] + ")")
+            if traffic else "not captured for these sources",
             "kernel": f"qgemv {wt} [{N}x{K}] {label}: graph of {copies} back-to-back launches over "
                       f"{copies} weight copies ({copies * N * K * bpe / 1e6:.0f} MB > L2)",
             "bytes_per_launch": nbytes, "us_per_launch": ms * 1000,
@@ -570,11 +680,13 @@ def main():
     ap.add_argument("--ref-decode", type=int, default=2, help="oracle decode steps per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kquant", action="store_true", help="skip the secondary Q4_K_M line")
+    ap.add_argument("--configs", default="1,2,4", help="other configs to run over their own workloads ('' = none)")
     args = ap.parse_args()
     cfg = synth.CONFIGS[args.config]
     args.prompt = args.prompt or cfg.prompt_len
     args.decode = args.decode or cfg.n_decode
     world, rank, local = dist_setup()
+    args.rank = rank
     if args.impl == "reference":
         run_reference(args, cfg, world, rank)
     else:

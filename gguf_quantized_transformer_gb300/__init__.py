@@ -78,6 +78,10 @@ def lib():
         L.af_qweight_destroy.restype = None
         L.af_attention_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
         L.af_attention_decode_static.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+        L.af_attention_prefill.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
+        L.af_debug_stall.argtypes = [vp, ctypes.c_uint32]
+        L.af_qweight_status.argtypes = [vp, vp]
+        L.af_qweight_debug_stall.argtypes = [vp, ctypes.c_uint32, vp]
         f32 = ctypes.c_float
         L.af_sample.argtypes = [vp, i32, vp, i32, f32, f32, f32, f32, vp, vp]
         L.af_model_sample.argtypes = [vp, vp, vp, i32, f32, f32, f32, f32, vp]
@@ -218,6 +222,18 @@ def af_qweight_destroy(w):
     lib().af_qweight_destroy(w)
 
 
+def af_qweight_status(w, stream=None):
+    return check(lib().af_qweight_status(w, _stream(stream)))
+
+
+def af_qweight_debug_stall(w, polls: int, stream=None):
+    return check(lib().af_qweight_debug_stall(w, polls, _stream(stream)))
+
+
+def af_debug_stall(m, polls: int):
+    return check(lib().af_debug_stall(m, polls))
+
+
 def af_attention_decode(q_dev, k_dev, v_dev, kv_dtype: int, n_heads: int, n_kv_heads: int, head_dim: int, ctx: int,
                         pos: int, out_dev, stream=None):
     return check(lib().af_attention_decode(_ptr(q_dev), _ptr(k_dev), _ptr(v_dev), kv_dtype, n_heads, n_kv_heads,
@@ -228,6 +244,12 @@ def af_attention_decode_static(q_dev, k_dev, v_dev, kv_dtype: int, n_heads: int,
                                ctx: int, pos: int, out_dev, stream=None):
     return check(lib().af_attention_decode_static(_ptr(q_dev), _ptr(k_dev), _ptr(v_dev), kv_dtype, n_heads,
                                                   n_kv_heads, head_dim, ctx, pos, _ptr(out_dev), _stream(stream)))
+
+
+def af_attention_prefill(q_dev, k_dev, v_dev, kv_dtype: int, n_heads: int, n_kv_heads: int, head_dim: int, ctx: int,
+                         start_pos: int, n: int, out_dev, stream=None):
+    return check(lib().af_attention_prefill(_ptr(q_dev), _ptr(k_dev), _ptr(v_dev), kv_dtype, n_heads, n_kv_heads,
+                                            head_dim, ctx, start_pos, n, _ptr(out_dev), _stream(stream)))
 
 
 def af_sample(logits_dev, n_vocab: int, recent_dev, n_recent: int, repeat_penalty: float, temperature: float,

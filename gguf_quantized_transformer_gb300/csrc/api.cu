@@ -175,6 +175,8 @@ struct af_model {
     __half* a16[2] = {};     // [chunk][H*D] attention output, fp16 hi / lo
     __half* h16[2] = {};     // [chunk][F] SwiGLU output, fp16 hi / lo
     int* tok = nullptr;      // [chunk]
+    int* tok_host = nullptr;  // [chunk] page-locked staging of af_prefill's token ids
+    cudaEvent_t tok_ev = nullptr;  // the copy out of tok_host has completed
     float* logits = nullptr; // [V] default logits
     GemvScratch gs;
     AttnScratch as;
@@ -212,6 +214,22 @@ Epi epi_qkv_plan(af_model* m, int l) {
     e.vcache = m->vl(l);
     e.rope = m->rope;
     return e;
+}
+}  // namespace
+
+namespace {
+// Synchronise the model's stream and report its error word; a reported error is cleared, so only calls that
+// ran after the report can raise it again.
+int read_err(af_model* m) {
+    CK(cudaMemcpyAsync(&m->err_host, m->gs.err, 4, cudaMemcpyDeviceToHost, m->s));
+    CK(cudaStreamSynchronize(m->s));
+    if (m->err_host) {
+        const unsigned code = m->err_host;
+        CK(cudaMemsetAsync(m->gs.err, 0, 4, m->s));
+        CK(cudaStreamSynchronize(m->s));
+        return fail(AF_ETIMEOUT, "a bounded device-side wait gave up (code %u)", code);
+    }
+    return AF_OK;
 }
 }  // namespace
 
@@ -258,6 +276,8 @@ void af_model_destroy(af_model* m) {
     if (!m) return;
     if (m->gexec) cudaGraphExecDestroy(m->gexec);
     if (m->s) cudaStreamSynchronize(m->s);
+    if (m->tok_ev) cudaEventDestroy(m->tok_ev);
+    if (m->tok_host) cudaFreeHost(m->tok_host);
     m->A.free_all();
     if (m->own_stream) cudaStreamDestroy(m->s);
     delete m;
@@ -374,7 +394,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     m->tok = (int*)A.get((size_t)S * 4);
     m->logits = (float*)A.get((size_t)V * 4);
     m->st = (StepState*)A.get(sizeof(StepState));
-    m->gs.err = (unsigned*)A.get(sizeof(unsigned));
+    m->gs.err = (unsigned*)A.get(kErrWords * sizeof(unsigned));
     m->as.ns = std::max(attn_decode_splits(c.n_heads, c.n_kv_heads, c.max_ctx), decode_attn_splits(c.n_kv_heads));
     m->as.part = (float*)A.get(attn_decode_part_elems(c.n_heads, D, m->as.ns) * 4);
     m->as.cnt = (unsigned*)A.get((size_t)c.n_kv_heads * 4);
@@ -447,11 +467,20 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     {
         cudaError_t e = qgemv_prepare();
         if (!e) e = qgemm_prepare();
-        if (!e) e = cudaMemsetAsync(m->gs.err, 0, sizeof(unsigned), s);
+        if (!e) e = cudaMemsetAsync(m->gs.err, 0, kErrWords * sizeof(unsigned), s);
         if (!e) e = cudaMemsetAsync(m->as.cnt, 0, (size_t)c.n_kv_heads * 4, s);
         if (!e) e = cudaMemsetAsync(m->st, 0, sizeof(StepState), s);
         if (!e) e = cudaStreamSynchronize(s);
         if (e) return cuda_fail(e, "model init");
+        if (cudaMallocHost(&m->tok_host, (size_t)S * 4) != cudaSuccess ||
+            cudaEventCreateWithFlags(&m->tok_ev, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            if (m->tok_ev) cudaEventDestroy(m->tok_ev);
+            if (m->tok_host) cudaFreeHost(m->tok_host);
+            m->tok_ev = nullptr;
+            m->tok_host = nullptr;
+            return oom("token staging");
+        }
     }
     *out = m;
     return AF_OK;
@@ -464,10 +493,7 @@ const int32_t* af_model_next_token_dev(const af_model* m) { return m ? &m->st->n
 int af_model_sync(af_model* m, int32_t* next_token_host) {
     if (!m) return fail(AF_EINVAL, "null model");
     if (next_token_host) CK(cudaMemcpyAsync(next_token_host, &m->st->next_token, 4, cudaMemcpyDeviceToHost, m->s));
-    CK(cudaMemcpyAsync(&m->err_host, m->gs.err, 4, cudaMemcpyDeviceToHost, m->s));
-    CK(cudaStreamSynchronize(m->s));
-    if (m->err_host) return fail(AF_ETIMEOUT, "a bounded device-side wait gave up (code %u)", m->err_host);
-    return AF_OK;
+    return read_err(m);
 }
 
 int af_model_kv_cache(const af_model* m, void** k_dev, void** v_dev) {
@@ -482,6 +508,14 @@ int af_reset(af_model* m) {
     const size_t kvb = af_kv_bytes(&m->c) / 2;
     CK(cudaMemsetAsync(m->kc, 0, kvb, m->s));
     CK(cudaMemsetAsync(m->vc, 0, kvb, m->s));
+    CK(cudaMemsetAsync(m->gs.err, 0, 4, m->s));
+    return AF_OK;
+}
+
+int af_debug_stall(af_model* m, uint32_t polls) {
+    if (!m) return fail(AF_EINVAL, "null model");
+    CK(cudaStreamSynchronize(m->s));
+    CK(cudaMemcpy(m->gs.err + 1, &polls, 4, cudaMemcpyHostToDevice));
     return AF_OK;
 }
 
@@ -626,7 +660,12 @@ int af_prefill(af_model* m, const int32_t* tokens_host, int32_t n, int32_t start
     for (int i = 0; i < n; i++)
         if (tokens_host[i] < 0 || tokens_host[i] >= m->c.n_vocab)
             return fail(AF_ERANGE, "token %d at index %d outside [0, %d)", tokens_host[i], i, m->c.n_vocab);
-    CK(cudaMemcpyAsync(m->tok, tokens_host, (size_t)n * 4, cudaMemcpyHostToDevice, m->s));
+    // through the model's page-locked staging buffer: the caller's buffer is free once this returns, and the
+    // staging buffer is rewritten only after the previous call's copy out of it has completed
+    CK(cudaEventSynchronize(m->tok_ev));
+    std::memcpy(m->tok_host, tokens_host, (size_t)n * 4);
+    CK(cudaMemcpyAsync(m->tok, m->tok_host, (size_t)n * 4, cudaMemcpyHostToDevice, m->s));
+    CK(cudaEventRecord(m->tok_ev, m->s));
     return prefill_impl(m, m->tok, n, start_pos, logits_dev);
 }
 
@@ -676,9 +715,7 @@ int af_decode_step(af_model* m, int32_t token, int32_t pos, float* logits_dev, i
     }
     if (next_token_host) {
         CK(cudaMemcpyAsync(next_token_host, &m->st->next_token, 4, cudaMemcpyDeviceToHost, m->s));
-        CK(cudaMemcpyAsync(&m->err_host, m->gs.err, 4, cudaMemcpyDeviceToHost, m->s));
-        CK(cudaStreamSynchronize(m->s));
-        if (m->err_host) return fail(AF_ETIMEOUT, "a bounded device-side wait gave up (code %u)", m->err_host);
+        return read_err(m);
     }
     return AF_OK;
 }
@@ -705,7 +742,7 @@ int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t 
     if (!w) return fail(AF_ENOMEM, "host allocation failed");
     cudaStream_t s = (cudaStream_t)stream;
     w->p = make_planes(w->A, wtype, N, K);
-    w->gs.err = (unsigned*)w->A.get(sizeof(unsigned));
+    w->gs.err = (unsigned*)w->A.get(kErrWords * sizeof(unsigned));
     if (!w->p.qs || !w->gs.err) {
         af_qweight_destroy(w);
         return fail(AF_ENOMEM, "device allocation failed");
@@ -713,7 +750,7 @@ int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t 
     cudaError_t e = qgemv_prepare();
     if (!e) e = qgemm_prepare();
     if (!e) e = repack_into(w->p, blocks_dev, N, 0, 1, s);
-    if (!e) e = cudaMemsetAsync(w->gs.err, 0, sizeof(unsigned), s);
+    if (!e) e = cudaMemsetAsync(w->gs.err, 0, kErrWords * sizeof(unsigned), s);
     if (!e) e = cudaStreamSynchronize(s);
     if (e) {
         af_qweight_destroy(w);
@@ -745,6 +782,27 @@ int af_qgemm(const af_qweight* wc, const float* X_dev, int32_t M, float* Y_dev, 
     }
     CK(launch_split_f16(X_dev, w->x16[0], w->x16[1], (int64_t)M * w->p.K, s));
     CK(launch_qgemm(w->p, w->x16[0], w->x16[1], w->p.K, M, epi_simple(EPI_STORE, Y_dev, w->p.N), w->gs.err, s));
+    return AF_OK;
+}
+
+int af_qweight_status(const af_qweight* w, void* stream) {
+    if (!w) return fail(AF_EINVAL, "null argument");
+    cudaStream_t s = (cudaStream_t)stream;
+    unsigned code = 0;
+    CK(cudaMemcpyAsync(&code, w->gs.err, 4, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    if (code) {
+        CK(cudaMemsetAsync(w->gs.err, 0, 4, s));
+        CK(cudaStreamSynchronize(s));
+        return fail(AF_ETIMEOUT, "a bounded device-side wait gave up (code %u)", code);
+    }
+    return AF_OK;
+}
+
+int af_qweight_debug_stall(af_qweight* w, uint32_t polls, void* stream) {
+    if (!w) return fail(AF_EINVAL, "null argument");
+    CK(cudaStreamSynchronize((cudaStream_t)stream));
+    CK(cudaMemcpy(w->gs.err + 1, &polls, 4, cudaMemcpyHostToDevice));
     return AF_OK;
 }
 
@@ -784,6 +842,41 @@ int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev
     return AF_OK;
 }
 
+int af_attention_prefill(const float* q_dev, const void* k_dev, const void* v_dev, int32_t kv_dtype, int32_t H,
+                         int32_t KVH, int32_t D, int32_t ctx, int32_t start_pos, int32_t n, float* out_dev,
+                         void* stream) {
+    if (!q_dev || !k_dev || !v_dev || !out_dev) return fail(AF_EINVAL, "null argument");
+    if (kv_dtype != AF_F32 && kv_dtype != AF_F16) return fail(AF_EINVAL, "bad kv_dtype");
+    if (H <= 0 || KVH <= 0 || D <= 0 || ctx <= 0) return fail(AF_EINVAL, "sizes must be positive");
+    if (!attn_supported(H, KVH, D)) return fail(AF_ENOTIMPL, "unsupported head_dim / group size");
+    if (n < 1 || n > 512) return fail(AF_ERANGE, "n=%d outside [1, 512]", n);
+    if (start_pos < 0 || (int64_t)start_pos + n > ctx)
+        return fail(AF_ERANGE, "positions %d..%d outside the cache (%d slots)", start_pos, start_pos + n - 1, ctx);
+    if (((uintptr_t)q_dev | (uintptr_t)k_dev | (uintptr_t)v_dev) & 15) return fail(AF_EINVAL, "unaligned pointer");
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t ne = (size_t)n * H * D;
+    void* buf = nullptr;  // out_hi, out_lo planes, then the error words
+    if (cudaMalloc(&buf, ne * 4 + 256) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(AF_ENOMEM, "scratch");
+    }
+    __half* hi = (__half*)buf;
+    __half* lo = hi + ne;
+    unsigned* err = (unsigned*)((char*)buf + ne * 4);
+    unsigned err_host = 0;
+    cudaError_t e = cudaMemsetAsync(err, 0, 4, s);
+    if (!e) e = launch_attn_prefill(q_dev, (int64_t)H * D, k_dev, v_dev, kv_dtype == AF_F16, H, KVH, D, ctx, start_pos, n,
+                                    hi, lo, (int64_t)H * D, err, s);
+    if (!e) e = launch_join_f16(hi, lo, out_dev, (int64_t)ne, s);
+    if (!e) e = cudaMemcpyAsync(&err_host, err, 4, cudaMemcpyDeviceToHost, s);
+    cudaError_t e2 = cudaStreamSynchronize(s);
+    cudaFree(buf);
+    if (e) return fail(AF_ECUDA, "prefill attention: %s", cudaGetErrorString(e));
+    if (e2) return fail(AF_ECUDA, "prefill attention sync: %s", cudaGetErrorString(e2));
+    if (err_host) return fail(AF_ETIMEOUT, "a bounded device-side wait gave up (code %u)", err_host);
+    return AF_OK;
+}
+
 // Same computation without allocating: the split scratch is a file-scope device
 // array (attn_static.cu).  For callers that cannot allocate mid-step: a serving
 // loop with work queued on other streams cannot take the device-wide
@@ -798,10 +891,14 @@ int af_attention_decode_static(const float* q_dev, const void* k_dev, const void
     if (pos < 0 || pos >= ctx) return fail(AF_ERANGE, "pos %d outside [0, %d)", pos, ctx);
     AttnScratch as;
     as.ns = attn_decode_splits(H, KVH, ctx);
-    if (KVH > kStaticAttnMaxKVH) return fail(AF_ERANGE, "n_kv_heads %d above the fixed scratch (%d)", KVH, kStaticAttnMaxKVH);
-    if (attn_decode_part_elems(H, D, as.ns) > kStaticAttnPartFloats)
-        return fail(AF_ERANGE, "split partials (%zu floats) above the fixed scratch (%zu)",
-                    attn_decode_part_elems(H, D, as.ns), kStaticAttnPartFloats);
+    // the cluster path keeps its partials in shared memory: only the split path needs the counters and partials
+    if (!attn_decode_uses_cluster(ctx)) {
+        if (KVH > kStaticAttnMaxKVH)
+            return fail(AF_ERANGE, "n_kv_heads %d above the fixed scratch (%d)", KVH, kStaticAttnMaxKVH);
+        if (attn_decode_part_elems(H, D, as.ns) > kStaticAttnPartFloats)
+            return fail(AF_ERANGE, "split partials (%zu floats) above the fixed scratch (%zu)",
+                        attn_decode_part_elems(H, D, as.ns), kStaticAttnPartFloats);
+    }
     CK(attn_static_scratch(&as.part, &as.cnt, &as.err));
     CK(launch_attn_decode(q_dev, k_dev, v_dev, kv_dtype == AF_F16, H, KVH, D, ctx, nullptr, pos, as, out_dev,
                           (cudaStream_t)stream));

@@ -17,6 +17,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "tma.cuh"
@@ -361,9 +362,9 @@ __global__ void __launch_bounds__(kDecThreads, (!CL && G <= 4) ? 2 : 1)
             for (int w = 0; w < kDecWarps; w++) o += red_o[w * G * D + t];
             my[(t / D) * PST + t % D] = o;
         }
-        if (tid < G) {
-            my[tid * PST + D] = m_s[tid];
-            my[tid * PST + D + 1] = l_s[tid];
+        if (tid < G) {  // an aborted split publishes a NaN weight, so the merged output of its kv head is NaN
+            my[tid * PST + D] = abort_f ? 0.f : m_s[tid];
+            my[tid * PST + D + 1] = abort_f ? CUDART_NAN_F : l_s[tid];
         }
     } else {
         pdl_wait();  // the output and the split scratch are in use until the previous kernels finish
@@ -505,14 +506,19 @@ cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int 
     auto k = attn_decode_kernel<D, G, KT, CL>;
     // the largest dynamic shared memory this instantiation was opened to, per device (set before a launch
     // that needs more; launches inside a stream capture reuse what was set before it)
-    static int opened[16] = {};
+    static int opened[kMaxDevices] = {};
+    static std::mutex mu;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e) return e;
-    if (dev < 0 || dev >= 16 || opened[dev] < (int)smem) {
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e) return e;
-        if (dev >= 0 && dev < 16) opened[dev] = (int)smem;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (opened[dev] < (int)smem) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e) return e;
+            opened[dev] = (int)smem;
+        }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ns, KVH);
@@ -544,6 +550,8 @@ cudaError_t dispatch_decode(const float* q, const void* kc, const void* vc, int 
 }
 
 }  // namespace
+
+bool attn_decode_uses_cluster(int max_ctx) { return max_ctx <= kC * kClMaxSplit; }
 
 bool attn_supported(int H, int KVH, int D) {
     if (KVH <= 0 || H % KVH) return false;
@@ -581,7 +589,7 @@ cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, i
                                cudaStream_t s) {
     const int G = H / KVH;
     // the path depends on the cache size only (a captured decode step replays at every position)
-    const bool cl = max_ctx <= kC * kClMaxSplit;
+    const bool cl = attn_decode_uses_cluster(max_ctx);
     const int ns = attn_decode_splits(H, KVH, max_ctx);
     if (!cl && scr.ns < ns) return cudaErrorInvalidValue;  // scratch sized for fewer splits
     if ((reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & 15) return cudaErrorInvalidValue;

@@ -28,7 +28,6 @@ static_assert(kStaticAttnCntBytes % 256 == 0, "partials start 256-byte aligned")
 
 static __device__ __align__(256) unsigned char g_attn_static[kStaticAttnBytes];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 

@@ -164,11 +164,17 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, f
 // ---------------------------------------------------------------------------
 // Host-side launchers (defined in the .cu files).
 // ---------------------------------------------------------------------------
+// Device error words of a model or a standalone weight: err[0] is the DEV_* code a kernel records when one of
+// its bounded waits gives up (zero when healthy); err[1] is test instrumentation read by the decode GEMV: when
+// nonzero, the GEMV's first wait polls an mbarrier nothing arrives on that many times and then takes its timeout
+// path, so the error reporting can be exercised without a fault or a hang.
+constexpr int kErrWords = 2;
 struct GemvScratch {
-    unsigned* err = nullptr;  // device error word (DEV_OK / DEV_TIMEOUT), zero when healthy
+    unsigned* err = nullptr;  // device, kErrWords words (above)
 };
 
 int num_sms();
+constexpr int kMaxDevices = 64;  // per-device state (kernel attributes, static scratch addresses)
 
 cudaError_t launch_repack(const uint8_t* src, const Planes& P, int N, int row0, int step, cudaStream_t s);
 cudaError_t launch_rope_table(float2* tab, int max_ctx, int head_dim, double base, double yarn_scale,
@@ -179,6 +185,8 @@ cudaError_t launch_rmsnorm_rows(const float* x, int n, int E, const float* w, fl
                                 cudaStream_t s);
 // x (fp32) -> fp16 hi + lo planes.
 cudaError_t launch_split_f16(const float* x, __half* hi, __half* lo, int64_t n, cudaStream_t s);
+// fp16 hi + lo planes -> out = hi + lo (fp32).
+cudaError_t launch_join_f16(const __half* hi, const __half* lo, float* out, int64_t n, cudaStream_t s);
 
 // y-part of the decode path: one matrix-vector product with optional RMSNorm
 // prologue (norm_w != nullptr) and a fused epilogue.
@@ -202,6 +210,10 @@ struct AttnScratch {
     unsigned* err = nullptr;  // device error word (a bounded wait gave up)
     int ns = 0;               // splits the partials have room for
 };
+// Whether decode attention over a cache of max_ctx slots takes the cluster path (partials merged through
+// distributed shared memory: no global scratch) rather than the split path (partials and arrival counters in
+// the scratch).  The path depends on the cache size only.
+bool attn_decode_uses_cluster(int max_ctx);
 // Splits the decode attention launches (grid.x) for this shape.
 int attn_decode_splits(int n_heads, int n_kv_heads, int max_ctx);
 size_t attn_decode_part_elems(int n_heads, int head_dim, int ns);

@@ -257,6 +257,20 @@ cudaError_t launch_split_f16(const float* x, __half* hi, __half* lo, int64_t n, 
     return cudaGetLastError();
 }
 
+__global__ void join_f16_kernel(const __half* __restrict__ hi, const __half* __restrict__ lo, float* __restrict__ out,
+                                int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = __half2float(hi[i]) + __half2float(lo[i]);
+}
+
+cudaError_t launch_join_f16(const __half* hi, const __half* lo, float* out, int64_t n, cudaStream_t s) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    if (blocks < 1) blocks = 1;
+    join_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>(hi, lo, out, n);
+    return cudaGetLastError();
+}
+
 __global__ void step_begin_kernel(StepState* st, int token, int pos, unsigned* bar_count) {
     st->token = token >= 0 ? token : st->next_token;
     st->pos = pos;

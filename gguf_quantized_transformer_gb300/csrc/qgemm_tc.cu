@@ -29,6 +29,8 @@
 // drains what it issued and frees its TMEM before returning.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "tcgen05.cuh"
 #include "tma.cuh"
@@ -490,8 +492,19 @@ bool make_map(CUtensorMap* map, const __half* base, int rows, int cols, int64_t 
 
 }  // namespace
 
+namespace {
+std::mutex g_prep_mu;
+bool g_prepared[kMaxDevices] = {};
+}  // namespace
+
 cudaError_t qgemm_prepare() {
-    cudaError_t e = cudaSuccess;
+    // once per device (kernel attributes are per device), outside any stream capture
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_prep_mu);
+    if (g_prepared[dev]) return cudaSuccess;
 #define AF_QGEMM_ATTR(WT, BN)                                                                                  \
     if (!e) e = cudaFuncSetAttribute(qgemm_tc_kernel<WT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
                                      TcCfg<WT, BN>::kSmemBytes);
@@ -506,6 +519,7 @@ cudaError_t qgemm_prepare() {
     AF_QGEMM_ATTR(AF_Q6_K, 256)
     AF_QGEMM_ATTR(AF_Q6_K, 128)
 #undef AF_QGEMM_ATTR
+    if (!e) g_prepared[dev] = true;
     return e;
 }
 

@@ -377,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float2 rope_s[64];
     __shared__ unsigned long long amax_s;
     __shared__ volatile int abort_flag;
+    __shared__ uint64_t never;  // an mbarrier nothing arrives on (the error path's test hook, below)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int rs = warp / WK, wk = warp % WK;
@@ -403,8 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         abort_flag = 0;
         amax_s = 0ull;
+        mbar_init(&never, 1);
         fence_mbar_init();
     }
+    // err[1] != 0 (test instrumentation): the first stage wait polls `never` that many times, gives up and takes
+    // the timeout path (error code, drain of the copies in flight, early return) exactly as a real timeout would
+    const unsigned stall = err[1];
     __syncthreads();
     const uint64_t pol = policy_evict_first();
     auto issue = [&](int st) {  // one thread: stage st (rows r0 + st*R ..) into its slot
@@ -467,8 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = st % ring;
         const unsigned par = (unsigned)((st / ring) & 1);
         bool ok = false;
-        for (unsigned it = 0; it < kWaitLimit && !ok; it++) {
-            ok = mbar_try_wait(&full[slot], par);
+        uint64_t* bar = (stall && st == 0) ? &never : &full[slot];
+        const unsigned lim = (stall && st == 0) ? stall : kWaitLimit;
+        for (unsigned it = 0; it < lim && !ok; it++) {
+            ok = mbar_try_wait(bar, par);
             if (!ok && abort_flag) break;
         }
         if (!ok) {

@@ -136,8 +136,11 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
  * row r attends to slots 0..start_pos+r.  The caller runs longer prompts as
  * consecutive chunks with increasing start_pos.  If logits_dev is not NULL it
  * receives the n_vocab fp32 logits of the last row.  tokens_host is copied
- * before the call returns.  Errors: AF_EINVAL, AF_ERANGE (token id outside
- * [0, n_vocab) or positions past max_ctx), AF_ECUDA.
+ * into the model's page-locked staging buffer before the call returns, so the
+ * caller may reuse it at once (pageable or page-locked alike); the call first
+ * waits for the previous af_prefill's copy out of that buffer.  Not for stream
+ * capture (use af_prefill_dev there).  Errors: AF_EINVAL, AF_ERANGE (token id
+ * outside [0, n_vocab) or positions past max_ctx), AF_ECUDA.
  */
 int af_prefill(af_model* m, const int32_t* tokens_host, int32_t n, int32_t start_pos, float* logits_dev);
 
@@ -157,7 +160,10 @@ int af_decode_step(af_model* m, int32_t token, int32_t pos, float* logits_dev, i
 
 /* Synchronise the model's stream.  Returns AF_ETIMEOUT if a bounded device-side
  * wait of an earlier call gave up, else AF_OK; if next_token_host is not NULL it
- * receives the greedy token of the last call that produced logits. */
+ * receives the greedy token of the last call that produced logits.  A reported
+ * timeout is cleared (af_decode_step with next_token_host reports and clears the
+ * same way), so a later call reports only what happened after it.  The outputs
+ * of the calls that timed out are not valid. */
 int af_model_sync(af_model* m, int32_t* next_token_host);
 
 /* Greedy token of the last af_decode_step / af_prefill with logits (device int32, valid after the stream). */
@@ -167,7 +173,7 @@ const int32_t* af_model_next_token_dev(const af_model* m);
  * in kv_dtype (Airframe "GPU_PIPELINE.md", "KV cache" layout).  Owned by the model. */
 int af_model_kv_cache(const af_model* m, void** k_dev, void** v_dev);
 
-/* Zero the KV cache (the service is stateless between requests). */
+/* Zero the KV cache (the service is stateless between requests) and the error word. */
 int af_reset(af_model* m);
 
 /* Model's stream (as given to af_model_create). */
@@ -203,6 +209,12 @@ int af_debug_trace(af_model* m, uint64_t* trace_dev);
 
 void af_model_destroy(af_model* m);
 
+/* Test instrumentation of the error path: with polls != 0 the first wait of every decode GEMV launched
+ * afterwards polls an mbarrier that nothing arrives on `polls` times, then takes its timeout path (error
+ * word set, its bulk copies drained, early return) as a real timeout would; 0 turns it off.  Synchronises
+ * the model's stream.  Lets a test see AF_ETIMEOUT without a fault or a hang. */
+int af_debug_stall(af_model* m, uint32_t polls);
+
 /*
  * Standalone quantized matmuls.
  * af_qweight_create repacks a [N, K] block matrix (N even, K a whole number
@@ -227,6 +239,14 @@ int af_qgemv(const af_qweight* w, const float* x_dev, float* y_dev, void* stream
 int af_qgemm(const af_qweight* w, const float* X_dev, int32_t M, float* Y_dev, void* stream);
 void af_qweight_destroy(af_qweight* w);
 
+/* Synchronise `stream` and report w's error word: AF_ETIMEOUT if a bounded device-side wait of an af_qgemv /
+ * af_qgemm on w gave up since the last report (the word is then cleared; those outputs are not valid), else
+ * AF_OK. */
+int af_qweight_status(const af_qweight* w, void* stream);
+
+/* Test instrumentation: as af_debug_stall, for the af_qgemv calls on w (synchronises `stream`). */
+int af_qweight_debug_stall(af_qweight* w, uint32_t polls, void* stream);
+
 /*
  * Standalone causal GQA attention for one query row at position pos over a
  * caller's cache (Airframe per-layer ops: softmax(q K^T / sqrt(D)) V over
@@ -235,7 +255,8 @@ void af_qweight_destroy(af_qweight* w);
  *   k_dev, v_dev  [KVH][ctx][D] in kv_dtype
  *   out_dev fp32 [H*D]
  * Scratch (split partials) is allocated per call and freed after the stream
- * completes (the call synchronises `stream`).
+ * completes (the call synchronises `stream`).  AF_ETIMEOUT if a bounded
+ * device-side wait gave up.
  */
 int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev, int32_t kv_dtype, int32_t n_heads,
                         int32_t n_kv_heads, int32_t head_dim, int32_t ctx, int32_t pos, float* out_dev, void* stream);
@@ -248,12 +269,17 @@ int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev
  * kernel and same result as af_attention_decode, but stream-ordered: it does
  * not synchronise `stream`.
  * Scratch: one file-scope device array of this library (4 MiB of split
- * partials + 1024 arrival counters + an error word that a device-side wait
- * timeout sets; this call does not read it back).  Calls with n_kv_heads > 1024 or whose
- * partials need more than 2^20 floats (n_heads * splits * (head_dim + 4),
- * splits = ceil(2 * SMs / n_kv_heads)) return AF_ERANGE before launching.
+ * partials + 1024 arrival counters + an error word), used only when ctx >
+ * 2048 (shorter caches take the cluster path, which merges in shared memory).
+ * On that path, calls with n_kv_heads > 1024 or whose partials need more than
+ * 2^20 floats (n_heads * splits * (head_dim + 4), splits = max(2 * SMs /
+ * n_kv_heads, ceil(ctx * G / 16384))) return AF_ERANGE before launching.
+ * Errors on the device: the call does not wait for the kernel, so it cannot
+ * report AF_ETIMEOUT; if a bounded device-side wait gives up, every output
+ * value of the affected kv heads is NaN instead.
  * The counters must start at zero: they are zero when the library is loaded
- * and every call that completes leaves them zero.  All calls on a device
+ * and every launch leaves them zero, a timed-out one included (each CTA
+ * still arrives, and the last one resets the counter).  All calls on a device
  * share the one array, so calls that may overlap in time (different streams
  * without ordering between them) race and give wrong results: order them on
  * one stream.  The first call on each device looks up the array's address
@@ -263,6 +289,23 @@ int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev
 int af_attention_decode_static(const float* q_dev, const void* k_dev, const void* v_dev, int32_t kv_dtype,
                                int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, int32_t ctx, int32_t pos,
                                float* out_dev, void* stream);
+
+/*
+ * Standalone causal prefill attention (the tensor-core kernel af_prefill runs;
+ * Airframe per-layer ops: softmax(q K^T / sqrt(D)) V, causal; dotLLM
+ * "Attention on GPU": GQA group = H / KVH) for n query rows at positions
+ * start_pos..start_pos+n-1 over a caller's cache.  Test entry point.
+ *   q_dev   fp32 [n][H*D] (already rotated), row r at position start_pos + r
+ *   k_dev, v_dev  [KVH][ctx][D] in kv_dtype (16-byte aligned); row r attends
+ *           to slots 0..start_pos+r
+ *   out_dev fp32 [n][H*D]: the fp16 hi + lo output planes of the kernel, summed
+ * 1 <= n <= 512, start_pos + n <= ctx (AF_ERANGE).  The output planes are
+ * allocated per call; the call synchronises `stream`.  AF_ETIMEOUT if a
+ * bounded device-side wait gave up.
+ */
+int af_attention_prefill(const float* q_dev, const void* k_dev, const void* v_dev, int32_t kv_dtype, int32_t n_heads,
+                         int32_t n_kv_heads, int32_t head_dim, int32_t ctx, int32_t start_pos, int32_t n,
+                         float* out_dev, void* stream);
 
 /*
  * Sampler chain on the device (Airframe GPU pipeline, sampler: "repetition

@@ -79,6 +79,7 @@ def lib():
             L.orc_model_create.restype = vp
             L.orc_forward.argtypes = [vp, vp, i64, i64, vp, vp, ctypes.c_int]
             L.orc_kv_read.argtypes = [vp, i32, i32, i64, vp, vp]
+            L.orc_kv_write.argtypes = [vp, i32, i32, i64, i64, vp, vp]
             L.orc_model_destroy.argtypes = [vp]
             L.orc_model_destroy.restype = None
             L.orc_argmax.argtypes = [vp, i64]
@@ -276,6 +277,15 @@ class Model:
         if lib().orc_kv_read(self.h, layer, kvh, pos, _p(k), _p(v)):
             raise IndexError("slot out of range")
         return k, v
+
+    def kv_write(self, layer: int, kvh: int, pos0: int, k, v):
+        """Set slots pos0.. of (layer, kv head) to k, v [n][head_dim] (values of the cache's element type)."""
+        k = np.ascontiguousarray(k, dtype=np.float64)
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        if k.shape != v.shape or k.ndim != 2 or k.shape[1] != self.cfg.head_dim:
+            raise ValueError("k, v must be [n][head_dim]")
+        if lib().orc_kv_write(self.h, layer, kvh, pos0, k.shape[0], _p(k), _p(v)):
+            raise IndexError("slots out of range")
 
     def __del__(self):
         h = getattr(self, "h", None)

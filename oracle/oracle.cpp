@@ -444,6 +444,18 @@ int orc_kv_read(const orc_model* m, int32_t layer, int32_t kvh, int64_t pos, dou
     return 0;
 }
 
+int orc_kv_write(orc_model* m, int32_t layer, int32_t kvh, int64_t pos0, int64_t n, const double* k,
+                 const double* v) {
+    const orc_config& c = m->c;
+    if (layer < 0 || layer >= c.n_layers || kvh < 0 || kvh >= c.n_kv_heads || pos0 < 0 || n < 0 ||
+        pos0 + n > m->slots)
+        return -1;
+    const size_t base = (((size_t)layer * c.n_kv_heads + kvh) * m->slots + pos0) * c.head_dim;
+    std::memcpy(&m->kcache[base], k, sizeof(double) * c.head_dim * n);
+    std::memcpy(&m->vcache[base], v, sizeof(double) * c.head_dim * n);
+    return 0;
+}
+
 int64_t orc_argmax(const double* v, int64_t n) {
     int64_t best = 0;
     for (int64_t i = 1; i < n; i++)

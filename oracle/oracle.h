@@ -106,6 +106,11 @@ int orc_forward(orc_model* m, const int32_t* tokens, int64_t n, int64_t start_po
                 int n_threads);
 /* Read cache slot (layer, kv head, pos): head_dim values of K and of V. */
 int orc_kv_read(const orc_model* m, int32_t layer, int32_t kvh, int64_t pos, double* k, double* v);
+/* Set cache slots pos0..pos0+n-1 of (layer, kv head): k, v [n][head_dim], stored as given (the caller passes
+ * values of the cache's element type).  A plain setter: it lets a test start from a cache prefix that both sides
+ * hold. */
+int orc_kv_write(orc_model* m, int32_t layer, int32_t kvh, int64_t pos0, int64_t n, const double* k,
+                 const double* v);
 void orc_model_destroy(orc_model* m);
 /* Greedy token: argmax, lowest index on ties. */
 int64_t orc_argmax(const double* v, int64_t n);

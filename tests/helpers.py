@@ -53,3 +53,68 @@ def gpu_model(hm, max_chunk=512):
     torch.cuda.synchronize()
     del d  # the model holds its own repacked copy
     return m
+
+
+def check_capture(got, ref, what, worst=None):
+    """Residual stream after the embedding and after every layer: got, ref [L+1, n, E]."""
+    for l in range(ref.shape[0]):
+        err = rms_rel_err(got[l], ref[l])
+        if worst is not None:
+            worst["layer"] = max(worst.get("layer", 0.0), err)
+        assert err <= LAYER_TOL, f"{what}: layer {l} err {err:.3e}"
+
+
+def check_logits(got, ref, what, worst=None):
+    import oracle
+    err = rms_rel_err(got, ref)
+    if worst is not None:
+        worst["logits"] = max(worst.get("logits", 0.0), err)
+    assert err <= LAYER_TOL, f"{what}: logits err {err:.3e}"
+    if top2_margin(ref) > ARGMAX_MARGIN:
+        assert int(np.argmax(got)) == oracle.argmax(ref), what
+
+
+def run_parity(af, cfg, seed, chunks, n_decode, kv_slots, start=0, prefix=None):
+    """Prefill the prompt in `chunks` from position `start`, then n_decode greedy steps under teacher forcing,
+    comparing every layer's residual stream and the logits with the oracle.  prefix(om, gm), if given, fills
+    cache slots [0, start) of both models before the first chunk.  Returns the worst errors seen."""
+    import torch
+
+    import oracle
+    import synth
+    hm = synth.HostModel(cfg, seed)
+    prompt = hm.prompt(sum(chunks) + start)[start:]
+    om = oracle.Model.from_host(hm, kv_slots=kv_slots)
+    gm = gpu_model(hm)
+    if prefix is not None:
+        prefix(om, gm)
+    L, E, V = cfg.n_layers, cfg.n_embd, cfg.n_vocab
+    logits = torch.empty(V, dtype=torch.float32, device="cuda")
+    worst = {}
+    p, i = start, 0
+    for ci, n in enumerate(chunks):
+        last = ci == len(chunks) - 1
+        ref_logits, ref_cap = om.forward(prompt[i:i + n], p, want_logits=last, capture=True)
+        cap = torch.empty(L + 1, n, E, dtype=torch.float32, device="cuda")
+        af.af_debug_capture(gm.h, cap)
+        gm.prefill(prompt[i:i + n], p, logits if last else None)
+        torch.cuda.synchronize()
+        check_capture(cap.cpu().numpy(), ref_cap, f"{cfg.name} prefill chunk {ci}", worst)
+        if last:
+            check_logits(logits.cpu().numpy(), ref_logits, f"{cfg.name} prefill logits", worst)
+        p += n
+        i += n
+    tok = oracle.argmax(ref_logits)
+    for step in range(n_decode):
+        ref_logits, ref_cap = om.forward([tok], p, capture=True)
+        cap = torch.empty(L + 1, 1, E, dtype=torch.float32, device="cuda")
+        af.af_debug_capture(gm.h, cap)
+        nxt = gm.decode(tok, p, logits, want_next=True)
+        got = logits.cpu().numpy()
+        check_capture(cap.cpu().numpy(), ref_cap, f"{cfg.name} decode step {step}", worst)
+        check_logits(got, ref_logits, f"{cfg.name} decode step {step}", worst)
+        assert nxt == int(np.argmax(got))  # device argmax = argmax of the device logits
+        tok = oracle.argmax(ref_logits)  # teacher forcing
+        p += 1
+    gm.close()
+    return worst

@@ -134,13 +134,34 @@ def test_static_attention_rejects_oversize():
     # (the pointers are never dereferenced on the host)
     af = pytest.importorskip("gguf_quantized_transformer_gb300")
     L = af.lib()
+    # (caches above 2048 slots: the split path, the only one that uses the fixed scratch)
     # more kv heads than arrival counters
-    assert L.af_attention_decode_static(1, 1, 1, af.AF_F16, 1028, 1028, 64, 16, 0, 1, None) == af.AF_ERANGE
+    assert L.af_attention_decode_static(1, 1, 1, af.AF_F16, 1028, 1028, 64, 4096, 0, 1, None) == af.AF_ERANGE
     assert "n_kv_heads" in af.af_last_error()
     # partials: 8192 heads x >= 1 split x 132 floats > 2^20
-    assert L.af_attention_decode_static(1, 1, 1, af.AF_F16, 8192, 1024, 128, 16, 0, 1, None) == af.AF_ERANGE
+    assert L.af_attention_decode_static(1, 1, 1, af.AF_F16, 8192, 1024, 128, 4096, 0, 1, None) == af.AF_ERANGE
     assert "partials" in af.af_last_error()
     assert af.af_kv_bytes(af.af_config()) == 0
+
+
+def test_new_entry_points_validate_on_the_host():
+    # argument checks that return before any launch (the pointers are never dereferenced on the host)
+    af = pytest.importorskip("gguf_quantized_transformer_gb300")
+    L = af.lib()
+    ok = dict(kv=af.AF_F16, H=32, KVH=8, D=128, ctx=1024)
+    def pf(q=1, start=0, n=4, ctx=1024, kv=af.AF_F16, H=32, KVH=8, D=128, out=16):
+        return L.af_attention_prefill(q, 16, 16, kv, H, KVH, D, ctx, start, n, out, None)
+    assert pf(q=None) == af.AF_EINVAL
+    assert pf(out=None) == af.AF_EINVAL
+    assert pf(kv=7) == af.AF_EINVAL
+    assert pf(n=0) == af.AF_ERANGE and pf(n=513) == af.AF_ERANGE
+    assert pf(start=1022, n=4) == af.AF_ERANGE and pf(start=-1) == af.AF_ERANGE
+    assert pf(D=96) == af.AF_ENOTIMPL and pf(H=24, KVH=8) == af.AF_ENOTIMPL
+    assert pf(q=8) == af.AF_EINVAL  # not 16-byte aligned
+    assert ok
+    assert L.af_qweight_status(None, None) == af.AF_EINVAL
+    assert L.af_qweight_debug_stall(None, 1, None) == af.AF_EINVAL
+    assert L.af_debug_stall(None, 1) == af.AF_EINVAL
 
 
 def test_product_path_has_no_cpu_fallback():

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import ARGMAX_MARGIN, LAYER_TOL, gpu_model, rms_rel_err, top2_margin
+from helpers import LAYER_TOL, check_capture, check_logits, gpu_model, rms_rel_err, run_parity
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -28,55 +28,6 @@ def af():
     af.build()
     af.lib()
     return af
-
-
-def _check_capture(got, ref, what):
-    # got, ref: [L+1, n, E]
-    for l in range(ref.shape[0]):
-        err = rms_rel_err(got[l], ref[l])
-        assert err <= LAYER_TOL, f"{what}: layer {l} err {err:.3e}"
-
-
-def _check_logits(got, ref, what):
-    err = rms_rel_err(got, ref)
-    assert err <= LAYER_TOL, f"{what}: logits err {err:.3e}"
-    if top2_margin(ref) > ARGMAX_MARGIN:
-        assert int(np.argmax(got)) == oracle.argmax(ref), what
-
-
-def run_parity(af, cfg, seed, chunks, n_decode, kv_slots):
-    """chunks: list of chunk lengths of the prompt."""
-    hm = synth.HostModel(cfg, seed)
-    prompt = hm.prompt(sum(chunks))
-    om = oracle.Model.from_host(hm, kv_slots=kv_slots)
-    gm = gpu_model(hm)
-    L, E, V = cfg.n_layers, cfg.n_embd, cfg.n_vocab
-    logits = torch.empty(V, dtype=torch.float32, device="cuda")
-    p = 0
-    for ci, n in enumerate(chunks):
-        last = ci == len(chunks) - 1
-        ref_logits, ref_cap = om.forward(prompt[p:p + n], p, want_logits=last, capture=True)
-        cap = torch.empty(L + 1, n, E, dtype=torch.float32, device="cuda")
-        af.af_debug_capture(gm.h, cap)
-        gm.prefill(prompt[p:p + n], p, logits if last else None)
-        torch.cuda.synchronize()
-        _check_capture(cap.cpu().numpy(), ref_cap, f"{cfg.name} prefill chunk {ci}")
-        if last:
-            _check_logits(logits.cpu().numpy(), ref_logits, f"{cfg.name} prefill logits")
-        p += n
-    tok = oracle.argmax(ref_logits)
-    for step in range(n_decode):
-        ref_logits, ref_cap = om.forward([tok], p, capture=True)
-        cap = torch.empty(L + 1, 1, E, dtype=torch.float32, device="cuda")
-        af.af_debug_capture(gm.h, cap)
-        nxt = gm.decode(tok, p, logits, want_next=True)
-        got = logits.cpu().numpy()
-        _check_capture(cap.cpu().numpy(), ref_cap, f"{cfg.name} decode step {step}")
-        _check_logits(got, ref_logits, f"{cfg.name} decode step {step}")
-        assert nxt == int(np.argmax(got))  # device argmax = argmax of the device logits
-        tok = oracle.argmax(ref_logits)  # teacher forcing
-        p += 1
-    gm.close()
 
 
 def test_config0_full_workload(af):
@@ -280,8 +231,8 @@ def test_decode_parity_in_persistent_mode(af):
         af.af_debug_capture(gm.h, cap)
         gm.decode(tok, p, logits)
         torch.cuda.synchronize()
-        _check_capture(cap.cpu().numpy(), ref_cap, f"persistent decode pos {p}")
-        _check_logits(logits.cpu().numpy(), ref_logits, f"persistent decode pos {p}")
+        check_capture(cap.cpu().numpy(), ref_cap, f"persistent decode pos {p}")
+        check_logits(logits.cpu().numpy(), ref_logits, f"persistent decode pos {p}")
         tok = oracle.argmax(ref_logits)
     gm.close()
 

@@ -356,6 +356,32 @@ def test_kv_slots_written_exactly_and_rounded(tiny):
                     assert all(oracle.round_f16(x) == x for x in k)
 
 
+def test_kv_write_sets_the_slots_forward_reads(tiny):
+    """A cache prefix set with kv_write is the one the next chunk attends to: copying the slots a real prefill
+    wrote into a fresh model gives the same continuation, bit for bit (and kv_read returns what was set)."""
+    cfg = tiny.cfg
+    toks = tiny.prompt()
+    a = oracle.Model.from_host(tiny)
+    a.forward(toks[:20], 0, want_logits=False)
+    la, ca = a.forward(toks[20:], 20, capture=True)
+    b = oracle.Model.from_host(tiny)
+    for l in range(cfg.n_layers):
+        for g in range(cfg.n_kv_heads):
+            kv = [a.kv_read(l, g, p) for p in range(20)]
+            k = np.stack([x[0] for x in kv])
+            v = np.stack([x[1] for x in kv])
+            b.kv_write(l, g, 0, k, v)
+            assert all(np.array_equal(b.kv_read(l, g, p)[0], k[p]) for p in range(20))
+    lb, cb = b.forward(toks[20:], 20, capture=True)
+    assert np.array_equal(la, lb) and np.array_equal(ca, cb)
+    # a different prefix changes the continuation (the setter is not a no-op)
+    b.kv_write(0, 0, 3, np.ones((1, cfg.head_dim)), np.ones((1, cfg.head_dim)))
+    lc, _ = b.forward(toks[20:], 20)
+    assert not np.array_equal(la, lc)
+    with pytest.raises(IndexError):
+        b.kv_write(0, 0, cfg.max_ctx - 1, np.ones((2, cfg.head_dim)), np.ones((2, cfg.head_dim)))
+
+
 def test_rope_position_matters_in_model(tiny):
     # same token at two different positions with an empty cache otherwise: K differs only by the rotation
     cfg = tiny.cfg
