@@ -478,6 +478,13 @@ def kquant_run(af, args, dev, hbm_peak, tc_peak, steps=2, warmup=1):
     return out
 
 
+def workload_prompt(cfg):
+    """Prompt tokens of a config's workload.  Where the prompt and the decode steps do not both fit the stated cache
+    (the TinyLlama-shaped config: a 2048-token prompt and 128 decode steps at max_ctx 2048), the cache size is kept
+    and the prompt is shortened so that the last decode step writes the last slot."""
+    return min(cfg.prompt_len, cfg.max_ctx - cfg.n_decode)
+
+
 def config_runs(af, args, dev, hbm_peak, tc_peak):
     """Every other full-size config over its own workload (the headline config is the main line)."""
     out = {}
@@ -486,7 +493,8 @@ def config_runs(af, args, dev, hbm_peak, tc_peak):
             continue
         cfg = synth.CONFIGS[idx]
         try:
-            line = workload_run(af, cfg, synth.seed_of(idx), cfg.prompt_len, cfg.n_decode, cfg.chunk, dev, hbm_peak,
+            P = workload_prompt(cfg)
+            line = workload_run(af, cfg, synth.seed_of(idx), P, cfg.n_decode, cfg.chunk, dev, hbm_peak,
                                 tc_peak, steps=1, warmup=1, cpu=args.rank == 0 and not args.no_cpu_baseline)
             if cfg.max_ctx > 8192:  # long context: decode attention is half the bytes of a token; its roofline
                 line["attn_roofline"] = attn_roofline(af, cfg, cfg.prompt_len, dev, hbm_peak)

@@ -9,9 +9,10 @@
 // memory, pass 2 exponentiates against the CTA maximum and accumulates P V.
 // Each CTA stores (o, max, sum) for its range; the last CTA of a kv head to
 // finish (acq_rel counter) merges the splits with the usual max-rescaling.
-// For caches of up to kC * kClMaxSplit slots the kC splits of a kv head form a
-// thread-block cluster instead and merge through distributed shared memory
-// (attn_decode_kernel's CL path).
+// For caches of up to kC * kClMaxSplit slots the kC = 8 splits of a kv head
+// form a thread-block cluster instead and merge through distributed shared
+// memory (attn_decode_kernel's CL path): no partials in global memory, no
+// fence, counter or second round trip.
 //
 // Prefill attention runs on the tensor cores (attn_prefill_tc.cu).
 #include <math_constants.h>
@@ -58,24 +59,24 @@ constexpr int kMinPerSplit = 64;  // positions per split before another split is
 constexpr int kRing = 96 * 1024;     // tile ring budget (two CTAs per SM)
 constexpr int kRingCl = 176 * 1024;  // tile ring budget of the cluster path (one CTA per SM)
 constexpr int kMaxStages = 12;
-constexpr int kMaxScores = 64 * 1024;  // score buffer budget: split length x G floats
-// Cluster path: the kC CTAs of one kv head form a thread-block cluster and merge through distributed
-// shared memory; taken when every split has at most kClMaxSplit slots.  Longer splits stream more tiles
-// through one CTA than its per-tile work keeps up with (measured: 16.7 us against 11.1 us for the split
-// path at position 4200 of an 8192-slot cache), so the cluster path serves caches of up to 2048 slots.
+// Cluster path: the kC CTAs of one kv head form a thread-block cluster of one CTA per SM and merge through
+// distributed shared memory; taken when every split has at most kClMaxSplit slots, i.e. for caches of up to
+// 2048 slots, and when the device can schedule such clusters.  Longer caches take the split path: with few
+// kv heads the clusters cover few SMs (measured: 16-CTA clusters of 16 warps took 18.6 us at position 4200 of
+// an 8192-slot cache against 12.2 us for the split path, and 10.2 us against 6.2 us at position 128).
 constexpr int kC = 8;
 constexpr int kClMaxSplit = 256;
+constexpr int kClWarps = 8;
 
-// cache slots per pipeline tile: at least 64 and at least 16 KB (one bulk copy each)
+// cache slots per pipeline tile: 16 KB of K (and 16 KB of V), one bulk copy each (smaller copies stream slower)
 template <int D, typename KT>
 __host__ __device__ constexpr int dec_tile() {
-    return 16384 / (D * (int)sizeof(KT)) > 64 ? 16384 / (D * (int)sizeof(KT)) : 64;
+    return 16384 / (D * (int)sizeof(KT));
 }
+// stages (K tile + V tile) in the ring budget
 template <int D, typename KT, bool CL>
 __host__ __device__ constexpr int dec_stages() {
-    return (CL ? kRingCl : kRing) / (dec_tile<D, KT>() * D * (int)sizeof(KT)) < kMaxStages
-               ? (CL ? kRingCl : kRing) / (dec_tile<D, KT>() * D * (int)sizeof(KT))
-               : kMaxStages;
+    return (CL ? kRingCl : kRing) / (2 * 16384) < kMaxStages ? (CL ? kRingCl : kRing) / (2 * 16384) : kMaxStages;
 }
 
 __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
@@ -126,38 +127,53 @@ __device__ __forceinline__ void dec_split(int n, int ns, int& ns_eff, int& chunk
     ns_eff = (n + chunk - 1) / chunk;
 }
 
-// Decode attention, CTA (s, g): kv head g, slots [s*chunk, ...).  The K tiles
-// and then the V tiles of the range (contiguous in the cache) stream through a
-// ring of S shared-memory slots, one bulk copy (cp.async.bulk, mbarrier
-// completion) per tile; every wait is bounded.
-//   pass 1 (K tiles): lanes (LPK per slot, 8 dims each) score 32/LPK slots per
-//                     warp step for all G heads; scores go to shared memory
-//   softmax:          split maximum per head, p = exp(s - max) in place, sum
-//   pass 2 (V tiles): warp w takes slots w, w+8, ..; lane l dims l*DV..; all
-//                     heads per lane; warps are summed at the end
+// Decode attention, CTA (s, g): kv head g, slots [s*chunk, ...) of the cache.
+// The range streams through a ring of S stages; a stage is the K tile and the
+// V tile (TS slots each, 16 KB) of the same slots, two bulk copies
+// (cp.async.bulk) with an mbarrier each.  Every warp takes its own SPW = TS / 8
+// slots of every stage and keeps an online softmax of its own (running
+// maximum, running sum and the G x D output accumulator), so warps never wait
+// for one another inside the loop: a stage is refilled by the last warp that
+// is done with it (shared counter), and the only CTA barrier comes after the
+// loop, where the warps' states are combined into the CTA's partial.
+//   scores: lanes (LPK = D / 8 per slot, 8 dims each) score KPW = 32 / LPK
+//           slots per warp step for all G heads (q pre-scaled by 1/sqrt(D) in
+//           registers); a transpose-reduce leaves head li / LPH of the slot in
+//           lane li, so each lane tracks the running maximum and sum of one head
+//   P V:    the warp's probabilities go through shared memory; lane l owns
+//           dims l*DV.. of all heads: acc = acc * corr + sum_j p_j V_j
 // Split path (CL = false): two CTAs per SM where the registers allow, partials in global memory, merged by
 // the last CTA of the kv head.  Cluster path (CL = true): the kC splits of a kv head are one cluster, one CTA
 // per SM with a deeper ring; each keeps its partial in shared memory and, after a cluster barrier, CTA r
 // merges output slice r from all of them through distributed shared memory (no counter, fence or atomic).
+// Every mbarrier wait is bounded; a CTA that gives up records DEV_TIMEOUT, drains its copies and publishes a
+// NaN weight, so the merged output of its kv head is NaN.
 template <int D, int G, typename KT, bool CL>
-__global__ void __launch_bounds__(kDecThreads, (!CL && G <= 4) ? 2 : 1)
+__global__ void __launch_bounds__(CL ? kClWarps * 32 : kDecThreads, (!CL && G <= 4) ? 2 : 1)
     attn_decode_kernel(const float* __restrict__ q, const KT* __restrict__ kc, const KT* __restrict__ vc, int max_ctx,
                        const int* __restrict__ pos_dev, int pos_arg, float* __restrict__ part,
                        unsigned* __restrict__ cnt, float* __restrict__ out, unsigned* __restrict__ err) {
-    constexpr int kTile = dec_tile<D, KT>();
-    constexpr int TB = kTile * D * (int)sizeof(KT);  // tile bytes
-    constexpr int S = dec_stages<D, KT, CL>();
-    constexpr int LPK = D / 8;    // pass 1: lanes per slot
-    constexpr int KPW = 32 / LPK; // pass 1: slots per warp step
-    constexpr int DV = D / 32;    // pass 2: dims per lane
-    static_assert(S >= 2, "ring too small");
-    extern __shared__ __align__(128) uint8_t dsm[];
-    float* sc = reinterpret_cast<float*>(dsm + S * TB);  // [split length][G] scores, then probabilities
-    __shared__ float red[kDecWarps][G];
-    __shared__ float m_s[G], l_s[G];
+    constexpr int TS = dec_tile<D, KT>();            // slots per stage
+    constexpr int TB = TS * D * (int)sizeof(KT);     // bytes of one K (or V) tile
+    constexpr int S = dec_stages<D, KT, CL>();       // ring depth
+    constexpr int NW = CL ? kClWarps : kDecWarps;    // warps
+    constexpr int NT = NW * 32;
+    constexpr int SPW = TS / NW;                     // slots of a warp per stage
+    constexpr int LPK = D / 8;                       // scores: lanes per slot
+    constexpr int KPW = 32 / LPK;                    // scores: slots per warp step
+    constexpr int LPH = LPK / G;                     // lanes per head after the transpose-reduce
+    constexpr int STEPS = SPW / KPW;                 // score steps per warp per stage
+    constexpr int DV = D / 32;                       // P V: dims per lane
+    static_assert(S >= 2 && S <= kMaxStages, "ring depth");
+    static_assert(LPH >= 1 && STEPS >= 1 && SPW % KPW == 0, "lane mapping");
+    extern __shared__ __align__(128) uint8_t dsm[];  // S x [K tile | V tile]; after the loop: combine scratch
+    __shared__ uint64_t kfull[kMaxStages], vfull[kMaxStages];  // tile landed (transaction bytes)
+    __shared__ unsigned issues[kMaxStages];  // copies issued into the stage slot so far
+    __shared__ unsigned done[kMaxStages];    // warps done with the slot's current stage
+    __shared__ __align__(16) float pw[NW][SPW][G];  // a warp's probabilities of the current stage
+    __shared__ float cw[NW][G];                     // a warp's rescale factors of the current stage
+    __shared__ float wm[NW][G], wl[NW][G];   // warps' running maxima and sums
     __shared__ unsigned last;
-    __shared__ uint64_t full[kMaxStages];    // tile landed in slot (transaction bytes)
-    __shared__ unsigned issues[kMaxStages];  // copies issued into the slot so far
     __shared__ volatile int abort_f;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -170,7 +186,7 @@ __global__ void __launch_bounds__(kDecThreads, (!CL && G <= 4) ? 2 : 1)
     int ns_eff, chunk;
     dec_split(n, ns, ns_eff, chunk);
     const int j0 = s * chunk;
-    const int nl = min(n, j0 + chunk) - j0;
+    const int nl = s < ns_eff ? min(n, j0 + chunk) - j0 : 0;
     const KT* K = kc + ((int64_t)g * max_ctx + j0) * D;
     const KT* V = vc + ((int64_t)g * max_ctx + j0) * D;
     constexpr int PST = D + 4;  // partial row: o[0..D-1], max, sum, 2 pad (16-byte rows)
@@ -179,41 +195,44 @@ __global__ void __launch_bounds__(kDecThreads, (!CL && G <= 4) ? 2 : 1)
 
     if (tid == 0) {
         for (int i = 0; i < S; i++) {
-            mbar_init(&full[i], 1);
+            mbar_init(&kfull[i], 1);
+            mbar_init(&vfull[i], 1);
             issues[i] = 0;
+            done[i] = 0;
         }
         abort_f = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    if (s < ns_eff) {
-        const int nt = (nl + kTile - 1) / kTile, T = 2 * nt;
-        auto issue = [&](int t) {  // one thread: tile t (K tiles 0..nt-1, then V tiles) into slot t % S
-            const int tt = t < nt ? t : t - nt;
-            const int keys = min(kTile, nl - tt * kTile);
-            const KT* src = (t < nt ? K : V) + (int64_t)tt * kTile * D;
-            const int slot = t % S;
-            const unsigned bytes = (unsigned)(keys * D * (int)sizeof(KT));
-            issues[slot]++;
-            mbar_arrive_expect_tx(&full[slot], bytes);
-            bulk_g2s(dsm + slot * TB, src, bytes, &full[slot]);
-        };
-        // tiles without slot pos stream in before waiting for the previous kernel
-        if (tid == 0) {
-            const bool has_pos = j0 + nl == n;
-            bool waited = false;
-            for (int t = 0; t < min(S, T); t++) {
-                if (has_pos && !waited && (t == nt - 1 || t == T - 1)) {
-                    pdl_wait();
-                    waited = true;
-                }
-                issue(t);
+    const int nst = (nl + TS - 1) / TS;
+    auto issue = [&](int t) {  // one thread: K and V tiles of stage t into slot t % S
+        const int keys = min(TS, nl - t * TS);
+        const int slot = t % S;
+        const unsigned bytes = (unsigned)(keys * D * (int)sizeof(KT));
+        uint8_t* dst = dsm + slot * 2 * TB;
+        issues[slot]++;
+        mbar_arrive_expect_tx(&kfull[slot], bytes);
+        bulk_g2s(dst, K + (int64_t)t * TS * D, bytes, &kfull[slot]);
+        mbar_arrive_expect_tx(&vfull[slot], bytes);
+        bulk_g2s(dst + TB, V + (int64_t)t * TS * D, bytes, &vfull[slot]);
+    };
+    // stages without slot pos stream in before waiting for the previous kernel
+    if (tid == 0 && nst > 0) {
+        const bool has_pos = j0 + nl == n;
+        bool waited = false;
+        for (int t = 0; t < min(S, nst); t++) {
+            if (has_pos && !waited && t == nst - 1) {
+                pdl_wait();
+                waited = true;
             }
+            issue(t);
         }
-        pdl_wait();
-        // q of the group's heads, pre-scaled by 1/sqrt(D): lane's 8 dims of each head
-        const int li = lane % LPK, ks = lane / LPK;
-        float qv[G][8];
+    }
+    pdl_wait();
+
+    const int li = lane % LPK, ks = lane / LPK, hl = li / LPH;
+    float qv[G][8];
+    {
         const float scale = rsqrtf((float)D);
 #pragma unroll
         for (int h = 0; h < G; h++) {
@@ -222,154 +241,167 @@ __global__ void __launch_bounds__(kDecThreads, (!CL && G <= 4) ? 2 : 1)
             qv[h][0] = a.x * scale; qv[h][1] = a.y * scale; qv[h][2] = a.z * scale; qv[h][3] = a.w * scale;
             qv[h][4] = b.x * scale; qv[h][5] = b.y * scale; qv[h][6] = b.z * scale; qv[h][7] = b.w * scale;
         }
-        // after pass 1's transpose-reduce, lane li of a slot's LPK lanes holds head li / LPH
-        constexpr int LPH = LPK / G;
-        static_assert(LPH >= 1, "group larger than the lanes of a slot");
-        const int hl = li / LPH;
-        float mloc = -CUDART_INF_F;  // running maximum of head hl's scores
-        float acc[G][DV];
+    }
+    float m_run = -CUDART_INF_F, l_run = 0.f;  // head hl of this lane, over the warp's slots so far
+    float acc[G][DV];
 #pragma unroll
-        for (int h = 0; h < G; h++)
+    for (int h = 0; h < G; h++)
 #pragma unroll
-            for (int e = 0; e < DV; e++) acc[h][e] = 0.f;
+        for (int e = 0; e < DV; e++) acc[h][e] = 0.f;
 
-        for (int t = 0; t < T; t++) {
-            bool ok = false;
-            for (unsigned it = 0; it < kWaitLimit && !ok; it++) {
-                ok = mbar_try_wait(&full[t % S], (unsigned)((t / S) & 1));
-                if (!ok && abort_f) break;
-            }
-            if (!ok) {
-                abort_f = 1;
-                atomicExch(err, (unsigned)DEV_TIMEOUT);
-            }
-            __syncthreads();
-            if (abort_f) break;  // uniform: read after the barrier
-            const uint8_t* tile = dsm + (t % S) * TB;
-            if (t < nt) {
-                // ---- pass 1: scores of this tile's slots
-                const int keys = min(kTile, nl - t * kTile);
+    auto wait_tile = [&](uint64_t* bar, unsigned par) {  // whole warp; false (uniformly) on a timeout or abort
+        bool ok = false;
+        for (unsigned it = 0; it < kWaitLimit && !ok; it++) {
+            ok = mbar_try_wait(bar, par);
+            if (!ok && abort_f) break;
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0 && !abort_f) {
+            abort_f = 1;
+            atomicExch(err, (unsigned)DEV_TIMEOUT);
+        }
+        return ok;
+    };
+
+    for (int t = 0; t < nst; t++) {
+        const int slot = t % S;
+        const unsigned par = (unsigned)((t / S) & 1);
+        const int keys = min(TS, nl - t * TS);
+        if (!wait_tile(&kfull[slot], par)) break;
+        const KT* kt = reinterpret_cast<const KT*>(dsm + slot * 2 * TB);
+        const KT* vt = reinterpret_cast<const KT*>(dsm + slot * 2 * TB + TB);
+        // ---- scores of the warp's slots: step st covers slots warp*SPW + st*KPW + (0..KPW-1)
+        float sreg[STEPS];
+        float mt = -CUDART_INF_F;
 #pragma unroll
-                for (int step = 0; step < kTile / kDecWarps / KPW; step++) {
-                    const int j = warp * (kTile / kDecWarps) + step * KPW + ks;  // slot within the tile
-                    float kf[8];
-                    if (j < keys) {
-                        load_vec<KT>(reinterpret_cast<const KT*>(tile) + j * D + li * 8, kf, 8);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; e++) kf[e] = 0.f;
-                    }
-                    float a[G];
-#pragma unroll
-                    for (int h = 0; h < G; h++) {
-                        a[h] = 0.f;
-#pragma unroll
-                        for (int e = 0; e < 8; e++) a[h] = fmaf(qv[h][e], kf[e], a[h]);
-                    }
-                    // transpose-reduce over the slot's LPK lanes: each exchange halves the heads a lane keeps
-#pragma unroll
-                    for (int half = G / 2, bit = LPK / 2; half >= 1; half >>= 1, bit >>= 1) {
-                        const bool up = li & bit;
-#pragma unroll
-                        for (int k = 0; k < half; k++) {
-                            const float send = up ? a[k] : a[k + half], keep = up ? a[k + half] : a[k];
-                            a[k] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
-                        }
-                    }
-                    float r = a[0];
-#pragma unroll
-                    for (int bit = LPH / 2; bit >= 1; bit >>= 1) r += __shfl_xor_sync(0xffffffffu, r, bit);
-                    if (j < keys) {
-                        if (li % LPH == 0) sc[(t * kTile + j) * G + hl] = r;
-                        mloc = fmaxf(mloc, r);
-                    }
-                }
+        for (int st = 0; st < STEPS; st++) {
+            const int j = warp * SPW + st * KPW + ks;
+            float kf[8];
+            if (j < keys) {
+                load_vec<KT>(kt + j * D + li * 8, kf, 8);
             } else {
-                const int tt = t - nt;
-                if (tt == 0) {
-                    // ---- softmax over the split: maximum, probabilities in place, sum
-                    {  // lanes of one head share li / LPH: combine the KPW slots of a step
-                        float m = mloc;
 #pragma unroll
-                        for (int o = LPK; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                        if (lane < LPK && li % LPH == 0) red[warp][hl] = m;
-                    }
-                    __syncthreads();
-                    if (tid < G) {
-                        float m = red[0][tid];
+                for (int e = 0; e < 8; e++) kf[e] = 0.f;
+            }
+            float a[G];
 #pragma unroll
-                        for (int w = 1; w < kDecWarps; w++) m = fmaxf(m, red[w][tid]);
-                        m_s[tid] = m;
-                    }
-                    __syncthreads();
-                    // G divides the block: thread tid always sees head tid % G
-                    const int hh = tid % G;
-                    const float mh = m_s[hh];
-                    float l = 0.f;
-                    for (int i = tid; i < nl * G; i += kDecThreads) {
-                        const float p = __expf(sc[i] - mh);
-                        sc[i] = p;
-                        l += p;
-                    }
+            for (int h = 0; h < G; h++) {
+                a[h] = 0.f;
 #pragma unroll
-                    for (int o = 16; o >= G; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-                    if (lane < G) red[warp][lane] = l;
-                    __syncthreads();
-                    if (tid < G) {
-                        float a = 0.f;
+                for (int e = 0; e < 8; e++) a[h] = fmaf(qv[h][e], kf[e], a[h]);
+            }
+            // transpose-reduce over the slot's LPK lanes: each exchange halves the heads a lane keeps
 #pragma unroll
-                        for (int w = 0; w < kDecWarps; w++) a += red[w][tid];
-                        l_s[tid] = a;
-                    }
-                    __syncthreads();
-                }
-                // ---- pass 2: P V over this tile's slots
-                const int keys = min(kTile, nl - tt * kTile);
-                for (int j = warp; j < keys; j += kDecWarps) {
-                    float vf[DV];
-                    load_small<DV>(reinterpret_cast<const KT*>(tile) + j * D + lane * DV, vf);
-                    const float* pj = sc + (tt * kTile + j) * G;
+            for (int half = G / 2, bit = LPK / 2; half >= 1; half >>= 1, bit >>= 1) {
+                const bool up = li & bit;
 #pragma unroll
-                    for (int h = 0; h < G; h++) {
-                        const float p = pj[h];
-#pragma unroll
-                        for (int e = 0; e < DV; e++) acc[h][e] = fmaf(p, vf[e], acc[h][e]);
-                    }
+                for (int k = 0; k < half; k++) {
+                    const float send = up ? a[k] : a[k + half], keep = up ? a[k + half] : a[k];
+                    a[k] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
                 }
             }
-            __syncthreads();  // every thread is done with slot t % S
-            if (tid == 0 && t + S < T) {
-                fence_proxy_async_shared();
-                issue(t + S);
+            float r = a[0];
+#pragma unroll
+            for (int bit = LPH / 2; bit >= 1; bit >>= 1) r += __shfl_xor_sync(0xffffffffu, r, bit);
+            sreg[st] = j < keys ? r : -CUDART_INF_F;
+            mt = fmaxf(mt, sreg[st]);
+        }
+        // ---- online softmax of head hl over this stage's slots of the warp (the KPW slot lanes share a head)
+#pragma unroll
+        for (int o = LPK; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+        const float m_new = fmaxf(m_run, mt);
+        const float corr = m_new == -CUDART_INF_F ? 1.f : __expf(m_run - m_new);
+        float psum = 0.f;
+#pragma unroll
+        for (int st = 0; st < STEPS; st++) {
+            const float p = sreg[st] == -CUDART_INF_F ? 0.f : __expf(sreg[st] - m_new);
+            psum += p;
+            if (li % LPH == 0) pw[warp][st * KPW + ks][hl] = p;
+        }
+#pragma unroll
+        for (int o = LPK; o < 32; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+        l_run = fmaf(l_run, corr, psum);
+        m_run = m_new;
+        if (lane < LPK && li % LPH == 0) cw[warp][hl] = corr;
+        __syncwarp();
+        // ---- P V over the warp's slots
+        if (!wait_tile(&vfull[slot], par)) break;
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            const float c = cw[warp][h];
+#pragma unroll
+            for (int e = 0; e < DV; e++) acc[h][e] *= c;
+        }
+#pragma unroll
+        for (int jj = 0; jj < SPW; jj++) {
+            const int j = warp * SPW + jj;
+            if (j < keys) {
+                float vf[DV];
+                load_small<DV>(vt + j * D + lane * DV, vf);
+                float p[G];
+#pragma unroll
+                for (int h = 0; h < G; h++) p[h] = pw[warp][jj][h];
+#pragma unroll
+                for (int h = 0; h < G; h++)
+#pragma unroll
+                    for (int e = 0; e < DV; e++) acc[h][e] = fmaf(p[h], vf[e], acc[h][e]);
             }
         }
-        if (abort_f) {  // drain the copies still in flight before the ring is reused or the CTA exits
-            if (tid == 0)
-                for (int i = 0; i < S; i++)
-                    if (issues[i]) mbar_wait_bounded(&full[i], (issues[i] - 1u) & 1u);
-            __syncthreads();
+        __syncwarp();
+        // ---- the last warp done with this stage refills its slot
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&done[slot], 1u) == (unsigned)NW - 1u) {
+                done[slot] = 0;
+                if (t + S < nst) {
+                    fence_proxy_async_shared();  // every warp's reads of the slot before the copies overwrite it
+                    issue(t + S);
+                }
+            }
         }
-        // sum the warps' partial outputs (the ring is free now)
-        float* red_o = reinterpret_cast<float*>(dsm);  // [warp][G][D]
-#pragma unroll
-        for (int h = 0; h < G; h++)
-#pragma unroll
-            for (int e = 0; e < DV; e++) red_o[(warp * G + h) * D + lane * DV + e] = acc[h][e];
+    }
+    __syncthreads();
+    if (abort_f) {  // drain the copies still in flight before the ring is reused or the CTA exits
+        if (tid == 0)
+            for (int i = 0; i < S; i++)
+                if (issues[i]) {
+                    mbar_wait_bounded(&kfull[i], (issues[i] - 1u) & 1u);
+                    mbar_wait_bounded(&vfull[i], (issues[i] - 1u) & 1u);
+                }
         __syncthreads();
-        for (int t = tid; t < G * D; t += kDecThreads) {
-            float o = 0.f;
+    }
+    // ---- combine the warps' states into the CTA's partial (the ring is free now)
+    float* red_o = reinterpret_cast<float*>(dsm);  // [warp][G][D]
 #pragma unroll
-            for (int w = 0; w < kDecWarps; w++) o += red_o[w * G * D + t];
-            my[(t / D) * PST + t % D] = o;
+    for (int h = 0; h < G; h++)
+#pragma unroll
+        for (int e = 0; e < DV; e++) red_o[(warp * G + h) * D + lane * DV + e] = acc[h][e];
+    if (lane < LPK && li % LPH == 0) {
+        wm[warp][hl] = m_run;
+        wl[warp][hl] = l_run;
+    }
+    __syncthreads();
+    if (nl > 0) {
+        for (int t = tid; t < G * D; t += NT) {
+            const int h = t / D, d = t % D;
+            float M = -CUDART_INF_F;
+#pragma unroll
+            for (int w = 0; w < NW; w++) M = fmaxf(M, wm[w][h]);
+            float o = 0.f, l = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; w++) {
+                const float e = wm[w][h] == -CUDART_INF_F ? 0.f : __expf(wm[w][h] - M);
+                o = fmaf(e, red_o[(w * G + h) * D + d], o);
+                l = fmaf(e, wl[w][h], l);
+            }
+            my[h * PST + d] = o;
+            if (d == 0) {  // an aborted split publishes a NaN weight, so the merged output of its kv head is NaN
+                my[h * PST + D] = abort_f ? 0.f : M;
+                my[h * PST + D + 1] = abort_f ? CUDART_NAN_F : l;
+            }
         }
-        if (tid < G) {  // an aborted split publishes a NaN weight, so the merged output of its kv head is NaN
-            my[tid * PST + D] = abort_f ? 0.f : m_s[tid];
-            my[tid * PST + D + 1] = abort_f ? CUDART_NAN_F : l_s[tid];
-        }
-    } else {
-        pdl_wait();  // the output and the split scratch are in use until the previous kernels finish
-        if (CL)      // an empty split: zero output, zero weight
-            for (int t = tid; t < G * PST; t += kDecThreads) po[t] = (t % PST == D) ? -CUDART_INF_F : 0.f;
+    } else if (CL) {  // an empty split: zero output, zero weight
+        for (int t = tid; t < G * PST; t += NT) po[t] = (t % PST == D) ? -CUDART_INF_F : 0.f;
     }
     if constexpr (CL) {
         __shared__ float wc[kC][G];  // merge weights of the cluster's splits
@@ -393,15 +425,15 @@ __global__ void __launch_bounds__(kDecThreads, (!CL && G <= 4) ? 2 : 1)
         __syncthreads();
         // output slice of this CTA (cluster rank s): all kC partial values of each output in flight together
         constexpr int OPC = G * D / kC;
-        for (int t = tid; t < OPC; t += kDecThreads) {
+        for (int t = tid; t < OPC; t += NT) {
             const int o = s * OPC + t, h = o / D, d = o % D;
             float v[kC];
 #pragma unroll
             for (int r = 0; r < kC; r++) v[r] = ld_dsmem(&po[h * PST + d], r);
-            float acc = 0.f;
+            float acc2 = 0.f;
 #pragma unroll
-            for (int r = 0; r < kC; r++) acc = fmaf(wc[r][h], v[r], acc);
-            out[(int64_t)(g * G + h) * D + d] = acc;
+            for (int r = 0; r < kC; r++) acc2 = fmaf(wc[r][h], v[r], acc2);
+            out[(int64_t)(g * G + h) * D + d] = acc2;
         }
         cluster_sync();  // no CTA leaves while another still reads its partial
         return;
@@ -420,12 +452,13 @@ __global__ void __launch_bounds__(kDecThreads, (!CL && G <= 4) ? 2 : 1)
     // batch of those partial-row loads into registers first, while warp h forms head h's weights with its
     // lanes over the splits, so the partials and the weights arrive in about one L2 round trip.
     constexpr int NF = G * D / 4;                // float4 outputs of the group
-    constexpr int P = kDecThreads / NF;          // threads per output float4
+    constexpr int P = NT / NF;          // threads per output float4
     constexpr int kBatch = 16;                   // partial loads in flight per thread
-    static_assert(P >= 1 && P * NF == kDecThreads, "merge mapping");
+    static_assert(P >= 1 && P * NF == NT, "merge mapping");
     const float* pg = part + ((int64_t)g * ns * G) * PST;
-    float* wm = sc;                // [ns_eff][G] split maxima, then merge weights
-    float* wl = sc + ns_eff * G;   // [ns_eff][G] split sums
+    // [ns_eff][G] split maxima (then merge weights) and sums, after the combine's scratch in the ring
+    float* mm = reinterpret_cast<float*>(dsm + NW * G * D * sizeof(float));
+    float* ml = mm + ns_eff * G;
     const int f = tid % NF, ph = tid / NF, hf = (4 * f) / D, df = (4 * f) % D;
     float4 v[kBatch];
     auto load_batch = [&](int s0) {
@@ -441,19 +474,19 @@ __global__ void __launch_bounds__(kDecThreads, (!CL && G <= 4) ? 2 : 1)
         const int h = warp;
         float M = -CUDART_INF_F;
         for (int ss = lane; ss < ns_eff; ss += 32) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(pg + ((int64_t)ss * G + h) * PST + D));
-            wm[ss * G + h] = ml.x;
-            wl[ss * G + h] = ml.y;
-            M = fmaxf(M, ml.x);
+            const float2 mlv = __ldcg(reinterpret_cast<const float2*>(pg + ((int64_t)ss * G + h) * PST + D));
+            mm[ss * G + h] = mlv.x;
+            ml[ss * G + h] = mlv.y;
+            M = fmaxf(M, mlv.x);
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float den = 0.f;
-        for (int ss = lane; ss < ns_eff; ss += 32) den = fmaf(__expf(wm[ss * G + h] - M), wl[ss * G + h], den);
+        for (int ss = lane; ss < ns_eff; ss += 32) den = fmaf(__expf(mm[ss * G + h] - M), ml[ss * G + h], den);
 #pragma unroll
         for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
         const float inv = 1.f / den;
-        for (int ss = lane; ss < ns_eff; ss += 32) wm[ss * G + h] = __expf(wm[ss * G + h] - M) * inv;
+        for (int ss = lane; ss < ns_eff; ss += 32) mm[ss * G + h] = __expf(mm[ss * G + h] - M) * inv;
     }
     __syncthreads();
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -463,7 +496,7 @@ __global__ void __launch_bounds__(kDecThreads, (!CL && G <= 4) ? 2 : 1)
         for (int i = 0; i < kBatch; i++) {
             const int ss = s0 + i * P;
             if (ss < ns_eff) {
-                const float w = wm[ss * G + hf];
+                const float w = mm[ss * G + hf];
                 a.x = fmaf(w, v[i].x, a.x);
                 a.y = fmaf(w, v[i].y, a.y);
                 a.z = fmaf(w, v[i].z, a.z);
@@ -499,9 +532,10 @@ template <int D, int G, typename KT, bool CL>
 cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int max_ctx, const int* pos_dev, int pos,
                             const AttnScratch& scr, int ns, float* out, int KVH, cudaStream_t s) {
     if (CL) ns = kC;
-    const int cap = std::max((max_ctx + ns - 1) / ns, std::max(2 * ns, kMinPerSplit));  // scores, or 2 merge words per split
-    const size_t smem =
-        (size_t)dec_stages<D, KT, CL>() * dec_tile<D, KT>() * D * sizeof(KT) + (size_t)cap * G * sizeof(float);
+    const int nw = CL ? kClWarps : kDecWarps;
+    // the ring; after the loop it holds the warps' outputs [nw][G][D], then the merge's [ns][G] maxima and sums
+    const size_t smem = (size_t)dec_stages<D, KT, CL>() * 2 * dec_tile<D, KT>() * D * sizeof(KT);
+    if ((size_t)nw * G * D * 4 + (size_t)ns * G * 8 > smem) return cudaErrorInvalidValue;
     if (smem > 222 * 1024) return cudaErrorInvalidValue;  // with the static shared memory, within 227 KB
     auto k = attn_decode_kernel<D, G, KT, CL>;
     // the largest dynamic shared memory this instantiation was opened to, per device (set before a launch
@@ -516,13 +550,14 @@ cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int 
         std::lock_guard<std::mutex> lk(mu);
         if (opened[dev] < (int)smem) {
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (!e && CL) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e) return e;
             opened[dev] = (int)smem;
         }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ns, KVH);
-    cfg.blockDim = dim3(kDecThreads);
+    cfg.blockDim = dim3(nw * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -551,7 +586,42 @@ cudaError_t dispatch_decode(const float* q, const void* kc, const void* vc, int 
 
 }  // namespace
 
-bool attn_decode_uses_cluster(int max_ctx) { return max_ctx <= kC * kClMaxSplit; }
+// Whether this device can schedule the cluster path's clusters (kC CTAs of one SM's worth of shared memory);
+// asked once per device.
+bool cluster_path_available() {
+    static int state[kMaxDevices] = {};  // 0 unknown, 1 yes, 2 no
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (!state[dev]) {
+        auto k = attn_decode_kernel<128, 4, __half, true>;
+        const int smem = dec_stages<128, __half, true>() * 2 * 16384;
+        int n = 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kC, 8);
+        cfg.blockDim = dim3(kClWarps * 32);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kC;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (!e) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (!e) e = cudaOccupancyMaxActiveClusters(&n, k, &cfg);
+        if (e) cudaGetLastError();
+        state[dev] = (!e && n > 0) ? 1 : 2;
+    }
+    return state[dev] == 1;
+}
+
+bool attn_decode_uses_cluster(int max_ctx) { return max_ctx <= kC * kClMaxSplit && cluster_path_available(); }
 
 bool attn_supported(int H, int KVH, int D) {
     if (KVH <= 0 || H % KVH) return false;
@@ -560,12 +630,10 @@ bool attn_supported(int H, int KVH, int D) {
 }
 
 int attn_decode_splits(int n_heads, int n_kv_heads, int max_ctx) {
-    // two CTAs per SM over all kv heads (their serial per-tile work overlaps); more splits only if a
-    // split's scores would not fit
-    int ns = 2 * num_sms() / n_kv_heads;
-    const int G = n_heads / n_kv_heads;
-    const int need = (int)(((int64_t)max_ctx * G * 4 + kMaxScores - 1) / kMaxScores);
-    if (ns < need) ns = need;
+    // two CTAs per SM over all kv heads (one wave)
+    (void)n_heads;
+    (void)max_ctx;
+    const int ns = 2 * num_sms() / n_kv_heads;
     return ns < 1 ? 1 : ns;
 }
 

@@ -270,10 +270,11 @@ int af_attention_decode(const float* q_dev, const void* k_dev, const void* v_dev
  * not synchronise `stream`.
  * Scratch: one file-scope device array of this library (4 MiB of split
  * partials + 1024 arrival counters + an error word), used only when ctx >
- * 2048 (shorter caches take the cluster path, which merges in shared memory).
+ * 2048 (shorter caches take the cluster path, which merges in distributed
+ * shared memory, where the device can schedule 8-CTA clusters).
  * On that path, calls with n_kv_heads > 1024 or whose partials need more than
- * 2^20 floats (n_heads * splits * (head_dim + 4), splits = max(2 * SMs /
- * n_kv_heads, ceil(ctx * G / 16384))) return AF_ERANGE before launching.
+ * 2^20 floats (n_heads * splits * (head_dim + 4), splits = max(1, 2 * SMs /
+ * n_kv_heads)) return AF_ERANGE before launching.
  * Errors on the device: the call does not wait for the kernel, so it cannot
  * report AF_ETIMEOUT; if a bounded device-side wait gives up, every output
  * value of the affected kv heads is NaN instead.

@@ -136,10 +136,10 @@ def test_static_attention_rejects_oversize():
     L = af.lib()
     # (caches above 2048 slots: the split path, the only one that uses the fixed scratch)
     # more kv heads than arrival counters
-    assert L.af_attention_decode_static(1, 1, 1, af.AF_F16, 1028, 1028, 64, 4096, 0, 1, None) == af.AF_ERANGE
+    assert L.af_attention_decode_static(1, 1, 1, af.AF_F16, 1028, 1028, 64, 16384, 0, 1, None) == af.AF_ERANGE
     assert "n_kv_heads" in af.af_last_error()
     # partials: 8192 heads x >= 1 split x 132 floats > 2^20
-    assert L.af_attention_decode_static(1, 1, 1, af.AF_F16, 8192, 1024, 128, 4096, 0, 1, None) == af.AF_ERANGE
+    assert L.af_attention_decode_static(1, 1, 1, af.AF_F16, 8192, 1024, 128, 16384, 0, 1, None) == af.AF_ERANGE
     assert "partials" in af.af_last_error()
     assert af.af_kv_bytes(af.af_config()) == 0
 

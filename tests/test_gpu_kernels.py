@@ -175,6 +175,9 @@ ATTN_CASES = [  # H, KVH, D, ctx, pos, kv dtype
     (32, 8, 128, 32768, 30720, "f32"), (32, 8, 128, 32768, 30783, "f32"), (16, 16, 128, 300, 299, "f16"),
     # one kv head: many splits, split length not dividing the sequence; ragged last tile
     (8, 1, 64, 10000, 9728, "f16"), (8, 1, 128, 4096, 4000, "f32"), (2, 2, 64, 200, 130, "f32"),
+    # group 8 with head_dim 128 and group 2 on either path; a cache just above the cluster path's
+    (64, 8, 128, 8192, 5000, "f16"), (64, 8, 128, 2048, 1500, "f16"), (16, 8, 64, 3000, 2999, "f32"),
+    (16, 8, 64, 1024, 1000, "f16"), (32, 8, 128, 2049, 2048, "f16"),
 ]
 
 

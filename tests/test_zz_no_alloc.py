@@ -41,9 +41,11 @@ def _case(seed, H, KVH, D, ctx, kvt):
             q, kc, vc)
 
 
-CALLS = [  # two calls in a row each: H, KVH, D, ctx, pos, kv dtype
-    [(32, 8, 128, 4096, 4095, "f16"), (32, 8, 128, 4096, 1000, "f16")],
+CALLS = [  # two calls in a row each: H, KVH, D, ctx, pos, kv dtype (above 2048 slots: the split path, which uses
+    # the fixed scratch; up to 2048: the cluster path)
+    [(32, 8, 128, 12288, 12287, "f16"), (32, 8, 128, 12288, 1000, "f16")],
     [(8, 4, 64, 512, 511, "f32"), (64, 8, 128, 2048, 2047, "f32")],
+    [(32, 4, 64, 3000, 2999, "f32"), (32, 8, 128, 2048, 2047, "f16")],
 ]
 
 
