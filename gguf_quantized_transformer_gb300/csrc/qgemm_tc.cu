@@ -1,8 +1,16 @@
 // Prefill GEMM on the 5th-generation tensor cores: Y[m][n] = sum_k X[m][k] W[n][k]
-// with W in Q4_0 / Q8_0 / Q4_K / Q5_K / Q6_K planes, dequantized tile by tile into shared memory
+// with W in Q4_0 / Q8_0 / Q4_K / Q5_K / Q6_K planes, dequantized tile by tile
 // and multiplied with tcgen05.mma into a TMEM accumulator (dotLLM "GPU
 // Inference", "Weight Strategy", approach 1: fused dequantize-in-kernel feeding
 // the tensor cores; dequantized values never touch device memory).
+//
+// Operands.  The MMA computes D[n][m] = sum_k W[n][k] X[m][k]: A is the
+// dequantized weight tile (128 rows of W = the 128 TMEM lanes), written by the
+// dequantizing warps straight from registers into tensor memory (tcgen05.st),
+// so it costs no shared-memory bandwidth; B is the X tile (BT = 128 or 256
+// rows of X), loaded by TMA into shared memory in the SWIZZLE_128B K-major
+// layout.  The accumulator holds one W row per TMEM lane and one X row per
+// column, so the epilogue's stores of a token run along n (coalesced).
 //
 // Precision.  A single fp16 product would round X and W to 11 significant
 // bits.  X arrives split as X_hi + X_lo (two fp16 planes written by the
@@ -11,18 +19,18 @@
 // integer code c, w_lo = fma(d, c, -w_hi) by HFMA2), and from an fp32 value
 // for the K-quants (formed from the unpacked sub-block scale and min).  Three
 // MMAs per K step accumulate
-//   X_hi W_hi + X_lo W_hi + X_hi W_lo
-// in fp32 (the dropped X_lo W_lo term is ~2^-22 relative); see TcCfg for the
-// measured cost of dropping X_hi W_lo.
+//   W_hi X_hi + W_hi X_lo + W_lo X_hi
+// in fp32 (the dropped W_lo X_lo term is ~2^-22 relative); see kProducts for the
+// measured cost of dropping W_lo X_hi.
 //
-// Tile 128 (rows of X) x BN (rows of W: 256, or 128 when N is small so the
-// grid still covers the SMs) x 64 (K), two to four stages (192 KB) in shared
-// memory, SWIZZLE_128B K-major operand layout:
+// Tile 128 (W rows) x BT (X rows) x 64 (K), S stages of the X tile in shared
+// memory and of the W tile in tensor memory:
 //   warp 0      : TMA producer for the X_hi / X_lo tiles (cp.async.bulk.tensor.2d)
 //   warp 1      : TMEM allocation; one lane issues the MMAs and commits
-//   warps 2..9  : dequantize the W tile (256 / BN threads per weight row) into
-//                 the W_hi (and W_lo) tiles; the raw blocks of the next K step
-//                 are loaded into registers before waiting for a free stage;
+//   warps 2..9  : two groups of four warps (one per TMEM lane quadrant) take
+//                 alternate K steps: load the raw blocks of their 32 rows two
+//                 steps ahead into registers, dequantize, split and store the
+//                 W_hi / W_lo tile into the stage's TMEM columns;
 //                 warps 2..5 then run the fused epilogue from TMEM
 //                 (tcgen05.ld, 32 columns at a time).
 // Every mbarrier wait is bounded; on a timeout the CTA records DEV_TIMEOUT,
@@ -39,27 +47,27 @@ namespace af {
 
 namespace {
 
-constexpr int BM = 128, BK = 64;
-constexpr int kATile = BM * BK * 2;  // 16 KB per fp16 plane
+constexpr int BW = 128, BK = 64;   // W rows (MMA M, TMEM lanes) and K per step
 constexpr int kThreads = 10 * 32;
-constexpr int kDequantThreads = 8 * 32;
 constexpr int kMaxStages = 4;
+constexpr int kTmemCols = 512;
 
-// Every weight keeps its fp16 remainder W_lo as a third product X_hi W_lo.  Rounding W to fp16 alone (two MMAs,
-// one stage more in the same shared memory) measured 17.3k against 15.4k prefill tok/s on the 8B Q4_0 shape, but
-// its worst layer error on a 17-token prompt was 1.67e-2 of the 2e-2 RMS bar (5.6e-3 with the third product), and
-// the bar is a maximum over all elements: a 4096-token prompt has ~240x more of them, which puts the expected
-// maximum near 2.05e-2.  The 8B Q4_K_M model reached 2.05e-2 already on the short prompt.
-template <int WT, int BN>
+// Every weight keeps its fp16 remainder W_lo as a third product W_lo X_hi.  Rounding W to fp16 alone (two MMAs)
+// measured 17.3k against 15.4k prefill tok/s on the 8B Q4_0 shape with the previous tile layout, but its worst
+// layer error on a 17-token prompt was 1.67e-2 of the 2e-2 RMS bar (5.6e-3 with the third product), and the bar is
+// a maximum over all elements: a 4096-token prompt has ~240x more of them, which puts the expected maximum near
+// 2.05e-2.  The 8B Q4_K_M model reached 2.05e-2 already on the short prompt.
+constexpr int kProducts = 3;
+
+template <int BT>
 struct TcCfg {
-    static constexpr bool kWLo = true;  // W_lo tile and third MMA
-    static constexpr int kBTile = BN * BK * 2;  // one fp16 plane
-    static constexpr int kStageBytes = 2 * kATile + (kWLo ? 2 : 1) * kBTile;
-    static constexpr int kStages = kWLo ? (BN == 256 ? 2 : 3) : (BN == 256 ? 3 : 4);  // 192 KB of stages
+    static constexpr int kXTile = BT * BK * 2;                    // one fp16 plane of the X tile
+    static constexpr int kStageBytes = 2 * kXTile;                // X_hi, X_lo
+    static constexpr int kStages = BT == 256 ? 3 : 4;             // 192 / 128 KB of X stages
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
-    static constexpr int TPR = kDequantThreads / BN;                // dequant threads per weight row
-    static constexpr int BPT = 2 / TPR;                              // 32-weight blocks per thread per K step
-    static constexpr uint32_t kIdesc = idesc_f16(BM, BN);
+    static constexpr int kACol = BT;                              // W stages: 64 TMEM columns each after D
+    static_assert(kACol + 64 * kStages <= kTmemCols, "TMEM columns");
+    static constexpr uint32_t kIdesc = idesc_f16(BW, BT);
 };
 
 // One 32-weight block as loaded from the weight rows: quant bytes and the fp16 scale bits.
@@ -300,13 +308,13 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 }
 
 struct TcSmem {
-    uint64_t full_a[kMaxStages];  // X tiles landed (TMA transaction bytes)
-    uint64_t full_b[kMaxStages];  // W tiles written (kDequantThreads arrivals)
-    uint64_t empty[kMaxStages];   // MMAs reading the stage finished (commit)
-    uint64_t done;                // all MMAs finished (commit)
+    uint64_t xfull[kMaxStages];  // X tiles landed (TMA transaction bytes)
+    uint64_t afull[kMaxStages];  // W tile stored in TMEM (one arrival per quadrant warp)
+    uint64_t empty[kMaxStages];  // MMAs reading the stage finished (commit)
+    uint64_t done;               // all MMAs finished (commit)
     uint32_t tmem_base;
     volatile int abort;
-    int issued_a;  // X tile loads issued so far
+    int issued_x;  // X tile loads issued so far
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, unsigned parity, TcSmem& sm, unsigned* err) {
@@ -319,40 +327,66 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, unsigned parity, Tc
     return false;
 }
 
-template <int WT, int BN>
+// Epilogue of one quadrant warp: lane l holds W row n (= n0 + 32 quad + l) of the accumulator, i.e. output
+// column n for every X row of the tile.  The fused epilogues take adjacent column pairs (n, n + 1) of one output
+// row, so lanes 2p and 2p + 1 trade halves: for tokens j (even) and j + 1, lane 2p gets row 2p + 1's value of
+// token j and lane 2p + 1 gets row 2p's value of token j + 1; each lane then applies the pair of one token.
+template <int KIND>
+__device__ __forceinline__ void epi_pair_k(const Epi& e, int m, int n, float v0, float v1) {
+    Epi k = e;
+    k.kind = KIND;  // constant: the switch in epi_pair folds away
+    epi_pair(k, m, n, v0, v1);
+}
+
+template <int KIND, int BT>
+__device__ __forceinline__ void epilogue(const Epi& epi, uint32_t lane_base, int lane, int n, int N, int m0, int M) {
+    const int np = n & ~1;  // the pair's first column
+    const bool odd = lane & 1;
+    for (int c0 = 0; c0 < BT; c0 += 32) {
+        float v[32];
+        tmem_ld32(lane_base + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 1], 1);
+            const int m = m0 + c0 + j + (odd ? 1 : 0);
+            const float v0 = odd ? got : v[j], v1 = odd ? v[j + 1] : got;
+            if (m < M && np < N) epi_pair_k<KIND>(epi, m, np, v0, v1);
+        }
+    }
+}
+
+template <int WT, int BT>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo, Planes W,
                     int M, Epi epi, unsigned* err) {
-    using C = TcCfg<WT, BN>;
+    using C = TcCfg<BT>;
     constexpr int kStages = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     __shared__ TcSmem sm;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int n0 = blockIdx.x * BW, m0 = blockIdx.y * BT;
     const int nk = (W.K + BK - 1) / BK;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; s++) {
-            mbar_init(&sm.full_a[s], 1);
-            mbar_init(&sm.full_b[s], kDequantThreads);
+            mbar_init(&sm.xfull[s], 1);
+            mbar_init(&sm.afull[s], 4);
             mbar_init(&sm.empty[s], 1);
         }
         mbar_init(&sm.done, 1);
         sm.abort = 0;
-        sm.issued_a = 0;
+        sm.issued_x = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(&sm.tmem_base, BN);  // fp32 accumulator, BN columns
+    if (warp == 1) tmem_alloc(&sm.tmem_base, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    auto a_hi = [&](int s) { return smem + s * C::kStageBytes; };
-    auto a_lo = [&](int s) { return smem + s * C::kStageBytes + kATile; };
-    auto b_hi = [&](int s) { return smem + s * C::kStageBytes + 2 * kATile; };
-    auto b_lo = [&](int s) { return smem + s * C::kStageBytes + 2 * kATile + C::kBTile; };
+    auto x_hi = [&](int s) { return smem + s * C::kStageBytes; };
+    auto x_lo = [&](int s) { return smem + s * C::kStageBytes + C::kXTile; };
 
     if (warp == 0) {
         // ---------------- TMA producer: X_hi, X_lo tiles
@@ -360,10 +394,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ks = 0; ks < nk; ks++) {
                 const int s = ks % kStages, u = ks / kStages;
                 if (u > 0 && !wait_or_abort(&sm.empty[s], (u - 1) & 1, sm, err)) break;
-                mbar_arrive_expect_tx(&sm.full_a[s], 2 * kATile);
-                tma_load_2d(a_hi(s), &map_hi, ks * BK, m0, &sm.full_a[s]);
-                tma_load_2d(a_lo(s), &map_lo, ks * BK, m0, &sm.full_a[s]);
-                sm.issued_a = ks + 1;
+                mbar_arrive_expect_tx(&sm.xfull[s], 2 * C::kXTile);
+                tma_load_2d(x_hi(s), &map_hi, ks * BK, m0, &sm.xfull[s]);
+                tma_load_2d(x_lo(s), &map_lo, ks * BK, m0, &sm.xfull[s]);
+                sm.issued_x = ks + 1;
             }
         }
     } else if (warp == 1) {
@@ -371,76 +405,85 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             for (int ks = 0; ks < nk; ks++) {
                 const int s = ks % kStages, u = ks / kStages;
-                if (!wait_or_abort(&sm.full_a[s], u & 1, sm, err)) break;
-                if (!wait_or_abort(&sm.full_b[s], u & 1, sm, err)) break;
+                if (!wait_or_abort(&sm.xfull[s], u & 1, sm, err)) break;
+                if (!wait_or_abort(&sm.afull[s], u & 1, sm, err)) break;
                 tc_fence_after();
-                const uint32_t ah = smem_u32(a_hi(s)), al = smem_u32(a_lo(s));
-                const uint32_t bh = smem_u32(b_hi(s)), bl = smem_u32(b_lo(s));
+                const uint32_t bh = smem_u32(x_hi(s)), bl = smem_u32(x_lo(s));
+                const uint32_t ah = tmem + (uint32_t)(C::kACol + 64 * s), al = ah + 32;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; kk++) {  // 16 fp16 = 32 bytes along K per MMA
-                    const uint32_t off = kk * 32;
+                for (int kk = 0; kk < BK / 16; kk++) {  // 16 fp16 along K per MMA: 8 TMEM columns, 32 bytes of B
                     const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
-                    mma_f16(tmem, umma_desc_sw128(ah + off), umma_desc_sw128(bh + off), C::kIdesc, acc);
-                    mma_f16(tmem, umma_desc_sw128(al + off), umma_desc_sw128(bh + off), C::kIdesc, 1u);
-                    if (C::kWLo) mma_f16(tmem, umma_desc_sw128(ah + off), umma_desc_sw128(bl + off), C::kIdesc, 1u);
+                    const uint64_t dh = umma_desc_sw128(bh + kk * 32), dl = umma_desc_sw128(bl + kk * 32);
+                    mma_f16_ts(tmem, ah + kk * 8, dh, C::kIdesc, acc);
+                    mma_f16_ts(tmem, ah + kk * 8, dl, C::kIdesc, 1u);
+                    if (kProducts == 3) mma_f16_ts(tmem, al + kk * 8, dh, C::kIdesc, 1u);
                 }
-                mma_commit(&sm.empty[s]);  // frees the stage when these MMAs complete
+                mma_commit(&sm.empty[s]);  // frees the stage (X smem and W TMEM) when these MMAs complete
             }
             mma_commit(&sm.done);  // always: also after a break, so the drain can wait on it
         }
     } else {
-        // ---------------- dequantize W rows into the fp16 hi / lo tiles
-        const int dt = tid - 64;                // 0..255
-        const int r = dt / C::TPR;              // weight row n0 + r of the tile
-        const int bsel = dt % C::TPR;           // which block of a K step (two threads per row)
+        // ---------------- dequantize W rows into the stage's TMEM columns
+        const int quad = warp & 3;            // TMEM lanes this warp may access
+        const int grp = (warp - 2) >> 2;      // K steps grp, grp + 2, ...
+        const int r = quad * 32 + lane;       // weight row n0 + r = TMEM lane
         const int n = n0 + r;
         const bool valid = n < W.N;
-        RawBlk<WT> cur[C::BPT], nxt[C::BPT];
-        auto fetch = [&](int ks, RawBlk<WT> (&b)[C::BPT]) {
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        // the raw blocks of this group's next two K steps are in flight while one is converted (weights mostly
+        // come from DRAM: about four K steps of MMA time hide that latency)
+        RawBlk<WT> cur[2], nxt[2], nxt2[2];
+        auto fetch = [&](int ks, RawBlk<WT> (&b)[2]) {
 #pragma unroll
-            for (int i = 0; i < C::BPT; i++) {
-                if (valid) load_blk(W, n, ks * 2 + (C::TPR == 1 ? i : bsel), b[i]);
+            for (int i = 0; i < 2; i++) {
+                if (valid && ks < nk) load_blk(W, n, ks * 2 + i, b[i]);
                 else zero_blk(b[i]);
             }
         };
-        fetch(0, cur);
-        for (int ks = 0; ks < nk; ks++) {
+        fetch(grp, cur);
+        fetch(grp + 2, nxt);
+        for (int ks = grp; ks < nk; ks += 2) {
             const int s = ks % kStages, u = ks / kStages;
-            if (ks + 1 < nk) fetch(ks + 1, nxt);  // next K step's blocks in flight while this one is converted
-            if (u > 0 && !wait_or_abort(&sm.empty[s], (u - 1) & 1, sm, err)) break;
+            fetch(ks + 4, nxt2);
+            uint32_t hi[32], lo[32];
 #pragma unroll
-            for (int i = 0; i < C::BPT; i++) {
-                uint4 hi[4], lo[4];
-                deq_blk(cur[i], hi, lo);
-                const int c0 = 4 * (C::TPR == 1 ? i : bsel);  // first 16-byte chunk of this block in the row
+            for (int i = 0; i < 2; i++) {
+                uint4 h4[4], l4[4];
+                deq_blk(cur[i], h4, l4);
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
-                    *reinterpret_cast<uint4*>(b_hi(s) + sw128(r, c0 + q)) = hi[q];
-                    if (C::kWLo) *reinterpret_cast<uint4*>(b_lo(s) + sw128(r, c0 + q)) = lo[q];
+                    hi[16 * i + 4 * q + 0] = h4[q].x; hi[16 * i + 4 * q + 1] = h4[q].y;
+                    hi[16 * i + 4 * q + 2] = h4[q].z; hi[16 * i + 4 * q + 3] = h4[q].w;
+                    lo[16 * i + 4 * q + 0] = l4[q].x; lo[16 * i + 4 * q + 1] = l4[q].y;
+                    lo[16 * i + 4 * q + 2] = l4[q].z; lo[16 * i + 4 * q + 3] = l4[q].w;
                 }
             }
-            fence_proxy_async_shared();  // generic-proxy writes -> visible to the tensor core
-            mbar_arrive(&sm.full_b[s]);
+            // the stage's previous MMAs must be done before its W columns are overwritten (warp-uniform wait)
+            if (u > 0 && !__all_sync(0xffffffffu, wait_or_abort(&sm.empty[s], (u - 1) & 1, sm, err))) break;
+            tc_fence_after();
+            const uint32_t col = (uint32_t)(C::kACol + 64 * s);
+            tmem_st32(lane_base + col, hi);
+            if (kProducts == 3) tmem_st32(lane_base + col + 32, lo);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.afull[s]);
 #pragma unroll
-            for (int i = 0; i < C::BPT; i++) cur[i] = nxt[i];
+            for (int i = 0; i < 2; i++) {
+                cur[i] = nxt[i];
+                nxt[i] = nxt2[i];
+            }
         }
         // ---------------- epilogue (warps 2..5: TMEM lane quadrant = warp % 4)
         if (warp < 6) {
-            // tcgen05.ld below is warp-collective: the whole warp takes the same branch
+            // tcgen05.ld is warp-collective: the whole warp takes the same branch
             if (__all_sync(0xffffffffu, wait_or_abort(&sm.done, 0, sm, err))) {
                 tc_fence_after();
-                const int quad = warp & 3;
-                const int m = m0 + quad * 32 + lane;
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    float v[32];
-                    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0, v);
-                    if (m < M) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 2) {
-                            const int nn = n0 + c0 + j;
-                            if (nn < W.N) epi_pair(epi, m, nn, v[j], v[j + 1]);
-                        }
-                    }
+                switch (epi.kind) {  // one loop per kind, so the loop body has no dispatch
+                    case EPI_RESID: epilogue<EPI_RESID, BT>(epi, lane_base, lane, n, W.N, m0, M); break;
+                    case EPI_QKV: epilogue<EPI_QKV, BT>(epi, lane_base, lane, n, W.N, m0, M); break;
+                    case EPI_SWIGLU: epilogue<EPI_SWIGLU, BT>(epi, lane_base, lane, n, W.N, m0, M); break;
+                    default: epilogue<EPI_STORE, BT>(epi, lane_base, lane, n, W.N, m0, M); break;
                 }
             }
         }
@@ -450,13 +493,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (sm.abort && tid == 0) {  // let every MMA and copy that was issued finish before leaving
         mbar_wait_bounded(&sm.done, 0);
         // loads older than the last kStages were consumed by the MMA issuer, i.e. complete
-        for (int ks = max(0, sm.issued_a - kStages); ks < sm.issued_a; ks++)
-            mbar_wait_bounded(&sm.full_a[ks % kStages], (ks / kStages) & 1);
+        for (int ks = max(0, sm.issued_x - kStages); ks < sm.issued_x; ks++)
+            mbar_wait_bounded(&sm.xfull[ks % kStages], (ks / kStages) & 1);
     }
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_free(tmem, BN);
+        tmem_free(tmem, kTmemCols);
     }
 }
 
@@ -477,13 +520,13 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D map over an fp16 [rows][ld] plane, box 64 (K) x 128 (rows), SWIZZLE_128B, zero fill out of bounds.
-bool make_map(CUtensorMap* map, const __half* base, int rows, int cols, int64_t ld) {
+// 2-D map over an fp16 [rows][ld] plane, box 64 (K) x box_rows, SWIZZLE_128B, zero fill out of bounds.
+bool make_map(CUtensorMap* map, const __half* base, int rows, int cols, int64_t ld, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    const cuuint32_t box[2] = {BK, BM};
+    const cuuint32_t box[2] = {BK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -505,9 +548,9 @@ cudaError_t qgemm_prepare() {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_prep_mu);
     if (g_prepared[dev]) return cudaSuccess;
-#define AF_QGEMM_ATTR(WT, BN)                                                                                  \
-    if (!e) e = cudaFuncSetAttribute(qgemm_tc_kernel<WT, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                     TcCfg<WT, BN>::kSmemBytes);
+#define AF_QGEMM_ATTR(WT, BT)                                                                                  \
+    if (!e) e = cudaFuncSetAttribute(qgemm_tc_kernel<WT, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                     TcCfg<BT>::kSmemBytes);
     AF_QGEMM_ATTR(AF_Q4_0, 256)
     AF_QGEMM_ATTR(AF_Q4_0, 128)
     AF_QGEMM_ATTR(AF_Q8_0, 256)
@@ -528,27 +571,28 @@ cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo
     if (M < 1) return cudaSuccess;
     if (ldx % 8 || (reinterpret_cast<uintptr_t>(X_hi) & 15) || (reinterpret_cast<uintptr_t>(X_lo) & 15))
         return cudaErrorInvalidValue;  // TMA: 16-byte aligned base and row stride
+    const int nt = (W.N + BW - 1) / BW;
+    // 256 X rows per tile (W dequantized once per 256 rows) unless that leaves SMs without a tile
+    const bool wide = (int64_t)nt * ((M + 255) / 256) >= num_sms();
+    const int BT = wide ? 256 : 128;
     CUtensorMap mh, ml;
-    if (!make_map(&mh, X_hi, M, W.K, ldx) || !make_map(&ml, X_lo, M, W.K, ldx)) return cudaErrorInvalidValue;
-    const int mt = (M + BM - 1) / BM;
-    // 256-wide tiles unless that leaves a third or more of the SMs without a tile
-    const bool narrow = (int64_t)((W.N + 255) / 256) * mt * 3 < (int64_t)num_sms() * 2;
-#define AF_QGEMM_LAUNCH(WT, BN)                                                                                   \
-    qgemm_tc_kernel<WT, BN><<<dim3((W.N + BN - 1) / BN, mt), kThreads, TcCfg<WT, BN>::kSmemBytes, s>>>(mh, ml, W, M, epi, \
-                                                                                                 err)
-#define AF_QGEMM_TYPES(BN)                                          \
+    if (!make_map(&mh, X_hi, M, W.K, ldx, BT) || !make_map(&ml, X_lo, M, W.K, ldx, BT)) return cudaErrorInvalidValue;
+    const dim3 grid(nt, (M + BT - 1) / BT);
+#define AF_QGEMM_LAUNCH(WT, BTV) \
+    qgemm_tc_kernel<WT, BTV><<<grid, kThreads, TcCfg<BTV>::kSmemBytes, s>>>(mh, ml, W, M, epi, err)
+#define AF_QGEMM_TYPES(BTV)                                         \
     switch (W.wtype) {                                              \
-        case AF_Q4_0: AF_QGEMM_LAUNCH(AF_Q4_0, BN); break;          \
-        case AF_Q8_0: AF_QGEMM_LAUNCH(AF_Q8_0, BN); break;          \
-        case AF_Q4_K: AF_QGEMM_LAUNCH(AF_Q4_K, BN); break;          \
-        case AF_Q5_K: AF_QGEMM_LAUNCH(AF_Q5_K, BN); break;          \
-        case AF_Q6_K: AF_QGEMM_LAUNCH(AF_Q6_K, BN); break;          \
+        case AF_Q4_0: AF_QGEMM_LAUNCH(AF_Q4_0, BTV); break;         \
+        case AF_Q8_0: AF_QGEMM_LAUNCH(AF_Q8_0, BTV); break;         \
+        case AF_Q4_K: AF_QGEMM_LAUNCH(AF_Q4_K, BTV); break;         \
+        case AF_Q5_K: AF_QGEMM_LAUNCH(AF_Q5_K, BTV); break;         \
+        case AF_Q6_K: AF_QGEMM_LAUNCH(AF_Q6_K, BTV); break;         \
         default: return cudaErrorInvalidValue;                      \
     }
-    if (narrow) {
-        AF_QGEMM_TYPES(128)
-    } else {
+    if (wide) {
         AF_QGEMM_TYPES(256)
+    } else {
+        AF_QGEMM_TYPES(128)
     }
 #undef AF_QGEMM_TYPES
 #undef AF_QGEMM_LAUNCH

@@ -268,7 +268,9 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // dotLLM, "CUDA components": a quantized KV cache, "Q8_0/Q4_0 + FP16 window".  The pages name the parts only.
 // Reading: a slot is written in fp16; once it lies outside the step's window (slot <= b - W, b = the step's
 // last position, W = kv_window) it is replaced by the Q8_0 / Q4_0 quantization of its fp16 values, per
-// 32-element block along head_dim.  The quantizer takes its decisions in fp32 on those fp16 values:
+// 32-element block along head_dim.  A step (a prefill chunk or a decode step) is never longer than the window
+// (n <= W), so a slot retires in a later step than the one that writes it, and every row of a step sees the
+// slots of that step in fp16.  The quantizer takes its decisions in fp32 on those fp16 values:
 //   Q8_0: d = fp16(max|v| / 127), q = clamp(round-half-away(v / d), -127, 127)  (floor(r + 0.5) in fp32), v' = d q
 //   Q4_0: m = the element of largest |v| (first on ties), d = fp16(m / -8),
 //         n = clamp(floor(v / d + 8.5), 0, 15), v' = d (n - 8)
@@ -403,12 +405,16 @@ int orc_layer_offsets(const orc_config* c, uint64_t off[10]) {
     return 0;
 }
 
-// Airframe GPU_PIPELINE.md, "KV cache": L * KVH * max_ctx * head_dim * elem, times 2 (K and V).
+// Airframe GPU_PIPELINE.md, "KV cache": L * KVH * max_ctx * head_dim * elem, times 2 (K and V).  A quantized
+// cache holds every slot twice: in fp16 (as written; a retired slot holds its quantized values there) and in
+// the quantized store of 34 (Q8_0) or 18 (Q4_0) bytes per 32 values ("Shimmy v2.0 Architecture",
+// Quantization).  The fp16 copy is what prefill attention reads; decode reads the quantized store for retired
+// slots, which is where the bandwidth goes.
 uint64_t orc_kv_bytes(const orc_config* c) {
     const uint64_t rows = (uint64_t)c->n_layers * c->n_kv_heads * 2;  // K and V
-    if (c->kv_f16 == KV_Q8_0 || c->kv_f16 == KV_Q4_0)  // quantized store of every slot + fp16 window of kv_window slots
-        return rows * ((uint64_t)c->max_ctx * (c->head_dim / 32) * (c->kv_f16 == KV_Q8_0 ? 34 : 18) +
-                       (uint64_t)c->kv_window * c->head_dim * 2);
+    if (c->kv_f16 == KV_Q8_0 || c->kv_f16 == KV_Q4_0)
+        return rows * c->max_ctx *
+               ((uint64_t)c->head_dim * 2 + (uint64_t)(c->head_dim / 32) * (c->kv_f16 == KV_Q8_0 ? 34 : 18));
     return rows * c->max_ctx * c->head_dim * (c->kv_f16 ? 2 : 4);
 }
 
@@ -595,6 +601,7 @@ int orc_forward(orc_model* m, const int32_t* tokens, int64_t n, int64_t start_po
     const int64_t QD = H * D, KVD = KVH * D;
     const int32_t head_wtype = c.out_wtype ? c.out_wtype : c.wtype;
     const bool quantized_kv = c.kv_f16 == KV_Q8_0 || c.kv_f16 == KV_Q4_0;
+    if (quantized_kv && n > c.kv_window) return -3;  // a step longer than the window (see the reading above)
     const int64_t retire_to = start_pos + n - 1 - c.kv_window;  // last slot outside this step's window
 
     std::vector<double> X(n * E), Y(n * E), Q(n * QD), K(n * KVD), V(n * KVD), A(n * QD), O(n * E);

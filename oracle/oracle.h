@@ -99,7 +99,7 @@ uint64_t orc_kv_bytes(const orc_config* c);
  * KV cache with kv_slots positions (<= max_ctx; 0 means max_ctx). */
 orc_model* orc_model_create(const orc_config* c, const uint8_t* const* layer_blobs, const uint8_t* token_embd,
                             const float* output_norm, const uint8_t* output, int64_t kv_slots);
-/* Forward n tokens at absolute positions start_pos..start_pos+n-1.
+/* Forward n tokens at absolute positions start_pos..start_pos+n-1 (a quantized cache: n <= kv_window, else -3).
  * logits: [n_vocab] for the last row (nullable).  capture: [n_layers+1][n][n_embd]
  * residual stream after the embedding and after each layer (nullable). */
 int orc_forward(orc_model* m, const int32_t* tokens, int64_t n, int64_t start_pos, double* logits, double* capture,

@@ -3,7 +3,7 @@
 dotLLM's CUDA components name a quantized KV cache "Q8_0/Q4_0 + FP16 window" and nothing more; the reading
 (stated in oracle.cpp): a slot is written in fp16, and once it lies more than kv_window positions behind a
 step's last position it is replaced by the Q8_0 / Q4_0 quantization of those fp16 values, per 32-element block
-along head_dim.  Pinned here by rows on the quantization grid (reproduced exactly), the quantization-step bound,
+along head_dim; a step is never longer than the window.  Pinned here by rows on the quantization grid (reproduced exactly), the quantization-step bound,
 a window that covers the whole sequence (bit-exact equality with the fp16 cache), and the slot-by-slot state of
 layer 0, whose K/V rows do not depend on attention.  No GPU needed.
 """
@@ -74,8 +74,9 @@ def test_layer0_slots_quantized_exactly_outside_the_window(kvt):
     hm, q = _model(kvt, W)
     _, f = _model("f16", 0)
     toks = hm.prompt(21)
-    q.forward(toks[:20], 0)
-    f.forward(toks[:20], 0)
+    for p in range(0, 20, 5):  # chunks no longer than the window
+        q.forward(toks[p:p + 5], p)
+        f.forward(toks[p:p + 5], p)
     b = 19
     for s in range(20):
         for g in range(hm.cfg.n_kv_heads):
@@ -99,21 +100,35 @@ def test_layer0_slots_quantized_exactly_outside_the_window(kvt):
 
 
 def test_small_window_deviation_grows_with_coarser_codes():
-    # with a 2-slot window most slots are quantized: the logits move away from the fp16 cache's, less for the
-    # 8-bit codes than for the 4-bit ones
-    _, f = _model("f16", 0)
+    # with a 2-slot window (chunks of 2, then decode steps) most slots are quantized: the logits move away from
+    # the fp16 cache's, less for the 8-bit codes than for the 4-bit ones
     hm, _ = _model("q8_0", 2)
     toks = hm.prompt(24)
-    lf, _ = f.forward(toks, 0)
-    dev = {}
-    for kvt in ("q8_0", "q4_0"):
-        _, q = _model(kvt, 2)
-        lq, _ = q.forward(toks, 0)
-        dev[kvt] = np.max(np.abs(lq - lf)) / np.sqrt(np.mean(lf ** 2))
+
+    def run(kvt):
+        _, m = _model(kvt, 2 if kvt != "f16" else 0)
+        for p in range(0, 20, 2):
+            m.forward(toks[p:p + 2], p, want_logits=False)
+        for p in range(20, 24):
+            lg, _ = m.forward(toks[p:p + 1], p)
+        return lg
+    lf = run("f16")
+    dev = {kvt: np.max(np.abs(run(kvt) - lf)) / np.sqrt(np.mean(lf ** 2)) for kvt in ("q8_0", "q4_0")}
     assert 0 < dev["q8_0"] < dev["q4_0"] < 1.0, dev
 
 
+@pytest.mark.parametrize("kvt", ["q8_0", "q4_0"])
+def test_step_longer_than_the_window_is_refused(kvt):
+    hm, q = _model(kvt, 4)
+    with pytest.raises(ValueError):
+        q.forward(hm.prompt(5), 0)
+    q.forward(hm.prompt(4), 0)  # a chunk of exactly the window is fine
+
+
 def test_quantized_kv_bytes():
+    # Llama-3-8B shape, 8192 slots: 32 layers x 8 kv heads x (K, V) rows of 128 values per slot, each slot held
+    # in fp16 (256 B) and in the Q8_0 store (4 blocks of 34 B: "Shimmy v2.0 Architecture", Quantization) or the
+    # Q4_0 store (4 blocks of 18 B).  Hand-computed: 512 rows x 8192 slots x (256 + 136) B and x (256 + 72) B.
     cfg = synth.CONFIGS[3].with_(kv_dtype="q8_0", kv_window=512)
-    rows = 32 * 8 * 2
-    assert oracle.kv_bytes(cfg) == rows * (8192 * (128 // 32) * 34 + 512 * 128 * 2)
+    assert oracle.kv_bytes(cfg) == 1_644_167_168
+    assert oracle.kv_bytes(cfg.with_(kv_dtype="q4_0")) == 1_375_731_712
