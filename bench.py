@@ -55,8 +55,12 @@ def decode_bytes_per_token(cfg, pos):
                            cfg.n_vocab, cfg.n_layers)
     layer_w = (E * (QD + 2 * KVD) + QD * E + 2 * F * E + F * E) * bpe + 2 * E * 4
     head = V * E * hbpe + E * 4 + E * bpe  # LM head + final norm + one embedding row
-    kvb = 2 if cfg.kv_dtype == "f16" else 4
-    kv = 2 * L * KVD * (pos + 1) * kvb
+    n = pos + 1
+    if cfg.kv_dtype in ("q8_0", "q4_0"):  # retired slots from the quantized store, the window from fp16
+        W = min(cfg.kv_window, n)
+        kv = 2 * L * KVD * ((n - W) * synth.BLOCK_BYTES[cfg.kv_dtype] / 32 + W * 2)
+    else:
+        kv = 2 * L * KVD * n * (2 if cfg.kv_dtype == "f16" else 4)
     return L * layer_w + head + kv
 
 
@@ -499,6 +503,10 @@ def config_runs(af, args, dev, hbm_peak, tc_peak):
             if cfg.max_ctx > 8192:  # long context: decode attention is half the bytes of a token; its roofline
                 line["attn_roofline"] = attn_roofline(af, cfg, cfg.prompt_len, dev, hbm_peak)
             out[f"config{idx}"] = line
+            if cfg.max_ctx > 8192:  # the same workload over a Q8_0 cache with a 512-slot fp16 window
+                qcfg = cfg.with_(kv_dtype="q8_0", kv_window=512)
+                out[f"config{idx}_kv_q8_0"] = workload_run(af, qcfg, synth.seed_of(idx), P, cfg.n_decode, cfg.chunk,
+                                                           dev, hbm_peak, tc_peak, steps=1, warmup=1)
         except Exception as e:  # a failed secondary line must not take the headline with it
             out[f"config{idx}"] = {"error": f"{type(e).__name__}: {e}"}
     return out

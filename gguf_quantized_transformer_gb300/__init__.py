@@ -12,9 +12,9 @@ from ._build import LIB_PATH, build  # noqa: F401
 
 AF_OK, AF_EINVAL, AF_ERANGE, AF_ENOMEM, AF_ECUDA, AF_ETIMEOUT, AF_ENOTIMPL = range(7)
 AF_Q4_0, AF_Q8_0, AF_Q4_K, AF_Q5_K, AF_Q6_K = 2, 8, 12, 13, 14
-AF_F32, AF_F16 = 0, 1
+AF_F32, AF_F16, AF_KV_Q8_0, AF_KV_Q4_0 = 0, 1, 2, 3
 WTYPE = {"q4_0": AF_Q4_0, "q8_0": AF_Q8_0, "q4_k": AF_Q4_K, "q5_k": AF_Q5_K, "q6_k": AF_Q6_K}
-KVTYPE = {"f32": AF_F32, "f16": AF_F16}
+KVTYPE = {"f32": AF_F32, "f16": AF_F16, "q8_0": AF_KV_Q8_0, "q4_0": AF_KV_Q4_0}
 STATUS_NAMES = {0: "AF_OK", 1: "AF_EINVAL", 2: "AF_ERANGE", 3: "AF_ENOMEM", 4: "AF_ECUDA", 5: "AF_ETIMEOUT",
                 6: "AF_ENOTIMPL"}
 
@@ -29,7 +29,8 @@ class af_config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("n_layers", "n_embd", "n_heads", "n_kv_heads", "head_dim", "n_ff",
                                                "n_vocab", "wtype", "kv_dtype", "max_ctx", "native_ctx",
                                                "max_chunk")] + \
-               [("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("out_wtype", ctypes.c_int32)]
+               [("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("out_wtype", ctypes.c_int32),
+                ("kv_window", ctypes.c_int32)]
 
 
 class af_weights(ctypes.Structure):
@@ -62,6 +63,7 @@ def lib():
         L.af_reset.argtypes = [vp]
         L.af_model_sync.argtypes = [vp, vp]
         L.af_model_kv_cache.argtypes = [vp, P(vp), P(vp)]
+        L.af_model_kv_store.argtypes = [vp, P(vp), P(vp), P(vp), P(vp)]
         L.af_model_stream.argtypes = [vp]
         L.af_model_stream.restype = vp
         L.af_debug_capture.argtypes = [vp, vp]
@@ -114,7 +116,7 @@ def make_config(cfg, max_chunk: int = 512) -> af_config:
     """af_config from a ModelConfig-like object (fields as in synth.configs)."""
     return af_config(cfg.n_layers, cfg.n_embd, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.n_ff, cfg.n_vocab,
                      WTYPE[cfg.wtype], KVTYPE[cfg.kv_dtype], cfg.max_ctx, cfg.native_ctx, max_chunk, cfg.rms_eps,
-                     cfg.rope_base, WTYPE[getattr(cfg, "out_wtype", "") or cfg.wtype])
+                     cfg.rope_base, WTYPE[getattr(cfg, "out_wtype", "") or cfg.wtype], getattr(cfg, "kv_window", 0))
 
 
 # ---------------------------------------------------------------- same-name entry points
@@ -171,6 +173,13 @@ def af_model_kv_cache(m):
     k, v = ctypes.c_void_p(), ctypes.c_void_p()
     check(lib().af_model_kv_cache(m, ctypes.byref(k), ctypes.byref(v)))
     return k.value, v.value
+
+
+def af_model_kv_store(m):
+    """(k_codes, k_scales, v_codes, v_scales) device pointers of a quantized cache's store."""
+    p = [ctypes.c_void_p() for _ in range(4)]
+    check(lib().af_model_kv_store(m, *[ctypes.byref(x) for x in p]))
+    return tuple(x.value for x in p)
 
 
 def af_reset(m):

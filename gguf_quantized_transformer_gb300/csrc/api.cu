@@ -63,6 +63,11 @@ size_t row_bytes(int wtype, size_t k) { return k / (size_t)block_elems(wtype) * 
 
 int head_wtype(const af_config* c) { return c->out_wtype ? c->out_wtype : c->wtype; }
 
+bool kv_quantized(const af_config* c) { return c->kv_dtype == AF_KV_Q8_0 || c->kv_dtype == AF_KV_Q4_0; }
+
+// bytes of one element of the (fp32 / fp16) cache; a quantized cache keeps an fp16 copy of every slot
+size_t kv_elem(const af_config* c) { return c->kv_dtype == AF_F32 ? 4 : 2; }
+
 // Tracks device allocations of one object so a failed create frees everything.
 struct Allocs {
     std::vector<void*> p;
@@ -125,7 +130,8 @@ int check_config(const af_config* c) {
     if (!c) return fail(AF_EINVAL, "null config");
     if (!block_bytes(c->wtype)) return fail(AF_EINVAL, "wtype must be AF_Q4_0, AF_Q8_0, AF_Q4_K, AF_Q5_K or AF_Q6_K");
     if (!block_bytes(head_wtype(c))) return fail(AF_EINVAL, "bad out_wtype");
-    if (c->kv_dtype != AF_F32 && c->kv_dtype != AF_F16) return fail(AF_EINVAL, "kv_dtype must be AF_F32 or AF_F16");
+    if (c->kv_dtype != AF_F32 && c->kv_dtype != AF_F16 && !kv_quantized(c))
+        return fail(AF_EINVAL, "kv_dtype must be AF_F32, AF_F16, AF_KV_Q8_0 or AF_KV_Q4_0");
     if (c->n_layers <= 0 || c->n_embd <= 0 || c->n_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
         c->n_ff <= 0 || c->n_vocab <= 0 || c->max_ctx <= 0)
         return fail(AF_EINVAL, "all sizes must be positive");
@@ -139,6 +145,13 @@ int check_config(const af_config* c) {
     if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return fail(AF_EINVAL, "bad rms_eps / rope_base");
     if (!attn_supported(c->n_heads, c->n_kv_heads, c->head_dim))
         return fail(AF_ENOTIMPL, "attention supports head_dim 64/128 and group size 1/2/4/8");
+    if (kv_quantized(c)) {
+        const int chunk = c->max_chunk ? c->max_chunk : 512;
+        if (c->kv_window < chunk)
+            return fail(AF_EINVAL, "kv_window (%d) must be at least max_chunk (%d): a step may not outrun the window",
+                        c->kv_window, chunk);
+        if (c->max_ctx % 4) return fail(AF_ENOTIMPL, "a quantized cache needs max_ctx a multiple of 4");
+    }
     if (c->n_embd % 64 || c->n_ff % 64 || (c->n_heads * c->head_dim) % 64 || c->n_vocab % 2)
         return fail(AF_ENOTIMPL, "n_embd, n_ff, n_heads*head_dim must be multiples of 64 and n_vocab even");
     {
@@ -195,8 +208,23 @@ struct af_model {
     int E() const { return c.n_embd; }
     int QD() const { return c.n_heads * c.head_dim; }
     int KVD() const { return c.n_kv_heads * c.head_dim; }
-    void* kl(int l) const { return (char*)kc + (size_t)l * kv_layer_elems * (c.kv_dtype == AF_F16 ? 2 : 4); }
-    void* vl(int l) const { return (char*)vc + (size_t)l * kv_layer_elems * (c.kv_dtype == AF_F16 ? 2 : 4); }
+    KvStore kvq;  // quantized store (kvq.qtype == 0: the cache is not quantized)
+
+    void* kl(int l) const { return (char*)kc + (size_t)l * kv_layer_elems * kv_elem(&c); }
+    void* vl(int l) const { return (char*)vc + (size_t)l * kv_layer_elems * kv_elem(&c); }
+    KvLayerStore kvq_layer(int l) const {
+        KvLayerStore q;
+        if (!kvq.qtype) return q;
+        const size_t rows = (size_t)l * kv_layer_elems / c.head_dim;  // slot rows before layer l
+        const int cb = kv_code_bytes(kvq.qtype, c.head_dim);
+        q.kq = kvq.kq + rows * cb;
+        q.vq = kvq.vq + rows * cb;
+        q.ks = kvq.ks + rows * (c.head_dim / 32);
+        q.vs = kvq.vs + rows * (c.head_dim / 32);
+        q.qtype = kvq.qtype;
+        q.window = kvq.window;
+        return q;
+    }
 };
 
 namespace {
@@ -209,7 +237,7 @@ Epi epi_qkv_plan(af_model* m, int l) {
     e.kvd = m->KVD();
     e.head_dim = m->c.head_dim;
     e.max_ctx = m->c.max_ctx;
-    e.kv_f16 = m->c.kv_dtype == AF_F16;
+    e.kv_f16 = m->c.kv_dtype != AF_F32;
     e.kcache = m->kl(l);
     e.vcache = m->vl(l);
     e.rope = m->rope;
@@ -269,7 +297,14 @@ int af_layer_offsets(const af_config* c, uint64_t off[10]) {
 
 uint64_t af_kv_bytes(const af_config* c) {
     if (!c || c->n_layers <= 0 || c->n_kv_heads <= 0 || c->max_ctx <= 0 || c->head_dim <= 0) return 0;
-    return (uint64_t)c->n_layers * c->n_kv_heads * c->max_ctx * c->head_dim * (c->kv_dtype == AF_F16 ? 2 : 4) * 2;
+    const uint64_t rows = (uint64_t)c->n_layers * c->n_kv_heads * 2;
+    if (kv_quantized(c)) {
+        if (c->head_dim % 32) return 0;
+        return rows * c->max_ctx *
+               ((uint64_t)c->head_dim * 2 + (uint64_t)(c->head_dim / 32) * (c->kv_dtype == AF_KV_Q8_0 ? 34 : 18));
+    }
+    if (c->kv_dtype != AF_F32 && c->kv_dtype != AF_F16) return 0;
+    return rows * c->max_ctx * c->head_dim * (c->kv_dtype == AF_F16 ? 2 : 4);
 }
 
 void af_model_destroy(af_model* m) {
@@ -367,11 +402,22 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
 
     // KV cache, RoPE table
     m->kv_layer_elems = (size_t)c.n_kv_heads * c.max_ctx * D;
-    const size_t kvb = af_kv_bytes(&c) / 2;
+    const size_t kvb = (size_t)c.n_layers * m->kv_layer_elems * kv_elem(&c);  // K (or V) cache, fp16 when quantized
     m->kc = A.get(kvb);
     m->vc = A.get(kvb);
     m->rope = (float2*)A.get((size_t)c.max_ctx * (D / 2) * sizeof(float2));
     if (!m->kc || !m->vc || !m->rope) return oom("KV cache");
+    if (kv_quantized(&c)) {  // the quantized store: codes and scales of every slot row
+        const size_t rows = (size_t)c.n_layers * c.n_kv_heads * c.max_ctx;
+        const int cb = kv_code_bytes(c.kv_dtype, D);
+        m->kvq.qtype = c.kv_dtype;
+        m->kvq.window = c.kv_window;
+        m->kvq.kq = (uint8_t*)A.get(rows * cb);
+        m->kvq.vq = (uint8_t*)A.get(rows * cb);
+        m->kvq.ks = (__half*)A.get(rows * (D / 32) * 2);
+        m->kvq.vs = (__half*)A.get(rows * (D / 32) * 2);
+        if (!m->kvq.kq || !m->kvq.vq || !m->kvq.ks || !m->kvq.vs) return oom("quantized KV store");
+    }
     const double ys = (c.native_ctx > 0 && c.max_ctx > c.native_ctx) ? (double)c.max_ctx / c.native_ctx : 1.0;
     {
         cudaError_t e = cudaMemsetAsync(m->kc, 0, kvb, s);
@@ -430,7 +476,8 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
         P.abort = words + 2;
         P.err = m->gs.err;
         std::vector<LayerPlan> lp(c.n_layers);
-        bool ok = head_wtype(&c) == wt;  // the persistent kernel decodes every matrix as one type
+        // the persistent kernel decodes every matrix as one type and reads an fp32 / fp16 cache
+        bool ok = head_wtype(&c) == wt && !kv_quantized(&c);
         for (int l = 0; l < c.n_layers; l++) {
             const LayerW& lw = m->L[l];
             LayerPlan& L = lp[l];
@@ -503,9 +550,19 @@ int af_model_kv_cache(const af_model* m, void** k_dev, void** v_dev) {
     return AF_OK;
 }
 
+int af_model_kv_store(const af_model* m, void** k_codes, void** k_scales, void** v_codes, void** v_scales) {
+    if (!m || !k_codes || !k_scales || !v_codes || !v_scales) return fail(AF_EINVAL, "null argument");
+    if (!m->kvq.qtype) return fail(AF_EINVAL, "the model's KV cache is not quantized");
+    *k_codes = m->kvq.kq;
+    *k_scales = m->kvq.ks;
+    *v_codes = m->kvq.vq;
+    *v_scales = m->kvq.vs;
+    return AF_OK;
+}
+
 int af_reset(af_model* m) {
     if (!m) return fail(AF_EINVAL, "null model");
-    const size_t kvb = af_kv_bytes(&m->c) / 2;
+    const size_t kvb = (size_t)m->c.n_layers * m->kv_layer_elems * kv_elem(&m->c);
     CK(cudaMemsetAsync(m->kc, 0, kvb, m->s));
     CK(cudaMemsetAsync(m->vc, 0, kvb, m->s));
     CK(cudaMemsetAsync(m->gs.err, 0, 4, m->s));
@@ -568,7 +625,7 @@ Epi epi_qkv(af_model* m, int l, float* qout, const int* pos_dev, int pos0) {
     e.kvd = m->KVD();
     e.head_dim = m->c.head_dim;
     e.max_ctx = m->c.max_ctx;
-    e.kv_f16 = m->c.kv_dtype == AF_F16;
+    e.kv_f16 = m->c.kv_dtype != AF_F32;
     e.kcache = m->kl(l);
     e.vcache = m->vl(l);
     e.rope = m->rope;
@@ -585,11 +642,16 @@ int decode_body(af_model* m, float* logits) {
     CK(launch_embed(m->emb, &m->st->token, 1, m->x, m->E(), s));
     int rc = capture_copy(m, 0, 1);
     if (rc) return rc;
+    // a quantized cache: the slot that leaves the window in this step (pos - window) retires, in every layer
+    if (m->kvq.qtype)
+        CK(launch_kv_retire(m->kvq, (__half*)m->kc, (__half*)m->vc, c.n_layers, c.n_kv_heads, c.max_ctx, c.head_dim,
+                            pos_dev, 0, 1, s));
     for (int l = 0; l < c.n_layers; l++) {
         const LayerW& lw = m->L[l];
+        const KvLayerStore qs = m->kvq_layer(l);
         CK(launch_qgemv(lw.qkv, m->x, lw.attn_norm, c.rms_eps, epi_qkv(m, l, m->q, pos_dev, 0), m->gs, s));
-        CK(launch_attn_decode(m->q, m->kl(l), m->vl(l), c.kv_dtype == AF_F16, c.n_heads, c.n_kv_heads, c.head_dim,
-                              c.max_ctx, pos_dev, 0, m->as, m->attn, s));
+        CK(launch_attn_decode(m->q, m->kl(l), m->vl(l), c.kv_dtype != AF_F32, c.n_heads, c.n_kv_heads, c.head_dim,
+                              c.max_ctx, pos_dev, 0, m->as, m->attn, s, qs.qtype ? &qs : nullptr));
         CK(launch_qgemv(lw.o, m->attn, nullptr, 0.f, epi_simple(EPI_RESID, m->x, m->E()), m->gs, s));
         CK(launch_qgemv(lw.gu, m->x, lw.ffn_norm, c.rms_eps, epi_simple(EPI_SWIGLU, m->h, c.n_ff), m->gs, s));
         CK(launch_qgemv(lw.down, m->h, nullptr, 0.f, epi_simple(EPI_RESID, m->x, m->E()), m->gs, s));
@@ -610,12 +672,16 @@ int prefill_impl(af_model* m, const int* tok_dev, int n, int start_pos, float* l
     CK(launch_embed(m->emb, tok_dev, n, m->x, E, s));
     int rc = capture_copy(m, 0, n);
     if (rc) return rc;
+    // a quantized cache: the n slots that leave the window in this step retire before any attention reads them
+    if (m->kvq.qtype)
+        CK(launch_kv_retire(m->kvq, (__half*)m->kc, (__half*)m->vc, c.n_layers, c.n_kv_heads, c.max_ctx, c.head_dim,
+                            nullptr, start_pos - m->kvq.window, n, s));
     for (int l = 0; l < c.n_layers; l++) {
         const LayerW& lw = m->L[l];
         CK(launch_rmsnorm_rows(m->x, n, E, lw.attn_norm, c.rms_eps, m->y16[0], m->y16[1], s));
         CK(launch_qgemm(lw.qkv, m->y16[0], m->y16[1], E, n, epi_qkv(m, l, m->q, nullptr, start_pos),
                         m->gs.err, s));
-        CK(launch_attn_prefill(m->q, QD, m->kl(l), m->vl(l), c.kv_dtype == AF_F16, c.n_heads, c.n_kv_heads,
+        CK(launch_attn_prefill(m->q, QD, m->kl(l), m->vl(l), c.kv_dtype != AF_F32, c.n_heads, c.n_kv_heads,
                                c.head_dim, c.max_ctx, start_pos, n, m->a16[0], m->a16[1], QD, m->gs.err, s));
         CK(launch_qgemm(lw.o, m->a16[0], m->a16[1], QD, n, epi_simple(EPI_RESID, m->x, E), m->gs.err, s));
         CK(launch_rmsnorm_rows(m->x, n, E, lw.ffn_norm, c.rms_eps, m->y16[0], m->y16[1], s));

@@ -528,6 +528,430 @@ __global__ void __launch_bounds__(CL ? kClWarps * 32 : kDecThreads, (!CL && G <=
     if (tid == 0) cnt[g] = 0u;
 }
 
+// ---------------------------------------------------------------------------------------------------------
+// Decode attention over a quantized cache (AF_KV_Q8_0 / AF_KV_Q4_0, split path): the slots that left the window
+// (below cut = pos + 1 - window) are read from the quantized store, the window from the fp16 cache.  A CTA's
+// range [j0, j0 + nl) (j0 a multiple of 4) is cut at `cut` into a store segment, streamed in stages of TQ slots
+// (codes and scales of K, then of V: four bulk copies), and an fp16 segment, streamed as in attn_decode_kernel.
+// The per-warp online softmax, the combine and the split merge are attn_decode_kernel's.
+
+// One warp's share of one stage: scores of its slots, online-softmax update, P V.  ldk(j, li, kf) gives the 8
+// K values of slot j at dims li*8.., ldv(j, lane, vf) the DV V values at dims lane*DV..; wait_v() waits for the
+// stage's V data (false: give up).  Returns false if it gave up.
+template <int D, int G, int SPW, class LoadK, class LoadV, class WaitV>
+__device__ __forceinline__ bool warp_stage(const float (&qv)[G][8], int keys, int warp, int lane, LoadK ldk, LoadV ldv,
+                                           WaitV wait_v, float& m_run, float& l_run, float (&acc)[G][D / 32],
+                                           float (*pw)[G], float* cw) {
+    constexpr int LPK = D / 8, KPW = 32 / LPK, LPH = LPK / G, STEPS = SPW / KPW, DV = D / 32;
+    const int li = lane % LPK, ks = lane / LPK, hl = li / LPH;
+    float sreg[STEPS];
+    float mt = -CUDART_INF_F;
+#pragma unroll
+    for (int st = 0; st < STEPS; st++) {
+        const int j = warp * SPW + st * KPW + ks;
+        float kf[8];
+        if (j < keys) {
+            ldk(j, li, kf);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++) kf[e] = 0.f;
+        }
+        float a[G];
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            a[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; e++) a[h] = fmaf(qv[h][e], kf[e], a[h]);
+        }
+#pragma unroll
+        for (int half = G / 2, bit = LPK / 2; half >= 1; half >>= 1, bit >>= 1) {
+            const bool up = li & bit;
+#pragma unroll
+            for (int k = 0; k < half; k++) {
+                const float send = up ? a[k] : a[k + half], keep = up ? a[k + half] : a[k];
+                a[k] = keep + __shfl_xor_sync(0xffffffffu, send, bit);
+            }
+        }
+        float r = a[0];
+#pragma unroll
+        for (int bit = LPH / 2; bit >= 1; bit >>= 1) r += __shfl_xor_sync(0xffffffffu, r, bit);
+        sreg[st] = j < keys ? r : -CUDART_INF_F;
+        mt = fmaxf(mt, sreg[st]);
+    }
+#pragma unroll
+    for (int o = LPK; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+    const float m_new = fmaxf(m_run, mt);
+    const float corr = m_new == -CUDART_INF_F ? 1.f : __expf(m_run - m_new);
+    float psum = 0.f;
+#pragma unroll
+    for (int st = 0; st < STEPS; st++) {
+        const float p = sreg[st] == -CUDART_INF_F ? 0.f : __expf(sreg[st] - m_new);
+        psum += p;
+        if (li % LPH == 0) pw[st * KPW + ks][hl] = p;
+    }
+#pragma unroll
+    for (int o = LPK; o < 32; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+    l_run = fmaf(l_run, corr, psum);
+    m_run = m_new;
+    if (lane < LPK && li % LPH == 0) cw[hl] = corr;
+    __syncwarp();
+    if (!wait_v()) return false;
+#pragma unroll
+    for (int h = 0; h < G; h++) {
+        const float c = cw[h];
+#pragma unroll
+        for (int e = 0; e < DV; e++) acc[h][e] *= c;
+    }
+#pragma unroll
+    for (int jj = 0; jj < SPW; jj++) {
+        const int j = warp * SPW + jj;
+        if (j < keys) {
+            float vf[DV];
+            ldv(j, lane, vf);
+#pragma unroll
+            for (int h = 0; h < G; h++) {
+                const float p = pw[jj][h];
+#pragma unroll
+                for (int e = 0; e < DV; e++) acc[h][e] = fmaf(p, vf[e], acc[h][e]);
+            }
+        }
+    }
+    __syncwarp();
+    return true;
+}
+
+constexpr int kQTile = 128;             // slots per store stage
+constexpr int kRingQ = 104 * 1024;      // ring budget of the quantized-cache kernel (two CTAs per SM)
+
+template <int D, int QT>
+struct KvqCfg {
+    static constexpr int TS = dec_tile<D, __half>();                      // fp16 stage slots
+    static constexpr int CB = QT == AF_KV_Q8_0 ? D : D / 2;               // code bytes per slot
+    static constexpr int SB = D / 32 * 2;                                 // scale bytes per slot
+    static constexpr int QCODES = kQTile * CB, QSC = kQTile * SB;         // bytes of one K (or V) store tile
+    static constexpr int FST = 2 * TS * D * 2;                            // fp16 stage
+    static constexpr int QST = 2 * (QCODES + QSC);                        // store stage
+    static constexpr int SLOT = ((FST > QST ? FST : QST) + 127) / 128 * 128;
+    static constexpr int S = kRingQ / SLOT < kMaxStages ? kRingQ / SLOT : kMaxStages;
+};
+
+template <int D, int G, int QT>
+__global__ void __launch_bounds__(kDecThreads, G <= 4 ? 2 : 1)
+    attn_decode_kvq_kernel(const float* __restrict__ q, const __half* __restrict__ kc, const __half* __restrict__ vc,
+                           KvLayerStore qs, int max_ctx, const int* __restrict__ pos_dev, int pos_arg,
+                           float* __restrict__ part, unsigned* __restrict__ cnt, float* __restrict__ out,
+                           unsigned* __restrict__ err) {
+    using C = KvqCfg<D, QT>;
+    constexpr int S = C::S, TS = C::TS, NW = kDecWarps, NT = kDecThreads;
+    constexpr int LPK = D / 8, LPH = LPK / G, DV = D / 32;
+    constexpr int SPWF = TS / NW, SPWQ = kQTile / NW, SPWM = SPWF > SPWQ ? SPWF : SPWQ;
+    static_assert(S >= 2, "ring depth");
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ uint64_t kfull[kMaxStages], vfull[kMaxStages];
+    __shared__ unsigned issues[kMaxStages], done[kMaxStages];
+    __shared__ __align__(16) float pw[NW][SPWM][G];
+    __shared__ float cw[NW][G];
+    __shared__ float wm[NW][G], wl[NW][G];
+    __shared__ unsigned last;
+    __shared__ volatile int abort_f;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = blockIdx.y, s = blockIdx.x, ns = gridDim.x;
+    pdl_launch_dependents();
+    const int pos = pos_dev ? *pos_dev : pos_arg;
+    const int n = pos + 1;
+    const int cut = max(0, n - qs.window);  // slots below cut have retired (the newest, cut - 1, in this step)
+    int ns_eff, chunk;
+    dec_split(n, ns, ns_eff, chunk);
+    chunk = (chunk + 3) & ~3;  // store tiles start on 4-slot boundaries (16-byte aligned scale copies)
+    ns_eff = (n + chunk - 1) / chunk;
+    const int j0 = s * chunk;
+    const int nl = s < ns_eff ? min(n, j0 + chunk) - j0 : 0;
+    const int qb = min(max(cut, j0), j0 + nl);  // store segment [j0, qb), fp16 segment [qb, j0 + nl)
+    const int nstq = (qb - j0 + kQTile - 1) / kQTile;
+    const int nst = nstq + (j0 + nl - qb + TS - 1) / TS;
+    const int64_t rb = (int64_t)g * max_ctx;  // first slot row of this kv head in the layer
+    constexpr int PST = D + 4;
+    float* my = part + ((int64_t)(g * ns + s) * G) * PST;
+
+    if (tid == 0) {
+        for (int i = 0; i < S; i++) {
+            mbar_init(&kfull[i], 1);
+            mbar_init(&vfull[i], 1);
+            issues[i] = 0;
+            done[i] = 0;
+        }
+        abort_f = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto stage_keys = [&](int t) {
+        return t < nstq ? min(kQTile, qb - j0 - t * kQTile) : min(TS, j0 + nl - qb - (t - nstq) * TS);
+    };
+    auto issue = [&](int t) {  // one thread: stage t into slot t % S
+        const int slot = t % S, keys = stage_keys(t);
+        uint8_t* dst = dsm + slot * C::SLOT;
+        issues[slot]++;
+        if (t < nstq) {
+            const int64_t j = rb + j0 + (int64_t)t * kQTile;
+            const int k4 = (keys + 3) & ~3;  // whole 4-slot groups (max_ctx is a multiple of 4)
+            const unsigned cbytes = (unsigned)(k4 * C::CB), sbytes = (unsigned)(k4 * C::SB);
+            mbar_arrive_expect_tx(&kfull[slot], cbytes + sbytes);
+            bulk_g2s(dst, qs.kq + j * C::CB, cbytes, &kfull[slot]);
+            bulk_g2s(dst + C::QCODES, reinterpret_cast<const uint8_t*>(qs.ks) + j * C::SB, sbytes, &kfull[slot]);
+            mbar_arrive_expect_tx(&vfull[slot], cbytes + sbytes);
+            bulk_g2s(dst + C::QCODES + C::QSC, qs.vq + j * C::CB, cbytes, &vfull[slot]);
+            bulk_g2s(dst + 2 * C::QCODES + C::QSC, reinterpret_cast<const uint8_t*>(qs.vs) + j * C::SB, sbytes,
+                     &vfull[slot]);
+        } else {
+            const int64_t j = rb + qb + (int64_t)(t - nstq) * TS;
+            const unsigned bytes = (unsigned)(keys * D * 2);
+            mbar_arrive_expect_tx(&kfull[slot], bytes);
+            bulk_g2s(dst, kc + j * D, bytes, &kfull[slot]);
+            mbar_arrive_expect_tx(&vfull[slot], bytes);
+            bulk_g2s(dst + TS * D * 2, vc + j * D, bytes, &vfull[slot]);
+        }
+    };
+    // stages holding slot pos (written by this step's QKV) or slot cut - 1 (retired in this step) wait for the
+    // previous kernels; the rest stream in before
+    if (tid == 0 && nst > 0) {
+        bool waited = false;
+        for (int t = 0; t < min(S, nst); t++) {
+            const bool late = (t == nst - 1 && j0 + nl == n) || (t == nstq - 1 && qb == cut && cut > j0);
+            if (late && !waited) {
+                pdl_wait();
+                waited = true;
+            }
+            issue(t);
+        }
+    }
+    pdl_wait();
+
+    const int li = lane % LPK, hl = li / LPH;
+    float qv[G][8];
+    {
+        const float scale = rsqrtf((float)D);
+#pragma unroll
+        for (int h = 0; h < G; h++) {
+            const float4 a = *reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8);
+            const float4 b = *reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8 + 4);
+            qv[h][0] = a.x * scale; qv[h][1] = a.y * scale; qv[h][2] = a.z * scale; qv[h][3] = a.w * scale;
+            qv[h][4] = b.x * scale; qv[h][5] = b.y * scale; qv[h][6] = b.z * scale; qv[h][7] = b.w * scale;
+        }
+    }
+    float m_run = -CUDART_INF_F, l_run = 0.f;
+    float acc[G][DV];
+#pragma unroll
+    for (int h = 0; h < G; h++)
+#pragma unroll
+        for (int e = 0; e < DV; e++) acc[h][e] = 0.f;
+
+    auto wait_tile = [&](uint64_t* bar, unsigned par) {
+        bool ok = false;
+        for (unsigned it = 0; it < kWaitLimit && !ok; it++) {
+            ok = mbar_try_wait(bar, par);
+            if (!ok && abort_f) break;
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0 && !abort_f) {
+            abort_f = 1;
+            atomicExch(err, (unsigned)DEV_TIMEOUT);
+        }
+        return ok;
+    };
+
+    for (int t = 0; t < nst; t++) {
+        const int slot = t % S;
+        const unsigned par = (unsigned)((t / S) & 1);
+        const int keys = stage_keys(t);
+        if (!wait_tile(&kfull[slot], par)) break;
+        const uint8_t* base = dsm + slot * C::SLOT;
+        auto wait_v = [&]() { return wait_tile(&vfull[slot], par); };
+        bool ok;
+        if (t < nstq) {
+            const uint8_t* kq8 = base;
+            const __half* ksc = reinterpret_cast<const __half*>(base + C::QCODES);
+            const uint8_t* vq8 = base + C::QCODES + C::QSC;
+            const __half* vsc = reinterpret_cast<const __half*>(base + 2 * C::QCODES + C::QSC);
+            auto ldk = [&](int j, int l8, float (&kf)[8]) {
+                const float d = __half2float(ksc[j * (D / 32) + l8 / 4]);
+                if (QT == AF_KV_Q8_0) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(kq8 + j * C::CB + l8 * 8);
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        kf[e] = (float)(int)(signed char)(w.x >> (8 * e)) * d;
+                        kf[4 + e] = (float)(int)(signed char)(w.y >> (8 * e)) * d;
+                    }
+                } else {
+                    const unsigned w = *reinterpret_cast<const unsigned*>(kq8 + j * C::CB + l8 * 4);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) kf[e] = (float)((int)((w >> (4 * e)) & 15u) - 8) * d;
+                }
+            };
+            auto ldv = [&](int j, int ln, float (&vf)[DV]) {
+                const float d = __half2float(vsc[j * (D / 32) + (ln * DV) / 32]);
+                if (QT == AF_KV_Q8_0) {
+                    if (DV == 4) {
+                        const unsigned w = *reinterpret_cast<const unsigned*>(vq8 + j * C::CB + ln * 4);
+#pragma unroll
+                        for (int e = 0; e < DV; e++) vf[e] = (float)(int)(signed char)(w >> (8 * e)) * d;
+                    } else {
+                        const unsigned short w = *reinterpret_cast<const unsigned short*>(vq8 + j * C::CB + ln * 2);
+#pragma unroll
+                        for (int e = 0; e < DV; e++) vf[e] = (float)(int)(signed char)(w >> (8 * e)) * d;
+                    }
+                } else {
+                    unsigned w;
+                    if (DV == 4) w = *reinterpret_cast<const unsigned short*>(vq8 + j * C::CB + ln * 2);
+                    else w = vq8[j * C::CB + ln];
+#pragma unroll
+                    for (int e = 0; e < DV; e++) vf[e] = (float)((int)((w >> (4 * e)) & 15u) - 8) * d;
+                }
+            };
+            ok = warp_stage<D, G, SPWQ>(qv, keys, warp, lane, ldk, ldv, wait_v, m_run, l_run, acc,
+                                        reinterpret_cast<float(*)[G]>(&pw[warp][0][0]), cw[warp]);
+        } else {
+            const __half* kt = reinterpret_cast<const __half*>(base);
+            const __half* vt = reinterpret_cast<const __half*>(base + TS * D * 2);
+            auto ldk = [&](int j, int l8, float (&kf)[8]) { load_vec<__half>(kt + j * D + l8 * 8, kf, 8); };
+            auto ldv = [&](int j, int ln, float (&vf)[DV]) { load_small<DV>(vt + j * D + ln * DV, vf); };
+            ok = warp_stage<D, G, SPWF>(qv, keys, warp, lane, ldk, ldv, wait_v, m_run, l_run, acc,
+                                        reinterpret_cast<float(*)[G]>(&pw[warp][0][0]), cw[warp]);
+        }
+        if (!ok) break;
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&done[slot], 1u) == (unsigned)NW - 1u) {
+                done[slot] = 0;
+                if (t + S < nst) {
+                    fence_proxy_async_shared();
+                    issue(t + S);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (abort_f) {
+        if (tid == 0)
+            for (int i = 0; i < S; i++)
+                if (issues[i]) {
+                    mbar_wait_bounded(&kfull[i], (issues[i] - 1u) & 1u);
+                    mbar_wait_bounded(&vfull[i], (issues[i] - 1u) & 1u);
+                }
+        __syncthreads();
+    }
+    float* red_o = reinterpret_cast<float*>(dsm);  // [warp][G][D]
+#pragma unroll
+    for (int h = 0; h < G; h++)
+#pragma unroll
+        for (int e = 0; e < DV; e++) red_o[(warp * G + h) * D + lane * DV + e] = acc[h][e];
+    if (lane < LPK && li % LPH == 0) {
+        wm[warp][hl] = m_run;
+        wl[warp][hl] = l_run;
+    }
+    __syncthreads();
+    if (nl > 0)
+        for (int t = tid; t < G * D; t += NT) {
+            const int h = t / D, d = t % D;
+            float M = -CUDART_INF_F;
+#pragma unroll
+            for (int w = 0; w < NW; w++) M = fmaxf(M, wm[w][h]);
+            float o = 0.f, l = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; w++) {
+                const float e = wm[w][h] == -CUDART_INF_F ? 0.f : __expf(wm[w][h] - M);
+                o = fmaf(e, red_o[(w * G + h) * D + d], o);
+                l = fmaf(e, wl[w][h], l);
+            }
+            my[h * PST + d] = o;
+            if (d == 0) {
+                my[h * PST + D] = abort_f ? 0.f : M;
+                my[h * PST + D + 1] = abort_f ? CUDART_NAN_F : l;
+            }
+        }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last = (atomicAdd(&cnt[g], 1u) == (unsigned)ns - 1u);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    // merge the ns_eff partials of this kv head (as attn_decode_kernel's split path)
+    float* mm = reinterpret_cast<float*>(dsm + NW * G * D * sizeof(float));
+    const float* pg = part + ((int64_t)g * ns * G) * PST;
+    if (warp < G) {
+        const int h = warp;
+        float M = -CUDART_INF_F;
+        for (int ss = lane; ss < ns_eff; ss += 32) M = fmaxf(M, __ldcg(pg + ((int64_t)ss * G + h) * PST + D));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float den = 0.f;
+        for (int ss = lane; ss < ns_eff; ss += 32) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(pg + ((int64_t)ss * G + h) * PST + D));
+            const float e = __expf(ml.x - M);
+            mm[ss * G + h] = e;
+            den = fmaf(e, ml.y, den);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        const float inv = 1.f / den;
+        for (int ss = lane; ss < ns_eff; ss += 32) mm[ss * G + h] *= inv;
+    }
+    __syncthreads();
+    for (int t = tid; t < G * D; t += NT) {
+        const int h = t / D, d = t % D;
+        float a = 0.f;
+#pragma unroll 8
+        for (int ss = 0; ss < ns_eff; ss++) a = fmaf(mm[ss * G + h], __ldcg(pg + ((int64_t)ss * G + h) * PST + d), a);
+        out[(int64_t)(g * G + h) * D + d] = a;
+    }
+    if (tid == 0) cnt[g] = 0u;
+}
+
+template <int D, int G, int QT>
+cudaError_t launch_kvq_t(const float* q, const void* kc, const void* vc, const KvLayerStore& qs, int max_ctx,
+                         const int* pos_dev, int pos, const AttnScratch& scr, int ns, float* out, int KVH,
+                         cudaStream_t s) {
+    using C = KvqCfg<D, QT>;
+    const size_t smem = (size_t)C::S * C::SLOT;
+    if ((size_t)kDecWarps * G * D * 4 + (size_t)ns * G * 4 > smem) return cudaErrorInvalidValue;
+    auto k = attn_decode_kvq_kernel<D, G, QT>;
+    static int opened[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!opened[dev]) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e) return e;
+            opened[dev] = 1;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ns, KVH);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, q, (const __half*)kc, (const __half*)vc, qs, max_ctx, pos_dev, pos, scr.part,
+                              scr.cnt, out, scr.err);
+}
+
+template <int D, int G>
+cudaError_t dispatch_kvq(const float* q, const void* kc, const void* vc, const KvLayerStore& qs, int max_ctx,
+                         const int* pos_dev, int pos, const AttnScratch& scr, int ns, float* out, int KVH,
+                         cudaStream_t s) {
+    if (qs.qtype == AF_KV_Q8_0)
+        return launch_kvq_t<D, G, AF_KV_Q8_0>(q, kc, vc, qs, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
+    return launch_kvq_t<D, G, AF_KV_Q4_0>(q, kc, vc, qs, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
+}
+
 template <int D, int G, typename KT, bool CL>
 cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int max_ctx, const int* pos_dev, int pos,
                             const AttnScratch& scr, int ns, float* out, int KVH, cudaStream_t s) {
@@ -654,8 +1078,17 @@ size_t attn_decode_part_elems(int n_heads, int head_dim, int ns) { return (size_
 
 cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, int kv_f16, int H, int KVH, int D,
                                int max_ctx, const int* pos_dev, int pos, const AttnScratch& scr, float* out,
-                               cudaStream_t s) {
+                               cudaStream_t s, const KvLayerStore* qs) {
     const int G = H / KVH;
+    if (qs && qs->qtype) {  // quantized cache: split path over the store and the fp16 window
+        const int ns = attn_decode_splits(H, KVH, max_ctx);
+        if (scr.ns < ns || max_ctx % 4) return cudaErrorInvalidValue;
+        if ((reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc) | reinterpret_cast<uintptr_t>(qs->kq) |
+             reinterpret_cast<uintptr_t>(qs->vq) | reinterpret_cast<uintptr_t>(qs->ks) |
+             reinterpret_cast<uintptr_t>(qs->vs)) & 15)
+            return cudaErrorInvalidValue;
+        AF_ATTN_DISPATCH(dispatch_kvq, q, kc, vc, *qs, max_ctx, pos_dev, pos, scr, ns, out, KVH, s)
+    }
     // the path depends on the cache size only (a captured decode step replays at every position)
     const bool cl = attn_decode_uses_cluster(max_ctx);
     const int ns = attn_decode_splits(H, KVH, max_ctx);

@@ -203,6 +203,36 @@ cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo
                          unsigned* err, cudaStream_t s);
 cudaError_t qgemm_prepare();
 
+// Quantized KV cache (AF_KV_Q8_0 / AF_KV_Q4_0): every slot lives in the fp16 cache; slots that left the window
+// also live in the quantized store, as codes (Q8_0: D int8 values in element order; Q4_0: D / 2 bytes, byte j
+// = n(2j) | n(2j + 1) << 4 with n = q + 8) and D / 32 fp16 scales per slot, in the cache's
+// [layer][kv head][slot] order.
+struct KvStore {
+    uint8_t* kq = nullptr;
+    uint8_t* vq = nullptr;
+    __half* ks = nullptr;
+    __half* vs = nullptr;
+    int qtype = 0;   // AF_KV_Q8_0 / AF_KV_Q4_0, 0 = the cache is not quantized
+    int window = 0;  // slots kept fp16 behind a step's last position
+};
+__host__ __device__ inline int kv_code_bytes(int qtype, int D) { return qtype == AF_KV_Q8_0 ? D : D / 2; }
+
+// One layer's view of the quantized store, for decode attention.
+struct KvLayerStore {
+    const uint8_t* kq = nullptr;
+    const uint8_t* vq = nullptr;
+    const __half* ks = nullptr;
+    const __half* vs = nullptr;
+    int qtype = 0;
+    int window = 0;
+};
+
+// Retire slots first..first+count-1 (with pos_dev: the one slot *pos_dev - window) of every layer and kv head:
+// quantize the slot's fp16 K and V rows into the store and write fp16(d q) back into the fp16 cache.  Slots
+// below 0 are skipped.
+cudaError_t launch_kv_retire(const KvStore& st, __half* kc, __half* vc, int L, int KVH, int max_ctx, int D,
+                             const int* pos_dev, int first, int count, cudaStream_t s);
+
 // Attention
 struct AttnScratch {
     float* part = nullptr;    // [KVH][NS][G][D+2]
@@ -217,9 +247,11 @@ bool attn_decode_uses_cluster(int max_ctx);
 // Splits the decode attention launches (grid.x) for this shape.
 int attn_decode_splits(int n_heads, int n_kv_heads, int max_ctx);
 size_t attn_decode_part_elems(int n_heads, int head_dim, int ns);
+// qs (nullable): the layer's quantized store; kc, vc are then the fp16 cache and retired slots (below
+// pos + 1 - window) are read from the store.
 cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, int kv_f16, int H, int KVH, int D,
                                int max_ctx, const int* pos_dev, int pos, const AttnScratch& scr, float* out,
-                               cudaStream_t s);
+                               cudaStream_t s, const KvLayerStore* qs = nullptr);
 // Causal prefill attention on the tensor cores: S query rows at positions pos0.. (q fp32 [S][ldq], rotated),
 // output as fp16 hi + lo planes [S][ldo].  err: device error word.
 cudaError_t launch_attn_prefill(const float* q, int64_t ldq, const void* kc, const void* vc, int kv_f16, int H,

@@ -77,7 +77,15 @@ typedef enum af_status {
 } af_status;
 
 typedef enum af_wtype { AF_Q4_0 = 2, AF_Q8_0 = 8, AF_Q4_K = 12, AF_Q5_K = 13, AF_Q6_K = 14 } af_wtype; /* GGUF's type numbers */
-typedef enum af_dtype { AF_F32 = 0, AF_F16 = 1 } af_dtype;
+/* KV cache element types.  AF_KV_Q8_0 / AF_KV_Q4_0: a quantized cache with an fp16 window (dotLLM, "CUDA
+ * components": "Q8_0/Q4_0 + FP16 window"): a slot is written in fp16; once it lies more than kv_window
+ * positions behind a step's last position it is replaced by the Q8_0 / Q4_0 quantization of its fp16 values,
+ * per 32 values along head_dim (Q8_0: d = fp16(max|v| / 127), q = clamp(round-half-away(v / d), -127, 127);
+ * Q4_0: d = fp16(m / -8) with m the value of largest magnitude, n = clamp(floor(v / d + 8.5), 0, 15),
+ * q = n - 8; decisions in fp32 on the fp16 values), and reads of the slot see d * q.  Decode attention reads
+ * retired slots from the quantized store; prefill attention reads the fp16 copy, where a retired slot holds
+ * fp16(d * q). */
+typedef enum af_dtype { AF_F32 = 0, AF_F16 = 1, AF_KV_Q8_0 = 2, AF_KV_Q4_0 = 3 } af_dtype;
 
 typedef struct af_config {
     int32_t n_layers, n_embd, n_heads, n_kv_heads, head_dim, n_ff, n_vocab;
@@ -90,6 +98,8 @@ typedef struct af_config {
     float rope_base;    /* RoPE base */
     int32_t out_wtype;  /* af_wtype of the LM head (output.weight); 0 = wtype (a Q4_K_M model: Q4_K layers and
                            embedding with a Q6_K head) */
+    int32_t kv_window;  /* quantized caches: slots kept in fp16 behind a step's last position; at least max_chunk, so
+                           a step is never longer than the window (ignored for AF_F32 / AF_F16) */
 } af_config;
 
 /*
@@ -114,7 +124,9 @@ typedef struct af_qweight af_qweight;
 int af_layer_offsets(const af_config* cfg, uint64_t off[10]);
 
 /* KV cache bytes, n_layers * n_kv_heads * max_ctx * head_dim * elem * 2
- * (Airframe "GPU_PIPELINE.md", "KV cache" size formula). 0 on a bad config. */
+ * (Airframe "GPU_PIPELINE.md", "KV cache" size formula).  A quantized cache holds every slot twice, in fp16
+ * and in the quantized store: n_layers * n_kv_heads * 2 * max_ctx * (head_dim * 2 + head_dim / 32 * B),
+ * B = 34 (Q8_0) or 18 (Q4_0) bytes per 32 values.  0 on a bad config. */
 uint64_t af_kv_bytes(const af_config* cfg);
 
 /*
@@ -125,7 +137,8 @@ uint64_t af_kv_bytes(const af_config* cfg);
  * its own, which is ordered with the legacy default stream.
  * Supported: head_dim in {64, 128}, n_heads % n_kv_heads == 0 with
  * n_heads / n_kv_heads in {1, 2, 4, 8}, n_embd, n_ff, n_heads*head_dim
- * multiples of 64, even n_vocab.  Errors: AF_EINVAL, AF_ENOMEM, AF_ECUDA,
+ * multiples of 64, even n_vocab; quantized caches: kv_window >= max_chunk and
+ * max_ctx a multiple of 4.  Errors: AF_EINVAL, AF_ENOMEM, AF_ECUDA,
  * AF_ENOTIMPL (valid but unsupported shape).  *out is NULL on failure.
  */
 int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_model** out);
@@ -170,10 +183,19 @@ int af_model_sync(af_model* m, int32_t* next_token_host);
 const int32_t* af_model_next_token_dev(const af_model* m);
 
 /* Device pointers of the model's KV cache: K and V each [n_layers][n_kv_heads][max_ctx][head_dim]
- * in kv_dtype (Airframe "GPU_PIPELINE.md", "KV cache" layout).  Owned by the model. */
+ * in kv_dtype, fp16 for a quantized cache (Airframe "GPU_PIPELINE.md", "KV cache" layout).  Owned by the
+ * model. */
 int af_model_kv_cache(const af_model* m, void** k_dev, void** v_dev);
 
-/* Zero the KV cache (the service is stateless between requests) and the error word. */
+/* The quantized store of a quantized cache (AF_EINVAL otherwise): per slot of [n_layers][n_kv_heads][max_ctx],
+ * the codes (Q8_0: head_dim int8 values q in element order; Q4_0: head_dim / 2 bytes, byte j holding
+ * n = q + 8 of element 2j in its low and of element 2j + 1 in its high nibble) in *codes, and head_dim / 32 fp16
+ * scales d in *scales; k_ for K, v_ for V.  Valid for slots that have retired.  Owned by the model. */
+int af_model_kv_store(const af_model* m, void** k_codes, void** k_scales, void** v_codes, void** v_scales);
+
+/* Zero the KV cache (the service is stateless between requests) and the error word.  Steps after it start
+ * again at position 0; with a quantized cache, each step must start where the previous one ended (the
+ * slots that leave the window are retired by the step that passes them). */
 int af_reset(af_model* m);
 
 /* Model's stream (as given to af_model_create). */

@@ -74,7 +74,7 @@ def check_logits(got, ref, what, worst=None):
         assert int(np.argmax(got)) == oracle.argmax(ref), what
 
 
-def run_parity(af, cfg, seed, chunks, n_decode, kv_slots, start=0, prefix=None):
+def run_parity(af, cfg, seed, chunks, n_decode, kv_slots, start=0, prefix=None, max_chunk=512):
     """Prefill the prompt in `chunks` from position `start`, then n_decode greedy steps under teacher forcing,
     comparing every layer's residual stream and the logits with the oracle.  prefix(om, gm), if given, fills
     cache slots [0, start) of both models before the first chunk.  Returns the worst errors seen."""
@@ -85,7 +85,7 @@ def run_parity(af, cfg, seed, chunks, n_decode, kv_slots, start=0, prefix=None):
     hm = synth.HostModel(cfg, seed)
     prompt = hm.prompt(sum(chunks) + start)[start:]
     om = oracle.Model.from_host(hm, kv_slots=kv_slots)
-    gm = gpu_model(hm)
+    gm = gpu_model(hm, max_chunk=max_chunk)
     if prefix is not None:
         prefix(om, gm)
     L, E, V = cfg.n_layers, cfg.n_embd, cfg.n_vocab
@@ -118,3 +118,14 @@ def run_parity(af, cfg, seed, chunks, n_decode, kv_slots, start=0, prefix=None):
         p += 1
     gm.close()
     return worst
+
+
+def device_array(ptr, shape, typestr):
+    """A torch view of device memory the library owns (the owner must outlive the view)."""
+    import torch
+
+    class _Cuda:
+        def __init__(self):
+            n = int(np.prod(shape))
+            self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (ptr, False), "version": 3}
+    return torch.as_tensor(_Cuda(), device="cuda").view(*shape)

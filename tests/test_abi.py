@@ -164,6 +164,32 @@ def test_new_entry_points_validate_on_the_host():
     assert L.af_debug_stall(None, 1) == af.AF_EINVAL
 
 
+@pytest.mark.parametrize("kvt", ["q8_0", "q4_0"])
+def test_quantized_kv_bytes_match_oracle(kvt):
+    af = _af()
+    cfg = synth.CONFIGS[3].with_(kv_dtype=kvt, kv_window=512)
+    assert af.af_kv_bytes(af.make_config(cfg)) == oracle.kv_bytes(cfg)
+
+
+def test_quantized_kv_config_validation():
+    # host-side checks in af_model_create, before any device work (dummy pointers are never dereferenced)
+    af = _af()
+    L = af.lib()
+    cfg = synth.CONFIGS[0].with_(kv_dtype="q8_0", kv_window=8)
+    blobs = (ctypes.c_void_p * cfg.n_layers)(*([16] * cfg.n_layers))
+    w = af.af_weights(blobs, 16, 16, 16)
+    h = ctypes.c_void_p()
+    c = af.make_config(cfg, max_chunk=16)  # window shorter than a chunk
+    assert L.af_model_create(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(h)) == af.AF_EINVAL
+    assert "kv_window" in af.af_last_error()
+    c = af.make_config(cfg.with_(max_ctx=66), max_chunk=8)  # slots not a multiple of 4
+    assert L.af_model_create(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(h)) == af.AF_ENOTIMPL
+    c = af.make_config(cfg, max_chunk=8)
+    c.kv_dtype = 9
+    assert L.af_model_create(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(h)) == af.AF_EINVAL
+    assert L.af_model_kv_store(None, None, None, None, None) == af.AF_EINVAL
+
+
 def test_product_path_has_no_cpu_fallback():
     # the package must not import the oracle or any CPU implementation
     pkg = os.path.join(ROOT, "gguf_quantized_transformer_gb300")
