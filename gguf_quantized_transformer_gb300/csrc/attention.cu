@@ -127,6 +127,99 @@ __device__ __forceinline__ void dec_split(int n, int ns, int& ns_eff, int& chunk
     ns_eff = (n + chunk - 1) / chunk;
 }
 
+// Offset of the merge's maxima / weights in a CTA's scratch: after the warps' combine buffer and after the
+// merge's own per-thread float4 reduction area (which starts at the scratch base).
+__host__ __device__ constexpr int merge_scratch_off(int combine_bytes, int nt) {
+    return combine_bytes > nt * 16 ? combine_bytes : nt * 16;
+}
+
+// Merge of the ns_eff split partials of kv head g by the last CTA to finish (split path):
+//   o_h = sum_s exp(m_s - M) o_s / sum_s exp(m_s - M) l_s.
+// Each of the NT threads owns float4 f of the group's G x D outputs and the splits ph, ph + P, ..; it issues a
+// batch of those partial-row loads into registers first, while warp h forms head h's weights with its lanes
+// over the splits, so the partials and the weights arrive in about one L2 round trip.  scratch: shared memory
+// for max(NT * 16, 2 * ns_eff * G * 4) bytes.
+template <int D, int G, int NT>
+__device__ __forceinline__ void merge_splits(const float* __restrict__ part, int g, int ns, int ns_eff,
+                                             float* __restrict__ out, unsigned* __restrict__ cnt, uint8_t* red_smem,
+                                             float* mm, int tid) {
+    constexpr int PST = D + 4;
+    constexpr int NF = G * D / 4;  // float4 outputs of the group
+    constexpr int P = NT / NF;     // threads per output float4
+    constexpr int kBatch = 16;     // partial loads in flight per thread
+    static_assert(P >= 1 && P * NF == NT, "merge mapping");
+    const int lane = tid & 31, warp = tid >> 5;
+    const float* pg = part + ((int64_t)g * ns * G) * PST;
+    float* ml = mm + ns_eff * G;  // [ns_eff][G] split maxima (then merge weights), sums
+    const int f = tid % NF, ph = tid / NF, hf = (4 * f) / D, df = (4 * f) % D;
+    float4 v[kBatch];
+    auto load_batch = [&](int s0) {
+#pragma unroll
+        for (int i = 0; i < kBatch; i++) {
+            const int ss = s0 + i * P;
+            v[i] = ss < ns_eff ? __ldcg(reinterpret_cast<const float4*>(pg + ((int64_t)ss * G + hf) * PST + df))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    load_batch(ph);
+    if (warp < G) {
+        const int h = warp;
+        float M = -CUDART_INF_F;
+        for (int ss = lane; ss < ns_eff; ss += 32) {
+            const float2 mlv = __ldcg(reinterpret_cast<const float2*>(pg + ((int64_t)ss * G + h) * PST + D));
+            mm[ss * G + h] = mlv.x;
+            ml[ss * G + h] = mlv.y;
+            M = fmaxf(M, mlv.x);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float den = 0.f;
+        for (int ss = lane; ss < ns_eff; ss += 32) den = fmaf(__expf(mm[ss * G + h] - M), ml[ss * G + h], den);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        const float inv = 1.f / den;
+        for (int ss = lane; ss < ns_eff; ss += 32) mm[ss * G + h] = __expf(mm[ss * G + h] - M) * inv;
+    }
+    __syncthreads();
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = ph; s0 < ns_eff; s0 += kBatch * P) {
+        if (s0 != ph) load_batch(s0);
+#pragma unroll
+        for (int i = 0; i < kBatch; i++) {
+            const int ss = s0 + i * P;
+            if (ss < ns_eff) {
+                const float w = mm[ss * G + hf];
+                a.x = fmaf(w, v[i].x, a.x);
+                a.y = fmaf(w, v[i].y, a.y);
+                a.z = fmaf(w, v[i].z, a.z);
+                a.w = fmaf(w, v[i].w, a.w);
+            }
+        }
+    }
+    // the P phases of an output, summed in a fixed order
+    float4* red4 = reinterpret_cast<float4*>(red_smem);
+    if (P > 1) {
+        red4[ph * NF + f] = a;
+        __syncthreads();
+        if (ph == 0)
+            for (int pp = 1; pp < P; pp++) {
+                const float4 b = red4[pp * NF + f];
+                a.x += b.x;
+                a.y += b.y;
+                a.z += b.z;
+                a.w += b.w;
+            }
+    }
+    if (ph == 0) {
+        float* o = out + (int64_t)(g * G + hf) * D + df;
+        o[0] = a.x;
+        o[1] = a.y;
+        o[2] = a.z;
+        o[3] = a.w;
+    }
+    if (tid == 0) cnt[g] = 0u;
+}
+
 // Decode attention, CTA (s, g): kv head g, slots [s*chunk, ...) of the cache.
 // The range streams through a ring of S stages; a stage is the K tile and the
 // V tile (TS slots each, 16 KB) of the same slots, two bulk copies
@@ -447,85 +540,373 @@ __global__ void __launch_bounds__(CL ? kClWarps * 32 : kDecThreads, (!CL && G <=
     __syncthreads();
     if (!last) return;
     __threadfence();
-    // Merge the ns_eff partials of this kv head: o_h = sum_s exp(m_s - M) o_s / sum_s exp(m_s - M) l_s.
-    // Each thread owns float4 f of the group's G x D outputs and the splits ph, ph + P, ..; it issues a
-    // batch of those partial-row loads into registers first, while warp h forms head h's weights with its
-    // lanes over the splits, so the partials and the weights arrive in about one L2 round trip.
-    constexpr int NF = G * D / 4;                // float4 outputs of the group
-    constexpr int P = NT / NF;          // threads per output float4
-    constexpr int kBatch = 16;                   // partial loads in flight per thread
-    static_assert(P >= 1 && P * NF == NT, "merge mapping");
-    const float* pg = part + ((int64_t)g * ns * G) * PST;
-    // [ns_eff][G] split maxima (then merge weights) and sums, after the combine's scratch in the ring
-    float* mm = reinterpret_cast<float*>(dsm + NW * G * D * sizeof(float));
-    float* ml = mm + ns_eff * G;
-    const int f = tid % NF, ph = tid / NF, hf = (4 * f) / D, df = (4 * f) % D;
-    float4 v[kBatch];
-    auto load_batch = [&](int s0) {
-#pragma unroll
-        for (int i = 0; i < kBatch; i++) {
-            const int ss = s0 + i * P;
-            v[i] = ss < ns_eff ? __ldcg(reinterpret_cast<const float4*>(pg + ((int64_t)ss * G + hf) * PST + df))
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    merge_splits<D, G, NT>(part, g, ns, ns_eff, out, cnt, dsm,
+                           reinterpret_cast<float*>(dsm + merge_scratch_off(NW * G * D * 4, NT)), tid);
+}
+
+// ---------------------------------------------------------------------------------------------------------
+// Decode attention over an fp16 cache on the tensor cores (split path).  Same split, stages, merge and
+// per-warp online softmax as attn_decode_kernel, with the score and P V products as mma.sync m16n8k16 (fp16 in,
+// fp32 accumulate) over 16-slot tiles of a warp's slots:
+//   scores  S^T[16 slots][8] = K[16 slots][D] Qc^T[D][8], Qc = (q_hi of the G heads | q_lo of the G heads) with
+//           1/sqrt(D) folded in; the score of head h is column h plus column 4 + h;
+//   P V     O^T[D][8] += V^T[D][16 slots] Pc[16 slots][8], Pc = (p_hi | p_lo) per head, through shared memory.
+// The fp16 cache is exact in fp16, so with q and p split into hi + lo the products keep near-fp32 precision.
+// K and V tiles arrive by TMA (cp.async.bulk.tensor, SWIZZLE_128B, boxes of 64 dims), so the ldmatrix fragment
+// loads (K as rows, V transposed) are free of bank conflicts.  Group sizes up to 4 (8 columns).
+constexpr int kTcWarps = 4;
+
+__device__ __forceinline__ void tma_load_tile(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+// shared address of 16-byte chunk `chunk` (8 fp16 along D) of row `row` in a tile of `rows` rows stored as
+// SWIZZLE_128B atoms of 64 dims (atom a at a * rows * 128 bytes); the tile base is 1024-byte aligned
+__device__ __forceinline__ uint32_t sw_addr(uint32_t base, int rows, int row, int chunk) {
+    return base + (uint32_t)((chunk >> 3) * rows * 128 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kTcWarps * 32, 2)
+    attn_decode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                          const float* __restrict__ q, int max_ctx, const int* __restrict__ pos_dev, int pos_arg,
+                          float* __restrict__ part, unsigned* __restrict__ cnt, float* __restrict__ out,
+                          unsigned* __restrict__ err) {
+    constexpr int NW = kTcWarps, NT = NW * 32;
+    constexpr int TS = dec_tile<D, __half>();  // slots per stage (16 KB of K)
+    constexpr int TB = TS * D * 2;
+    constexpr int S = kRing / (2 * TB) < kMaxStages ? kRing / (2 * TB) : kMaxStages;
+    constexpr int SPW = TS / NW;               // slots of a warp per stage
+    constexpr int MT = SPW / 16;               // 16-slot MMA tiles of a warp per stage
+    constexpr int KS = D / 16;                 // K steps of the score MMA
+    constexpr int DT = D / 16;                 // 16-dim tiles of the P V MMA
+    static_assert(G <= 4 && S >= 2 && MT >= 1 && SPW % 16 == 0, "shape");
+    extern __shared__ __align__(128) uint8_t dsm[];  // S x [K tile | V tile] (aligned to 1024 below), 64-dim SW128 atoms
+    __shared__ uint64_t kfull[kMaxStages], vfull[kMaxStages];
+    __shared__ unsigned issues[kMaxStages], done[kMaxStages];
+    __shared__ __align__(16) __half pc[NW][8][16];  // a warp's Pc tile, column-major: [col][slot]
+    __shared__ float wm[NW][G], wl[NW][G];
+    __shared__ unsigned last;
+    __shared__ volatile int abort_f;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = blockIdx.y, s = blockIdx.x, ns = gridDim.x;
+    pdl_launch_dependents();
+    if (tid == 0) {  // the tensor maps' descriptors, ahead of their first use
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&kmap) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&vmap) : "memory");
+    }
+    const int pos = pos_dev ? *pos_dev : pos_arg;
+    const int n = pos + 1;
+    int ns_eff, chunk;
+    dec_split(n, ns, ns_eff, chunk);
+    const int j0 = s * chunk;
+    const int nl = s < ns_eff ? min(n, j0 + chunk) - j0 : 0;
+    const int nst = (nl + TS - 1) / TS;
+    const int row0 = g * max_ctx + j0;  // tensor-map row of the range's first slot
+    constexpr int PST = D + 4;
+    float* my = part + ((int64_t)(g * ns + s) * G) * PST;
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~(uintptr_t)1023);
+
+    if (tid == 0) {
+        for (int i = 0; i < S; i++) {
+            mbar_init(&kfull[i], 1);
+            mbar_init(&vfull[i], 1);
+            issues[i] = 0;
+            done[i] = 0;
         }
-    };
-    load_batch(ph);
-    if (warp < G) {
-        const int h = warp;
-        float M = -CUDART_INF_F;
-        for (int ss = lane; ss < ns_eff; ss += 32) {
-            const float2 mlv = __ldcg(reinterpret_cast<const float2*>(pg + ((int64_t)ss * G + h) * PST + D));
-            mm[ss * G + h] = mlv.x;
-            ml[ss * G + h] = mlv.y;
-            M = fmaxf(M, mlv.x);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float den = 0.f;
-        for (int ss = lane; ss < ns_eff; ss += 32) den = fmaf(__expf(mm[ss * G + h] - M), ml[ss * G + h], den);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        const float inv = 1.f / den;
-        for (int ss = lane; ss < ns_eff; ss += 32) mm[ss * G + h] = __expf(mm[ss * G + h] - M) * inv;
+        abort_f = 0;
+        fence_mbar_init();
     }
     __syncthreads();
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = ph; s0 < ns_eff; s0 += kBatch * P) {
-        if (s0 != ph) load_batch(s0);
+    auto issue = [&](int t) {  // one thread: K and V boxes of stage t into slot t % S (rows past the range are
+                               // read too and masked; past the array they are zero-filled)
+        const int slot = t % S;
+        uint8_t* dst = ring + slot * 2 * TB;
+        issues[slot]++;
+        mbar_arrive_expect_tx(&kfull[slot], TB);
 #pragma unroll
-        for (int i = 0; i < kBatch; i++) {
-            const int ss = s0 + i * P;
-            if (ss < ns_eff) {
-                const float w = mm[ss * G + hf];
-                a.x = fmaf(w, v[i].x, a.x);
-                a.y = fmaf(w, v[i].y, a.y);
-                a.z = fmaf(w, v[i].z, a.z);
-                a.w = fmaf(w, v[i].w, a.w);
+        for (int a = 0; a < D / 64; a++) tma_load_tile(dst + a * TS * 128, &kmap, 64 * a, row0 + t * TS, &kfull[slot]);
+        mbar_arrive_expect_tx(&vfull[slot], TB);
+#pragma unroll
+        for (int a = 0; a < D / 64; a++)
+            tma_load_tile(dst + TB + a * TS * 128, &vmap, 64 * a, row0 + t * TS, &vfull[slot]);
+    };
+    if (tid == 0 && nst > 0) {
+        const bool has_pos = j0 + nl == n;
+        bool waited = false;
+        for (int t = 0; t < min(S, nst); t++) {
+            if (has_pos && !waited && t == nst - 1) {
+                pdl_wait();
+                waited = true;
+            }
+            issue(t);
+        }
+    }
+    pdl_wait();
+
+    // B fragments of Qc (constant): thread holds column cn = lane / 4 (head cn % 4, hi if cn < 4) at K rows
+    // 2 (lane % 4) + {0, 1} and + 8 of every K step
+    const int quad = lane & 3, cn = lane >> 2;
+    uint32_t qb[KS][2];
+    {
+        const int h = cn & 3;
+        const float scale = rsqrtf((float)D);
+        const float* qh = q + (int64_t)(g * G + (h < G ? h : 0)) * D;
+#pragma unroll
+        for (int kk = 0; kk < KS; kk++) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int k = kk * 16 + 2 * quad + (e & 1) + 8 * (e >> 1);
+                const float x = h < G ? qh[k] * scale : 0.f;
+                const float hi = __half2float(__float2half_rn(x));
+                v[e] = cn < 4 ? hi : x - hi;
+            }
+            qb[kk][0] = pack_h2(v[0], v[1]);
+            qb[kk][1] = pack_h2(v[2], v[3]);
+        }
+    }
+    // online softmax state: a lane with quad < 2 tracks heads 2 quad, 2 quad + 1 (columns of its score fragment)
+    float m_run[2] = {-CUDART_INF_F, -CUDART_INF_F}, l_run[2] = {0.f, 0.f};
+    float oacc[DT][4];
+#pragma unroll
+    for (int d = 0; d < DT; d++)
+#pragma unroll
+        for (int e = 0; e < 4; e++) oacc[d][e] = 0.f;
+
+    auto wait_tile = [&](uint64_t* bar, unsigned par) {
+        bool ok = false;
+        for (unsigned it = 0; it < kWaitLimit && !ok; it++) {
+            ok = mbar_try_wait(bar, par);
+            if (!ok && abort_f) break;
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0 && !abort_f) {
+            abort_f = 1;
+            atomicExch(err, (unsigned)DEV_TIMEOUT);
+        }
+        return ok;
+    };
+    const uint32_t pcw = smem_u32(&pc[warp][0][0]);
+
+    for (int t = 0; t < nst; t++) {
+        const int slot = t % S;
+        const unsigned par = (unsigned)((t / S) & 1);
+        const int keys = min(TS, nl - t * TS);
+        if (!wait_tile(&kfull[slot], par)) break;
+        const uint32_t kt = smem_u32(ring + slot * 2 * TB), vt = kt + TB;
+        bool vready = false;
+#pragma unroll
+        for (int mt = 0; mt < MT; mt++) {
+            const int r0 = warp * SPW + mt * 16;  // first slot of this tile within the stage
+            // ---- scores
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KS; kk++) {
+                uint32_t a[4];
+                ldsm_x4(sw_addr(kt, TS, r0 + (lane & 15), 2 * kk + (lane >> 4)), a);
+                mma16816(c, a, qb[kk][0], qb[kk][1]);
+            }
+            // c: rows r0 + cn, r0 + cn + 8; columns 2 quad, 2 quad + 1.  Score = hi column + lo column (quad ^ 2).
+            float sc[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) sc[e] = c[e] + __shfl_xor_sync(0xffffffffu, c[e], 2);
+            const bool v0 = r0 + cn < keys, v1 = r0 + cn + 8 < keys;
+            if (!v0) sc[0] = sc[1] = -CUDART_INF_F;
+            if (!v1) sc[2] = sc[3] = -CUDART_INF_F;
+            float corr[2], p[4];
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {  // heads 2 quad + hh (meaningful for quad < 2)
+                float mt2 = fmaxf(sc[hh], sc[2 + hh]);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) mt2 = fmaxf(mt2, __shfl_xor_sync(0xffffffffu, mt2, o));
+                const float m_new = fmaxf(m_run[hh], mt2);
+                corr[hh] = m_new == -CUDART_INF_F ? 1.f : __expf(m_run[hh] - m_new);
+                p[hh] = sc[hh] == -CUDART_INF_F ? 0.f : __expf(sc[hh] - m_new);
+                p[2 + hh] = sc[2 + hh] == -CUDART_INF_F ? 0.f : __expf(sc[2 + hh] - m_new);
+                l_run[hh] = fmaf(l_run[hh], corr[hh], p[hh] + p[2 + hh]);
+                m_run[hh] = m_new;
+            }
+            // Pc tile: column h = p_hi of head h, column 4 + h = p_lo; rows = the tile's 16 slots
+            if (quad < 2) {
+                __half* pw = &pc[warp][0][0];
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const int h = 2 * quad + (e & 1), r = cn + 8 * (e >> 1);
+                    const __half ph = __float2half_rn(p[e]);
+                    pw[h * 16 + r] = ph;
+                    pw[(4 + h) * 16 + r] = __float2half_rn(p[e] - __half2float(ph));
+                }
+            }
+            __syncwarp();
+            // the O^T accumulator's columns 2 quad, 2 quad + 1 are heads (2 quad) % 4.. (hi or lo): rescale both
+            const float cr0 = __shfl_sync(0xffffffffu, corr[0], (lane & ~3) | (quad & 1));
+            const float cr1 = __shfl_sync(0xffffffffu, corr[1], (lane & ~3) | (quad & 1));
+#pragma unroll
+            for (int d = 0; d < DT; d++) {
+                oacc[d][0] *= cr0;
+                oacc[d][1] *= cr1;
+                oacc[d][2] *= cr0;
+                oacc[d][3] *= cr1;
+            }
+            // ---- P V
+            if (!vready) {
+                if (!wait_tile(&vfull[slot], par)) break;
+                vready = true;
+            }
+            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&pc[warp][cn][2 * quad]);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&pc[warp][cn][2 * quad + 8]);
+#pragma unroll
+            for (int d = 0; d < DT; d++) {
+                // V^T tile (dims 16 d.., slots r0..): matrices (dims 0-7 | 8-15) x (slots 0-7 | 8-15), transposed
+                const int mq = lane >> 3;
+                uint32_t a[4];
+                ldsm_x4_t(sw_addr(vt, TS, r0 + (lane & 7) + 8 * (mq >> 1), 2 * d + (mq & 1)), a);
+                mma16816(oacc[d], a, b0, b1);
+            }
+            __syncwarp();  // the Pc tile is reused by the next MMA tile
+        }
+        if (abort_f) break;
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&done[slot], 1u) == (unsigned)NW - 1u) {
+                done[slot] = 0;
+                if (t + S < nst) {
+                    fence_proxy_async_shared();
+                    issue(t + S);
+                }
             }
         }
     }
-    // the P phases of an output, summed in a fixed order (the ring is free)
-    float4* red4 = reinterpret_cast<float4*>(dsm);
-    if (P > 1) {
-        red4[ph * NF + f] = a;
+    __syncthreads();
+    if (abort_f) {
+        if (tid == 0)
+            for (int i = 0; i < S; i++)
+                if (issues[i]) {
+                    mbar_wait_bounded(&kfull[i], (issues[i] - 1u) & 1u);
+                    mbar_wait_bounded(&vfull[i], (issues[i] - 1u) & 1u);
+                }
         __syncthreads();
-        if (ph == 0)
-            for (int pp = 1; pp < P; pp++) {
-                const float4 b = red4[pp * NF + f];
-                a.x += b.x;
-                a.y += b.y;
-                a.z += b.z;
-                a.w += b.w;
+    }
+    // ---- combine the warps: O = hi column + lo column; lanes with quad < 2 hold heads 2 quad, 2 quad + 1
+    float* red_o = reinterpret_cast<float*>(ring);  // [warp][G][D]
+#pragma unroll
+    for (int d = 0; d < DT; d++) {
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) o[e] = oacc[d][e] + __shfl_xor_sync(0xffffffffu, oacc[d][e], 2);
+        if (quad < 2)
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int h = 2 * quad + (e & 1), dim = 16 * d + cn + 8 * (e >> 1);
+                if (h < G) red_o[(warp * G + h) * D + dim] = o[e];
             }
     }
-    if (ph == 0) {
-        float* o = out + (int64_t)(g * G + hf) * D + df;
-        o[0] = a.x;
-        o[1] = a.y;
-        o[2] = a.z;
-        o[3] = a.w;
+    // l: per-lane partial sums over the lane's rows; reduce over the 8 lanes of each quad
+#pragma unroll
+    for (int hh = 0; hh < 2; hh++)
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], o);
+    if (lane < 2)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++)
+            if (2 * lane + hh < G) {
+                wm[warp][2 * lane + hh] = m_run[hh];
+                wl[warp][2 * lane + hh] = l_run[hh];
+            }
+    __syncthreads();
+    if (nl > 0)
+        for (int t = tid; t < G * D; t += NT) {
+            const int h = t / D, d = t % D;
+            float M = -CUDART_INF_F;
+#pragma unroll
+            for (int w = 0; w < NW; w++) M = fmaxf(M, wm[w][h]);
+            float o = 0.f, l = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; w++) {
+                const float e = wm[w][h] == -CUDART_INF_F ? 0.f : __expf(wm[w][h] - M);
+                o = fmaf(e, red_o[(w * G + h) * D + d], o);
+                l = fmaf(e, wl[w][h], l);
+            }
+            my[h * PST + d] = o;
+            if (d == 0) {
+                my[h * PST + D] = abort_f ? 0.f : M;
+                my[h * PST + D + 1] = abort_f ? CUDART_NAN_F : l;
+            }
+        }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last = (atomicAdd(&cnt[g], 1u) == (unsigned)ns - 1u);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    merge_splits<D, G, NT>(part, g, ns, ns_eff, out, cnt, ring,
+                           reinterpret_cast<float*>(ring + merge_scratch_off(NW * G * D * 4, NT)), tid);
+}
+
+template <int D, int G>
+cudaError_t launch_tc_t(const float* q, const void* kc, const void* vc, int max_ctx, const int* pos_dev, int pos,
+                        const AttnScratch& scr, int ns, float* out, int KVH, cudaStream_t s) {
+    constexpr int TS = dec_tile<D, __half>();
+    constexpr int TB = TS * D * 2;
+    constexpr int S = kRing / (2 * TB) < kMaxStages ? kRing / (2 * TB) : kMaxStages;
+    const size_t smem = (size_t)S * 2 * TB + 1024;  // + alignment of the ring to 1024 bytes
+    if ((size_t)merge_scratch_off(kTcWarps * G * D * 4, kTcWarps * 32) + (size_t)ns * G * 8 > (size_t)S * 2 * TB)
+        return cudaErrorInvalidValue;
+    CUtensorMap km, vm;
+    if (!make_tmap_f16(&km, kc, (uint64_t)KVH * max_ctx, D, D, 64, TS) ||
+        !make_tmap_f16(&vm, vc, (uint64_t)KVH * max_ctx, D, D, 64, TS))
+        return cudaErrorInvalidValue;
+    auto k = attn_decode_tc_kernel<D, G>;
+    static int opened[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!opened[dev]) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e) return e;
+            opened[dev] = 1;
+        }
     }
-    if (tid == 0) cnt[g] = 0u;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ns, KVH);
+    cfg.blockDim = dim3(kTcWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, km, vm, q, max_ctx, pos_dev, pos, scr.part, scr.cnt, out, scr.err);
 }
 
 // ---------------------------------------------------------------------------------------------------------
@@ -875,36 +1256,8 @@ __global__ void __launch_bounds__(kDecThreads, G <= 4 ? 2 : 1)
     __syncthreads();
     if (!last) return;
     __threadfence();
-    // merge the ns_eff partials of this kv head (as attn_decode_kernel's split path)
-    float* mm = reinterpret_cast<float*>(dsm + NW * G * D * sizeof(float));
-    const float* pg = part + ((int64_t)g * ns * G) * PST;
-    if (warp < G) {
-        const int h = warp;
-        float M = -CUDART_INF_F;
-        for (int ss = lane; ss < ns_eff; ss += 32) M = fmaxf(M, __ldcg(pg + ((int64_t)ss * G + h) * PST + D));
-#pragma unroll
-        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float den = 0.f;
-        for (int ss = lane; ss < ns_eff; ss += 32) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(pg + ((int64_t)ss * G + h) * PST + D));
-            const float e = __expf(ml.x - M);
-            mm[ss * G + h] = e;
-            den = fmaf(e, ml.y, den);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        const float inv = 1.f / den;
-        for (int ss = lane; ss < ns_eff; ss += 32) mm[ss * G + h] *= inv;
-    }
-    __syncthreads();
-    for (int t = tid; t < G * D; t += NT) {
-        const int h = t / D, d = t % D;
-        float a = 0.f;
-#pragma unroll 8
-        for (int ss = 0; ss < ns_eff; ss++) a = fmaf(mm[ss * G + h], __ldcg(pg + ((int64_t)ss * G + h) * PST + d), a);
-        out[(int64_t)(g * G + h) * D + d] = a;
-    }
-    if (tid == 0) cnt[g] = 0u;
+    merge_splits<D, G, NT>(part, g, ns, ns_eff, out, cnt, dsm,
+                           reinterpret_cast<float*>(dsm + merge_scratch_off(NW * G * D * 4, NT)), tid);
 }
 
 template <int D, int G, int QT>
@@ -913,7 +1266,8 @@ cudaError_t launch_kvq_t(const float* q, const void* kc, const void* vc, const K
                          cudaStream_t s) {
     using C = KvqCfg<D, QT>;
     const size_t smem = (size_t)C::S * C::SLOT;
-    if ((size_t)kDecWarps * G * D * 4 + (size_t)ns * G * 4 > smem) return cudaErrorInvalidValue;
+    if ((size_t)merge_scratch_off(kDecWarps * G * D * 4, kDecThreads) + (size_t)ns * G * 8 > smem)
+        return cudaErrorInvalidValue;
     auto k = attn_decode_kvq_kernel<D, G, QT>;
     static int opened[kMaxDevices] = {};
     static std::mutex mu;
@@ -959,7 +1313,7 @@ cudaError_t launch_decode_t(const float* q, const void* kc, const void* vc, int 
     const int nw = CL ? kClWarps : kDecWarps;
     // the ring; after the loop it holds the warps' outputs [nw][G][D], then the merge's [ns][G] maxima and sums
     const size_t smem = (size_t)dec_stages<D, KT, CL>() * 2 * dec_tile<D, KT>() * D * sizeof(KT);
-    if ((size_t)nw * G * D * 4 + (size_t)ns * G * 8 > smem) return cudaErrorInvalidValue;
+    if ((size_t)merge_scratch_off(nw * G * D * 4, nw * 32) + (size_t)ns * G * 8 > smem) return cudaErrorInvalidValue;
     if (smem > 222 * 1024) return cudaErrorInvalidValue;  // with the static shared memory, within 227 KB
     auto k = attn_decode_kernel<D, G, KT, CL>;
     // the largest dynamic shared memory this instantiation was opened to, per device (set before a launch
@@ -1094,6 +1448,17 @@ cudaError_t launch_attn_decode(const float* q, const void* kc, const void* vc, i
     const int ns = attn_decode_splits(H, KVH, max_ctx);
     if (!cl && scr.ns < ns) return cudaErrorInvalidValue;  // scratch sized for fewer splits
     if ((reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & 15) return cudaErrorInvalidValue;
+    if (!cl && kv_f16 && G <= 4) {  // fp16 cache on the split path: the tensor-core kernel
+        switch (D * 100 + G) {
+            case 6401: return launch_tc_t<64, 1>(q, kc, vc, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
+            case 6402: return launch_tc_t<64, 2>(q, kc, vc, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
+            case 6404: return launch_tc_t<64, 4>(q, kc, vc, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
+            case 12801: return launch_tc_t<128, 1>(q, kc, vc, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
+            case 12802: return launch_tc_t<128, 2>(q, kc, vc, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
+            case 12804: return launch_tc_t<128, 4>(q, kc, vc, max_ctx, pos_dev, pos, scr, ns, out, KVH, s);
+            default: break;
+        }
+    }
     AF_ATTN_DISPATCH(dispatch_decode, q, kc, vc, kv_f16, max_ctx, pos_dev, pos, scr, ns, out, KVH, cl, s)
 }
 

@@ -5,8 +5,10 @@
 //
 // CTA (query tile, kv head g): 128 query vectors = QT = 128/G rows x the G
 // heads of the group (vector v = h * QT + row), so every K/V tile is used by
-// all heads of the group.  Keys stream in tiles of BKV slots (128 for an fp16
-// cache, 64 for fp32).  Two passes over the keys:
+// all heads of the group.  Keys stream in tiles of BKV = 64 slots: one bulk
+// copy each of the tile's raw K and V rows into a staging buffer, issued while
+// the previous tile is multiplied, so the loads overlap the MMAs and the
+// softmax.  Two passes over the keys:
 //   pass A: S = Q_hi K_hi^T (one MMA per 16-wide K step) -> per-row maximum m;
 //   pass B: S = Q K^T exactly (hi/lo split, below) -> p = exp(s - m) with the
 //           causal mask, row sums l, P (fp16 hi + lo) written to shared memory,
@@ -20,8 +22,9 @@
 // accumulate: near-fp32 scores and outputs.
 //
 // Operands live in shared memory in the SWIZZLE_128B K-major layout, written
-// by the CTA's threads (Q from the fp32 q rows; K rows as they are; V
-// transposed so that keys run along K of the P V product).  One thread issues
+// by the CTA's threads (Q from the fp32 q rows; K rows as they are and V
+// transposed, so that keys run along K of the P V product, both from the
+// staging buffer).  One thread issues
 // the MMAs; warps 0-3 own the 128 TMEM lanes (one query vector each) for the
 // softmax and the epilogue (every tcgen05.ld is executed by whole warps under
 // warp-uniform conditions).  Every wait on the MMA barrier is bounded.
@@ -42,7 +45,7 @@ constexpr int kOCol = 128;
 template <int D, typename KT>
 struct PCfg {
     static constexpr bool SPLIT_KV = sizeof(KT) == 4;  // fp32 cache: K and V need hi + lo
-    static constexpr int BKV = SPLIT_KV ? 64 : 128;    // keys per tile
+    static constexpr int BKV = 64;                     // keys per tile
     static constexpr int Q_BYTES = BQ * D * 2;         // one fp16 plane
     static constexpr int K_BYTES = BKV * D * 2;
     static constexpr int V_BYTES = D * BKV * 2;
@@ -55,7 +58,10 @@ struct PCfg {
     static constexpr int OFF_VL = OFF_VH + V_BYTES;
     static constexpr int OFF_PH = OFF_VL + (SPLIT_KV ? V_BYTES : 0);
     static constexpr int OFF_PL = OFF_PH + P_BYTES;
-    static constexpr int SMEM = OFF_PL + P_BYTES + 1024;  // + 1024-byte alignment slack
+    static constexpr int RAW_BYTES = BKV * D * (int)sizeof(KT);  // one tile of raw cache rows
+    static constexpr int OFF_RK = OFF_PL + P_BYTES;              // staging: raw K rows, then raw V rows
+    static constexpr int OFF_RV = OFF_RK + RAW_BYTES;
+    static constexpr int SMEM = OFF_RV + RAW_BYTES + 1024;       // + 1024-byte alignment slack
 };
 
 // Byte offset of 16-byte chunk c (8 fp16 along K) of row r in an operand of R rows stored as
@@ -106,6 +112,7 @@ __device__ __forceinline__ uint4 pack8_f16(const float (&w)[8]) {  // exact for 
 
 struct PSmem {
     uint64_t mma_bar;
+    uint64_t raw_bar;  // staging filled (transaction bytes)
     uint32_t tmem_base;
     volatile int abort;
 };
@@ -146,6 +153,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     if (tid == 0) {
         mbar_init(&sm.mma_bar, 1);
+        mbar_init(&sm.raw_bar, 1);
         sm.abort = 0;
         fence_mbar_init();
     }
@@ -154,6 +162,34 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+
+    // ---- staging of raw cache rows: one bulk copy of the keys of tile t (K, and V in pass B), issued by one
+    // thread; every wait is bounded, and the phase flips once per fill.
+    const KT* stK = reinterpret_cast<const KT*>(smem + C::OFF_RK);
+    const KT* stV = reinterpret_cast<const KT*>(smem + C::OFF_RV);
+    unsigned raw_phase = 0;
+    auto raw_issue = [&](int t, bool with_v) {  // thread 0 only
+        const int keys = min(BKV, nkeys - t * BKV);
+        const unsigned bytes = (unsigned)(keys * D * (int)sizeof(KT));
+        mbar_arrive_expect_tx(&sm.raw_bar, with_v ? 2 * bytes : bytes);
+        bulk_g2s(smem + C::OFF_RK, K + (int64_t)t * BKV * D, bytes, &sm.raw_bar);
+        if (with_v) bulk_g2s(smem + C::OFF_RV, V + (int64_t)t * BKV * D, bytes, &sm.raw_bar);
+    };
+    auto raw_wait = [&]() {  // all threads; false after a timeout (the fill stays pending for the drain)
+        const bool ok = mbar_wait_bounded(&sm.raw_bar, raw_phase);
+        if (!ok) {
+            sm.abort = 1;
+            atomicExch(err, (unsigned)DEV_TIMEOUT);
+            return false;
+        }
+        raw_phase ^= 1u;
+        return true;
+    };
+    bool raw_pending = false;  // thread 0: a fill it issued has not been waited for (the drain on abort)
+    if (tid == 0) {
+        raw_issue(0, false);
+        raw_pending = true;
+    }
 
     // ---- Q tile: vector v = h * QT + row, scaled by 1/sqrt(D), split hi + lo
     {
@@ -183,7 +219,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int key = t * BKV + j;
             float w[8];
             if (key < nkeys) {
-                ld8(K + (int64_t)key * D + 8 * c, w);
+                ld8(stK + (int64_t)j * D + 8 * c, w);
             } else {
 #pragma unroll
                 for (int e = 0; e < 8; e++) w[e] = 0.f;
@@ -207,7 +243,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             for (int e = 0; e < 8; e++) {
                 const int key = t * BKV + 8 * kg + e;
                 if (key < nkeys) {
-                    ld2(V + (int64_t)key * D + 2 * dp, a[e], b[e]);
+                    ld2(stV + (int64_t)(8 * kg + e) * D + 2 * dp, a[e], b[e]);
                 } else {
                     a[e] = 0.f;
                     b[e] = 0.f;
@@ -246,8 +282,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     // ---- pass A: row maxima from Q_hi K_hi^T
     for (int t = 0; t < ntiles && !sm.abort; t++) {
+        if (__syncthreads_or(!raw_wait())) break;  // block-uniform
+        raw_pending = false;
         load_k(t, false);
         publish();
+        if (tid == 0 && !sm.abort) {  // the staging is free: the next tile (pass B starts over at tile 0 with V)
+            fence_proxy_async_shared();
+            if (t + 1 < ntiles) raw_issue(t + 1, false);
+            else raw_issue(0, true);
+            raw_pending = true;
+        }
         if (tid == 0) {
             for (int kk = 0; kk < D / 16; kk++)
                 mma_f16(tmem, op_desc(sbase + C::OFF_QH, BQ, kk), op_desc(sbase + C::OFF_KH, BKV, kk), kIdS,
@@ -276,9 +320,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     // ---- pass B: exact scores, P, O += P V
     for (int t = 0; t < ntiles && !sm.abort; t++) {
+        if (__syncthreads_or(!raw_wait())) break;  // block-uniform
+        raw_pending = false;
         load_k(t, true);
         load_v(t);
         publish();
+        if (tid == 0 && !sm.abort && t + 1 < ntiles) {
+            fence_proxy_async_shared();
+            raw_issue(t + 1, true);
+            raw_pending = true;
+        }
         if (tid == 0) {
             for (int kk = 0; kk < D / 16; kk++) {
                 const uint64_t kh = op_desc(sbase + C::OFF_KH, BKV, kk);
@@ -361,7 +412,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (sm.abort && tid == 0) mbar_wait_bounded(&sm.mma_bar, phase ^ 1u);  // let an issued MMA group finish
+    if (sm.abort && tid == 0) {
+        mbar_wait_bounded(&sm.mma_bar, phase ^ 1u);  // let an issued MMA group finish
+        if (raw_pending) mbar_wait_bounded(&sm.raw_bar, raw_phase);  // and a staging fill in flight
+    }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();

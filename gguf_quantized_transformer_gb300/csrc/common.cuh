@@ -1,5 +1,6 @@
 // Shared device/host definitions of the CUDA library (not part of the C ABI).
 #pragma once
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -196,6 +197,11 @@ cudaError_t launch_qgemv(const Planes& W, const float* x, const float* norm_w, f
 cudaError_t qgemv_prepare();
 // Largest number of K chunks (Kp / chunk_weights) a GEMV supports.
 int qgemv_max_chunks();
+
+// A 2-D TMA tensor map over an fp16 [rows][ld] array: box box_cols (innermost, 64 for SWIZZLE_128B) x box_rows,
+// SWIZZLE_128B, zero fill outside the array.  false if the driver refuses it.
+bool make_tmap_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_cols,
+                   uint32_t box_rows);
 
 // Prefill GEMM on the tensor cores: Y = X W^T for M rows with a fused epilogue.  X is given as fp16
 // hi + lo planes [M][ldx] (ldx % 8 == 0, 16-byte aligned).  err: device error word.
