@@ -5,29 +5,34 @@
 //
 // CTA (query tile, kv head g): 128 query vectors = QT = 128/G rows x the G
 // heads of the group (vector v = h * QT + row), so every K/V tile is used by
-// all heads of the group.  Keys stream in tiles of BKV = 64 slots: one bulk
-// copy each of the tile's raw K and V rows into a staging buffer, issued while
-// the previous tile is multiplied, so the loads overlap the MMAs and the
-// softmax.  Two passes over the keys:
-//   pass A: S = Q_hi K_hi^T (one MMA per 16-wide K step) -> per-row maximum m;
-//   pass B: S = Q K^T exactly (hi/lo split, below) -> p = exp(s - m) with the
-//           causal mask, row sums l, P (fp16 hi + lo) written to shared memory,
-//           O += P V accumulated in TMEM across all key tiles.
-// With the maximum known before pass B nothing is ever rescaled; the output
-// is O / l, written as the fp16 hi + lo planes the O-projection GEMM reads.
+// all heads of the group.  One pass over the keys in tiles of BKV slots (64 for
+// an fp16 cache, 32 for fp32), with warps specialised and the tiles pipelined:
+//   warp 9      : bulk copies of each tile's raw K and V rows into a staging
+//                 buffer (the next tile streams in while this one is converted);
+//   warps 4..7  : convert the staged rows into the MMA operands of one of two
+//                 buffers: K rows as they are (split hi + lo for fp32) and V
+//                 transposed, so that keys run along K of the P V product;
+//   warp 8      : one lane issues S = Q K^T for tile t, then O += P V for tile
+//                 t - 1, each followed by a commit;
+//   warps 0..3  : own the 128 TMEM lanes (one query vector each): the online
+//                 softmax of S with the causal mask, P (fp16 hi + lo) into one
+//                 of two buffers, and the epilogue.
+// The running maximum is rescaled lazily: P uses a reference maximum that only
+// moves (rescaling O in TMEM and the row sum) when a tile's maximum exceeds it
+// by more than kLazy, so p <= e^kLazy and fp16 P stays in range.  O / l does not
+// depend on the reference, so the result is the same as with the exact maximum.
+// The output is O / l, written as the fp16 hi + lo planes the O-projection GEMM
+// reads.
 //
 // Precision.  Q (scaled by 1/sqrt(D)) and P are split into fp16 hi + lo; an
 // fp16 cache is exact in fp16, an fp32 cache is split too.  The products
 // kept are A_hi B_hi + A_lo B_hi (+ A_hi B_lo for an fp32 cache), fp32
 // accumulate: near-fp32 scores and outputs.
 //
-// Operands live in shared memory in the SWIZZLE_128B K-major layout, written
-// by the CTA's threads (Q from the fp32 q rows; K rows as they are and V
-// transposed, so that keys run along K of the P V product, both from the
-// staging buffer).  One thread issues
-// the MMAs; warps 0-3 own the 128 TMEM lanes (one query vector each) for the
-// softmax and the epilogue (every tcgen05.ld is executed by whole warps under
-// warp-uniform conditions).  Every wait on the MMA barrier is bounded.
+// Operands live in shared memory in the SWIZZLE_128B K-major layout.  Every
+// tcgen05.ld / st is executed by whole warps under warp-uniform conditions,
+// and every mbarrier wait is bounded: a CTA that gives up records DEV_TIMEOUT,
+// lets what it issued finish and frees its TMEM.
 #include <math_constants.h>
 
 #include "common.cuh"
@@ -36,33 +41,6 @@
 namespace af {
 
 namespace {
-
-constexpr int kPThreads = 256;
-constexpr int BQ = 128;          // query vectors per CTA = TMEM lanes
-constexpr int kTmemCols = 256;   // S at column 0 (BKV columns), O at column 128 (D columns)
-constexpr int kOCol = 128;
-
-template <int D, typename KT>
-struct PCfg {
-    static constexpr bool SPLIT_KV = sizeof(KT) == 4;  // fp32 cache: K and V need hi + lo
-    static constexpr int BKV = 64;                     // keys per tile
-    static constexpr int Q_BYTES = BQ * D * 2;         // one fp16 plane
-    static constexpr int K_BYTES = BKV * D * 2;
-    static constexpr int V_BYTES = D * BKV * 2;
-    static constexpr int P_BYTES = BQ * BKV * 2;
-    static constexpr int OFF_QH = 0;
-    static constexpr int OFF_QL = OFF_QH + Q_BYTES;
-    static constexpr int OFF_KH = OFF_QL + Q_BYTES;
-    static constexpr int OFF_KL = OFF_KH + K_BYTES;
-    static constexpr int OFF_VH = OFF_KL + (SPLIT_KV ? K_BYTES : 0);
-    static constexpr int OFF_VL = OFF_VH + V_BYTES;
-    static constexpr int OFF_PH = OFF_VL + (SPLIT_KV ? V_BYTES : 0);
-    static constexpr int OFF_PL = OFF_PH + P_BYTES;
-    static constexpr int RAW_BYTES = BKV * D * (int)sizeof(KT);  // one tile of raw cache rows
-    static constexpr int OFF_RK = OFF_PL + P_BYTES;              // staging: raw K rows, then raw V rows
-    static constexpr int OFF_RV = OFF_RK + RAW_BYTES;
-    static constexpr int SMEM = OFF_RV + RAW_BYTES + 1024;       // + 1024-byte alignment slack
-};
 
 // Byte offset of 16-byte chunk c (8 fp16 along K) of row r in an operand of R rows stored as
 // SWIZZLE_128B atoms of 64 K-elements: atom c/8 is a [R][128 B] block.
@@ -110,24 +88,77 @@ __device__ __forceinline__ uint4 pack8_f16(const float (&w)[8]) {  // exact for 
     return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
+
+constexpr int kPWarps = 10;
+constexpr int kPThreads = kPWarps * 32;
+constexpr int BQ = 128;          // query vectors per CTA = TMEM lanes
+constexpr int kTmemCols = 256;   // S buffers at columns 0 and BKV, O at column 128 (D columns)
+constexpr int kOCol = 128;
+constexpr float kLazy = 8.f;     // the reference maximum moves when a tile exceeds it by more than this
+
+template <int D, typename KT>
+struct PCfg {
+    static constexpr bool SPLIT_KV = sizeof(KT) == 4;  // fp32 cache: K and V need hi + lo
+    static constexpr int BKV = 64;                     // keys per tile (a whole 128-byte row of a P / V^T atom)
+    static constexpr int NBUF = SPLIT_KV ? 1 : 2;      // operand buffers (an fp32 cache's hi + lo fill one's room)
+    static constexpr int Q_BYTES = BQ * D * 2;         // one fp16 plane
+    static constexpr int K_BYTES = BKV * D * 2;
+    static constexpr int V_BYTES = D * BKV * 2;
+    static constexpr int P_BYTES = BQ * BKV * 2;
+    // one operand buffer: K hi (+ lo), V hi (+ lo), P hi + lo
+    static constexpr int B_KH = 0;
+    static constexpr int B_KL = B_KH + K_BYTES;
+    static constexpr int B_VH = B_KL + (SPLIT_KV ? K_BYTES : 0);
+    static constexpr int B_VL = B_VH + V_BYTES;
+    static constexpr int B_PH = B_VL + (SPLIT_KV ? V_BYTES : 0);
+    static constexpr int B_PL = B_PH + P_BYTES;
+    static constexpr int BUF = (B_PL + P_BYTES + 1023) / 1024 * 1024;
+    static constexpr int OFF_QH = 0;
+    static constexpr int OFF_QL = Q_BYTES;
+    static constexpr int OFF_BUF = 2 * Q_BYTES;        // the operand buffers
+    static constexpr int RAW_BYTES = BKV * D * (int)sizeof(KT);
+    static constexpr int OFF_RK = OFF_BUF + NBUF * BUF;  // staging: raw K rows, then raw V rows
+    static constexpr int OFF_RV = OFF_RK + RAW_BYTES;
+    static constexpr int SMEM = OFF_RV + RAW_BYTES + 1024;  // + 1024-byte alignment slack
+};
+
 struct PSmem {
-    uint64_t mma_bar;
-    uint64_t raw_bar;  // staging filled (transaction bytes)
+    uint64_t raw_full;     // staging filled (transaction bytes)
+    uint64_t raw_empty;    // staging converted (4 converter warps)
+    uint64_t op_full[2];   // K / V operands of buffer t % NBUF written (4 converter warps)
+    uint64_t op_free[2];   // P V of buffer t % NBUF done: its operands and P are free (commit)
+    uint64_t s_full[2];    // S of tile t in TMEM columns (t & 1) * BKV computed (commit)
+    uint64_t p_full[2];    // P of tile t written, O rescaled if needed (4 softmax warps), indexed t & 1
+    uint64_t done;         // every MMA finished (commit)
     uint32_t tmem_base;
+    int fills;             // staging fills issued (for the drain on abort)
     volatile int abort;
 };
 
-// Bounded wait on the MMA barrier (all threads); false after a timeout (recorded once).
-__device__ __forceinline__ bool wait_mma(PSmem& sm, unsigned parity, unsigned* err) {
-    if (mbar_wait_bounded(&sm.mma_bar, parity)) return true;
+// Bounded wait of a whole warp; false (warp-uniformly) after a timeout or when the CTA aborts.
+__device__ __forceinline__ bool pwait(uint64_t* bar, unsigned parity, PSmem& sm, unsigned* err) {
+    bool ok = false;
+    for (unsigned i = 0; i < kWaitLimit && !ok; i++) {
+        ok = mbar_try_wait(bar, parity);
+        if (!ok && sm.abort) break;
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && (threadIdx.x & 31) == 0 && !sm.abort) {
+        sm.abort = 1;
+        atomicExch(err, (unsigned)DEV_TIMEOUT);
+    }
+    return ok;
+}
+// the same for one thread (the MMA issuer and the copy producer)
+__device__ __forceinline__ bool pwait1(uint64_t* bar, unsigned parity, PSmem& sm, unsigned* err) {
+    for (unsigned i = 0; i < kWaitLimit; i++) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (sm.abort) return false;
+    }
     sm.abort = 1;
     atomicExch(err, (unsigned)DEV_TIMEOUT);
     return false;
 }
-
-}  // namespace
-
-namespace {
 
 template <int D, int G, typename KT>
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -152,8 +183,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const KT* V = vc + (int64_t)g * max_ctx * D;
 
     if (tid == 0) {
-        mbar_init(&sm.mma_bar, 1);
-        mbar_init(&sm.raw_bar, 1);
+        mbar_init(&sm.raw_full, 1);
+        mbar_init(&sm.raw_empty, 4);
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&sm.op_full[b], 4);
+            mbar_init(&sm.s_full[b], 1);
+            mbar_init(&sm.p_full[b], 4);
+            mbar_init(&sm.op_free[b], 1);
+        }
+        mbar_init(&sm.done, 1);
+        sm.fills = 0;
         sm.abort = 0;
         fence_mbar_init();
     }
@@ -162,36 +201,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    constexpr int NB = C::NBUF;
+    auto buf = [&](int b) { return smem + C::OFF_BUF + b * C::BUF; };
 
-    // ---- staging of raw cache rows: one bulk copy of the keys of tile t (K, and V in pass B), issued by one
-    // thread; every wait is bounded, and the phase flips once per fill.
-    const KT* stK = reinterpret_cast<const KT*>(smem + C::OFF_RK);
-    const KT* stV = reinterpret_cast<const KT*>(smem + C::OFF_RV);
-    unsigned raw_phase = 0;
-    auto raw_issue = [&](int t, bool with_v) {  // thread 0 only
-        const int keys = min(BKV, nkeys - t * BKV);
-        const unsigned bytes = (unsigned)(keys * D * (int)sizeof(KT));
-        mbar_arrive_expect_tx(&sm.raw_bar, with_v ? 2 * bytes : bytes);
-        bulk_g2s(smem + C::OFF_RK, K + (int64_t)t * BKV * D, bytes, &sm.raw_bar);
-        if (with_v) bulk_g2s(smem + C::OFF_RV, V + (int64_t)t * BKV * D, bytes, &sm.raw_bar);
-    };
-    auto raw_wait = [&]() {  // all threads; false after a timeout (the fill stays pending for the drain)
-        const bool ok = mbar_wait_bounded(&sm.raw_bar, raw_phase);
-        if (!ok) {
-            sm.abort = 1;
-            atomicExch(err, (unsigned)DEV_TIMEOUT);
-            return false;
-        }
-        raw_phase ^= 1u;
-        return true;
-    };
-    bool raw_pending = false;  // thread 0: a fill it issued has not been waited for (the drain on abort)
-    if (tid == 0) {
-        raw_issue(0, false);
-        raw_pending = true;
-    }
-
-    // ---- Q tile: vector v = h * QT + row, scaled by 1/sqrt(D), split hi + lo
+    // ---- Q tile (all threads): vector v = h * QT + row, scaled by 1/sqrt(D), split hi + lo
     {
         const float scale = rsqrtf((float)D);
         for (int i = tid; i < BQ * (D / 8); i += kPThreads) {
@@ -212,209 +225,238 @@ __global__ void __launch_bounds__(kPThreads, 1)
             *reinterpret_cast<uint4*>(smem + C::OFF_QL + op_off(BQ, v, c)) = lo;
         }
     }
-    // K tile t: rows = keys, K axis = D
-    auto load_k = [&](int t, bool with_lo) {
-        for (int i = tid; i < BKV * (D / 8); i += kPThreads) {
-            const int j = i / (D / 8), c = i % (D / 8);
-            const int key = t * BKV + j;
-            float w[8];
-            if (key < nkeys) {
-                ld8(stK + (int64_t)j * D + 8 * c, w);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; e++) w[e] = 0.f;
+    fence_proxy_async_shared();  // Q (generic-proxy writes) -> visible to the tensor core
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (warp == 9) {
+        // ---------------- staging producer: raw K and V rows of tile t (one bulk copy each)
+        if (lane == 0) {
+            for (int t = 0; t < ntiles; t++) {
+                if (t > 0 && !pwait1(&sm.raw_empty, (t - 1) & 1, sm, err)) break;
+                const int keys = min(BKV, nkeys - t * BKV);
+                const unsigned bytes = (unsigned)(keys * D * (int)sizeof(KT));
+                mbar_arrive_expect_tx(&sm.raw_full, 2 * bytes);
+                bulk_g2s(smem + C::OFF_RK, K + (int64_t)t * BKV * D, bytes, &sm.raw_full);
+                bulk_g2s(smem + C::OFF_RV, V + (int64_t)t * BKV * D, bytes, &sm.raw_full);
+                sm.fills = t + 1;
             }
-            if (C::SPLIT_KV) {
-                uint4 hi, lo;
-                split8(w, hi, lo);
-                *reinterpret_cast<uint4*>(smem + C::OFF_KH + op_off(BKV, j, c)) = hi;
-                if (with_lo) *reinterpret_cast<uint4*>(smem + C::OFF_KL + op_off(BKV, j, c)) = lo;
-            } else {
-                *reinterpret_cast<uint4*>(smem + C::OFF_KH + op_off(BKV, j, c)) = pack8_f16(w);
-            }
+            // every fill is consumed before the converters finish, so nothing is in flight past the final barrier
+            // unless the CTA aborted (then the drain below waits for the last fill)
         }
-    };
-    // V tile t transposed: rows = d, K axis = keys (thread: dims 2dp, 2dp+1 of 8 keys)
-    auto load_v = [&](int t) {
-        for (int i = tid; i < (D / 2) * (BKV / 8); i += kPThreads) {
-            const int dp = i % (D / 2), kg = i / (D / 2);
-            float a[8], b[8];
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const int key = t * BKV + 8 * kg + e;
-                if (key < nkeys) {
-                    ld2(stV + (int64_t)(8 * kg + e) * D + 2 * dp, a[e], b[e]);
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------- converters: staging -> K / V operands of buffer t % NBUF
+        const int ct = tid - 128;  // 0..127
+        const KT* stK = reinterpret_cast<const KT*>(smem + C::OFF_RK);
+        const KT* stV = reinterpret_cast<const KT*>(smem + C::OFF_RV);
+        for (int t = 0; t < ntiles; t++) {
+            const int b = t % NB;
+            if (!pwait(&sm.raw_full, t & 1, sm, err)) break;
+            // the buffer's previous tile (t - NBUF) is multiplied: P V done
+            if (t >= NB && !pwait(&sm.op_free[b], ((t - NB) / NB) & 1, sm, err)) break;
+            uint8_t* ob = buf(b);
+            // K tile: rows = keys, K axis = D
+            for (int i = ct; i < BKV * (D / 8); i += 128) {
+                const int j = i / (D / 8), c = i % (D / 8);
+                float w[8];
+                if (t * BKV + j < nkeys) {
+                    ld8(stK + (int64_t)j * D + 8 * c, w);
                 } else {
-                    a[e] = 0.f;
-                    b[e] = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; e++) w[e] = 0.f;
+                }
+                if (C::SPLIT_KV) {
+                    uint4 hi, lo;
+                    split8(w, hi, lo);
+                    *reinterpret_cast<uint4*>(ob + C::B_KH + op_off(BKV, j, c)) = hi;
+                    *reinterpret_cast<uint4*>(ob + C::B_KL + op_off(BKV, j, c)) = lo;
+                } else {
+                    *reinterpret_cast<uint4*>(ob + C::B_KH + op_off(BKV, j, c)) = pack8_f16(w);
                 }
             }
-            if (C::SPLIT_KV) {
-                uint4 ah, al, bh, bl;
-                split8(a, ah, al);
-                split8(b, bh, bl);
-                *reinterpret_cast<uint4*>(smem + C::OFF_VH + op_off(D, 2 * dp, kg)) = ah;
-                *reinterpret_cast<uint4*>(smem + C::OFF_VH + op_off(D, 2 * dp + 1, kg)) = bh;
-                *reinterpret_cast<uint4*>(smem + C::OFF_VL + op_off(D, 2 * dp, kg)) = al;
-                *reinterpret_cast<uint4*>(smem + C::OFF_VL + op_off(D, 2 * dp + 1, kg)) = bl;
-            } else {
-                *reinterpret_cast<uint4*>(smem + C::OFF_VH + op_off(D, 2 * dp, kg)) = pack8_f16(a);
-                *reinterpret_cast<uint4*>(smem + C::OFF_VH + op_off(D, 2 * dp + 1, kg)) = pack8_f16(b);
-            }
-        }
-    };
-    // generic-proxy writes of the operands -> visible to the tensor core; then one thread issues
-    auto publish = [&]() {
-        fence_proxy_async_shared();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    };
-
-    // softmax state of this thread's query vector (warps 0..3: TMEM lane = vector)
-    const int v = warp * 32 + lane;
-    const int rr = v % QT;
-    const bool vrow = warp < 4 && rr < nrows;
-    const int qpos = pos0 + r0 + rr;
-    float m = -CUDART_INF_F, l = 0.f;
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    unsigned phase = 0;
-
-    // ---- pass A: row maxima from Q_hi K_hi^T
-    for (int t = 0; t < ntiles && !sm.abort; t++) {
-        if (__syncthreads_or(!raw_wait())) break;  // block-uniform
-        raw_pending = false;
-        load_k(t, false);
-        publish();
-        if (tid == 0 && !sm.abort) {  // the staging is free: the next tile (pass B starts over at tile 0 with V)
-            fence_proxy_async_shared();
-            if (t + 1 < ntiles) raw_issue(t + 1, false);
-            else raw_issue(0, true);
-            raw_pending = true;
-        }
-        if (tid == 0) {
-            for (int kk = 0; kk < D / 16; kk++)
-                mma_f16(tmem, op_desc(sbase + C::OFF_QH, BQ, kk), op_desc(sbase + C::OFF_KH, BKV, kk), kIdS,
-                        kk > 0 ? 1u : 0u);
-            mma_commit(&sm.mma_bar);
-        }
-        const bool ok = __all_sync(0xffffffffu, wait_mma(sm, phase, err));  // warp-uniform for tcgen05.ld
-        phase ^= 1u;
-        tc_fence_after();
-        if (ok && warp < 4) {
+            // V tile transposed: rows = d, K axis = keys (thread: dims 2dp, 2dp + 1 of 8 keys)
+            for (int i = ct; i < (D / 2) * (BKV / 8); i += 128) {
+                const int dp = i % (D / 2), kg = i / (D / 2);
+                float a[8], bb[8];
 #pragma unroll
-            for (int c32 = 0; c32 < BKV / 32; c32++) {
-                float s[32];
-                tmem_ld32(lane_addr + (uint32_t)(c32 * 32), s);
-#pragma unroll
-                for (int e = 0; e < 32; e++) {
-                    const int key = t * BKV + c32 * 32 + e;
-                    if (key <= qpos) m = fmaxf(m, s[e]);
+                for (int e = 0; e < 8; e++) {
+                    if (t * BKV + 8 * kg + e < nkeys) {
+                        ld2(stV + (int64_t)(8 * kg + e) * D + 2 * dp, a[e], bb[e]);
+                    } else {
+                        a[e] = 0.f;
+                        bb[e] = 0.f;
+                    }
+                }
+                if (C::SPLIT_KV) {
+                    uint4 ah, al, bh, bl;
+                    split8(a, ah, al);
+                    split8(bb, bh, bl);
+                    *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp, kg)) = ah;
+                    *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp + 1, kg)) = bh;
+                    *reinterpret_cast<uint4*>(ob + C::B_VL + op_off(D, 2 * dp, kg)) = al;
+                    *reinterpret_cast<uint4*>(ob + C::B_VL + op_off(D, 2 * dp + 1, kg)) = bl;
+                } else {
+                    *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp, kg)) = pack8_f16(a);
+                    *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp + 1, kg)) = pack8_f16(bb);
                 }
             }
-        }
-        tc_fence_before();
-        __syncthreads();
-    }
-    if (!vrow) m = 0.f;
-
-    // ---- pass B: exact scores, P, O += P V
-    for (int t = 0; t < ntiles && !sm.abort; t++) {
-        if (__syncthreads_or(!raw_wait())) break;  // block-uniform
-        raw_pending = false;
-        load_k(t, true);
-        load_v(t);
-        publish();
-        if (tid == 0 && !sm.abort && t + 1 < ntiles) {
-            fence_proxy_async_shared();
-            raw_issue(t + 1, true);
-            raw_pending = true;
-        }
-        if (tid == 0) {
-            for (int kk = 0; kk < D / 16; kk++) {
-                const uint64_t kh = op_desc(sbase + C::OFF_KH, BKV, kk);
-                mma_f16(tmem, op_desc(sbase + C::OFF_QH, BQ, kk), kh, kIdS, kk > 0 ? 1u : 0u);
-                mma_f16(tmem, op_desc(sbase + C::OFF_QL, BQ, kk), kh, kIdS, 1u);
-                if (C::SPLIT_KV)
-                    mma_f16(tmem, op_desc(sbase + C::OFF_QH, BQ, kk), op_desc(sbase + C::OFF_KL, BKV, kk), kIdS, 1u);
+            fence_proxy_async_shared();  // the operands -> visible to the tensor core
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sm.raw_empty);   // the staging may be refilled
+                mbar_arrive(&sm.op_full[b]);  // the operands of tile t are ready
             }
-            mma_commit(&sm.mma_bar);
         }
-        bool ok = __all_sync(0xffffffffu, wait_mma(sm, phase, err));
-        phase ^= 1u;
-        tc_fence_after();
-        if (ok && warp < 4) {
+    } else if (warp == 8) {
+        // ---------------- MMA issuer: S(t), then O += P V for tile t - 1
+        if (lane == 0) {
+            auto issue_pv = [&](int t) {
+                const int b = t % NB;
+                const uint8_t* ob = buf(b);
+                const uint32_t ph = smem_u32(ob + C::B_PH), pl = smem_u32(ob + C::B_PL);
+                const uint32_t vh = smem_u32(ob + C::B_VH), vl = smem_u32(ob + C::B_VL);
+                for (int kk = 0; kk < BKV / 16; kk++) {
+                    const uint64_t dvh = op_desc(vh, D, kk);
+                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                    mma_f16(tmem + kOCol, op_desc(ph, BQ, kk), dvh, kIdO, acc);
+                    mma_f16(tmem + kOCol, op_desc(pl, BQ, kk), dvh, kIdO, 1u);
+                    if (C::SPLIT_KV) mma_f16(tmem + kOCol, op_desc(ph, BQ, kk), op_desc(vl, D, kk), kIdO, 1u);
+                }
+                mma_commit(&sm.op_free[b]);
+            };
+            // with one operand buffer the converters wait for P V(t - 1) before they fill it for tile t, so that
+            // P V goes first; with two, S(t) goes first so that the softmax of tile t overlaps P V(t - 1)
+            int t = 0;
+            for (; t < ntiles; t++) {
+                const int b = t % NB;
+                if (NB == 1 && t > 0) {
+                    if (!pwait1(&sm.p_full[(t - 1) & 1], ((t - 1) >> 1) & 1, sm, err)) break;
+                    tc_fence_after();
+                    issue_pv(t - 1);
+                }
+                if (!pwait1(&sm.op_full[b], (t / NB) & 1, sm, err)) break;
+                tc_fence_after();
+                const uint8_t* ob = buf(b);
+                const uint32_t kh = smem_u32(ob + C::B_KH), kl = smem_u32(ob + C::B_KL);
+                const uint32_t scol = tmem + (uint32_t)((t & 1) * BKV);
+                for (int kk = 0; kk < D / 16; kk++) {
+                    const uint64_t dkh = op_desc(kh, BKV, kk);
+                    mma_f16(scol, op_desc(sbase + C::OFF_QH, BQ, kk), dkh, kIdS, kk > 0 ? 1u : 0u);
+                    mma_f16(scol, op_desc(sbase + C::OFF_QL, BQ, kk), dkh, kIdS, 1u);
+                    if (C::SPLIT_KV) mma_f16(scol, op_desc(sbase + C::OFF_QH, BQ, kk), op_desc(kl, BKV, kk), kIdS, 1u);
+                }
+                mma_commit(&sm.s_full[t & 1]);
+                if (NB > 1 && t > 0) {  // the previous tile's P is ready: its P V
+                    if (!pwait1(&sm.p_full[(t - 1) & 1], ((t - 1) >> 1) & 1, sm, err)) break;
+                    tc_fence_after();
+                    issue_pv(t - 1);
+                }
+            }
+            if (t == ntiles && !sm.abort && pwait1(&sm.p_full[(t - 1) & 1], ((t - 1) >> 1) & 1, sm, err)) {
+                tc_fence_after();
+                issue_pv(t - 1);
+            }
+            mma_commit(&sm.done);  // always: also after a break, so the drain can wait on it
+        }
+    } else {
+        // ---------------- softmax warps 0..3: TMEM lane = query vector
+        const int v = warp * 32 + lane;
+        const int rr = v % QT;
+        const bool vrow = rr < nrows;
+        const int qpos = pos0 + r0 + rr;
+        float m_ref = -CUDART_INF_F, l = 0.f;
+        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        for (int t = 0; t < ntiles; t++) {
+            const int b = t % NB, sb = t & 1;
+            if (!pwait(&sm.s_full[sb], (t >> 1) & 1, sm, err)) break;
+            tc_fence_after();
+            float mt = -CUDART_INF_F;  // this tile's maximum of the row (S is read twice from TMEM: max, then p)
 #pragma unroll
             for (int c32 = 0; c32 < BKV / 32; c32++) {
-                float s[32];
-                tmem_ld32(lane_addr + (uint32_t)(c32 * 32), s);
+                float s32[32];
+                tmem_ld32(lane_addr + (uint32_t)(sb * BKV + c32 * 32), s32);
+#pragma unroll
+                for (int e = 0; e < 32; e++)
+                    if (vrow && t * BKV + c32 * 32 + e <= qpos) mt = fmaxf(mt, s32[e]);
+            }
+            // the reference maximum moves only when this tile exceeds it by more than kLazy
+            const bool move = mt > m_ref + kLazy;
+            if (__any_sync(0xffffffffu, move && t > 0)) {
+                // O holds tiles < t: wait for the previous P V, then rescale this warp's rows (warp-collective)
+                if (!pwait(&sm.op_free[(t - 1) % NB], ((t - 1) / NB) & 1, sm, err)) break;
+                tc_fence_after();
+                const float f = move ? __expf(m_ref - mt) : 1.f;
+#pragma unroll
+                for (int c32 = 0; c32 < D / 32; c32++) {
+                    float o[32];
+                    tmem_ld32(lane_addr + (uint32_t)(kOCol + c32 * 32), o);
+                    uint32_t ou[32];
+#pragma unroll
+                    for (int e = 0; e < 32; e++) ou[e] = __float_as_uint(o[e] * f);
+                    tmem_st32(lane_addr + (uint32_t)(kOCol + c32 * 32), ou);
+                }
+                tmem_st_wait();
+                l *= f;
+            }
+            if (move) m_ref = mt;
+            // P of tile t into buffer b (its previous P, of tile t - NBUF, was consumed: the converters waited on
+            // that P V before writing this buffer's operands, and S(t) came after)
+            uint8_t* ob = buf(b);
+#pragma unroll
+            for (int c32 = 0; c32 < BKV / 32; c32++) {
+                float s32[32];
+                tmem_ld32(lane_addr + (uint32_t)(sb * BKV + c32 * 32), s32);
 #pragma unroll
                 for (int q8 = 0; q8 < 4; q8++) {
                     float w[8];
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         const int key = t * BKV + c32 * 32 + q8 * 8 + e;
-                        const float p = (vrow && key <= qpos) ? __expf(s[q8 * 8 + e] - m) : 0.f;
+                        const float p = (vrow && key <= qpos) ? __expf(s32[q8 * 8 + e] - m_ref) : 0.f;
                         l += p;
                         w[e] = p;
                     }
                     uint4 hi, lo;
                     split8(w, hi, lo);
-                    const int c = c32 * 4 + q8;  // 16-byte chunk along the keys
-                    *reinterpret_cast<uint4*>(smem + C::OFF_PH + op_off(BQ, v, c)) = hi;
-                    *reinterpret_cast<uint4*>(smem + C::OFF_PL + op_off(BQ, v, c)) = lo;
+                    *reinterpret_cast<uint4*>(ob + C::B_PH + op_off(BQ, v, c32 * 4 + q8)) = hi;
+                    *reinterpret_cast<uint4*>(ob + C::B_PL + op_off(BQ, v, c32 * 4 + q8)) = lo;
                 }
             }
+            fence_proxy_async_shared();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.p_full[sb]);
         }
-        publish();
-        if (sm.abort) break;
-        if (tid == 0) {
-            for (int kk = 0; kk < BKV / 16; kk++) {
-                const uint64_t vh = op_desc(sbase + C::OFF_VH, D, kk);
-                const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
-                mma_f16(tmem + kOCol, op_desc(sbase + C::OFF_PH, BQ, kk), vh, kIdO, acc);
-                mma_f16(tmem + kOCol, op_desc(sbase + C::OFF_PL, BQ, kk), vh, kIdO, 1u);
-                if (C::SPLIT_KV)
-                    mma_f16(tmem + kOCol, op_desc(sbase + C::OFF_PH, BQ, kk), op_desc(sbase + C::OFF_VL, D, kk),
-                            kIdO, 1u);
-            }
-            mma_commit(&sm.mma_bar);
-        }
-        ok = __all_sync(0xffffffffu, wait_mma(sm, phase, err));
-        phase ^= 1u;
-        tc_fence_after();
-        tc_fence_before();
-        __syncthreads();  // P, K and V buffers are free for the next tile
-    }
-
-    // ---- epilogue: O / l as fp16 hi + lo.  tcgen05.ld is warp-collective: whole warps 0..3 load,
-    // only the lanes of valid query rows store.
-    if (!sm.abort && warp < 4) {
-        const float inv = vrow ? 1.f / l : 0.f;
-        const int64_t o0 = (int64_t)(r0 + rr) * ldo + (int64_t)(g * G + v / QT) * D;
+        // ---- epilogue: O / l as fp16 hi + lo (whole warps load; lanes of valid rows store)
+        if (__all_sync(0xffffffffu, !sm.abort) && pwait(&sm.done, 0, sm, err)) {
+            tc_fence_after();
+            const float inv = vrow ? 1.f / l : 0.f;
+            const int64_t o0 = (int64_t)(r0 + rr) * ldo + (int64_t)(g * G + v / QT) * D;
 #pragma unroll
-        for (int c32 = 0; c32 < D / 32; c32++) {
-            float o[32];
-            tmem_ld32(lane_addr + (uint32_t)(kOCol + c32 * 32), o);
-            if (vrow) {
+            for (int c32 = 0; c32 < D / 32; c32++) {
+                float o[32];
+                tmem_ld32(lane_addr + (uint32_t)(kOCol + c32 * 32), o);
+                if (vrow) {
 #pragma unroll
-                for (int q8 = 0; q8 < 4; q8++) {
-                    float w[8];
+                    for (int q8 = 0; q8 < 4; q8++) {
+                        float w[8];
 #pragma unroll
-                    for (int e = 0; e < 8; e++) w[e] = o[q8 * 8 + e] * inv;
-                    uint4 hi, lo;
-                    split8(w, hi, lo);
-                    *reinterpret_cast<uint4*>(out_hi + o0 + c32 * 32 + q8 * 8) = hi;
-                    *reinterpret_cast<uint4*>(out_lo + o0 + c32 * 32 + q8 * 8) = lo;
+                        for (int e = 0; e < 8; e++) w[e] = o[q8 * 8 + e] * inv;
+                        uint4 hi, lo;
+                        split8(w, hi, lo);
+                        *reinterpret_cast<uint4*>(out_hi + o0 + c32 * 32 + q8 * 8) = hi;
+                        *reinterpret_cast<uint4*>(out_lo + o0 + c32 * 32 + q8 * 8) = lo;
+                    }
                 }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (sm.abort && tid == 0) {
-        mbar_wait_bounded(&sm.mma_bar, phase ^ 1u);  // let an issued MMA group finish
-        if (raw_pending) mbar_wait_bounded(&sm.raw_bar, raw_phase);  // and a staging fill in flight
+    if (sm.abort && tid == 0) {  // let the issued MMAs and the last staging fill issued finish before leaving
+        mbar_wait_bounded(&sm.done, 0);
+        if (sm.fills > 0) mbar_wait_bounded(&sm.raw_full, (unsigned)((sm.fills - 1) & 1));
     }
     __syncthreads();
     if (warp == 0) {
@@ -422,6 +464,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         tmem_free(tmem, kTmemCols);
     }
 }
+
+}  // namespace
+
+namespace {
 
 template <int D, int G, typename KT>
 cudaError_t launch_pf(const float* q, int64_t ldq, const void* kc, const void* vc, int KVH, int max_ctx, int pos0,
