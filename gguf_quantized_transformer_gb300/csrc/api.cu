@@ -461,7 +461,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
         P.D = D;
         P.max_ctx = c.max_ctx;
         P.kv_f16 = c.kv_dtype == AF_F16;
-        P.attn_splits = std::min(decode_attn_splits(c.n_kv_heads), 1216 / (c.n_heads / c.n_kv_heads));
+        P.attn_splits = std::min(decode_attn_splits(c.n_kv_heads), m->as.ns);  // within the partials buffer
         P.eps = c.rms_eps;
         P.layers = m->d_layers;
         P.emb = m->emb;
@@ -501,7 +501,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
         P.head.nw = m->out_norm;
         P.head.epi = epi_simple(EPI_LOGITS, m->logits, 0);
         P.head.epi.argmax = &m->st->argmax;
-        m->persistent_ok = ok && E / num_sms() + 2 <= decode_max_cta_rows() && E <= 4096;
+        m->persistent_ok = ok && E / num_sms() + 2 <= decode_max_cta_rows() && decode_configure(P, lp[0]);
         cudaError_t e = cudaMemcpyAsync(m->d_layers, lp.data(), sizeof(LayerPlan) * c.n_layers, cudaMemcpyHostToDevice, s);
         if (!e) e = cudaMemsetAsync(words, 0, 4 * sizeof(unsigned), s);
         if (!e) e = cudaStreamSynchronize(s);  // lp is a host temporary

@@ -277,12 +277,12 @@ constexpr size_t kStaticAttnPartFloats = (size_t)1 << 20;  // split partials (4 
 cudaError_t attn_static_scratch(float** part, unsigned** cnt, unsigned** err);
 
 // One GEMV of the persistent decode kernel: matrix, input, optional RMSNorm
-// weight, stage shape (R rows per ring slot, WK warps along K) and epilogue.
+// weight, rows per stage R and epilogue.
 struct GemvTask {
     Planes W;
     const float* x = nullptr;
     const float* nw = nullptr;
-    int R = 0, WK = 0;
+    int R = 0;
     Epi epi;
 };
 
@@ -294,8 +294,12 @@ struct LayerPlan {
 
 struct StepState;
 
+constexpr int kMaxSlotsP = 16;  // stage slots of the persistent decode kernel (one owner warp each)
+
 struct DecodePlan {
     int wtype = 0, n_layers = 0, H = 0, KVH = 0, D = 0, max_ctx = 0, kv_f16 = 0, attn_splits = 0;
+    int nslot = 0, slot_bytes = 0, att_T = 0;  // stage slots; cache slots per attention stage
+    int ximg_bytes = 0, tab_bytes = 0;         // bytes of the x image / attention scratch region, of the schedule
     float eps = 0.f;
     const LayerPlan* layers = nullptr;  // device array [n_layers]
     Planes emb;
@@ -303,7 +307,7 @@ struct DecodePlan {
     float* x = nullptr;
     float* q = nullptr;
     float* attn = nullptr;
-    float* attn_part = nullptr;  // [KVH][splits][G][D+2]
+    float* attn_part = nullptr;  // [KVH][splits][G][D+4]
     unsigned* attn_cnt = nullptr;  // [KVH], zero between steps
     StepState* st = nullptr;
     unsigned* bar_count = nullptr;  // grid barrier (zero-initialised)
@@ -317,6 +321,10 @@ struct DecodePlan {
 bool decode_gemv_task(const Planes& W, GemvTask& t);
 int decode_attn_splits(int n_kv_heads);
 int decode_max_cta_rows();
+// Slot size and count, attention stage length and scratch of a plan whose head task, splits and shapes are
+// set, given the host copy of a layer's tasks (every layer has the same shapes); false if the kernel cannot
+// run it.
+bool decode_configure(DecodePlan& p, const LayerPlan& l0);
 cudaError_t decode_prepare(const DecodePlan& p);
 cudaError_t launch_decode(const DecodePlan& p, cudaStream_t s);
 

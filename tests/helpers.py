@@ -74,10 +74,11 @@ def check_logits(got, ref, what, worst=None):
         assert int(np.argmax(got)) == oracle.argmax(ref), what
 
 
-def run_parity(af, cfg, seed, chunks, n_decode, kv_slots, start=0, prefix=None, max_chunk=512):
+def run_parity(af, cfg, seed, chunks, n_decode, kv_slots, start=0, prefix=None, max_chunk=512, decode_mode=None):
     """Prefill the prompt in `chunks` from position `start`, then n_decode greedy steps under teacher forcing,
     comparing every layer's residual stream and the logits with the oracle.  prefix(om, gm), if given, fills
-    cache slots [0, start) of both models before the first chunk.  Returns the worst errors seen."""
+    cache slots [0, start) of both models before the first chunk; decode_mode, if given, is set on the GPU
+    model (af_set_decode_mode).  Returns the worst errors seen."""
     import torch
 
     import oracle
@@ -86,6 +87,8 @@ def run_parity(af, cfg, seed, chunks, n_decode, kv_slots, start=0, prefix=None, 
     prompt = hm.prompt(sum(chunks) + start)[start:]
     om = oracle.Model.from_host(hm, kv_slots=kv_slots)
     gm = gpu_model(hm, max_chunk=max_chunk)
+    if decode_mode is not None:
+        af.af_set_decode_mode(gm.h, decode_mode)
     if prefix is not None:
         prefix(om, gm)
     L, E, V = cfg.n_layers, cfg.n_embd, cfg.n_vocab

@@ -14,7 +14,11 @@ slots start_pos..; "Shimmy v2.0 Architecture", Extended Context (YaRN)).
   * 2-layer versions of the Llama-3-8B Q4_0 and Q8_0/YaRN shapes through the
     whole model: two 512-token chunks then decode steps, and a 512-token chunk
     at start_pos 29696 over a cache prefix both sides hold (YaRN theta at
-    t ~ 30k, ~460 key tiles per query tile).
+    t ~ 30k, ~460 key tiles per query tile);
+  * the same decode steps through the persistent decode kernel
+    (AF_DECODE_PERSISTENT): its streamed attention over an fp16 cache after
+    1024 positions, and over an fp32 cache at t ~ 30k (about a hundred
+    stages per split).
 
 Tolerances: attention outputs within 1e-3 normwise per row (the standalone
 bar); layer outputs and logits within 2e-2 * RMS(oracle).  The worst errors
@@ -105,6 +109,13 @@ def test_long_context_shape_two_full_chunks(af):
     print(f"\n{cfg.name} 2 layers, 2 x 512 + 4: worst layer {worst['layer']:.2e}, logits {worst['logits']:.2e}")
 
 
+def test_llama3_8b_shape_persistent_decode(af):
+    """Two 512-token chunks, then 4 decode steps through the persistent kernel (Q4_0, fp16 cache, 2 layers)."""
+    cfg = synth.CONFIGS[3].with_(n_layers=2)
+    worst = run_parity(af, cfg, synth.seed_of(3), [512, 512], 4, 1024 + 4, decode_mode=af.AF_DECODE_PERSISTENT)
+    print(f"\n{cfg.name} 2 layers, persistent decode: worst layer {worst['layer']:.2e}, logits {worst['logits']:.2e}")
+
+
 def test_long_context_chunk_at_29696(af):
     """A 512-token chunk at start_pos 29696 over a seeded cache prefix (slots 0..29695, fp32 values both sides
     hold), then 2 decode steps from 30208: RoPE with the YaRN scale at t ~ 30k, attention over ~30k keys."""
@@ -127,8 +138,11 @@ def test_long_context_chunk_at_29696(af):
                 om.kv_write(l, g, 0, k.astype(np.float64), v.astype(np.float64))
         torch.cuda.synchronize()
 
-    worst = run_parity(af, cfg, synth.seed_of(4), [512], 2, start + 512 + 2, start=start, prefix=prefix)
-    print(f"\n{cfg.name} 2 layers, 512 at {start} + 2: worst layer {worst['layer']:.2e}, logits {worst['logits']:.2e}")
+    for mode in (af.AF_DECODE_KERNELS, af.AF_DECODE_PERSISTENT):
+        worst = run_parity(af, cfg, synth.seed_of(4), [512], 2, start + 512 + 2, start=start, prefix=prefix,
+                           decode_mode=mode)
+        print(f"\n{cfg.name} 2 layers, 512 at {start} + 2 (decode mode {mode}): worst layer {worst['layer']:.2e}, "
+              f"logits {worst['logits']:.2e}")
 
 
 def _wrap_f32(ptr, nbytes):

@@ -205,10 +205,9 @@ def test_persistent_decode_matches_kernel_mode(af, idx):
             tok = int(np.argmax(out[-1]))  # same host-side token sequence for both modes
         res[mode] = out
         m.close()
-    # the two modes hold x in different fixed-point widths (24-bit per block in the persistent kernel,
-    # 16-bit in the GEMV kernels: relative error <= 2^-16 of a block's maximum); over 16 layers that
-    # moves the largest logit deviation to ~1e-3 of the logits' RMS.  Each mode is held to the
-    # oracle's layer bar by its own parity test; this one checks that they agree closely.
+    # both modes hold x in the same 16-bit fixed point per block, but split and sum the attention and
+    # the GEMV rows in different orders; each mode is held to the oracle's layer bar by its own parity
+    # test, this one checks that they agree closely.
     for a, b in zip(res[af.AF_DECODE_PERSISTENT], res[af.AF_DECODE_KERNELS]):
         assert rms_rel_err(a, b) <= 4e-3
 
