@@ -193,6 +193,7 @@ struct af_model {
     float* logits = nullptr; // [V] default logits
     GemvScratch gs;
     AttnScratch as;
+    GemmSplit gsplit;  // split-K scratch of the prefill GEMMs
     StepState* st = nullptr;
     float* capture = nullptr;
     unsigned long long* trace = nullptr;
@@ -265,6 +266,7 @@ struct af_qweight {
     Planes p;
     Allocs A;
     GemvScratch gs;
+    GemmSplit gsplit;  // split-K scratch of af_qgemm (sized for 512 rows; calls on one weight are serialized)
     __half* x16[2] = {};  // af_qgemm operand: X as fp16 hi / lo, grown on demand
     int x16_rows = 0;
 };
@@ -445,6 +447,21 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
     m->as.part = (float*)A.get(attn_decode_part_elems(c.n_heads, D, m->as.ns) * 4);
     m->as.cnt = (unsigned*)A.get((size_t)c.n_kv_heads * 4);
     m->as.err = m->gs.err;
+    {  // split-K scratch: the largest any layer GEMM wants at a full chunk
+        const int NK[4][2] = {{QD + 2 * m->KVD(), E}, {E, QD}, {2 * F, E}, {E, F}};
+        size_t ws = 0;
+        int tiles = 0;
+        for (const auto& nk : NK) {
+            ws = std::max(ws, qgemm_ws_bytes(nk[0], nk[1], S));
+            tiles = std::max(tiles, qgemm_tiles(nk[0], S));
+        }
+        if (ws) {
+            m->gsplit.ws = (float*)A.get(ws);
+            m->gsplit.ws_bytes = m->gsplit.ws ? ws : 0;
+            m->gsplit.cnt = (unsigned*)A.get((size_t)tiles * 4);
+            m->gsplit.cnt_n = m->gsplit.cnt ? tiles : 0;
+        }
+    }
     if (!m->x || !m->q || !m->attn || !m->h || !m->y16[0] || !m->y16[1] || !m->a16[0] || !m->a16[1] || !m->h16[0] || !m->h16[1] || !m->tok || !m->logits || !m->st ||
         !m->gs.err || !m->as.part || !m->as.cnt)
         return oom("activations");
@@ -516,6 +533,7 @@ int af_model_create(const af_config* cfg, const af_weights* w, void* stream, af_
         if (!e) e = qgemm_prepare();
         if (!e) e = cudaMemsetAsync(m->gs.err, 0, kErrWords * sizeof(unsigned), s);
         if (!e) e = cudaMemsetAsync(m->as.cnt, 0, (size_t)c.n_kv_heads * 4, s);
+        if (!e && m->gsplit.cnt) e = cudaMemsetAsync(m->gsplit.cnt, 0, (size_t)m->gsplit.cnt_n * 4, s);
         if (!e) e = cudaMemsetAsync(m->st, 0, sizeof(StepState), s);
         if (!e) e = cudaStreamSynchronize(s);
         if (e) return cuda_fail(e, "model init");
@@ -680,16 +698,18 @@ int prefill_impl(af_model* m, const int* tok_dev, int n, int start_pos, float* l
         const LayerW& lw = m->L[l];
         CK(launch_rmsnorm_rows(m->x, n, E, lw.attn_norm, c.rms_eps, m->y16[0], m->y16[1], s));
         CK(launch_qgemm(lw.qkv, m->y16[0], m->y16[1], E, n, epi_qkv(m, l, m->q, nullptr, start_pos),
-                        m->gs.err, s));
+                        m->gs.err, s, &m->gsplit));
         CK(launch_attn_prefill(m->q, QD, m->kl(l), m->vl(l), c.kv_dtype != AF_F32, c.n_heads, c.n_kv_heads,
                                c.head_dim, c.max_ctx, start_pos, n, m->a16[0], m->a16[1], QD, m->gs.err, s));
-        CK(launch_qgemm(lw.o, m->a16[0], m->a16[1], QD, n, epi_simple(EPI_RESID, m->x, E), m->gs.err, s));
+        CK(launch_qgemm(lw.o, m->a16[0], m->a16[1], QD, n, epi_simple(EPI_RESID, m->x, E), m->gs.err, s,
+                        &m->gsplit));
         CK(launch_rmsnorm_rows(m->x, n, E, lw.ffn_norm, c.rms_eps, m->y16[0], m->y16[1], s));
         Epi eg = epi_simple(EPI_SWIGLU, nullptr, F);
         eg.out16 = m->h16[0];
         eg.out16_lo = m->h16[1];
-        CK(launch_qgemm(lw.gu, m->y16[0], m->y16[1], E, n, eg, m->gs.err, s));
-        CK(launch_qgemm(lw.down, m->h16[0], m->h16[1], F, n, epi_simple(EPI_RESID, m->x, E), m->gs.err, s));
+        CK(launch_qgemm(lw.gu, m->y16[0], m->y16[1], E, n, eg, m->gs.err, s, &m->gsplit));
+        CK(launch_qgemm(lw.down, m->h16[0], m->h16[1], F, n, epi_simple(EPI_RESID, m->x, E), m->gs.err, s,
+                        &m->gsplit));
         rc = capture_copy(m, l + 1, n);
         if (rc) return rc;
     }
@@ -809,6 +829,12 @@ int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t 
     cudaStream_t s = (cudaStream_t)stream;
     w->p = make_planes(w->A, wtype, N, K);
     w->gs.err = (unsigned*)w->A.get(kErrWords * sizeof(unsigned));
+    if (const size_t ws = qgemm_ws_bytes(N, K, 512)) {
+        w->gsplit.ws = (float*)w->A.get(ws);
+        w->gsplit.ws_bytes = w->gsplit.ws ? ws : 0;
+        w->gsplit.cnt = (unsigned*)w->A.get((size_t)qgemm_tiles(N, 512) * 4);
+        w->gsplit.cnt_n = w->gsplit.cnt ? qgemm_tiles(N, 512) : 0;
+    }
     if (!w->p.qs || !w->gs.err) {
         af_qweight_destroy(w);
         return fail(AF_ENOMEM, "device allocation failed");
@@ -817,6 +843,7 @@ int af_qweight_create(int32_t wtype, const void* blocks_dev, int32_t N, int32_t 
     if (!e) e = qgemm_prepare();
     if (!e) e = repack_into(w->p, blocks_dev, N, 0, 1, s);
     if (!e) e = cudaMemsetAsync(w->gs.err, 0, kErrWords * sizeof(unsigned), s);
+    if (!e && w->gsplit.cnt) e = cudaMemsetAsync(w->gsplit.cnt, 0, (size_t)w->gsplit.cnt_n * 4, s);
     if (!e) e = cudaStreamSynchronize(s);
     if (e) {
         af_qweight_destroy(w);
@@ -847,7 +874,8 @@ int af_qgemm(const af_qweight* wc, const float* X_dev, int32_t M, float* Y_dev, 
         if (!w->x16_rows) return fail(AF_ENOMEM, "operand buffer");
     }
     CK(launch_split_f16(X_dev, w->x16[0], w->x16[1], (int64_t)M * w->p.K, s));
-    CK(launch_qgemm(w->p, w->x16[0], w->x16[1], w->p.K, M, epi_simple(EPI_STORE, Y_dev, w->p.N), w->gs.err, s));
+    CK(launch_qgemm(w->p, w->x16[0], w->x16[1], w->p.K, M, epi_simple(EPI_STORE, Y_dev, w->p.N), w->gs.err, s,
+                    &w->gsplit));
     return AF_OK;
 }
 

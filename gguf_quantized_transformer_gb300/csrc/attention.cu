@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(CL ? kClWarps * 32 : kDecThreads, (!CL && G <=
     pdl_launch_dependents();
     // the position word is written before the kernels of a step start; everything else the previous
     // kernel writes (q, the cache slot at pos) is read after griddepcontrol.wait
-    const int pos = pos_dev ? *pos_dev : pos_arg;
+    const int pos = pos_dev ? __ldcg(pos_dev) : pos_arg;
     const int n = pos + 1;
     int ns_eff, chunk;
     dec_split(n, ns, ns_eff, chunk);
@@ -329,8 +329,8 @@ __global__ void __launch_bounds__(CL ? kClWarps * 32 : kDecThreads, (!CL && G <=
         const float scale = rsqrtf((float)D);
 #pragma unroll
         for (int h = 0; h < G; h++) {
-            const float4 a = *reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8);
-            const float4 b = *reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8 + 4);
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8));
+            const float4 b = __ldcg(reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8 + 4));
             qv[h][0] = a.x * scale; qv[h][1] = a.y * scale; qv[h][2] = a.z * scale; qv[h][3] = a.w * scale;
             qv[h][4] = b.x * scale; qv[h][5] = b.y * scale; qv[h][6] = b.z * scale; qv[h][7] = b.w * scale;
         }
@@ -609,6 +609,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     __shared__ unsigned issues[kMaxStages], done[kMaxStages];
     __shared__ __align__(16) __half pc[NW][8][16];  // a warp's Pc tile, column-major: [col][slot]
     __shared__ float wm[NW][G], wl[NW][G];
+    __shared__ __align__(16) float qs[G * D];      // q of the group's heads (one coalesced L2 read)
     __shared__ unsigned last;
     __shared__ volatile int abort_f;
 
@@ -619,7 +620,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         asm volatile("prefetch.tensormap [%0];" ::"l"(&kmap) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&vmap) : "memory");
     }
-    const int pos = pos_dev ? *pos_dev : pos_arg;
+    const int pos = pos_dev ? __ldcg(pos_dev) : pos_arg;
     const int n = pos + 1;
     int ns_eff, chunk;
     dec_split(n, ns, ns_eff, chunk);
@@ -667,6 +668,9 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
         }
     }
     pdl_wait();
+    for (int i = tid; i < G * D / 4; i += NT)  // q was written by the previous kernel: through L2
+        reinterpret_cast<float4*>(qs)[i] = __ldcg(reinterpret_cast<const float4*>(q + (int64_t)g * G * D) + i);
+    __syncthreads();
 
     // B fragments of Qc (constant): thread holds column cn = lane / 4 (head cn % 4, hi if cn < 4) at K rows
     // 2 (lane % 4) + {0, 1} and + 8 of every K step
@@ -675,7 +679,7 @@ __global__ void __launch_bounds__(kTcWarps * 32, 2)
     {
         const int h = cn & 3;
         const float scale = rsqrtf((float)D);
-        const float* qh = q + (int64_t)(g * G + (h < G ? h : 0)) * D;
+        const float* qh = qs + (h < G ? h : 0) * D;
 #pragma unroll
         for (int kk = 0; kk < KS; kk++) {
             float v[4];
@@ -1039,7 +1043,7 @@ __global__ void __launch_bounds__(kDecThreads, G <= 4 ? 2 : 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = blockIdx.y, s = blockIdx.x, ns = gridDim.x;
     pdl_launch_dependents();
-    const int pos = pos_dev ? *pos_dev : pos_arg;
+    const int pos = pos_dev ? __ldcg(pos_dev) : pos_arg;
     const int n = pos + 1;
     const int cut = max(0, n - qs.window);  // slots below cut have retired (the newest, cut - 1, in this step)
     int ns_eff, chunk;
@@ -1114,8 +1118,8 @@ __global__ void __launch_bounds__(kDecThreads, G <= 4 ? 2 : 1)
         const float scale = rsqrtf((float)D);
 #pragma unroll
         for (int h = 0; h < G; h++) {
-            const float4 a = *reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8);
-            const float4 b = *reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8 + 4);
+            const float4 a = __ldcg(reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8));
+            const float4 b = __ldcg(reinterpret_cast<const float4*>(q + (int64_t)(g * G + h) * D + li * 8 + 4));
             qv[h][0] = a.x * scale; qv[h][1] = a.y * scale; qv[h][2] = a.z * scale; qv[h][3] = a.w * scale;
             qv[h][4] = b.x * scale; qv[h][5] = b.y * scale; qv[h][6] = b.z * scale; qv[h][7] = b.w * scale;
         }

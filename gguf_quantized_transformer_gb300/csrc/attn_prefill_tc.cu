@@ -67,6 +67,11 @@ __device__ __forceinline__ void ld8(const float* p, float (&w)[8]) {
     const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
     w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
+// 8 floats written by an earlier kernel, read through L2
+__device__ __forceinline__ void ld8_cg(const float* p, float (&w)[8]) {
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(p)), b = __ldcg(reinterpret_cast<const float4*>(p + 4));
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
 __device__ __forceinline__ void ld2(const __half* p, float& a, float& b) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(p));
     a = f.x;
@@ -182,6 +187,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const KT* K = kc + (int64_t)g * max_ctx * D;
     const KT* V = vc + (int64_t)g * max_ctx * D;
 
+    pdl_launch_dependents();
     if (tid == 0) {
         mbar_init(&sm.raw_full, 1);
         mbar_init(&sm.raw_empty, 4);
@@ -201,6 +207,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    pdl_wait();  // q and the cache rows of this chunk are written by the previous kernel
     constexpr int NB = C::NBUF;
     auto buf = [&](int b) { return smem + C::OFF_BUF + b * C::BUF; };
 
@@ -212,7 +219,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int h = v / QT, rr = v % QT;
             float w[8];
             if (rr < nrows) {
-                ld8(q + (int64_t)(r0 + rr) * ldq + (int64_t)(g * G + h) * D + 8 * c, w);
+                ld8_cg(q + (int64_t)(r0 + rr) * ldq + (int64_t)(g * G + h) * D + 8 * c, w);
 #pragma unroll
                 for (int e = 0; e < 8; e++) w[e] *= scale;
             } else {
@@ -477,10 +484,18 @@ cudaError_t launch_pf(const float* q, int64_t ldq, const void* kc, const void* v
     const int smem = PCfg<D, KT>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e) return e;
-    dim3 grid((S + QT - 1) / QT, KVH);
-    k<<<grid, kPThreads, smem, s>>>(q, ldq, (const KT*)kc, (const KT*)vc, max_ctx, pos0, S, out_hi, out_lo, ldo,
-                                    err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((S + QT - 1) / QT, KVH);
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, q, ldq, (const KT*)kc, (const KT*)vc, max_ctx, pos0, S, out_hi, out_lo, ldo,
+                              err);
 }
 
 template <int D, int G>

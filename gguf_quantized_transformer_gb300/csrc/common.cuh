@@ -105,16 +105,22 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
+// Reads across kernels.  A kernel launched with programmatic dependent launch starts before its predecessor
+// has finished, and the SM's L1 is not invalidated for it: a line that an earlier kernel cached on the same SM
+// can be stale (measured: row RMSNorm reading x through L1 after griddepcontrol.wait returned old values).  So
+// data written by an earlier kernel of a chain (activations, the residual, q, the position word) is read with
+// ld.global.cg, which goes to L2, after griddepcontrol.wait; only data no kernel writes (weights, norm weights,
+// the RoPE table) is read through L1.
 __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, float v1) {
     switch (e.kind) {
         case EPI_STORE: {
             e.out[(int64_t)m * e.ld + n] = v0;
             e.out[(int64_t)m * e.ld + n + 1] = v1;
         } break;
-        case EPI_RESID: {
+        case EPI_RESID: {  // the residual was written by an earlier kernel: read through L2 (note above)
             float* p = e.out + (int64_t)m * e.ld + n;
-            p[0] += v0;
-            p[1] += v1;
+            const float2 o = __ldcg(reinterpret_cast<const float2*>(p));
+            *reinterpret_cast<float2*>(p) = make_float2(o.x + v0, o.y + v1);
         } break;
         case EPI_SWIGLU: {  // columns (2r, 2r+1) hold (gate_r, up_r)
             float h = silu_f(v0) * v1;
@@ -132,7 +138,7 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float v0, f
             atomicMax(e.argmax, k > k1 ? k : k1);
         } break;
         case EPI_QKV: {
-            const int pos = (e.pos_dev ? *e.pos_dev : e.pos0) + m;
+            const int pos = (e.pos_dev ? __ldcg(e.pos_dev) : e.pos0) + m;
             const int D = e.head_dim;
             if (n < e.qd + e.kvd) {  // q or k: rotate the pair (2i, 2i+1) by theta(pos, i)
                 const int d = (n < e.qd ? n : n - e.qd) % D;
@@ -203,10 +209,22 @@ int qgemv_max_chunks();
 bool make_tmap_f16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_cols,
                    uint32_t box_rows);
 
+// Split-K scratch of the prefill GEMM: fp32 partial tiles and one arrival counter per output tile (zero between
+// launches; the last CTA of a tile resets its counter).  Launches on one stream may share it.
+struct GemmSplit {
+    float* ws = nullptr;
+    size_t ws_bytes = 0;
+    unsigned* cnt = nullptr;
+    int cnt_n = 0;
+};
+// Workspace bytes the GEMM's split K wants for an N x K weight at M rows (0: no split), and the counters it needs.
+size_t qgemm_ws_bytes(int N, int K, int M);
+int qgemm_tiles(int N, int M);
 // Prefill GEMM on the tensor cores: Y = X W^T for M rows with a fused epilogue.  X is given as fp16
-// hi + lo planes [M][ldx] (ldx % 8 == 0, 16-byte aligned).  err: device error word.
+// hi + lo planes [M][ldx] (ldx % 8 == 0, 16-byte aligned).  err: device error word.  split (nullable): scratch
+// for splitting K where it pays; the split is limited to what the scratch holds.
 cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo, int64_t ldx, int M, const Epi& epi,
-                         unsigned* err, cudaStream_t s);
+                         unsigned* err, cudaStream_t s, const GemmSplit* split = nullptr);
 cudaError_t qgemm_prepare();
 
 // Quantized KV cache (AF_KV_Q8_0 / AF_KV_Q4_0): every slot lives in the fp16 cache; slots that left the window

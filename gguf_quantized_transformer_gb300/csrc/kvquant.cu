@@ -15,7 +15,7 @@ namespace {
 // one thread per 32-value block of one row (layer, kv head, K or V, slot)
 __global__ void kv_retire_kernel(KvStore st, __half* __restrict__ kc, __half* __restrict__ vc, int L, int KVH,
                                  int max_ctx, int D, const int* __restrict__ pos_dev, int first, int count) {
-    if (pos_dev) first = *pos_dev - st.window;
+    if (pos_dev) first = __ldcg(pos_dev) - st.window;
     const int nb = D / 32;
     const int64_t total = (int64_t)count * L * KVH * 2 * nb;
     const int cb = kv_code_bytes(st.qtype, D);

@@ -3,6 +3,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace af {
 
@@ -216,27 +217,74 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return t;
 }
 
-// y = w * x / sqrt(mean(x^2) + eps) for each of n rows (one CTA per row), as fp16 hi + lo.
-__global__ void rmsnorm_rows_kernel(const float* __restrict__ x, int E, const float* __restrict__ w, float eps,
-                                    __half* __restrict__ y_hi, __half* __restrict__ y_lo) {
+// y = w * x / sqrt(mean(x^2) + eps) for each of n rows (one CTA per row), as fp16 hi + lo.  Rows of up to
+// kRmsMaxV * 4 * 256 elements (E % 4 == 0) stay in registers between the sum of squares and the scaling; the
+// norm weights are read before griddepcontrol.wait (they do not depend on the previous kernel).
+constexpr int kRmsThreads = 256;
+constexpr int kRmsMaxV = 8;  // float4 per thread
+__global__ void __launch_bounds__(kRmsThreads) rmsnorm_rows_kernel(const float* __restrict__ x, int E,
+                                                                   const float* __restrict__ w, float eps,
+                                                                   __half* __restrict__ y_hi,
+                                                                   __half* __restrict__ y_lo) {
     __shared__ float red[32];
-    const float* xr = x + (int64_t)blockIdx.x * E;
+    pdl_launch_dependents();
+    const int nv = E / 4, tid = threadIdx.x;
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    float4 wv[kRmsMaxV], xv[kRmsMaxV];
+#pragma unroll
+    for (int j = 0; j < kRmsMaxV; j++) {
+        const int i = tid + j * kRmsThreads;
+        wv[j] = i < nv ? w4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    pdl_wait();  // x is written by an earlier kernel: read through L2 (the note above epi_pair)
+    const float4* x4 = reinterpret_cast<const float4*>(x + (int64_t)blockIdx.x * E);
     float ss = 0.f;
-    for (int k = threadIdx.x; k < E; k += blockDim.x) ss += xr[k] * xr[k];
+#pragma unroll
+    for (int j = 0; j < kRmsMaxV; j++) {
+        const int i = tid + j * kRmsThreads;
+        xv[j] = i < nv ? __ldcg(x4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss = fmaf(xv[j].x, xv[j].x, fmaf(xv[j].y, xv[j].y, fmaf(xv[j].z, xv[j].z, fmaf(xv[j].w, xv[j].w, ss))));
+    }
     ss = block_sum(ss, red);
     const float inv = rsqrtf(ss / (float)E + eps);
-    for (int k = threadIdx.x; k < E; k += blockDim.x) {
-        const float v = w[k] * (xr[k] * inv);
-        const __half h = __float2half_rn(v);
-        y_hi[(int64_t)blockIdx.x * E + k] = h;
-        y_lo[(int64_t)blockIdx.x * E + k] = __float2half_rn(v - __half2float(h));
+    uint2* yh = reinterpret_cast<uint2*>(y_hi + (int64_t)blockIdx.x * E);
+    uint2* yl = reinterpret_cast<uint2*>(y_lo + (int64_t)blockIdx.x * E);
+#pragma unroll
+    for (int j = 0; j < kRmsMaxV; j++) {
+        const int i = tid + j * kRmsThreads;
+        if (i < nv) {
+            const float v[4] = {wv[j].x * (xv[j].x * inv), wv[j].y * (xv[j].y * inv), wv[j].z * (xv[j].z * inv),
+                                wv[j].w * (xv[j].w * inv)};
+            __half h[4], l[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                h[e] = __float2half_rn(v[e]);
+                l[e] = __float2half_rn(v[e] - __half2float(h[e]));
+            }
+            uint2 ph, pl;
+            ph.x = (unsigned)__half_as_ushort(h[0]) | ((unsigned)__half_as_ushort(h[1]) << 16);
+            ph.y = (unsigned)__half_as_ushort(h[2]) | ((unsigned)__half_as_ushort(h[3]) << 16);
+            pl.x = (unsigned)__half_as_ushort(l[0]) | ((unsigned)__half_as_ushort(l[1]) << 16);
+            pl.y = (unsigned)__half_as_ushort(l[2]) | ((unsigned)__half_as_ushort(l[3]) << 16);
+            yh[i] = ph;
+            yl[i] = pl;
+        }
     }
 }
 
 cudaError_t launch_rmsnorm_rows(const float* x, int n, int E, const float* w, float eps, __half* y_hi, __half* y_lo,
                                 cudaStream_t s) {
-    rmsnorm_rows_kernel<<<n, 256, 0, s>>>(x, E, w, eps, y_hi, y_lo);
-    return cudaGetLastError();
+    if (E % 4 || E > kRmsMaxV * 4 * kRmsThreads) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n);
+    cfg.blockDim = dim3(kRmsThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rmsnorm_rows_kernel, x, E, w, eps, y_hi, y_lo);
 }
 
 __global__ void split_f16_kernel(const float* __restrict__ x, __half* __restrict__ hi, __half* __restrict__ lo,

@@ -33,6 +33,12 @@
 //                 W_hi / W_lo tile into the stage's TMEM columns;
 //                 warps 2..5 then run the fused epilogue from TMEM
 //                 (tcgen05.ld, 32 columns at a time).
+// Split K.  A GEMM with few output tiles (small N) leaves SMs idle; it then runs
+// ksplit CTAs per tile, each over a contiguous range of the K steps.  Each CTA
+// stores its fp32 partial tile in a workspace; the last of a tile's CTAs to
+// arrive (arrival counter, no waiting) adds the ksplit partials in split order,
+// its own taken from TMEM, and runs the fused epilogue, so the result does not
+// depend on the arrival order.
 // Every mbarrier wait is bounded; on a timeout the CTA records DEV_TIMEOUT,
 // drains what it issued and frees its TMEM before returning.
 #include <cuda.h>
@@ -315,6 +321,7 @@ struct TcSmem {
     uint32_t tmem_base;
     volatile int abort;
     int issued_x;  // X tile loads issued so far
+    int last;      // split K: this CTA is the last of its tile to arrive
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, unsigned parity, TcSmem& sm, unsigned* err) {
@@ -355,10 +362,86 @@ __device__ __forceinline__ void epilogue(const Epi& epi, uint32_t lane_base, int
     }
 }
 
+// Named barrier of the four epilogue warps (warps 2..5).
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Split K: store this CTA's partial tile (row r = W row of TMEM lane r, BT fp32 columns) to the workspace.
+template <int BT>
+__device__ __forceinline__ void store_partial(float* part, uint32_t lane_base, int r) {
+    for (int c0 = 0; c0 < BT; c0 += 32) {
+        float v[32];
+        tmem_ld32(lane_base + (uint32_t)c0, v);
+        float4* dst = reinterpret_cast<float4*>(part + (size_t)r * BT + c0);
+#pragma unroll
+        for (int q = 0; q < 8; q++) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+}
+
+// Split K, last CTA of the tile: sum the ksplit partials of row r in split order (its own from TMEM) and apply
+// the epilogue as `epilogue` does.
+template <int KIND, int BT>
+__device__ __forceinline__ void epilogue_split(const Epi& epi, uint32_t lane_base, int lane, int n, int N, int m0,
+                                               int M, const float* tile_ws, int ksplit, int kz, int r) {
+    const int np = n & ~1;
+    const bool odd = lane & 1;
+    for (int c0 = 0; c0 < BT; c0 += 32) {
+        float own[32], v[32];
+        tmem_ld32(lane_base + (uint32_t)c0, own);
+#pragma unroll
+        for (int j = 0; j < 32; j++) v[j] = 0.f;
+        for (int z = 0; z < ksplit; z++) {
+            if (z == kz) {
+#pragma unroll
+                for (int j = 0; j < 32; j++) v[j] += own[j];
+            } else {
+                const float4* src =
+                    reinterpret_cast<const float4*>(tile_ws + ((size_t)z * BW + r) * BT + c0);
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    const float4 a = __ldcg(src + q);
+                    v[4 * q] += a.x;
+                    v[4 * q + 1] += a.y;
+                    v[4 * q + 2] += a.z;
+                    v[4 * q + 3] += a.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 1], 1);
+            const int m = m0 + c0 + j + (odd ? 1 : 0);
+            const float v0 = odd ? got : v[j], v1 = odd ? v[j + 1] : got;
+            if (m < M && np < N) epi_pair_k<KIND>(epi, m, np, v0, v1);
+        }
+    }
+}
+
+template <int BT>
+__device__ __forceinline__ void run_epilogue(const Epi& epi, uint32_t lane_base, int lane, int n, int N, int m0,
+                                             int M) {
+    switch (epi.kind) {  // one loop per kind, so the loop body has no dispatch
+        case EPI_RESID: epilogue<EPI_RESID, BT>(epi, lane_base, lane, n, N, m0, M); break;
+        case EPI_QKV: epilogue<EPI_QKV, BT>(epi, lane_base, lane, n, N, m0, M); break;
+        case EPI_SWIGLU: epilogue<EPI_SWIGLU, BT>(epi, lane_base, lane, n, N, m0, M); break;
+        default: epilogue<EPI_STORE, BT>(epi, lane_base, lane, n, N, m0, M); break;
+    }
+}
+
+template <int BT>
+__device__ __forceinline__ void run_epilogue_split(const Epi& epi, uint32_t lane_base, int lane, int n, int N, int m0,
+                                                   int M, const float* tile_ws, int ksplit, int kz, int r) {
+    switch (epi.kind) {
+        case EPI_RESID: epilogue_split<EPI_RESID, BT>(epi, lane_base, lane, n, N, m0, M, tile_ws, ksplit, kz, r); break;
+        case EPI_QKV: epilogue_split<EPI_QKV, BT>(epi, lane_base, lane, n, N, m0, M, tile_ws, ksplit, kz, r); break;
+        case EPI_SWIGLU: epilogue_split<EPI_SWIGLU, BT>(epi, lane_base, lane, n, N, m0, M, tile_ws, ksplit, kz, r); break;
+        default: epilogue_split<EPI_STORE, BT>(epi, lane_base, lane, n, N, m0, M, tile_ws, ksplit, kz, r); break;
+    }
+}
+
 template <int WT, int BT>
 __global__ void __launch_bounds__(kThreads, 1)
     qgemm_tc_kernel(const __grid_constant__ CUtensorMap map_hi, const __grid_constant__ CUtensorMap map_lo, Planes W,
-                    int M, Epi epi, unsigned* err) {
+                    int M, Epi epi, unsigned* err, int ksplit, float* __restrict__ ws, unsigned* __restrict__ cnt) {
     using C = TcCfg<BT>;
     constexpr int kStages = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -366,8 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n0 = blockIdx.x * BW, m0 = blockIdx.y * BT;
-    const int nk = (W.K + BK - 1) / BK;
+    const int nk_all = (W.K + BK - 1) / BK;
+    const int kz = blockIdx.z;  // this CTA's K steps: [k_lo, k_lo + nk)
+    const int k_lo = (int)((int64_t)nk_all * kz / ksplit);
+    const int nk = (int)((int64_t)nk_all * (kz + 1) / ksplit) - k_lo;
 
+    // programmatic dependent launch: the next kernel may start its own prologue; this one reads X (and writes
+    // its outputs) only after griddepcontrol.wait, while the weight tiles, which do not depend on the previous
+    // kernel, are fetched and dequantized before it
+    pdl_launch_dependents();
     if (tid == 0) {
         for (int s = 0; s < kStages; s++) {
             mbar_init(&sm.xfull[s], 1);
@@ -391,12 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------- TMA producer: X_hi, X_lo tiles
         if (lane == 0) {
+            pdl_wait();  // X is written by the previous kernel
             for (int ks = 0; ks < nk; ks++) {
                 const int s = ks % kStages, u = ks / kStages;
                 if (u > 0 && !wait_or_abort(&sm.empty[s], (u - 1) & 1, sm, err)) break;
                 mbar_arrive_expect_tx(&sm.xfull[s], 2 * C::kXTile);
-                tma_load_2d(x_hi(s), &map_hi, ks * BK, m0, &sm.xfull[s]);
-                tma_load_2d(x_lo(s), &map_lo, ks * BK, m0, &sm.xfull[s]);
+                tma_load_2d(x_hi(s), &map_hi, (k_lo + ks) * BK, m0, &sm.xfull[s]);
+                tma_load_2d(x_lo(s), &map_lo, (k_lo + ks) * BK, m0, &sm.xfull[s]);
                 sm.issued_x = ks + 1;
             }
         }
@@ -436,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto fetch = [&](int ks, RawBlk<WT> (&b)[2]) {
 #pragma unroll
             for (int i = 0; i < 2; i++) {
-                if (valid && ks < nk) load_blk(W, n, ks * 2 + i, b[i]);
+                if (valid && ks < nk) load_blk(W, n, (k_lo + ks) * 2 + i, b[i]);
                 else zero_blk(b[i]);
             }
         };
@@ -476,14 +567,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---------------- epilogue (warps 2..5: TMEM lane quadrant = warp % 4)
         if (warp < 6) {
+            pdl_wait();  // (already satisfied: the MMAs consumed X) before the epilogue's reads and writes
             // tcgen05.ld is warp-collective: the whole warp takes the same branch
-            if (__all_sync(0xffffffffu, wait_or_abort(&sm.done, 0, sm, err))) {
-                tc_fence_after();
-                switch (epi.kind) {  // one loop per kind, so the loop body has no dispatch
-                    case EPI_RESID: epilogue<EPI_RESID, BT>(epi, lane_base, lane, n, W.N, m0, M); break;
-                    case EPI_QKV: epilogue<EPI_QKV, BT>(epi, lane_base, lane, n, W.N, m0, M); break;
-                    case EPI_SWIGLU: epilogue<EPI_SWIGLU, BT>(epi, lane_base, lane, n, W.N, m0, M); break;
-                    default: epilogue<EPI_STORE, BT>(epi, lane_base, lane, n, W.N, m0, M); break;
+            const bool ok = __all_sync(0xffffffffu, wait_or_abort(&sm.done, 0, sm, err));
+            if (ok) tc_fence_after();
+            if (ksplit == 1) {
+                if (ok) run_epilogue<BT>(epi, lane_base, lane, n, W.N, m0, M);
+            } else {
+                // every CTA of the tile arrives, also after a timeout (the counter must return to zero)
+                const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+                float* tile_ws = ws + (size_t)tile * ksplit * BW * BT;
+                if (ok) store_partial<BT>(tile_ws + (size_t)kz * BW * BT, lane_base, r);
+                __threadfence();
+                epi_bar();
+                if (warp == 2 && lane == 0) sm.last = atomicAdd(&cnt[tile], 1u) == (unsigned)ksplit - 1u;
+                epi_bar();
+                if (sm.last) {
+                    __threadfence();
+                    if (ok) run_epilogue_split<BT>(epi, lane_base, lane, n, W.N, m0, M, tile_ws, ksplit, kz, r);
+                    if (warp == 2 && lane == 0) cnt[tile] = 0u;
                 }
             }
         }
@@ -579,20 +681,73 @@ cudaError_t qgemm_prepare() {
     return e;
 }
 
+namespace {
+// Tile width BT and K split for an N x K weight at M rows: the least estimated time, waves of CTAs x the time of
+// one CTA.  The per-CTA times are fitted to measurements of this kernel on the 8B and 1B Q4_0 shapes at M = 512
+// (every (BT, split) pair timed): K steps x 1.05 us + 8 us at BT = 256, x 0.83 us + 12 us at BT = 128; a split
+// CTA also stores its partial and the last one sums them, which measured as a fixed 28 us (BT = 256) or 13 us
+// (BT = 128).  A split keeps at least 8 K steps per CTA and fits the workspace and the counters.
+struct GemmShape {
+    int BT, ksplit;
+};
+GemmShape pick_gemm(int N, int K, int M, size_t ws_bytes, int cnt_n) {
+    constexpr int kMaxSplit = 4;
+    const int sms = num_sms();
+    const int nk = (K + BK - 1) / BK, nt = (N + BW - 1) / BW;
+    GemmShape best{128, 1};
+    double best_t = 1e30;
+    for (int BT : {256, 128}) {
+        const int mt = (M + BT - 1) / BT;
+        const double step = BT == 256 ? 1.05 : 0.83;
+        for (int ks = 1; ks <= kMaxSplit; ks++) {
+            if (ks > 1 && (nk / ks < 8 || (size_t)nt * mt * ks * BW * BT * 4 > ws_bytes || nt * mt > cnt_n)) break;
+            const double fixed = ks == 1 ? (BT == 256 ? 8.0 : 12.0) : (BT == 256 ? 28.0 : 13.0);
+            const int ctas = nt * mt * ks;
+            const double t = (double)((ctas + sms - 1) / sms) * ((double)nk / ks * step + fixed);
+            if (t < best_t - 1e-9) {
+                best_t = t;
+                best = {BT, ks};
+            }
+        }
+    }
+    return best;
+}
+}  // namespace
+
+size_t qgemm_ws_bytes(int N, int K, int M) {
+    const GemmShape g = pick_gemm(N, K, M, (size_t)-1, 1 << 30);
+    if (g.ksplit == 1) return 0;
+    const size_t tiles = (size_t)((N + BW - 1) / BW) * ((M + g.BT - 1) / g.BT);
+    return tiles * g.ksplit * BW * g.BT * 4;
+}
+
+int qgemm_tiles(int N, int M) { return ((N + BW - 1) / BW) * ((M + 127) / 128); }
+
 cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo, int64_t ldx, int M, const Epi& epi,
-                         unsigned* err, cudaStream_t s) {
+                         unsigned* err, cudaStream_t s, const GemmSplit* split) {
     if (M < 1) return cudaSuccess;
     if (ldx % 8 || (reinterpret_cast<uintptr_t>(X_hi) & 15) || (reinterpret_cast<uintptr_t>(X_lo) & 15))
         return cudaErrorInvalidValue;  // TMA: 16-byte aligned base and row stride
     const int nt = (W.N + BW - 1) / BW;
-    // 256 X rows per tile (W dequantized once per 256 rows) unless that leaves SMs without a tile
-    const bool wide = (int64_t)nt * ((M + 255) / 256) >= num_sms();
-    const int BT = wide ? 256 : 128;
+    const GemmShape g = split ? pick_gemm(W.N, W.K, M, split->ws_bytes, split->cnt_n) : pick_gemm(W.N, W.K, M, 0, 0);
+    const int BT = g.BT;
+    float* ws = g.ksplit > 1 ? split->ws : nullptr;
+    unsigned* cnt = g.ksplit > 1 ? split->cnt : nullptr;
     CUtensorMap mh, ml;
     if (!make_map(&mh, X_hi, M, W.K, ldx, BT) || !make_map(&ml, X_lo, M, W.K, ldx, BT)) return cudaErrorInvalidValue;
-    const dim3 grid(nt, (M + BT - 1) / BT);
-#define AF_QGEMM_LAUNCH(WT, BTV) \
-    qgemm_tc_kernel<WT, BTV><<<grid, kThreads, TcCfg<BTV>::kSmemBytes, s>>>(mh, ml, W, M, epi, err)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nt, (M + BT - 1) / BT, g.ksplit);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t le = cudaSuccess;
+#define AF_QGEMM_LAUNCH(WT, BTV)                                                                                \
+    cfg.dynamicSmemBytes = TcCfg<BTV>::kSmemBytes;                                                             \
+    le = cudaLaunchKernelEx(&cfg, qgemm_tc_kernel<WT, BTV>, mh, ml, W, M, epi, err, g.ksplit, ws, cnt)
 #define AF_QGEMM_TYPES(BTV)                                         \
     switch (W.wtype) {                                              \
         case AF_Q4_0: AF_QGEMM_LAUNCH(AF_Q4_0, BTV); break;         \
@@ -602,14 +757,14 @@ cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo
         case AF_Q6_K: AF_QGEMM_LAUNCH(AF_Q6_K, BTV); break;         \
         default: return cudaErrorInvalidValue;                      \
     }
-    if (wide) {
+    if (BT == 256) {
         AF_QGEMM_TYPES(256)
     } else {
         AF_QGEMM_TYPES(128)
     }
 #undef AF_QGEMM_TYPES
 #undef AF_QGEMM_LAUNCH
-    return cudaGetLastError();
+    return le;
 }
 
 }  // namespace af

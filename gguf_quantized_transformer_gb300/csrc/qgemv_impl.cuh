@@ -136,29 +136,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (tid == 0)
         for (int st = 0; st < min(nst, xslot); st++) issue(st);
+    // the position word is written before the step's first kernel starts and the RoPE table never: both are
+    // read before waiting for the previous kernel
+    int qpos = 0;
+    if (epi.kind == EPI_QKV) {
+        qpos = epi.pos_dev ? __ldcg(epi.pos_dev) : epi.pos0;
+        for (int i = tid; i < epi.head_dim / 2; i += kThreads) rope_s[i] = epi.rope[(int64_t)qpos * (epi.head_dim / 2) + i];
+    }
 
     pdl_wait();  // x (and the residual rows) are written by the previous kernel
 
     // RMSNorm prologue: every CTA reduces sum(x^2) over the whole input while it converts w (.) x
-    float ss = quantize_x<NORM>(x, nw, K, W.Kp / 32, xb, tid);
+    float ss = quantize_x<NORM, kThreads, true>(x, nw, K, W.Kp / 32, xb, tid);
     if (NORM) {
         for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         if (lane == 0) ssum[warp] = ss;
     }
     // epilogue inputs into shared memory
     if (epi.kind == EPI_RESID)
-        for (int i = tid; i < nrows; i += kThreads) xres[i] = epi.out[r0 + i];
+        for (int i = tid; i < nrows; i += kThreads) xres[i] = __ldcg(epi.out + r0 + i);
     GemvEpiCtx ectx;
     ectx.xres = xres;
     ectx.rope = rope_s;
     ectx.amax = &amax_s;
     ectx.r0 = r0;
     ectx.pos = 0;
-    if (epi.kind == EPI_QKV) {
-        ectx.pos = epi.pos_dev ? *epi.pos_dev : epi.pos0;
-        for (int i = tid; i < epi.head_dim / 2; i += kThreads)
-            rope_s[i] = epi.rope[(int64_t)ectx.pos * (epi.head_dim / 2) + i];
-    }
+    ectx.pos = qpos;
     __syncthreads();
 
     float rstd = 1.f;  // applied to each row's dot product (the images hold w (.) x)
