@@ -338,27 +338,83 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, unsigned parity, Tc
 // column n for every X row of the tile.  The fused epilogues take adjacent column pairs (n, n + 1) of one output
 // row, so lanes 2p and 2p + 1 trade halves: for tokens j (even) and j + 1, lane 2p gets row 2p + 1's value of
 // token j and lane 2p + 1 gets row 2p's value of token j + 1; each lane then applies the pair of one token.
+// Per 32 tokens, every value the epilogue reads (the residual, the RoPE rows) is loaded before any of its stores:
+// the compiler cannot reorder a load above a store that may alias it, so an interleaved load-store sequence would
+// pay one L2 round trip per pair.
 template <int KIND>
-__device__ __forceinline__ void epi_pair_k(const Epi& e, int m, int n, float v0, float v1) {
-    Epi k = e;
-    k.kind = KIND;  // constant: the switch in epi_pair folds away
-    epi_pair(k, m, n, v0, v1);
+__device__ __forceinline__ void epi_chunk(const Epi& e, const float (&v)[32], int lane, int n, int N, int mb, int M) {
+    const int np = n & ~1;  // the pair's first column
+    const bool odd = lane & 1;
+    float a0[16], a1[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        const float got = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 1], 1);
+        a0[j / 2] = odd ? got : v[j];
+        a1[j / 2] = odd ? v[j + 1] : got;
+    }
+    const int m1 = mb + (odd ? 1 : 0);  // token of pair i: m1 + 2 i
+    if (np >= N) return;
+    if (KIND == EPI_RESID) {
+        float2 old[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+            old[i] = m1 + 2 * i < M ? __ldcg(reinterpret_cast<const float2*>(e.out + (int64_t)(m1 + 2 * i) * e.ld + np))
+                                    : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+            if (m1 + 2 * i < M)
+                *reinterpret_cast<float2*>(e.out + (int64_t)(m1 + 2 * i) * e.ld + np) =
+                    make_float2(old[i].x + a0[i], old[i].y + a1[i]);
+    } else if (KIND == EPI_QKV) {
+        const int D = e.head_dim;
+        const bool rot = np < e.qd + e.kvd;  // q or k: rotate the pair (2i, 2i+1) by theta(pos, i)
+        const int d = (np < e.qd ? np : np - e.qd) % D;
+        const int pos1 = (e.pos_dev ? __ldcg(e.pos_dev) : e.pos0) + m1;
+        float2 cs[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+            cs[i] = rot && m1 + 2 * i < M ? e.rope[(int64_t)(pos1 + 2 * i) * (D / 2) + (d >> 1)] : make_float2(1.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const int m = m1 + 2 * i;
+            if (m >= M) continue;
+            float v0 = a0[i], v1 = a1[i];
+            if (rot) {
+                const float r0 = v0 * cs[i].x - v1 * cs[i].y, r1 = v0 * cs[i].y + v1 * cs[i].x;
+                v0 = r0;
+                v1 = r1;
+            }
+            if (np < e.qd) {
+                if (e.out) *reinterpret_cast<float2*>(e.out + (int64_t)m * e.ld + np) = make_float2(v0, v1);
+            } else {
+                const bool isk = np < e.qd + e.kvd;
+                const int c = isk ? np - e.qd : np - e.qd - e.kvd;
+                const int64_t idx = ((int64_t)(c / D) * e.max_ctx + pos1 + 2 * i) * D + c % D;
+                void* base = isk ? e.kcache : e.vcache;
+                if (e.kv_f16)
+                    *reinterpret_cast<__half2*>((__half*)base + idx) = __floats2half2_rn(v0, v1);
+                else
+                    *reinterpret_cast<float2*>((float*)base + idx) = make_float2(v0, v1);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            if (m1 + 2 * i < M) {
+                Epi k = e;
+                k.kind = KIND;  // constant: the switch in epi_pair folds away
+                epi_pair(k, m1 + 2 * i, np, a0[i], a1[i]);
+            }
+        }
+    }
 }
 
 template <int KIND, int BT>
 __device__ __forceinline__ void epilogue(const Epi& epi, uint32_t lane_base, int lane, int n, int N, int m0, int M) {
-    const int np = n & ~1;  // the pair's first column
-    const bool odd = lane & 1;
     for (int c0 = 0; c0 < BT; c0 += 32) {
         float v[32];
         tmem_ld32(lane_base + (uint32_t)c0, v);
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            const float got = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 1], 1);
-            const int m = m0 + c0 + j + (odd ? 1 : 0);
-            const float v0 = odd ? got : v[j], v1 = odd ? v[j + 1] : got;
-            if (m < M && np < N) epi_pair_k<KIND>(epi, m, np, v0, v1);
-        }
+        epi_chunk<KIND>(epi, v, lane, n, N, m0 + c0, M);
     }
 }
 
@@ -382,8 +438,6 @@ __device__ __forceinline__ void store_partial(float* part, uint32_t lane_base, i
 template <int KIND, int BT>
 __device__ __forceinline__ void epilogue_split(const Epi& epi, uint32_t lane_base, int lane, int n, int N, int m0,
                                                int M, const float* tile_ws, int ksplit, int kz, int r) {
-    const int np = n & ~1;
-    const bool odd = lane & 1;
     for (int c0 = 0; c0 < BT; c0 += 32) {
         float own[32], v[32];
         tmem_ld32(lane_base + (uint32_t)c0, own);
@@ -406,13 +460,7 @@ __device__ __forceinline__ void epilogue_split(const Epi& epi, uint32_t lane_bas
                 }
             }
         }
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            const float got = __shfl_xor_sync(0xffffffffu, odd ? v[j] : v[j + 1], 1);
-            const int m = m0 + c0 + j + (odd ? 1 : 0);
-            const float v0 = odd ? got : v[j], v1 = odd ? v[j + 1] : got;
-            if (m < M && np < N) epi_pair_k<KIND>(epi, m, np, v0, v1);
-        }
+        epi_chunk<KIND>(epi, v, lane, n, N, m0 + c0, M);
     }
 }
 
