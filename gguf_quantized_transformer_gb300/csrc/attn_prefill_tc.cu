@@ -83,6 +83,14 @@ __device__ __forceinline__ void ld2(const float* p, float& a, float& b) {
     b = f.y;
 }
 
+// 2^x by the hardware's approximate base-2 exponential (relative error about 2^-22; results below 2^-126 flush
+// to zero, which a probability of that size is)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint4 pack8_f16(const float (&w)[8]) {  // exact for values that are fp16
     uint32_t h[4];
 #pragma unroll
@@ -99,7 +107,9 @@ constexpr int kPThreads = kPWarps * 32;
 constexpr int BQ = 128;          // query vectors per CTA = TMEM lanes
 constexpr int kTmemCols = 256;   // S buffers at columns 0 and BKV, O at column 128 (D columns)
 constexpr int kOCol = 128;
-constexpr float kLazy = 8.f;     // the reference maximum moves when a tile exceeds it by more than this
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazy = 8.f * kLog2e;  // (log2 units) the reference maximum moves when a tile exceeds it by more:
+                                       // p = 2^(s - m) stays below e^8
 
 template <int D, typename KT>
 struct PCfg {
@@ -211,9 +221,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     constexpr int NB = C::NBUF;
     auto buf = [&](int b) { return smem + C::OFF_BUF + b * C::BUF; };
 
-    // ---- Q tile (all threads): vector v = h * QT + row, scaled by 1/sqrt(D), split hi + lo
+    // ---- Q tile (all threads): vector v = h * QT + row, scaled by log2(e) / sqrt(D) (scores in base-2 units:
+    // p = 2^(s - m) = e^(q.k/sqrt(D) - m')), split hi + lo
     {
-        const float scale = rsqrtf((float)D);
+        const float scale = rsqrtf((float)D) * kLog2e;
         for (int i = tid; i < BQ * (D / 8); i += kPThreads) {
             const int v = i / (D / 8), c = i % (D / 8);
             const int h = v / QT, rr = v % QT;
@@ -266,25 +277,43 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // K tile: rows = keys, K axis = D
             for (int i = ct; i < BKV * (D / 8); i += 128) {
                 const int j = i / (D / 8), c = i % (D / 8);
-                float w[8];
-                if (t * BKV + j < nkeys) {
-                    ld8(stK + (int64_t)j * D + 8 * c, w);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; e++) w[e] = 0.f;
-                }
+                const bool in = t * BKV + j < nkeys;
                 if (C::SPLIT_KV) {
+                    float w[8];
+                    if (in) {
+                        ld8(stK + (int64_t)j * D + 8 * c, w);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; e++) w[e] = 0.f;
+                    }
                     uint4 hi, lo;
                     split8(w, hi, lo);
                     *reinterpret_cast<uint4*>(ob + C::B_KH + op_off(BKV, j, c)) = hi;
                     *reinterpret_cast<uint4*>(ob + C::B_KL + op_off(BKV, j, c)) = lo;
-                } else {
-                    *reinterpret_cast<uint4*>(ob + C::B_KH + op_off(BKV, j, c)) = pack8_f16(w);
+                } else {  // fp16 rows: the chunk is already the operand's
+                    *reinterpret_cast<uint4*>(ob + C::B_KH + op_off(BKV, j, c)) =
+                        in ? *reinterpret_cast<const uint4*>(stK + (int64_t)j * D + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             // V tile transposed: rows = d, K axis = keys (thread: dims 2dp, 2dp + 1 of 8 keys)
             for (int i = ct; i < (D / 2) * (BKV / 8); i += 128) {
                 const int dp = i % (D / 2), kg = i / (D / 2);
+                if (!C::SPLIT_KV) {  // fp16: word e holds (dim 2dp, dim 2dp + 1) of key 8kg + e
+                    uint32_t wv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++)
+                        wv[e] = t * BKV + 8 * kg + e < nkeys
+                                    ? *reinterpret_cast<const uint32_t*>(stV + (int64_t)(8 * kg + e) * D + 2 * dp)
+                                    : 0u;
+                    uint4 a4, b4;
+                    a4.x = __byte_perm(wv[0], wv[1], 0x5410); b4.x = __byte_perm(wv[0], wv[1], 0x7632);
+                    a4.y = __byte_perm(wv[2], wv[3], 0x5410); b4.y = __byte_perm(wv[2], wv[3], 0x7632);
+                    a4.z = __byte_perm(wv[4], wv[5], 0x5410); b4.z = __byte_perm(wv[4], wv[5], 0x7632);
+                    a4.w = __byte_perm(wv[6], wv[7], 0x5410); b4.w = __byte_perm(wv[6], wv[7], 0x7632);
+                    *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp, kg)) = a4;
+                    *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp + 1, kg)) = b4;
+                    continue;
+                }
                 float a[8], bb[8];
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
@@ -379,13 +408,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (!pwait(&sm.s_full[sb], (t >> 1) & 1, sm, err)) break;
             tc_fence_after();
             float mt = -CUDART_INF_F;  // this tile's maximum of the row (S is read twice from TMEM: max, then p)
+            // below the diagonal for every row of the warp: no mask (rows past the chunk see zero q: harmless)
+            const bool whole = __all_sync(0xffffffffu, !vrow || t * BKV + BKV - 1 <= qpos);
 #pragma unroll
             for (int c32 = 0; c32 < BKV / 32; c32++) {
                 float s32[32];
                 tmem_ld32(lane_addr + (uint32_t)(sb * BKV + c32 * 32), s32);
+                if (whole) {
 #pragma unroll
-                for (int e = 0; e < 32; e++)
-                    if (vrow && t * BKV + c32 * 32 + e <= qpos) mt = fmaxf(mt, s32[e]);
+                    for (int e = 0; e < 32; e++) mt = fmaxf(mt, s32[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e++)
+                        if (vrow && t * BKV + c32 * 32 + e <= qpos) mt = fmaxf(mt, s32[e]);
+                }
             }
             // the reference maximum moves only when this tile exceeds it by more than kLazy
             const bool move = mt > m_ref + kLazy;
@@ -393,7 +429,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 // O holds tiles < t: wait for the previous P V, then rescale this warp's rows (warp-collective)
                 if (!pwait(&sm.op_free[(t - 1) % NB], ((t - 1) / NB) & 1, sm, err)) break;
                 tc_fence_after();
-                const float f = move ? __expf(m_ref - mt) : 1.f;
+                const float f = move ? ex2(m_ref - mt) : 1.f;
 #pragma unroll
                 for (int c32 = 0; c32 < D / 32; c32++) {
                     float o[32];
@@ -420,7 +456,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         const int key = t * BKV + c32 * 32 + q8 * 8 + e;
-                        const float p = (vrow && key <= qpos) ? __expf(s32[q8 * 8 + e] - m_ref) : 0.f;
+                        const float p = (whole || (vrow && key <= qpos)) ? ex2(s32[q8 * 8 + e] - m_ref) : 0.f;
                         l += p;
                         w[e] = p;
                     }
