@@ -35,7 +35,7 @@
 //                 (tcgen05.ld, 32 columns at a time).
 // Split K.  A GEMM with few output tiles (small N) leaves SMs idle; it then runs
 // ksplit CTAs per tile, each over a contiguous range of the K steps.  Each CTA
-// stores its fp32 partial tile in a workspace; the last of a tile's CTAs to
+// stores its fp32 partial tile (column-major, coalesced) in a workspace; the last of a tile's CTAs to
 // arrive (arrival counter, no waiting) adds the ksplit partials in split order,
 // its own taken from TMEM, and runs the fused epilogue, so the result does not
 // depend on the arrival order.
@@ -421,20 +421,20 @@ __device__ __forceinline__ void epilogue(const Epi& epi, uint32_t lane_base, int
 // Named barrier of the four epilogue warps (warps 2..5).
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Split K: store this CTA's partial tile (row r = W row of TMEM lane r, BT fp32 columns) to the workspace.
+// Split K: store this CTA's partial tile, column-major ([BT columns][BW rows] fp32): lane r of a quadrant warp holds
+// W row r, so each of its stores is one contiguous 128-byte line per warp.
 template <int BT>
 __device__ __forceinline__ void store_partial(float* part, uint32_t lane_base, int r) {
     for (int c0 = 0; c0 < BT; c0 += 32) {
         float v[32];
         tmem_ld32(lane_base + (uint32_t)c0, v);
-        float4* dst = reinterpret_cast<float4*>(part + (size_t)r * BT + c0);
 #pragma unroll
-        for (int q = 0; q < 8; q++) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int j = 0; j < 32; j++) part[(size_t)(c0 + j) * BW + r] = v[j];
     }
 }
 
 // Split K, last CTA of the tile: sum the ksplit partials of row r in split order (its own from TMEM) and apply
-// the epilogue as `epilogue` does.
+// the epilogue as `epilogue` does; the 32 loads of a partial's chunk are in flight together.
 template <int KIND, int BT>
 __device__ __forceinline__ void epilogue_split(const Epi& epi, uint32_t lane_base, int lane, int n, int N, int m0,
                                                int M, const float* tile_ws, int ksplit, int kz, int r) {
@@ -448,16 +448,12 @@ __device__ __forceinline__ void epilogue_split(const Epi& epi, uint32_t lane_bas
 #pragma unroll
                 for (int j = 0; j < 32; j++) v[j] += own[j];
             } else {
-                const float4* src =
-                    reinterpret_cast<const float4*>(tile_ws + ((size_t)z * BW + r) * BT + c0);
+                const float* src = tile_ws + (size_t)z * BW * BT + (size_t)c0 * BW + r;
+                float w[32];
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    const float4 a = __ldcg(src + q);
-                    v[4 * q] += a.x;
-                    v[4 * q + 1] += a.y;
-                    v[4 * q + 2] += a.z;
-                    v[4 * q + 3] += a.w;
-                }
+                for (int j = 0; j < 32; j++) w[j] = __ldcg(src + (size_t)j * BW);
+#pragma unroll
+                for (int j = 0; j < 32; j++) v[j] += w[j];
             }
         }
         epi_chunk<KIND>(epi, v, lane, n, N, m0 + c0, M);
@@ -732,9 +728,9 @@ cudaError_t qgemm_prepare() {
 namespace {
 // Tile width BT and K split for an N x K weight at M rows: the least estimated time, waves of CTAs x the time of
 // one CTA.  The per-CTA times are fitted to measurements of this kernel on the 8B and 1B Q4_0 shapes at M = 512
-// (every (BT, split) pair timed): K steps x 1.05 us + 8 us at BT = 256, x 0.83 us + 12 us at BT = 128; a split
-// CTA also stores its partial and the last one sums them, which measured as a fixed 28 us (BT = 256) or 13 us
-// (BT = 128).  A split keeps at least 8 K steps per CTA and fits the workspace and the counters.
+// (every (BT, split) pair timed, weights streamed from DRAM): K steps x 1.05 us + 8 us at BT = 256, x 0.83 us +
+// 12 us at BT = 128; a split CTA also stores its partial and the last one sums them, which measured as a fixed
+// 20 us (BT = 256) or 13 us (BT = 128).  A split keeps at least 8 K steps per CTA and fits the workspace and the counters.
 struct GemmShape {
     int BT, ksplit;
 };
@@ -749,7 +745,7 @@ GemmShape pick_gemm(int N, int K, int M, size_t ws_bytes, int cnt_n) {
         const double step = BT == 256 ? 1.05 : 0.83;
         for (int ks = 1; ks <= kMaxSplit; ks++) {
             if (ks > 1 && (nk / ks < 8 || (size_t)nt * mt * ks * BW * BT * 4 > ws_bytes || nt * mt > cnt_n)) break;
-            const double fixed = ks == 1 ? (BT == 256 ? 8.0 : 12.0) : (BT == 256 ? 28.0 : 13.0);
+            const double fixed = ks == 1 ? (BT == 256 ? 8.0 : 12.0) : (BT == 256 ? 20.0 : 13.0);
             const int ctas = nt * mt * ks;
             const double t = (double)((ctas + sms - 1) / sms) * ((double)nk / ks * step + fixed);
             if (t < best_t - 1e-9) {
