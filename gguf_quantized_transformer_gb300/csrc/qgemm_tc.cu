@@ -492,7 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ TcSmem sm;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * BW, m0 = blockIdx.y * BT;
+    // grid (M tiles, N tiles, splits): the M tiles of one weight tile are adjacent in launch order, so the weight
+    // rows come from DRAM once and from L2 for the other M tiles
+    const int n0 = blockIdx.y * BW, m0 = blockIdx.x * BT;
     const int nk_all = (W.K + BK - 1) / BK;
     const int kz = blockIdx.z;  // this CTA's K steps: [k_lo, k_lo + nk)
     const int k_lo = (int)((int64_t)nk_all * kz / ksplit);
@@ -780,7 +782,7 @@ cudaError_t launch_qgemm(const Planes& W, const __half* X_hi, const __half* X_lo
     CUtensorMap mh, ml;
     if (!make_map(&mh, X_hi, M, W.K, ldx, BT) || !make_map(&ml, X_lo, M, W.K, ldx, BT)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nt, (M + BT - 1) / BT, g.ksplit);
+    cfg.gridDim = dim3((M + BT - 1) / BT, nt, g.ksplit);
     cfg.blockDim = dim3(kThreads);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
