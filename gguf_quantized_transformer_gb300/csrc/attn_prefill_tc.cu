@@ -15,8 +15,8 @@
 //   warp 8      : one lane issues S = Q K^T for tile t, then O += P V for tile
 //                 t - 1, each followed by a commit;
 //   warps 0..3  : own the 128 TMEM lanes (one query vector each): the online
-//                 softmax of S with the causal mask, P (fp16 hi + lo) into one
-//                 of two buffers, and the epilogue.
+//                 softmax of S with the causal mask, P (fp16) into one of two
+//                 buffers, and the epilogue.
 // The running maximum is rescaled lazily: P uses a reference maximum that only
 // moves (rescaling O in TMEM and the row sum) when a tile's maximum exceeds it
 // by more than kLazy, so p <= e^kLazy and fp16 P stays in range.  O / l does not
@@ -24,10 +24,12 @@
 // The output is O / l, written as the fp16 hi + lo planes the O-projection GEMM
 // reads.
 //
-// Precision.  Q (scaled by 1/sqrt(D)) and P are split into fp16 hi + lo; an
-// fp16 cache is exact in fp16, an fp32 cache is split too.  The products
-// kept are A_hi B_hi + A_lo B_hi (+ A_hi B_lo for an fp32 cache), fp32
-// accumulate: near-fp32 scores and outputs.
+// Precision.  Q (scaled) is split into fp16 hi + lo, so the scores are
+// near-fp32: S = Q_hi K + Q_lo K (+ Q_hi K_lo for an fp32 cache, which is split
+// too; an fp16 cache is exact in fp16).  P is rounded to fp16 (a relative
+// error <= 2^-12 per weight, so O / l moves by at most about 2^-12 of the V
+// values' range; the row sum l keeps the unrounded p): O += P V_hi (+ P V_lo
+// for an fp32 cache), fp32 accumulate.
 //
 // Operands live in shared memory in the SWIZZLE_128B K-major layout.  Every
 // tcgen05.ld / st is executed by whole warps under warp-uniform conditions,
@@ -72,11 +74,6 @@ __device__ __forceinline__ void ld8_cg(const float* p, float (&w)[8]) {
     const float4 a = __ldcg(reinterpret_cast<const float4*>(p)), b = __ldcg(reinterpret_cast<const float4*>(p + 4));
     w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
-__device__ __forceinline__ void ld2(const __half* p, float& a, float& b) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(p));
-    a = f.x;
-    b = f.y;
-}
 __device__ __forceinline__ void ld2(const float* p, float& a, float& b) {
     const float2 f = *reinterpret_cast<const float2*>(p);
     a = f.x;
@@ -91,7 +88,7 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ uint4 pack8_f16(const float (&w)[8]) {  // exact for values that are fp16
+__device__ __forceinline__ uint4 pack8_f16(const float (&w)[8]) {  // round to nearest fp16
     uint32_t h[4];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
@@ -120,14 +117,13 @@ struct PCfg {
     static constexpr int K_BYTES = BKV * D * 2;
     static constexpr int V_BYTES = D * BKV * 2;
     static constexpr int P_BYTES = BQ * BKV * 2;
-    // one operand buffer: K hi (+ lo), V hi (+ lo), P hi + lo
+    // one operand buffer: K hi (+ lo), V hi (+ lo), P
     static constexpr int B_KH = 0;
     static constexpr int B_KL = B_KH + K_BYTES;
     static constexpr int B_VH = B_KL + (SPLIT_KV ? K_BYTES : 0);
     static constexpr int B_VL = B_VH + V_BYTES;
     static constexpr int B_PH = B_VL + (SPLIT_KV ? V_BYTES : 0);
-    static constexpr int B_PL = B_PH + P_BYTES;
-    static constexpr int BUF = (B_PL + P_BYTES + 1023) / 1024 * 1024;
+    static constexpr int BUF = (B_PH + P_BYTES + 1023) / 1024 * 1024;
     static constexpr int OFF_QH = 0;
     static constexpr int OFF_QL = Q_BYTES;
     static constexpr int OFF_BUF = 2 * Q_BYTES;        // the operand buffers
@@ -298,7 +294,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             // V tile transposed: rows = d, K axis = keys (thread: dims 2dp, 2dp + 1 of 8 keys)
             for (int i = ct; i < (D / 2) * (BKV / 8); i += 128) {
                 const int dp = i % (D / 2), kg = i / (D / 2);
-                if (!C::SPLIT_KV) {  // fp16: word e holds (dim 2dp, dim 2dp + 1) of key 8kg + e
+                if constexpr (!C::SPLIT_KV) {  // fp16: word e holds (dim 2dp, dim 2dp + 1) of key 8kg + e
                     uint32_t wv[8];
 #pragma unroll
                     for (int e = 0; e < 8; e++)
@@ -312,19 +308,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     a4.w = __byte_perm(wv[6], wv[7], 0x5410); b4.w = __byte_perm(wv[6], wv[7], 0x7632);
                     *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp, kg)) = a4;
                     *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp + 1, kg)) = b4;
-                    continue;
-                }
-                float a[8], bb[8];
+                } else {  // fp32: split hi + lo
+                    float a[8], bb[8];
 #pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    if (t * BKV + 8 * kg + e < nkeys) {
-                        ld2(stV + (int64_t)(8 * kg + e) * D + 2 * dp, a[e], bb[e]);
-                    } else {
-                        a[e] = 0.f;
-                        bb[e] = 0.f;
+                    for (int e = 0; e < 8; e++) {
+                        if (t * BKV + 8 * kg + e < nkeys) {
+                            ld2(stV + (int64_t)(8 * kg + e) * D + 2 * dp, a[e], bb[e]);
+                        } else {
+                            a[e] = 0.f;
+                            bb[e] = 0.f;
+                        }
                     }
-                }
-                if (C::SPLIT_KV) {
                     uint4 ah, al, bh, bl;
                     split8(a, ah, al);
                     split8(bb, bh, bl);
@@ -332,9 +326,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp + 1, kg)) = bh;
                     *reinterpret_cast<uint4*>(ob + C::B_VL + op_off(D, 2 * dp, kg)) = al;
                     *reinterpret_cast<uint4*>(ob + C::B_VL + op_off(D, 2 * dp + 1, kg)) = bl;
-                } else {
-                    *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp, kg)) = pack8_f16(a);
-                    *reinterpret_cast<uint4*>(ob + C::B_VH + op_off(D, 2 * dp + 1, kg)) = pack8_f16(bb);
                 }
             }
             fence_proxy_async_shared();  // the operands -> visible to the tensor core
@@ -350,13 +341,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
             auto issue_pv = [&](int t) {
                 const int b = t % NB;
                 const uint8_t* ob = buf(b);
-                const uint32_t ph = smem_u32(ob + C::B_PH), pl = smem_u32(ob + C::B_PL);
+                const uint32_t ph = smem_u32(ob + C::B_PH);
                 const uint32_t vh = smem_u32(ob + C::B_VH), vl = smem_u32(ob + C::B_VL);
                 for (int kk = 0; kk < BKV / 16; kk++) {
                     const uint64_t dvh = op_desc(vh, D, kk);
                     const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
                     mma_f16(tmem + kOCol, op_desc(ph, BQ, kk), dvh, kIdO, acc);
-                    mma_f16(tmem + kOCol, op_desc(pl, BQ, kk), dvh, kIdO, 1u);
                     if (C::SPLIT_KV) mma_f16(tmem + kOCol, op_desc(ph, BQ, kk), op_desc(vl, D, kk), kIdO, 1u);
                 }
                 mma_commit(&sm.op_free[b]);
@@ -460,10 +450,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         l += p;
                         w[e] = p;
                     }
-                    uint4 hi, lo;
-                    split8(w, hi, lo);
-                    *reinterpret_cast<uint4*>(ob + C::B_PH + op_off(BQ, v, c32 * 4 + q8)) = hi;
-                    *reinterpret_cast<uint4*>(ob + C::B_PL + op_off(BQ, v, c32 * 4 + q8)) = lo;
+                    *reinterpret_cast<uint4*>(ob + C::B_PH + op_off(BQ, v, c32 * 4 + q8)) = pack8_f16(w);
                 }
             }
             fence_proxy_async_shared();
