@@ -41,6 +41,13 @@
 // flight; the x images live in the last ring slots, which are filled only
 // after every lane has copied its x units into registers.
 //
+// A second kernel, qgemv_pw_kernel, serves the shapes where it measured faster
+// (few rows per CTA that all fit in shared memory, and the LM head): each
+// stage of R whole rows belongs to one warp, in a slot that warp owns; the warp
+// waits for it, computes its R rows over the whole K with the x units read from
+// the shared image, refills the slot and applies the epilogue, with no
+// cross-warp reduction.
+//
 // Every mbarrier wait is bounded; on a timeout the kernel records DEV_TIMEOUT
 // in its error word, drains its outstanding copies (bounded) and returns.
 #pragma once
@@ -67,6 +74,12 @@ constexpr int kRingBudget = 192 * 1024;  // ring, x images inside (one CTA per S
 constexpr int kMinStage = 24 * 1024;     // stage size target: enough work per warp between waits
 constexpr int kMaxStage = 64 * 1024;     // largest stage that still leaves three in the ring
 constexpr int kMaxGemvSmem = 208 * 1024;
+// per-warp kernel (qgemv_pw_kernel)
+constexpr int kPwMaxSlots = 2 * kWarps;
+constexpr int kPwSlotMax = 24 * 1024;      // stage size bound for streamed matrices (16-24 KB copies)
+constexpr int kPwMaxSmem = 216 * 1024;     // x image + slots (one CTA per SM)
+
+__host__ __device__ constexpr int pw_ximage_bytes(int Kp) { return ((Kp / 32) * kXBlkBytes + 127) & ~127; }
 
 template <int WT>
 __host__ __device__ constexpr int units_per_lane() { return WT == AF_Q8_0 ? 8 : 4; }
@@ -280,6 +293,230 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (epi.kind == EPI_LOGITS && tid == 0 && amax_s) atomicMax(epi.argmax, amax_s);
 }
 
+// ---------------------------------------------------------------- per-warp kernel
+template <int WT, bool NORM, int R>
+__global__ void __launch_bounds__(kThreads, 1)
+    qgemv_pw_kernel(Planes W, const float* __restrict__ x, const float* __restrict__ nw, float eps, Epi epi, int nslot,
+                 int slot_bytes, unsigned* __restrict__ err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ uint64_t full[kPwMaxSlots];
+    __shared__ unsigned issues[kPwMaxSlots];  // copies issued into the slot so far
+    __shared__ float ssum[kWarps];
+    __shared__ float xres[kMaxCtaRows];
+    __shared__ float2 rope_s[64];
+    __shared__ unsigned long long amax_s;
+    __shared__ volatile int abort_flag;
+    __shared__ uint64_t never;  // an mbarrier nothing arrives on (the error path's test hook, below)
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int N = W.N, K = W.K;
+    constexpr int UW = WT == AF_Q8_0 ? 16 : 32;  // weights per unit
+    const int NC = W.Kp / (32 * UW);              // chunks of 32 units (one per lane)
+    const int64_t pitch = W.qs_pitch();
+    const int sc_off = W.sc_off(), hb_off = W.hb_off();
+    // x image first, then the slots
+    XBlk* xb = reinterpret_cast<XBlk*>(smem);
+    uint8_t* ring = smem + pw_ximage_bytes(W.Kp);
+    const int np = N / 2;
+    const int pa = (int)((int64_t)np * blockIdx.x / gridDim.x), pb = (int)((int64_t)np * (blockIdx.x + 1) / gridDim.x);
+    const int r0 = 2 * pa, nrows = 2 * (pb - pa);
+    const int nst = (nrows + R - 1) / R;
+    // consumer warps and slots per warp: stage s belongs to warp s % WC; its i-th stage (s = warp + WC i) lives
+    // in slot warp + WC (i % S), so every slot has one owner, which waits its phases in order and refills it
+    const int WC = nslot < kWarps ? nslot : kWarps;
+    const int S = nslot / WC;
+
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int s = 0; s < nslot; s++) {
+            mbar_init(&full[s], 1);
+            issues[s] = 0;
+        }
+        abort_flag = 0;
+        amax_s = 0ull;
+        mbar_init(&never, 1);
+        fence_mbar_init();
+    }
+    // err[1] != 0 (test instrumentation): warp 0's first stage wait polls `never` that many times, gives up and
+    // takes the timeout path (error code, drain of the copies in flight, early return) exactly as a real timeout
+    const unsigned stall = err[1];
+    __syncthreads();
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int st, int slot) {  // one thread: rows r0 + st*R .. with their scales, one range
+        const int ra = r0 + st * R, nr = min(R, r0 + nrows - ra);
+        const unsigned bytes = (unsigned)(nr * pitch);
+        issues[slot]++;
+        mbar_arrive_expect_tx(&full[slot], bytes);
+        bulk_g2s_evict_first(ring + (size_t)slot * slot_bytes, W.qs + (int64_t)ra * pitch, bytes, &full[slot], pol);
+    };
+    // the first stage of every slot: weights do not depend on the previous kernel
+    if (tid == 0)
+        for (int st = 0; st < min(nst, nslot); st++) issue(st, st);
+    // the position word is written before the step's first kernel starts and the RoPE table never: both are
+    // read before waiting for the previous kernel
+    int qpos = 0;
+    if (epi.kind == EPI_QKV) {
+        qpos = epi.pos_dev ? __ldcg(epi.pos_dev) : epi.pos0;
+        for (int i = tid; i < epi.head_dim / 2; i += kThreads) rope_s[i] = epi.rope[(int64_t)qpos * (epi.head_dim / 2) + i];
+    }
+
+    pdl_wait();  // x (and the residual rows) are written by the previous kernel
+
+    // RMSNorm prologue: every CTA reduces sum(x^2) over the whole input while it converts w (.) x
+    float ss = quantize_x<NORM, kThreads, true>(x, nw, K, W.Kp / 32, xb, tid);
+    if (NORM) {
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) ssum[warp] = ss;
+    }
+    // epilogue inputs into shared memory
+    if (epi.kind == EPI_RESID)
+        for (int i = tid; i < nrows; i += kThreads) xres[i] = __ldcg(epi.out + r0 + i);
+    GemvEpiCtx ectx;
+    ectx.xres = xres;
+    ectx.rope = rope_s;
+    ectx.amax = &amax_s;
+    ectx.r0 = r0;
+    ectx.pos = 0;
+    ectx.pos = qpos;
+    __syncthreads();
+
+    float rstd = 1.f;  // applied to each row's dot product (the image holds w (.) x)
+    if (NORM) {
+        float t = 0.f;
+#pragma unroll
+        for (int i = 0; i < kWarps; i++) t += ssum[i];
+        rstd = rsqrtf(t / (float)K + eps);
+    }
+
+    if (warp < WC) {
+        for (int i = 0;; i++) {
+            const int st = warp + WC * i;
+            if (st >= nst) break;
+            const int slot = warp + WC * (i % S);
+            const unsigned par = (unsigned)((i / S) & 1);
+            bool ok = false;
+            uint64_t* bar = (stall && warp == 0 && i == 0) ? &never : &full[slot];
+            const unsigned lim = (stall && warp == 0 && i == 0) ? stall : kWaitLimit;
+            for (unsigned it = 0; it < lim && !ok; it++) {
+                ok = mbar_try_wait(bar, par);
+                if (!ok && abort_flag) break;
+            }
+            if (!ok) {
+                if (lane == 0) {
+                    abort_flag = 1;
+                    atomicExch(err, (unsigned)DEV_TIMEOUT);
+                }
+                break;
+            }
+            const uint8_t* sm = ring + (size_t)slot * slot_bytes;
+            const int ra = r0 + st * R, nr = min(R, r0 + nrows - ra);
+            float acc[R];
+#pragma unroll
+            for (int r = 0; r < R; r++) acc[r] = 0.f;
+            for (int c = 0; c < NC; c++) {
+                const int unit = c * 32 + lane;
+                Unit<WT> xu;
+                xu.load(xb, unit);
+#pragma unroll
+                for (int r = 0; r < R; r++) {
+                    if (r < nr) {  // warp-uniform
+                        if constexpr (WT == AF_Q5_K || WT == AF_Q6_K)
+                            acc[r] = xu.accumulate(sm + r * pitch, sc_off, hb_off, unit, acc[r]);
+                        else
+                            acc[r] = xu.accumulate(sm + r * pitch, sc_off, unit, acc[r]);
+                    }
+                }
+            }
+            __syncwarp();  // every lane is done reading the slot
+            if (lane == 0 && st + WC * S < nst) {
+                fence_proxy_async_shared();  // generic-proxy reads of the slot before the copy overwrites it
+                issue(st + WC * S, slot);
+            }
+            // lanes (32/R)*t .. hold the sum of acc[t]; lane (64/R)*p applies row pair p
+            const float rv = transpose_reduce<R>(acc, lane);
+            const float rv1 = __shfl_down_sync(0xffffffffu, rv, 32 / R);
+            if (lane % (64 / R) == 0) {
+                const int j0 = 2 * (lane / (64 / R));
+                if (j0 < nr) gemv_epi(epi, ectx, ra + j0, rv * rstd, rv1 * rstd);
+            }
+        }
+    }
+    __syncthreads();
+    if (abort_flag) {  // drain every copy still in flight before the CTA exits
+        if (tid == 0)
+            for (int s = 0; s < nslot; s++)
+                if (issues[s]) mbar_wait_bounded(&full[s], (issues[s] - 1u) & 1u);
+        __syncthreads();
+        return;
+    }
+    if (epi.kind == EPI_LOGITS && tid == 0 && amax_s) atomicMax(epi.argmax, amax_s);
+}
+
+struct PwShape {
+    int R, nslot, slot_bytes, smem;
+};
+
+// Rows per stage R (2, 4 or 8) and slots of the per-warp kernel.  When one CTA's rows fit in shared memory at once
+// (the QKV and O shapes), R spreads them over about all warps and every stage is issued before the previous kernel
+// ends; otherwise (the LM head's hundreds of rows per CTA) stages of 16-24 KB stream through as many slots as fit.
+PwShape pw_pick_shape(const Planes& W, int grid) {
+    const int pitch = (int)W.qs_pitch();
+    const int xbytes = pw_ximage_bytes(W.Kp);
+    const int budget = kPwMaxSmem - xbytes;
+    const int cta_rows = 2 * ((W.N / 2 + grid - 1) / grid);
+    PwShape s;
+    if ((int64_t)cta_rows * pitch + kWarps * 128 <= budget) {
+        s.R = 2;
+        while (s.R < 8 && (cta_rows + s.R - 1) / s.R > kWarps) s.R *= 2;
+    } else {
+        s.R = 8;
+        while (s.R > 2 && s.R * pitch > kPwSlotMax) s.R /= 2;
+    }
+    s.slot_bytes = (s.R * pitch + 127) & ~127;
+    s.nslot = budget / s.slot_bytes;
+    if (s.nslot > kWarps) s.nslot = s.nslot >= 2 * kWarps ? 2 * kWarps : kWarps;  // a multiple of the warps
+    s.smem = xbytes + s.nslot * s.slot_bytes;
+    return s;
+}
+
+// The per-warp kernel for matrices where it measured faster: few rows per CTA that all fit in shared memory
+// (QKV 6144 x 4096: 5.45 against 6.44 us; O 4096 x 4096: equal) and the LM head's many rows per CTA (128256 x
+// 4096: 50.8 against 57.5 us).  The ring kernel stays for gate/up (16.1 against 17.1 us) and down (11.2 / 13.3).
+bool use_pw(const Planes& W, int grid) {
+    const int cta_rows = 2 * ((W.N / 2 + grid - 1) / grid);
+    if (cta_rows >= 512) return true;
+    return cta_rows <= 64 && (int64_t)cta_rows * W.qs_pitch() + kWarps * 128 <= kPwMaxSmem - pw_ximage_bytes(W.Kp);
+}
+
+template <int WT, bool NORM, int R>
+cudaError_t pw_launch_t(const Planes& W, const float* x, const float* nw, float eps, const Epi& epi,
+                        const PwShape& sh, unsigned* err, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms());
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sh.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, qgemv_pw_kernel<WT, NORM, R>, W, x, nw, eps, epi, sh.nslot, sh.slot_bytes, err);
+}
+
+template <int WT, bool NORM>
+cudaError_t pw_dispatch(const Planes& W, const float* x, const float* nw, float eps, const Epi& epi, unsigned* err,
+                        cudaStream_t s) {
+    const PwShape sh = pw_pick_shape(W, num_sms());
+    if (sh.nslot < 1 || sh.smem > kPwMaxSmem) return cudaErrorInvalidValue;
+    if (epi.kind == EPI_RESID && 2 * ((W.N / 2 + num_sms() - 1) / num_sms()) > kMaxCtaRows) return cudaErrorInvalidValue;
+    switch (sh.R) {
+        case 2: return pw_launch_t<WT, NORM, 2>(W, x, nw, eps, epi, sh, err, s);
+        case 4: return pw_launch_t<WT, NORM, 4>(W, x, nw, eps, epi, sh, err, s);
+        default: return pw_launch_t<WT, NORM, 8>(W, x, nw, eps, epi, sh, err, s);
+    }
+}
+
 struct Shape {
     int WK, PPW, ring, xslot, stage_bytes, smem;
 };
@@ -334,6 +571,7 @@ cudaError_t launch_t(const Planes& W, const float* x, const float* nw, float eps
 template <int WT, bool NORM>
 cudaError_t dispatch(const Planes& W, const float* x, const float* nw, float eps, const Epi& epi, unsigned* err,
                      cudaStream_t s) {
+    if (use_pw(W, num_sms())) return pw_dispatch<WT, NORM>(W, x, nw, eps, epi, err, s);
     const Shape sh = pick_shape(W);
     if (sh.smem > kMaxGemvSmem || sh.ring > kMaxRing) return cudaErrorInvalidValue;
 #define AF_GEMV_CASE(WW, PP) \
@@ -355,6 +593,10 @@ cudaError_t set_attrs_t() {
 #define AF_GEMV_ATTR2(WW, PP) AF_GEMV_ATTR(WT, true, WW, PP) AF_GEMV_ATTR(WT, false, WW, PP)
     AF_GEMV_SHAPES(AF_GEMV_ATTR2)
 #undef AF_GEMV_ATTR2
+#define AF_PW_ATTR(NORM, RR) \
+    if (!e) e = cudaFuncSetAttribute(qgemv_pw_kernel<WT, NORM, RR>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPwMaxSmem);
+    AF_PW_ATTR(true, 2) AF_PW_ATTR(true, 4) AF_PW_ATTR(true, 8) AF_PW_ATTR(false, 2) AF_PW_ATTR(false, 4) AF_PW_ATTR(false, 8)
+#undef AF_PW_ATTR
     return e;
 }
 #undef AF_GEMV_ATTR
