@@ -475,6 +475,10 @@ PwShape pw_pick_shape(const Planes& W, int grid) {
     s.slot_bytes = (s.R * pitch + 127) & ~127;
     s.nslot = budget / s.slot_bytes;
     if (s.nslot > kWarps) s.nslot = s.nslot >= 2 * kWarps ? 2 * kWarps : kWarps;  // a multiple of the warps
+    // rows that fit at once: only the slots their stages take, so the neighbouring kernels of the decode chain
+    // (attention, about 100 KB) can be resident on the same SM and start their own copies early
+    const int nst = (cta_rows + s.R - 1) / s.R;
+    if ((int64_t)cta_rows * pitch + kWarps * 128 <= budget && nst < s.nslot) s.nslot = nst;
     s.smem = xbytes + s.nslot * s.slot_bytes;
     return s;
 }
