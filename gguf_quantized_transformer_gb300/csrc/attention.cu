@@ -56,7 +56,7 @@ __device__ __forceinline__ void load_vec<__half>(const __half* p, float* out, in
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMinPerSplit = 64;  // positions per split before another split is used
-constexpr int kRing = 96 * 1024;     // tile ring budget (two CTAs per SM)
+constexpr int kRing = 64 * 1024;     // tile ring budget (two CTAs per SM)
 constexpr int kRingCl = 176 * 1024;  // tile ring budget of the cluster path (one CTA per SM)
 constexpr int kMaxStages = 12;
 // Cluster path: the kC CTAs of one kv head form a thread-block cluster of one CTA per SM and merge through
