@@ -9,7 +9,8 @@
 // completion, L2 evict-first) into a shared-memory ring; the warp that
 // finishes a stage last refills its slot.  The first stages are issued before
 // griddepcontrol.wait (weights do not depend on the previous kernel), so the
-// ring (up to 192 KB) fills while the prologue runs.
+// ring (up to 112 KB, so that the CTAs of the kernels before and after it can
+// be resident on the same SM) fills while the prologue runs.
 //
 // Activations.  The prologue (all threads) reads x once: it reduces sum(x^2)
 // for the optional RMSNorm and converts w (.) x (the norm weight times x; the
@@ -70,7 +71,7 @@ constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtaRows = 512;        // residual rows a CTA may own (preloaded to shared memory)
 constexpr int kMaxRing = 12;
-constexpr int kRingBudget = 192 * 1024;  // ring, x images inside (one CTA per SM)
+constexpr int kRingBudget = 112 * 1024;  // ring, x images inside: room beside it for the neighbouring kernels' CTAs
 constexpr int kMinStage = 24 * 1024;     // stage size target: enough work per warp between waits
 constexpr int kMaxStage = 64 * 1024;     // largest stage that still leaves three in the ring
 constexpr int kMaxGemvSmem = 208 * 1024;
