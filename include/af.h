@@ -212,10 +212,12 @@ int af_debug_capture(af_model* m, float* hidden_dev);
  *     with programmatic dependent launch and replayed as a CUDA graph (see
  *     af_set_decode_graph).
  *   AF_DECODE_PERSISTENT: one cooperative launch per token, one CTA per SM,
- *     all layers separated by bounded grid barriers, the weights of the next
- *     matrix streaming into shared memory while the grid synchronises
- *     (n_embd <= 4096, Q4_0 or Q8_0 for every matrix including the LM head;
- *     AF_ENOTIMPL otherwise or where it cannot be resident).
+ *     phases (each matrix, attention) separated by bounded grid barriers; each
+ *     warp's shared-memory slot streams its next stage of weights or cache
+ *     tiles whatever phase it belongs to, so copies run ahead through the
+ *     barriers (Q4_0 or Q8_0 for every matrix including the LM head, an fp32 or
+ *     fp16 cache, head_dim 64 or 128, group 2, 4 or 8; AF_ENOTIMPL otherwise or
+ *     where it cannot be resident).  Measured slower than the default.
  */
 enum { AF_DECODE_PERSISTENT = 0, AF_DECODE_KERNELS = 1 };
 int af_set_decode_mode(af_model* m, int mode);
