@@ -2,7 +2,7 @@
  * CPU ORACLE for the GGUF-quantized Llama-style decoder forward pass.
  *
  * TEST INFRASTRUCTURE ONLY.  This is the plain, slow, obviously-correct fp64
- * restatement of what the surveyed pages define, used by the tests, by the
+ * restatement of what the cited pages define, used by the tests, by the
  * smoke check and by the timed CPU baseline.  No product code path may link,
  * load or call it, and it shares no code with the CUDA library.
  *

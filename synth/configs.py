@@ -1,6 +1,6 @@
 """Model shapes and workloads of the five synthetic decoders.
 
-Shapes follow the models the surveyed pages run: a tiny 2-layer decoder, a
+Shapes follow the models the cited pages run: a tiny 2-layer decoder, a
 TinyLlama-1.1B shape (the Airframe GPU-pipeline page's KV-cache example), a
 Llama-3.2-1B shape and a Llama-3-8B shape (the dotLLM "GPU Inference" page's
 VRAM-estimation table), plus the 8B shape with the YaRN extended context of the
