@@ -376,7 +376,7 @@ def run_ours(args, cfg, world, rank, local):
         line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "cpu": cpu_name(),
                                 "sample": f"{args.ref_decode} decode steps after a 4-token prefill "
                                           f"({dt:.1f} s, fp64, {threads} threads)",
-                                "per_config": {f"config{args.config}": oracle_baselines(hm, cfg),
+                                "per_config": {cfg.name: oracle_baselines(hm, cfg),
                                                **{k: v.get("cpu_baseline") for k, v in others.items()
                                                   if isinstance(v, dict)}}}
     if rank == 0:
@@ -502,13 +502,13 @@ def config_runs(af, args, dev, hbm_peak, tc_peak):
                                 tc_peak, steps=1, warmup=1, cpu=args.rank == 0 and not args.no_cpu_baseline)
             if cfg.max_ctx > 8192:  # long context: decode attention is half the bytes of a token; its roofline
                 line["attn_roofline"] = attn_roofline(af, cfg, cfg.prompt_len, dev, hbm_peak)
-            out[f"config{idx}"] = line
+            out[cfg.name] = line
             if cfg.max_ctx > 8192:  # the same workload over a Q8_0 cache with a 512-slot fp16 window
                 qcfg = cfg.with_(kv_dtype="q8_0", kv_window=512)
-                out[f"config{idx}_kv_q8_0"] = workload_run(af, qcfg, synth.seed_of(idx), P, cfg.n_decode, cfg.chunk,
+                out[cfg.name + "+kv_q8_0"] = workload_run(af, qcfg, synth.seed_of(idx), P, cfg.n_decode, cfg.chunk,
                                                            dev, hbm_peak, tc_peak, steps=1, warmup=1)
         except Exception as e:  # a failed secondary line must not take the headline with it
-            out[f"config{idx}"] = {"error": f"{type(e).__name__}: {e}"}
+            out[cfg.name] = {"error": f"{type(e).__name__}: {e}"}
     return out
 
 
